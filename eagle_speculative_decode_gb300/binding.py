@@ -1,0 +1,206 @@
+"""ctypes binding of libeagle3.so: the C ABI of include/eagle3.h under the same names.
+
+Argument marshalling only: device buffers are passed as integer addresses (e.g. a torch
+tensor's ``data_ptr()``), host arrays as numpy int32 arrays, streams as integer handles.
+Every computation happens in the CUDA library; if the library is missing this module
+raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libeagle3.so")
+
+EAGLE3_OK = 0
+EAGLE3_ERR_INVALID_ARG = -1
+EAGLE3_ERR_CAPACITY = -2
+EAGLE3_ERR_STATE = -3
+EAGLE3_ERR_CUDA = -4
+EAGLE3_ERR_DEVICE = -5
+EAGLE3_ERR_UNSUPPORTED = -6
+EAGLE3_SHRINK_GAMMA = 1
+EAGLE3_DEV_BAD_TOKEN = 1
+EAGLE3_DEV_BAD_PAGE = 2
+EAGLE3_DEV_BAD_POSITION = 4
+EAGLE3_DEV_BAD_LENGTH = 8
+
+EXPORTED = (
+    "eagle3_version", "eagle3_error_string", "eagle3_workspace_bytes", "eagle3_plan_gamma",
+    "eagle3_init", "eagle3_destroy", "eagle3_encode", "eagle3_prefill", "eagle3_draft_chain",
+    "eagle3_rewind", "eagle3_accept", "eagle3_rebuild_after_verify", "eagle3_get_status",
+    "eagle3_set_graph_mode",
+)
+
+
+class Eagle3Error(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {error_string(code)} ({code})")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("n_embd", ctypes.c_int), ("n_head", ctypes.c_int), ("n_head_kv", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("rope_dims", ctypes.c_int),
+                ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
+                ("n_ff", ctypes.c_int), ("draft_vocab", ctypes.c_int),
+                ("target_vocab", ctypes.c_int), ("max_batch", ctypes.c_int),
+                ("max_gamma", ctypes.c_int), ("max_cache_len", ctypes.c_int),
+                ("page_size", ctypes.c_int)]
+
+
+WEIGHT_FIELDS = ("fc", "in_norm", "hidden_norm", "q", "k", "v", "o", "post_norm", "gate", "up",
+                 "down", "final_norm", "lm_head", "embed", "d2t")
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_void_p) for f in WEIGHT_FIELDS]
+
+
+class KV(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("page_table", ctypes.c_void_p), ("num_pages", ctypes.c_int),
+                ("max_pages_per_seq", ctypes.c_int), ("kv_len", ctypes.c_void_p)]
+
+
+class Boundary(ctypes.Structure):
+    _fields_ = [("g", ctypes.c_void_p), ("tok", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libeagle3.so (built by eagle_speculative_decode_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "eagle_speculative_decode_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, ci, cu = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint
+    P = ctypes.POINTER
+    sig = {
+        "eagle3_version": (ci, []),
+        "eagle3_error_string": (ctypes.c_char_p, [ci]),
+        "eagle3_workspace_bytes": (ctypes.c_size_t, [P(Config)]),
+        "eagle3_plan_gamma": (ci, [ci, ci, ci, cu, P(ci)]),
+        "eagle3_init": (ci, [P(Config), P(Weights), vp, ctypes.c_size_t, vp, P(vp)]),
+        "eagle3_destroy": (ci, [vp]),
+        "eagle3_encode": (ci, [vp, vp, ci, vp, vp]),
+        "eagle3_prefill": (ci, [vp, ci, vp, ci, vp, vp, vp, P(KV), P(Boundary), vp]),
+        "eagle3_draft_chain": (ci, [vp, ci, ci, cu, vp, P(KV), P(Boundary), vp, vp, vp, vp, vp, vp]),
+        "eagle3_rewind": (ci, [vp, ci, P(KV), vp]),
+        "eagle3_accept": (ci, [vp, ci, ci, vp, vp, vp, vp, vp, vp]),
+        "eagle3_rebuild_after_verify": (ci, [vp, ci, ci, vp, vp, vp, vp, P(KV), P(Boundary), vp]),
+        "eagle3_get_status": (ci, [vp, P(ci)]),
+        "eagle3_set_graph_mode": (ci, [vp, ci]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def error_string(code: int) -> str:
+    return load().eagle3_error_string(int(code)).decode()
+
+
+def _check(code: int, where: str) -> int:
+    if code != EAGLE3_OK:
+        raise Eagle3Error(code, where)
+    return code
+
+
+def _host_i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+# -------------------------------------------------------------- thin wrappers
+
+def eagle3_version() -> int:
+    return load().eagle3_version()
+
+
+def eagle3_workspace_bytes(cfg: Config) -> int:
+    return int(load().eagle3_workspace_bytes(ctypes.byref(cfg)))
+
+
+def eagle3_plan_gamma(kv_len: int, gamma: int, max_cache_len: int, flags: int = 0) -> int:
+    """Returns gamma_eff; raises Eagle3Error (e.g. EAGLE3_ERR_CAPACITY)."""
+    out = ctypes.c_int(0)
+    _check(load().eagle3_plan_gamma(int(kv_len), int(gamma), int(max_cache_len), int(flags),
+                                    ctypes.byref(out)), "eagle3_plan_gamma")
+    return out.value
+
+
+def eagle3_init(cfg: Config, weights: Weights, workspace: int, workspace_bytes: int,
+                stream: int = 0) -> int:
+    ctx = ctypes.c_void_p(0)
+    _check(load().eagle3_init(ctypes.byref(cfg), ctypes.byref(weights), workspace,
+                              workspace_bytes, stream, ctypes.byref(ctx)), "eagle3_init")
+    return int(ctx.value)
+
+
+def eagle3_destroy(ctx: int) -> None:
+    _check(load().eagle3_destroy(ctx), "eagle3_destroy")
+
+
+def eagle3_set_graph_mode(ctx: int, enabled: bool) -> None:
+    _check(load().eagle3_set_graph_mode(ctx, 1 if enabled else 0), "eagle3_set_graph_mode")
+
+
+def eagle3_encode(ctx: int, aux: int, M: int, g: int, stream: int = 0) -> None:
+    _check(load().eagle3_encode(ctx, aux, int(M), g, stream), "eagle3_encode")
+
+
+def eagle3_prefill(ctx: int, B: int, tokens: int, P_max: int, next_tok: int, prompt_len_host,
+                   aux: int, kv: KV, bnd: Boundary, stream: int = 0) -> None:
+    pl = _host_i32(prompt_len_host)
+    _check(load().eagle3_prefill(ctx, int(B), tokens, int(P_max), next_tok,
+                                 pl.ctypes.data_as(ctypes.c_void_p), aux, ctypes.byref(kv),
+                                 ctypes.byref(bnd), stream), "eagle3_prefill")
+
+
+def eagle3_draft_chain(ctx: int, B: int, gamma: int, flags: int, kv_len_host, kv: KV,
+                       bnd: Boundary, draft_tok: int, draft_id: int | None = None,
+                       gamma_eff: int | None = None, logits_dbg: int | None = None,
+                       g_dbg: int | None = None, stream: int = 0) -> None:
+    kl = _host_i32(kv_len_host)
+    _check(load().eagle3_draft_chain(ctx, int(B), int(gamma), int(flags),
+                                     kl.ctypes.data_as(ctypes.c_void_p), ctypes.byref(kv),
+                                     ctypes.byref(bnd), draft_tok, draft_id, gamma_eff,
+                                     logits_dbg, g_dbg, stream), "eagle3_draft_chain")
+
+
+def eagle3_rewind(ctx: int, B: int, kv: KV, stream: int = 0) -> None:
+    _check(load().eagle3_rewind(ctx, int(B), ctypes.byref(kv), stream), "eagle3_rewind")
+
+
+def eagle3_accept(ctx: int, B: int, gamma: int, draft_tok: int, target_pred: int,
+                  gamma_eff: int | None, n_acc: int, bonus: int, stream: int = 0) -> None:
+    _check(load().eagle3_accept(ctx, int(B), int(gamma), draft_tok, target_pred, gamma_eff,
+                                n_acc, bonus, stream), "eagle3_accept")
+
+
+def eagle3_rebuild_after_verify(ctx: int, B: int, gamma: int, n_acc: int, draft_tok: int,
+                                bonus: int, verify_aux: int, kv: KV, bnd: Boundary,
+                                stream: int = 0) -> None:
+    _check(load().eagle3_rebuild_after_verify(ctx, int(B), int(gamma), n_acc, draft_tok, bonus,
+                                              verify_aux, ctypes.byref(kv), ctypes.byref(bnd),
+                                              stream), "eagle3_rebuild_after_verify")
+
+
+def eagle3_get_status(ctx: int) -> int:
+    """Synchronises; returns the device status word (0 = clean) without raising."""
+    s = ctypes.c_int(0)
+    rc = load().eagle3_get_status(ctx, ctypes.byref(s))
+    if rc not in (EAGLE3_OK, EAGLE3_ERR_DEVICE):
+        raise Eagle3Error(rc, "eagle3_get_status")
+    return s.value

@@ -1,0 +1,723 @@
+// C ABI of the EAGLE-3 drafter draft round: argument validation, workspace layout,
+// the round state machine and kernel orchestration (direct launches or a CUDA graph of
+// the gamma-step chain).  See include/eagle3.h for the contract of every entry point.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace e3;
+
+namespace {
+
+constexpr int kPrefillChunk = 512;   // prompt positions encoded per prefill chunk
+constexpr int kMaxSplits = 64;       // split-KV partitions per (sequence, kv head)
+constexpr int kSplitSlots = 4096;    // (sequence, kv head, split) partial slots
+constexpr int kMaxGraphs = 16;
+
+struct Layout {
+  size_t rope, q, attn_o, part_o, part_ml, attn_cnt, x1, act, gwork, tokwork, am_slot, am_cnt,
+      round_start, geff, status, genc, total;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool cfg_valid(const eagle3_config *c) {
+  if (!c) return false;
+  if (c->n_embd <= 0 || c->n_embd % 8) return false;
+  if (c->n_head <= 0 || c->n_head_kv <= 0 || c->n_head % c->n_head_kv) return false;
+  if (!attn_supported(c->head_dim, c->n_head / c->n_head_kv)) return false;
+  if (c->rope_dims < 0 || c->rope_dims % 2 || c->rope_dims > c->head_dim) return false;
+  if (!(c->rope_theta > 0.f) || !(c->rms_eps >= 0.f)) return false;
+  if (c->n_ff <= 0 || c->n_ff % 8) return false;
+  if (c->draft_vocab <= 0 || c->target_vocab <= 0) return false;
+  if (c->max_batch <= 0 || c->max_gamma <= 0 || c->max_gamma > 64) return false;
+  if (c->max_cache_len <= 1 || c->page_size <= 0) return false;
+  // one GEMV launch must hold one item's activations in shared memory
+  const size_t kmax = (size_t)std::max(std::max(3 * c->n_embd, 2 * c->n_embd),
+                                       std::max(c->n_ff, c->n_head * c->head_dim));
+  if (kmax * 4 > kGemvMaxXBytes) return false;
+  if ((size_t)c->max_batch * c->n_head_kv > (size_t)kSplitSlots) return false;
+  return true;
+}
+
+Layout make_layout(const eagle3_config &c) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = align_up(off, 256);
+    off = o + std::max<size_t>(bytes, 1);
+    return o;
+  };
+  const size_t B = c.max_batch, n = c.n_embd, hd = (size_t)c.n_head * c.head_dim;
+  const size_t G = c.n_head / c.n_head_kv;
+  L.rope = take((size_t)c.max_cache_len * (c.rope_dims / 2) * sizeof(float2));
+  L.q = take(B * hd * 4);
+  L.attn_o = take(B * hd * 4);
+  L.part_o = take((size_t)kSplitSlots * G * c.head_dim * 4);
+  L.part_ml = take((size_t)kSplitSlots * G * sizeof(float2));
+  L.attn_cnt = take(B * c.n_head_kv * 4);
+  L.x1 = take(B * n * 4);
+  L.act = take(B * (size_t)c.n_ff * 4);
+  L.gwork = take(B * n * 4);
+  L.tokwork = take(B * 4);
+  L.am_slot = take(B * 8);
+  L.am_cnt = take(64 * 4);
+  L.round_start = take(B * 4);
+  L.geff = take(B * 4);
+  L.status = take(4);
+  L.genc = take(std::max<size_t>(B * (c.max_gamma + 1), kPrefillChunk) * n * 4);
+  L.total = align_up(off, 256);
+  return L;
+}
+
+struct GraphKey {
+  int B, gamma, splits;
+  unsigned flags;
+  const void *ptrs[12];
+  int ints[3];
+  bool operator==(const GraphKey &o) const {
+    if (B != o.B || gamma != o.gamma || splits != o.splits || flags != o.flags) return false;
+    for (int i = 0; i < 12; ++i)
+      if (ptrs[i] != o.ptrs[i]) return false;
+    for (int i = 0; i < 3; ++i)
+      if (ints[i] != o.ints[i]) return false;
+    return true;
+  }
+};
+
+struct GraphEntry {
+  GraphKey key;
+  cudaGraphExec_t exec;
+  unsigned long long last_use;
+};
+
+}  // namespace
+
+struct eagle3_ctx {
+  eagle3_config c;
+  eagle3_weights w;
+  char *ws;
+  size_t ws_bytes;
+  Layout L;
+  float2 *rope;
+  float *q, *attn_o, *part_o, *x1, *act, *gwork, *genc;
+  float2 *part_ml;
+  unsigned *attn_cnt, *am_cnt;
+  unsigned long long *am_slot;
+  int32_t *tokwork, *round_start, *geff;
+  int *status;
+  int num_sms;
+  int graph_mode;
+  int round_open;
+  int open_B;
+  int rebuild_ok;
+  cudaStream_t last_stream;
+  cudaStream_t cap_stream;
+  std::vector<GraphEntry> graphs;
+  unsigned long long use_clock;
+};
+
+namespace {
+
+int cuda_err(cudaError_t e) { return e == cudaSuccess ? EAGLE3_OK : EAGLE3_ERR_CUDA; }
+
+bool kv_valid(const eagle3_ctx *ctx, const eagle3_kv *kv) {
+  if (!kv || !aligned16(kv->k_pool) || !aligned16(kv->v_pool) || !kv->page_table || !kv->kv_len)
+    return false;
+  if (kv->num_pages <= 0 || kv->max_pages_per_seq <= 0) return false;
+  if ((long long)kv->max_pages_per_seq * ctx->c.page_size < ctx->c.max_cache_len) return false;
+  return true;
+}
+
+GemvParams base_params(const eagle3_ctx *ctx) {
+  GemvParams p;
+  std::memset(&p, 0, sizeof(p));
+  const eagle3_config &c = ctx->c;
+  p.n_embd = c.n_embd;
+  p.n_head = c.n_head;
+  p.n_head_kv = c.n_head_kv;
+  p.head_dim = c.head_dim;
+  p.rope_dims = c.rope_dims;
+  p.n_ff = c.n_ff;
+  p.draft_vocab = c.draft_vocab;
+  p.target_vocab = c.target_vocab;
+  p.eps = c.rms_eps;
+  p.embed = ctx->w.embed;
+  p.rope = ctx->rope;
+  p.max_cache_len = c.max_cache_len;
+  p.page_size = c.page_size;
+  p.status = ctx->status;
+  return p;
+}
+
+void set_kv(GemvParams &p, const eagle3_kv *kv) {
+  p.k_pool = kv->k_pool;
+  p.v_pool = kv->v_pool;
+  p.page_table = kv->page_table;
+  p.num_pages = kv->num_pages;
+  p.max_pages = kv->max_pages_per_seq;
+}
+
+// Launch a GEMV over `items` activation rows in as many launches as shared memory needs.
+cudaError_t gemv_items(eagle3_ctx *ctx, GemvParams p, int items, cudaStream_t st, bool pdl) {
+  const int nb = gemv_items_per_launch(p.K, items);
+  for (int i0 = 0; i0 < items; i0 += nb) {
+    p.item0 = i0;
+    p.items = std::min(nb, items - i0);
+    cudaError_t e = gemv_launch(p, ctx->num_sms, st, pdl);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t enqueue_encode(eagle3_ctx *ctx, const uint16_t *aux, int M, float *g, cudaStream_t st,
+                           bool pdl) {
+  if (M <= 0) return cudaSuccess;
+  GemvParams p = base_params(ctx);
+  p.mode = GM_ENCODE;
+  p.rows = ctx->c.n_embd;
+  p.K = 3 * ctx->c.n_embd;
+  p.w0 = ctx->w.fc;
+  p.xb = aux;
+  p.out_f = g;
+  return gemv_items(ctx, p, M, st, pdl);
+}
+
+void kv_only_params(const eagle3_ctx *ctx, const eagle3_kv *kv, GemvParams &p) {
+  const eagle3_config &c = ctx->c;
+  set_kv(p, kv);
+  p.mode = GM_QKV;
+  p.row_base = c.n_head * c.head_dim;
+  p.rows = 2 * c.n_head_kv * c.head_dim;
+  p.K = 2 * c.n_embd;
+  p.w0 = ctx->w.q;
+  p.w1 = ctx->w.k;
+  p.w2 = ctx->w.v;
+  p.norm0 = ctx->w.in_norm;
+  p.norm1 = ctx->w.hidden_norm;
+}
+
+int choose_splits(const eagle3_ctx *ctx, int B, int max_len) {
+  const int per = B * ctx->c.n_head_kv;
+  int s = std::max(1, (2 * ctx->num_sms + per - 1) / per);
+  s = std::min(s, kMaxSplits);
+  s = std::min(s, std::max(1, kSplitSlots / per));
+  // at least ~64 keys per split
+  const int by_len = std::max(1, (max_len + 63) / 64);
+  s = std::min(s, by_len);
+  int p2 = 1;
+  while (p2 * 2 <= s) p2 *= 2;
+  return p2;
+}
+
+struct ChainArgs {
+  int B, gamma, splits;
+  unsigned flags;
+  const eagle3_kv *kv;
+  const eagle3_boundary *bnd;
+  int32_t *draft_tok, *draft_id, *gamma_eff;
+  float *logits_dbg, *g_dbg;
+};
+
+cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) {
+  const eagle3_config &c = ctx->c;
+  const int n = c.n_embd, qr = c.n_head * c.head_dim, kr = c.n_head_kv * c.head_dim;
+  const bool pdl = true;
+  cudaError_t e = launch_chain_begin(a.B, a.gamma, a.flags, c.max_cache_len, a.kv->kv_len,
+                                     ctx->round_start, ctx->geff, a.gamma_eff, ctx->status, st,
+                                     false);
+  if (e != cudaSuccess) return e;
+  for (int j = 0; j < a.gamma; ++j) {
+    // q/k/v + RoPE + KV append
+    GemvParams p = base_params(ctx);
+    set_kv(p, a.kv);
+    p.mode = GM_QKV;
+    p.rows = qr + 2 * kr;
+    p.row_base = 0;
+    p.K = 2 * n;
+    p.w0 = ctx->w.q;
+    p.w1 = ctx->w.k;
+    p.w2 = ctx->w.v;
+    p.norm0 = ctx->w.in_norm;
+    p.norm1 = ctx->w.hidden_norm;
+    p.pairs.kind = PAIR_CHAIN;
+    p.pairs.step = j;
+    p.pairs.gamma = a.gamma;
+    p.pairs.bnd_tok = a.bnd->tok;
+    p.pairs.bnd_g = a.bnd->g;
+    p.pairs.step_tok = ctx->tokwork;
+    p.pairs.step_g = ctx->gwork;
+    p.pairs.kv_len = a.kv->kv_len;
+    p.pairs.gamma_eff = ctx->geff;
+    p.out_f = ctx->q;
+    if ((e = gemv_items(ctx, p, a.B, st, pdl)) != cudaSuccess) return e;
+
+    // attention
+    AttnParams ap;
+    std::memset(&ap, 0, sizeof(ap));
+    ap.q = ctx->q;
+    ap.out = ctx->attn_o;
+    ap.k_pool = a.kv->k_pool;
+    ap.v_pool = a.kv->v_pool;
+    ap.page_table = a.kv->page_table;
+    ap.kv_len = a.kv->kv_len;
+    ap.gamma_eff = ctx->geff;
+    ap.step = j;
+    ap.num_pages = a.kv->num_pages;
+    ap.max_pages = a.kv->max_pages_per_seq;
+    ap.page_size = c.page_size;
+    ap.max_cache_len = c.max_cache_len;
+    ap.n_head = c.n_head;
+    ap.n_head_kv = c.n_head_kv;
+    ap.head_dim = c.head_dim;
+    ap.splits = a.splits;
+    ap.part_o = ctx->part_o;
+    ap.part_ml = ctx->part_ml;
+    ap.count = ctx->attn_cnt;
+    ap.status = ctx->status;
+    if ((e = attn_launch(ap, a.B, st, pdl)) != cudaSuccess) return e;
+
+    // o_proj + residual (pre-norm g of this step)
+    p = base_params(ctx);
+    p.mode = GM_O;
+    p.rows = n;
+    p.K = qr;
+    p.w0 = ctx->w.o;
+    p.xf = ctx->attn_o;
+    p.res = j == 0 ? a.bnd->g : ctx->gwork;
+    p.out_f = ctx->x1;
+    if ((e = gemv_items(ctx, p, a.B, st, pdl)) != cudaSuccess) return e;
+
+    // post-attention RMSNorm + gate/up + SiLU * up
+    p = base_params(ctx);
+    p.mode = GM_GATEUP;
+    p.rows = 2 * c.n_ff;
+    p.K = n;
+    p.w0 = ctx->w.gate;
+    p.w1 = ctx->w.up;
+    p.xf = ctx->x1;
+    p.norm0 = ctx->w.post_norm;
+    p.out_f = ctx->act;
+    if ((e = gemv_items(ctx, p, a.B, st, pdl)) != cudaSuccess) return e;
+
+    // down + fused-add residual -> gsum, the next g
+    p = base_params(ctx);
+    p.mode = GM_DOWN;
+    p.rows = n;
+    p.K = c.n_ff;
+    p.w0 = ctx->w.down;
+    p.xf = ctx->act;
+    p.res = ctx->x1;
+    p.out_f = ctx->gwork;
+    p.dbg_f = a.g_dbg;
+    p.dbg_stride_b = a.gamma * n;
+    p.dbg_off = j * n;
+    if ((e = gemv_items(ctx, p, a.B, st, pdl)) != cudaSuccess) return e;
+
+    // final RMSNorm + lm_head + argmax + d2t
+    p = base_params(ctx);
+    p.mode = GM_LMHEAD;
+    p.rows = c.draft_vocab;
+    p.K = n;
+    p.w0 = ctx->w.lm_head;
+    p.xf = ctx->gwork;
+    p.norm0 = ctx->w.final_norm;
+    p.am_slot = ctx->am_slot;
+    p.am_count = ctx->am_cnt;
+    p.d2t = ctx->w.d2t;
+    p.draft_tok = a.draft_tok;
+    p.draft_id = a.draft_id;
+    p.next_tok = ctx->tokwork;
+    p.gamma_eff = ctx->geff;
+    p.gamma = a.gamma;
+    p.step = j;
+    p.dbg_f = a.logits_dbg;
+    p.dbg_stride_b = a.gamma * c.draft_vocab;
+    p.dbg_off = j * c.draft_vocab;
+    if ((e = gemv_items(ctx, p, a.B, st, pdl)) != cudaSuccess) return e;
+  }
+  return launch_chain_end(a.B, a.kv->kv_len, ctx->round_start, ctx->geff, st, pdl);
+}
+
+GraphKey chain_key(const ChainArgs &a) {
+  GraphKey k;
+  std::memset(&k, 0, sizeof(k));
+  k.B = a.B;
+  k.gamma = a.gamma;
+  k.splits = a.splits;
+  k.flags = a.flags;
+  const void *p[12] = {a.kv->k_pool, a.kv->v_pool, a.kv->page_table, a.kv->kv_len, a.bnd->g,
+                       a.bnd->tok, a.draft_tok, a.draft_id, a.gamma_eff, a.logits_dbg, a.g_dbg,
+                       nullptr};
+  for (int i = 0; i < 12; ++i) k.ptrs[i] = p[i];
+  k.ints[0] = a.kv->num_pages;
+  k.ints[1] = a.kv->max_pages_per_seq;
+  return k;
+}
+
+cudaError_t run_chain_graph(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) {
+  const GraphKey key = chain_key(a);
+  for (auto &g : ctx->graphs) {
+    if (g.key == key) {
+      g.last_use = ++ctx->use_clock;
+      return cudaGraphLaunch(g.exec, st);
+    }
+  }
+  if (!ctx->cap_stream) {
+    cudaError_t e = cudaStreamCreateWithFlags(&ctx->cap_stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = cudaStreamBeginCapture(ctx->cap_stream, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return e;
+  const cudaError_t e_enq = enqueue_chain(ctx, a, ctx->cap_stream);
+  cudaGraph_t graph = nullptr;
+  e = cudaStreamEndCapture(ctx->cap_stream, &graph);
+  if (e_enq != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    return e_enq;
+  }
+  if (e != cudaSuccess) return e;
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return e;
+  if ((int)ctx->graphs.size() >= kMaxGraphs) {
+    auto old = std::min_element(ctx->graphs.begin(), ctx->graphs.end(),
+                                [](const GraphEntry &x, const GraphEntry &y) { return x.last_use < y.last_use; });
+    cudaGraphExecDestroy(old->exec);
+    ctx->graphs.erase(old);
+  }
+  ctx->graphs.push_back(GraphEntry{key, exec, ++ctx->use_clock});
+  return cudaGraphLaunch(exec, st);
+}
+
+}  // namespace
+
+// =========================================================================== C ABI
+
+extern "C" {
+
+int eagle3_version(void) { return (1 << 16) | 0; }
+
+const char *eagle3_error_string(int code) {
+  switch (code) {
+    case EAGLE3_OK: return "ok";
+    case EAGLE3_ERR_INVALID_ARG: return "invalid argument";
+    case EAGLE3_ERR_CAPACITY: return "kv_len + gamma + 1 exceeds max_cache_len";
+    case EAGLE3_ERR_STATE: return "call out of order for the round state";
+    case EAGLE3_ERR_CUDA: return "CUDA error";
+    case EAGLE3_ERR_DEVICE: return "device status word set";
+    case EAGLE3_ERR_UNSUPPORTED: return "unsupported geometry";
+    default: return "unknown error";
+  }
+}
+
+size_t eagle3_workspace_bytes(const eagle3_config *cfg) {
+  if (!cfg_valid(cfg)) return 0;
+  return make_layout(*cfg).total;
+}
+
+int eagle3_plan_gamma(int kv_len, int gamma, int max_cache_len, unsigned flags, int *gamma_eff) {
+  if (!gamma_eff || gamma < 1 || kv_len < 0 || max_cache_len < 1) return EAGLE3_ERR_INVALID_ARG;
+  if ((long long)kv_len + gamma + 1 <= max_cache_len) {
+    *gamma_eff = gamma;
+    return EAGLE3_OK;
+  }
+  if (!(flags & EAGLE3_SHRINK_GAMMA)) return EAGLE3_ERR_CAPACITY;
+  const long long g = (long long)max_cache_len - kv_len - 1;
+  if (g < 1) return EAGLE3_ERR_CAPACITY;
+  *gamma_eff = (int)g;
+  return EAGLE3_OK;
+}
+
+int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspace,
+                size_t workspace_bytes, eagle3_stream_t stream, eagle3_ctx **out) {
+  if (!out) return EAGLE3_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !w || !workspace) return EAGLE3_ERR_INVALID_ARG;
+  if (!cfg_valid(cfg)) return EAGLE3_ERR_UNSUPPORTED;
+  const void *wp[] = {w->fc, w->in_norm, w->hidden_norm, w->q, w->k, w->v, w->o, w->post_norm,
+                      w->gate, w->up, w->down, w->final_norm, w->lm_head, w->embed, w->d2t};
+  for (const void *p : wp)
+    if (!aligned16(p)) return EAGLE3_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return EAGLE3_ERR_INVALID_ARG;
+  const Layout L = make_layout(*cfg);
+  if (workspace_bytes < L.total) return EAGLE3_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  // d2t: every draft id must map to a distinct target id in range.
+  std::vector<int64_t> d2t(cfg->draft_vocab);
+  if (cudaMemcpy(d2t.data(), w->d2t, d2t.size() * sizeof(int64_t), cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return EAGLE3_ERR_CUDA;
+  {
+    std::vector<int64_t> t(d2t.size());
+    for (size_t i = 0; i < d2t.size(); ++i) {
+      t[i] = (int64_t)i + d2t[i];
+      if (t[i] < 0 || t[i] >= cfg->target_vocab) return EAGLE3_ERR_INVALID_ARG;
+    }
+    std::sort(t.begin(), t.end());
+    for (size_t i = 1; i < t.size(); ++i)
+      if (t[i] == t[i - 1]) return EAGLE3_ERR_INVALID_ARG;
+  }
+
+  eagle3_ctx *ctx = new (std::nothrow) eagle3_ctx();
+  if (!ctx) return EAGLE3_ERR_INVALID_ARG;
+  ctx->c = *cfg;
+  ctx->w = *w;
+  ctx->ws = static_cast<char *>(workspace);
+  ctx->ws_bytes = workspace_bytes;
+  ctx->L = L;
+  char *b = ctx->ws;
+  ctx->rope = reinterpret_cast<float2 *>(b + L.rope);
+  ctx->q = reinterpret_cast<float *>(b + L.q);
+  ctx->attn_o = reinterpret_cast<float *>(b + L.attn_o);
+  ctx->part_o = reinterpret_cast<float *>(b + L.part_o);
+  ctx->part_ml = reinterpret_cast<float2 *>(b + L.part_ml);
+  ctx->attn_cnt = reinterpret_cast<unsigned *>(b + L.attn_cnt);
+  ctx->x1 = reinterpret_cast<float *>(b + L.x1);
+  ctx->act = reinterpret_cast<float *>(b + L.act);
+  ctx->gwork = reinterpret_cast<float *>(b + L.gwork);
+  ctx->tokwork = reinterpret_cast<int32_t *>(b + L.tokwork);
+  ctx->am_slot = reinterpret_cast<unsigned long long *>(b + L.am_slot);
+  ctx->am_cnt = reinterpret_cast<unsigned *>(b + L.am_cnt);
+  ctx->round_start = reinterpret_cast<int32_t *>(b + L.round_start);
+  ctx->geff = reinterpret_cast<int32_t *>(b + L.geff);
+  ctx->status = reinterpret_cast<int *>(b + L.status);
+  ctx->genc = reinterpret_cast<float *>(b + L.genc);
+  ctx->graph_mode = 1;
+  ctx->last_stream = st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      gemv_prepare() != cudaSuccess) {
+    delete ctx;
+    return EAGLE3_ERR_CUDA;
+  }
+
+  // RoPE table: angle p * theta^(-2i/R) in double, stored as float32 (cos, sin).
+  const int half = cfg->rope_dims / 2;
+  if (half > 0) {
+    std::vector<float2> tab((size_t)cfg->max_cache_len * half);
+    for (int i = 0; i < half; ++i) {
+      const double inv = std::pow((double)cfg->rope_theta, -2.0 * i / cfg->rope_dims);
+      for (int p = 0; p < cfg->max_cache_len; ++p) {
+        const double a = (double)p * inv;
+        tab[(size_t)p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+      }
+    }
+    if (cudaMemcpy(ctx->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) !=
+        cudaSuccess) {
+      delete ctx;
+      return EAGLE3_ERR_CUDA;
+    }
+  }
+  // Counters and argmax slots start at zero and are returned to zero by their users.
+  cudaError_t e = cudaMemsetAsync(b + L.attn_cnt, 0, (size_t)cfg->max_batch * cfg->n_head_kv * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(b + L.am_slot, 0, (size_t)cfg->max_batch * 8, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(b + L.am_cnt, 0, 64 * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(b + L.status, 0, 4, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    delete ctx;
+    return EAGLE3_ERR_CUDA;
+  }
+  *out = ctx;
+  return EAGLE3_OK;
+}
+
+int eagle3_destroy(eagle3_ctx *ctx) {
+  if (!ctx) return EAGLE3_ERR_INVALID_ARG;
+  for (auto &g : ctx->graphs) cudaGraphExecDestroy(g.exec);
+  if (ctx->cap_stream) cudaStreamDestroy(ctx->cap_stream);
+  delete ctx;
+  return EAGLE3_OK;
+}
+
+int eagle3_set_graph_mode(eagle3_ctx *ctx, int enabled) {
+  if (!ctx) return EAGLE3_ERR_INVALID_ARG;
+  ctx->graph_mode = enabled ? 1 : 0;
+  return EAGLE3_OK;
+}
+
+int eagle3_encode(eagle3_ctx *ctx, const uint16_t *aux, int M, float *g, eagle3_stream_t stream) {
+  if (!ctx || M < 0) return EAGLE3_ERR_INVALID_ARG;
+  if (M == 0) return EAGLE3_OK;
+  if (!aligned16(aux) || !aligned16(g)) return EAGLE3_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ctx->last_stream = st;
+  return cuda_err(enqueue_encode(ctx, aux, M, g, st, true));
+}
+
+int eagle3_prefill(eagle3_ctx *ctx, int B, const int32_t *tokens, int P_max,
+                   const int32_t *next_tok, const int32_t *prompt_len_host, const uint16_t *aux,
+                   const eagle3_kv *kv, eagle3_boundary *bnd, eagle3_stream_t stream) {
+  if (!ctx || B < 1 || B > ctx->c.max_batch || P_max < 1) return EAGLE3_ERR_INVALID_ARG;
+  if (!tokens || !next_tok || !prompt_len_host || !aligned16(aux)) return EAGLE3_ERR_INVALID_ARG;
+  if (!kv_valid(ctx, kv) || !bnd || !aligned16(bnd->g) || !bnd->tok) return EAGLE3_ERR_INVALID_ARG;
+  if (ctx->round_open) return EAGLE3_ERR_STATE;
+  for (int b = 0; b < B; ++b) {
+    const int P = prompt_len_host[b];
+    if (P < 1 || P > P_max) return EAGLE3_ERR_INVALID_ARG;
+    if (P > ctx->c.max_cache_len) return EAGLE3_ERR_CAPACITY;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ctx->last_stream = st;
+  const int n = ctx->c.n_embd;
+  const size_t aux_row = (size_t)3 * n;
+  cudaError_t e = cudaSuccess;
+  for (int b = 0; b < B && e == cudaSuccess; ++b) {
+    const int P = prompt_len_host[b];
+    for (int p0 = 0; p0 < P && e == cudaSuccess; p0 += kPrefillChunk) {
+      const int cnt = std::min(kPrefillChunk, P - p0);
+      e = enqueue_encode(ctx, aux + ((size_t)b * P_max + p0) * aux_row, cnt, ctx->genc, st, true);
+      if (e != cudaSuccess) break;
+      const int pairs = std::min(cnt, P - 1 - p0);
+      if (pairs > 0) {
+        GemvParams p = base_params(ctx);
+        kv_only_params(ctx, kv, p);
+        p.pairs.kind = PAIR_PREFILL;
+        p.pairs.seq = b;
+        p.pairs.pos0 = p0;
+        p.pairs.tok_stride = P_max;
+        p.pairs.tokens = tokens;
+        p.pairs.enc_g = ctx->genc;
+        e = gemv_items(ctx, p, pairs, st, true);
+        if (e != cudaSuccess) break;
+      }
+      if (p0 + cnt == P)
+        e = launch_prefill_finish(b, n, P - 1, ctx->genc + (size_t)(P - 1 - p0) * n, next_tok,
+                                  bnd->g, bnd->tok, kv->kv_len, st);
+    }
+  }
+  ctx->rebuild_ok = 0;
+  return cuda_err(e);
+}
+
+int eagle3_draft_chain(eagle3_ctx *ctx, int B, int gamma, unsigned flags,
+                       const int32_t *kv_len_host, const eagle3_kv *kv,
+                       const eagle3_boundary *bnd, int32_t *draft_tok, int32_t *draft_id,
+                       int32_t *gamma_eff, float *logits_dbg, float *g_dbg,
+                       eagle3_stream_t stream) {
+  if (!ctx || B < 1 || B > ctx->c.max_batch) return EAGLE3_ERR_INVALID_ARG;
+  if (gamma < 1 || gamma > ctx->c.max_gamma) return EAGLE3_ERR_INVALID_ARG;
+  if (!kv_len_host || !kv_valid(ctx, kv) || !bnd || !aligned16(bnd->g) || !bnd->tok || !draft_tok)
+    return EAGLE3_ERR_INVALID_ARG;
+  if ((logits_dbg && !aligned16(logits_dbg)) || (g_dbg && !aligned16(g_dbg)))
+    return EAGLE3_ERR_INVALID_ARG;
+  if (flags & ~EAGLE3_SHRINK_GAMMA) return EAGLE3_ERR_INVALID_ARG;
+  if (ctx->round_open) return EAGLE3_ERR_STATE;
+  int max_len = 0;
+  for (int b = 0; b < B; ++b) {
+    int ge = 0;
+    const int r = eagle3_plan_gamma(kv_len_host[b], gamma, ctx->c.max_cache_len, flags, &ge);
+    if (r == EAGLE3_ERR_INVALID_ARG) return EAGLE3_ERR_INVALID_ARG;
+    if (r != EAGLE3_OK) return EAGLE3_ERR_CAPACITY;
+    max_len = std::max(max_len, kv_len_host[b] + ge);
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ctx->last_stream = st;
+  ChainArgs a;
+  a.B = B;
+  a.gamma = gamma;
+  a.flags = flags;
+  a.splits = choose_splits(ctx, B, max_len);
+  a.kv = kv;
+  a.bnd = bnd;
+  a.draft_tok = draft_tok;
+  a.draft_id = draft_id;
+  a.gamma_eff = gamma_eff;
+  a.logits_dbg = logits_dbg;
+  a.g_dbg = g_dbg;
+  const cudaError_t e = ctx->graph_mode ? run_chain_graph(ctx, a, st) : enqueue_chain(ctx, a, st);
+  if (e != cudaSuccess) return EAGLE3_ERR_CUDA;
+  ctx->round_open = 1;
+  ctx->open_B = B;
+  ctx->rebuild_ok = 0;
+  return EAGLE3_OK;
+}
+
+int eagle3_rewind(eagle3_ctx *ctx, int B, const eagle3_kv *kv, eagle3_stream_t stream) {
+  if (!ctx || !kv || !kv->kv_len) return EAGLE3_ERR_INVALID_ARG;
+  if (!ctx->round_open) return EAGLE3_ERR_STATE;
+  if (B != ctx->open_B) return EAGLE3_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ctx->last_stream = st;
+  const cudaError_t e = launch_rewind(B, kv->kv_len, ctx->round_start, st);
+  if (e != cudaSuccess) return EAGLE3_ERR_CUDA;
+  ctx->round_open = 0;
+  ctx->rebuild_ok = 1;
+  return EAGLE3_OK;
+}
+
+int eagle3_accept(eagle3_ctx *ctx, int B, int gamma, const int32_t *draft_tok,
+                  const int32_t *target_pred, const int32_t *gamma_eff, int32_t *n_acc,
+                  int32_t *bonus, eagle3_stream_t stream) {
+  if (!ctx || B < 1 || B > ctx->c.max_batch || gamma < 1 || gamma > ctx->c.max_gamma)
+    return EAGLE3_ERR_INVALID_ARG;
+  if (!draft_tok || !target_pred || !n_acc || !bonus) return EAGLE3_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ctx->last_stream = st;
+  return cuda_err(launch_accept(B, gamma, draft_tok, target_pred, gamma_eff, n_acc, bonus, st));
+}
+
+int eagle3_rebuild_after_verify(eagle3_ctx *ctx, int B, int gamma, const int32_t *n_acc,
+                                const int32_t *draft_tok, const int32_t *bonus,
+                                const uint16_t *verify_aux, const eagle3_kv *kv,
+                                eagle3_boundary *bnd, eagle3_stream_t stream) {
+  if (!ctx || B < 1 || B > ctx->c.max_batch || gamma < 1 || gamma > ctx->c.max_gamma)
+    return EAGLE3_ERR_INVALID_ARG;
+  if (!n_acc || !draft_tok || !bonus || !aligned16(verify_aux)) return EAGLE3_ERR_INVALID_ARG;
+  if (!kv_valid(ctx, kv) || !bnd || !aligned16(bnd->g) || !bnd->tok) return EAGLE3_ERR_INVALID_ARG;
+  if (ctx->round_open || !ctx->rebuild_ok) return EAGLE3_ERR_STATE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ctx->last_stream = st;
+  const int n = ctx->c.n_embd;
+  const int M = B * (gamma + 1);
+  cudaError_t e = enqueue_encode(ctx, verify_aux, M, ctx->genc, st, false);
+  if (e == cudaSuccess) {
+    GemvParams p = base_params(ctx);
+    kv_only_params(ctx, kv, p);
+    p.pairs.kind = PAIR_REBUILD;
+    p.pairs.gamma = gamma;
+    p.pairs.bnd_tok = bnd->tok;
+    p.pairs.bnd_g = bnd->g;
+    p.pairs.draft_tok = draft_tok;
+    p.pairs.enc_g = ctx->genc;
+    p.pairs.kv_len = kv->kv_len;
+    p.pairs.n_acc = n_acc;
+    e = gemv_items(ctx, p, M, st, true);
+  }
+  if (e == cudaSuccess)
+    e = launch_rebuild_finish(B, gamma, n, ctx->genc, n_acc, bonus, bnd->g, bnd->tok, kv->kv_len,
+                              ctx->c.max_cache_len, ctx->status, st);
+  if (e != cudaSuccess) return EAGLE3_ERR_CUDA;
+  ctx->rebuild_ok = 0;
+  return EAGLE3_OK;
+}
+
+int eagle3_get_status(eagle3_ctx *ctx, int *device_status) {
+  if (!ctx || !device_status) return EAGLE3_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(ctx->last_stream) != cudaSuccess) return EAGLE3_ERR_CUDA;
+  int s = 0;
+  if (cudaMemcpy(&s, ctx->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return EAGLE3_ERR_CUDA;
+  *device_status = s;
+  if (s != 0) {
+    if (cudaMemset(ctx->status, 0, sizeof(int)) != cudaSuccess) return EAGLE3_ERR_CUDA;
+    return EAGLE3_ERR_DEVICE;
+  }
+  return EAGLE3_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,193 @@
+// Split-KV GQA decode attention over the paged bf16 drafter KV cache.
+//
+// For each sequence b and q head h (kv head h / G, G = n_head / n_head_kv): softmax over
+// the keys 0..len-1 of (q . k) / sqrt(d), then sum of p * v ("memra_engine/eagle.rs",
+// ``attn``: fa_decode with scale 1/sqrt(head_dim); the new key is appended first).
+//
+// One CTA per (split, kv head, sequence): the G query heads that share a kv head are
+// served from one read of each K/V vector.  A key of d = 256 dims is spread over the 32
+// lanes of a warp (8 dims = 16 bytes per lane); smaller heads put several keys in a warp.
+// Each lane group keeps an online softmax (running max in the log2 domain, running sum,
+// running weighted V).  The CTA merges its warps in shared memory; with more than one
+// split the last CTA of a (sequence, kv head) to finish merges the splits' partials.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace e3 {
+
+constexpr int kAttnWarps = 4;
+constexpr int kAttnThreads = kAttnWarps * 32;
+
+template <int D, int G>
+__global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnParams p) {
+  constexpr int LPK = D / 8;        // lanes per key
+  constexpr int KPW = 32 / LPK;     // keys per warp pass
+  constexpr int NP = kAttnWarps * KPW;
+  __shared__ float2 sm_ml[NP][G];
+  __shared__ __align__(16) float sm_acc[NP][G][D];
+  __shared__ int last_sh;
+
+  const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int grp = lane / LPK, li = lane - grp * LPK;
+  const int H = p.n_head, Hkv = p.n_head_kv;
+
+  pdl_trigger();
+  pdl_wait();
+
+  const int L = p.kv_len[b];
+  const int ge = p.gamma_eff ? p.gamma_eff[b] : p.step + 1;
+  int len = L + min(p.step, max(ge - 1, 0)) + 1;
+  if (L < 0 || len > p.max_cache_len) {
+    if (tid == 0 && s == 0 && kvh == 0) set_status(p.status, EAGLE3_DEV_BAD_LENGTH);
+    len = min(max(len, 1), p.max_cache_len);
+  }
+  const int chunk = (len + p.splits - 1) / p.splits;
+  const int k0 = s * chunk;
+  const int k1 = min(len, k0 + chunk);
+
+  // q of the G heads, pre-scaled so that scores are in the log2 domain.
+  const float qscale = rsqrtf((float)D) * 1.4426950408889634f;
+  float qv[G][8];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float4 *qp = reinterpret_cast<const float4 *>(p.q + (size_t)b * H * D + (size_t)(kvh * G + g) * D + li * 8);
+    const float4 a = qp[0], c = qp[1];
+    qv[g][0] = a.x * qscale; qv[g][1] = a.y * qscale; qv[g][2] = a.z * qscale; qv[g][3] = a.w * qscale;
+    qv[g][4] = c.x * qscale; qv[g][5] = c.y * qscale; qv[g][6] = c.z * qscale; qv[g][7] = c.w * qscale;
+  }
+  float mx[G], sum[G], acc[G][8];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    mx[g] = -INFINITY;
+    sum[g] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[g][i] = 0.f;
+  }
+
+  const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
+  for (int key = k0 + warp * KPW + grp; key < k1; key += NP) {
+    const int pg = pt[key / p.page_size];
+    if (pg < 0 || pg >= p.num_pages) {
+      set_status(p.status, EAGLE3_DEV_BAD_PAGE);
+      continue;
+    }
+    const size_t off = (((size_t)pg * Hkv + kvh) * p.page_size + key % p.page_size) * D + li * 8;
+    const uint4 ku = *reinterpret_cast<const uint4 *>(p.k_pool + off);
+    const uint4 vu = *reinterpret_cast<const uint4 *>(p.v_pool + off);
+    const float kf[8] = {bf_lo(ku.x), bf_hi(ku.x), bf_lo(ku.y), bf_hi(ku.y),
+                         bf_lo(ku.z), bf_hi(ku.z), bf_lo(ku.w), bf_hi(ku.w)};
+    const float vf[8] = {bf_lo(vu.x), bf_hi(vu.x), bf_lo(vu.y), bf_hi(vu.y),
+                         bf_lo(vu.z), bf_hi(vu.z), bf_lo(vu.w), bf_hi(vu.w)};
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float sc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sc = fmaf(qv[g][i], kf[i], sc);
+#pragma unroll
+      for (int o = LPK / 2; o >= 1; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o, LPK);
+      const float mn = fmaxf(mx[g], sc);
+      const float corr = exp2f(mx[g] - mn);
+      const float pr = exp2f(sc - mn);
+      sum[g] = sum[g] * corr + pr;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[g][i] = fmaf(pr, vf[i], acc[g][i] * corr);
+      mx[g] = mn;
+    }
+  }
+
+  const int part = warp * KPW + grp;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (li == 0) sm_ml[part][g] = make_float2(mx[g], sum[g]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sm_acc[part][g][li * 8 + i] = acc[g][i];
+  }
+  __syncthreads();
+
+  const size_t slot = ((size_t)b * Hkv + kvh) * p.splits + s;
+  for (int e = tid; e < G * D; e += kAttnThreads) {
+    const int g = e / D, dim = e - g * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < NP; ++q) M = fmaxf(M, sm_ml[q][g].x);
+    float Ls = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int q = 0; q < NP; ++q) {
+        const float2 ml = sm_ml[q][g];
+        const float w = exp2f(ml.x - M);
+        Ls += ml.y * w;
+        O += sm_acc[q][g][dim] * w;
+      }
+    }
+    if (p.splits == 1) {
+      p.out[(size_t)b * H * D + (size_t)(kvh * G + g) * D + dim] = O / Ls;
+    } else {
+      p.part_o[(slot * G + g) * D + dim] = O;
+      if (dim == 0) p.part_ml[slot * G + g] = make_float2(M, Ls);
+    }
+  }
+  if (p.splits == 1) return;
+
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(p.count + (size_t)b * Hkv + kvh, 1u);
+    last_sh = (prev == (unsigned)p.splits - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!last_sh) return;
+  __threadfence();
+  const size_t slot0 = ((size_t)b * Hkv + kvh) * p.splits;
+  for (int e = tid; e < G * D; e += kAttnThreads) {
+    const int g = e / D, dim = e - g * D;
+    float M = -INFINITY;
+    for (int q = 0; q < p.splits; ++q) M = fmaxf(M, __ldcg(&p.part_ml[(slot0 + q) * G + g]).x);
+    float Ls = 0.f, O = 0.f;
+    for (int q = 0; q < p.splits; ++q) {
+      const float2 ml = __ldcg(&p.part_ml[(slot0 + q) * G + g]);
+      if (ml.x == -INFINITY) continue;
+      const float w = exp2f(ml.x - M);
+      Ls += ml.y * w;
+      O += __ldcg(&p.part_o[((slot0 + q) * G + g) * D + dim]) * w;
+    }
+    p.out[(size_t)b * H * D + (size_t)(kvh * G + g) * D + dim] = O / Ls;
+  }
+  if (tid == 0) p.count[(size_t)b * Hkv + kvh] = 0u;
+}
+
+template <int D, int G>
+static cudaError_t attn_launch_dg(const AttnParams &p, int B, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.splits, p.n_head_kv, B);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<D, G>, p);
+}
+
+bool attn_supported(int head_dim, int group) {
+  return (head_dim == 64 || head_dim == 128 || head_dim == 256) &&
+         (group == 1 || group == 2 || group == 4 || group == 8);
+}
+
+cudaError_t attn_launch(const AttnParams &p, int B, cudaStream_t st, bool pdl) {
+  const int G = p.n_head / p.n_head_kv;
+#define E3_ATTN_CASE(DD, GG) \
+  if (p.head_dim == DD && G == GG) return attn_launch_dg<DD, GG>(p, B, st, pdl);
+  E3_ATTN_CASE(64, 1) E3_ATTN_CASE(64, 2) E3_ATTN_CASE(64, 4) E3_ATTN_CASE(64, 8)
+  E3_ATTN_CASE(128, 1) E3_ATTN_CASE(128, 2) E3_ATTN_CASE(128, 4) E3_ATTN_CASE(128, 8)
+  E3_ATTN_CASE(256, 1) E3_ATTN_CASE(256, 2) E3_ATTN_CASE(256, 4) E3_ATTN_CASE(256, 8)
+#undef E3_ATTN_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace e3

@@ -1,0 +1,201 @@
+// Device helpers and launch-parameter structs shared by the EAGLE-3 drafter kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/eagle3.h"
+
+namespace e3 {
+
+constexpr int kGemvThreads = 256;
+constexpr int kGemvWarps = kGemvThreads / 32;
+
+// ------------------------------------------------------------------ PDL (griddepcontrol)
+// Programmatic dependent launch: a kernel may start while its predecessor drains.  Code
+// before pdl_wait() touches only constant data (weights); pdl_trigger() lets the next
+// kernel in the stream be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------- loads
+// Streaming 16-byte weight load: read-only path, no L1 allocation.
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Hint the L2 to fetch [p, p + bytes) (bytes a multiple of 16, p 16-byte aligned).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// bf16 pair in a 32-bit word -> two floats (exact widening).
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+__device__ __forceinline__ float bf1(uint16_t u) { return __uint_as_float(((uint32_t)u) << 16); }
+
+// float -> bf16 bits, round to nearest even (finite inputs).
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  uint32_t u = __float_as_uint(f);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+__device__ __forceinline__ void set_status(int *status, int bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// Order-preserving map of a float to uint32 (larger float -> larger key); -0 -> +0.
+__device__ __forceinline__ uint32_t float_order_key(float f) {
+  if (f == 0.0f) f = 0.0f;
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ------------------------------------------------------------------ item sources
+// A GEMV "item" is one activation row.  For the layer-input modes an item is a
+// (token, g, position) triple whose meaning depends on who launches the kernel.
+enum PairKind : int {
+  PAIR_CHAIN = 0,    // item = sequence b, draft step j
+  PAIR_REBUILD = 1,  // item = (b, i), i = 0..gamma
+  PAIR_PREFILL = 2,  // item = position p of one sequence
+};
+
+struct PairSource {
+  int kind;
+  int step;                  // chain: j
+  int gamma;                 // chain / rebuild: gamma
+  int seq;                   // prefill: the sequence
+  int pos0;                  // prefill: position of item 0
+  int tok_stride;            // prefill: row stride of tokens
+  const int32_t *bnd_tok;    // chain j == 0, rebuild i == 0
+  const float *bnd_g;        // [B, n]
+  const int32_t *step_tok;   // chain j > 0: token of this step per b [B]
+  const float *step_g;       // chain j > 0: g of this step [B, n]
+  const int32_t *draft_tok;  // rebuild: [B, gamma]
+  const float *enc_g;        // rebuild: [B, gamma + 1, n]; prefill: [items, n]
+  const int32_t *tokens;     // prefill: [*, tok_stride]
+  const int32_t *kv_len;     // [B]
+  const int32_t *gamma_eff;  // chain: [B]
+  const int32_t *n_acc;      // rebuild: [B]
+};
+
+struct PairItem {
+  int b;
+  int tok;
+  const float *g;
+  int pos;
+  bool write_kv;
+};
+
+__device__ __forceinline__ PairItem resolve_pair(const PairSource &s, int item, int n_embd) {
+  PairItem it;
+  if (s.kind == PAIR_CHAIN) {
+    it.b = item;
+    if (s.step == 0) {
+      it.tok = s.bnd_tok[item];
+      it.g = s.bnd_g + (size_t)item * n_embd;
+    } else {
+      it.tok = s.step_tok[item];
+      it.g = s.step_g + (size_t)item * n_embd;
+    }
+    it.pos = s.kv_len[item] + s.step;
+    it.write_kv = s.step < s.gamma_eff[item];
+  } else if (s.kind == PAIR_REBUILD) {
+    const int b = item / (s.gamma + 1), i = item % (s.gamma + 1);
+    it.b = b;
+    if (i == 0) {
+      it.tok = s.bnd_tok[b];
+      it.g = s.bnd_g + (size_t)b * n_embd;
+    } else {
+      it.tok = s.draft_tok[(size_t)b * s.gamma + (i - 1)];
+      it.g = s.enc_g + ((size_t)b * (s.gamma + 1) + (i - 1)) * n_embd;
+    }
+    it.pos = s.kv_len[b] + i;
+    it.write_kv = i <= s.n_acc[b];
+  } else {
+    it.b = s.seq;
+    const int p = s.pos0 + item;
+    it.tok = s.tokens[(size_t)s.seq * s.tok_stride + p + 1];
+    it.g = s.enc_g + (size_t)item * n_embd;
+    it.pos = p;
+    it.write_kv = true;
+  }
+  return it;
+}
+
+// ----------------------------------------------------------------- GEMV params
+enum GemvMode : int {
+  GM_ENCODE = 0,  // x = aux (bf16 [items, 3n]); y -> out_f [items, rows]
+  GM_QKV = 1,     // x = [RMS(embed) w_in ; RMS(g) w_hid]; rows: q | k | v (row_base skips q)
+  GM_O = 2,       // x = attention output; y + g -> x1
+  GM_GATEUP = 3,  // x = RMS(x1) w_post; rows interleave gate/up; silu(gate) * up -> act
+  GM_DOWN = 4,    // x = act; y + x1 -> gsum (next g)
+  GM_LMHEAD = 5,  // x = RMS(gsum) w_final; argmax + d2t
+};
+
+struct GemvParams {
+  int mode;
+  int rows;       // logical rows handled by this launch
+  int row_base;   // first logical row (QKV: q_rows to skip q)
+  int K;          // input width
+  int items;      // active items in this launch (<= NB)
+  int item0;      // global index of item 0
+  int n_embd, n_head, n_head_kv, head_dim, rope_dims, n_ff, draft_vocab, target_vocab;
+  float eps;
+  // weights
+  const uint16_t *w0, *w1, *w2;
+  const uint16_t *norm0, *norm1;
+  const uint16_t *embed;
+  // plain inputs
+  const uint16_t *xb;  // bf16 [items, K] (encode)
+  const float *xf;     // f32 [items, K] (o: attention output, down: act, gateup: x1, lmhead: gsum)
+  const float *res;    // residual [items, n] (o: g of the step, down: x1)
+  PairSource pairs;
+  // outputs
+  float *out_f;        // encode: g; qkv: q; o: x1; gateup: act; down: gsum
+  float *dbg_f;        // down: g_dbg [B, gamma, n] ; lmhead: logits_dbg [B, gamma, V_d]
+  int dbg_stride_b;    // elements between batch rows of dbg (gamma * n or gamma * V_d)
+  int dbg_off;         // element offset of this step in a batch row (j * n or j * V_d)
+  // KV
+  uint16_t *k_pool, *v_pool;
+  const int32_t *page_table;
+  int num_pages, max_pages, page_size, max_cache_len;
+  const float2 *rope;  // [max_cache_len][rope_dims / 2] (cos, sin)
+  // argmax
+  unsigned long long *am_slot;  // [max_batch]
+  unsigned int *am_count;       // arrival counter of the launch's CTAs
+  const int64_t *d2t;
+  int32_t *draft_tok;   // [B, gamma]
+  int32_t *draft_id;    // [B, gamma] or null
+  int32_t *next_tok;    // [B] token of the next step
+  const int32_t *gamma_eff;
+  int gamma, step;
+  int *status;
+};
+
+// ----------------------------------------------------------------- attention
+struct AttnParams {
+  const float *q;          // [B, H * d]
+  float *out;              // [B, H * d]
+  const uint16_t *k_pool, *v_pool;
+  const int32_t *page_table;
+  const int32_t *kv_len;   // [B]
+  const int32_t *gamma_eff;
+  int step;
+  int num_pages, max_pages, page_size, max_cache_len;
+  int n_head, n_head_kv, head_dim;
+  int splits;
+  float *part_o;           // [B, H_kv, splits, G, d]
+  float2 *part_ml;         // [B, H_kv, splits, G]
+  unsigned int *count;     // [B, H_kv]
+  int *status;
+};
+
+}  // namespace e3

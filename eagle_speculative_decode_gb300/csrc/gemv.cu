@@ -1,0 +1,551 @@
+// Weight-streaming GEMV for the drafter's projections at small batch (items <= 8).
+//
+// y[item, row] = sum_k W[row, k] * x[item, k] with bf16 weights in [out, in] row-major
+// and float32 activations/accumulators, fused with the op that feeds x (RMSNorm of the
+// layer input, of x1 or of gsum; the embedding gather; the 2n concat) and the op that
+// consumes y (partial RoPE + bf16 KV append, residual adds, SwiGLU, argmax + d2t).
+// Ops follow "memra_engine/eagle.rs", module doc "Op-sequence".
+//
+// Work split: the logical rows are cut into groups of R rows; every CTA owns a
+// contiguous, balanced range of groups and streams those rows with 16-byte
+// non-allocating loads, 256 threads side by side along K (so every warp moves 512
+// contiguous bytes per load).  Loads of the next tile are issued before the FMAs of the
+// current one (register double buffer) and the first tile is requested before the
+// kernel waits on its predecessor (PDL), so weight streaming overlaps the previous
+// kernel's tail.  x lives in shared memory as float32, split into two float4 planes
+// (elements 0-3 and 4-7 of each 8-element vector) so that each warp's LDS.128 is
+// conflict free.  Per-group partial sums are reduced across the CTA into a per-row
+// accumulator array in shared memory; the epilogue runs once all groups are done.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace e3 {
+
+template <int MODE>
+__device__ __forceinline__ const uint16_t *row_ptr(const GemvParams &p, int lr) {
+  const size_t K = (size_t)p.K;
+  if constexpr (MODE == GM_GATEUP) {
+    return ((lr & 1) ? p.w1 : p.w0) + (size_t)(lr >> 1) * K;
+  } else if constexpr (MODE == GM_QKV) {
+    const int d = p.head_dim, R = p.rope_dims;
+    const int qr = p.n_head * d, kr = p.n_head_kv * d;
+    if (lr < qr + kr) {
+      const bool isq = lr < qr;
+      const uint16_t *base = isq ? p.w0 : p.w1;
+      const int rr = isq ? lr : lr - qr;
+      const int head = rr / d, li = rr - head * d;
+      // RoPE partners (i, i + R/2) sit on adjacent logical rows 2i, 2i + 1.
+      const int dim = li < R ? ((li & 1) ? (li >> 1) + (R >> 1) : (li >> 1)) : li;
+      return base + ((size_t)head * d + dim) * K;
+    }
+    return p.w2 + (size_t)(lr - qr - kr) * K;
+  } else {
+    return p.w0 + (size_t)lr * K;
+  }
+}
+
+template <int N>
+struct Log2 {
+  static constexpr int value = (N >= 32) ? 5 : (N >= 16) ? 4 : (N >= 8) ? 3 : (N >= 4) ? 2 : (N >= 2) ? 1 : 0;
+};
+
+// Reduce N = 2^S values held by every lane across the warp.  Afterwards lane l holds
+// the warp total of value index idx(l) = bits 4..(5-S) of l read as an S-bit number;
+// lanes whose low (5-S) bits are zero are the designated writers.
+template <int N>
+__device__ __forceinline__ float warp_reduce_multi(float (&v)[N], int lane) {
+#pragma unroll
+  for (int cnt = N, o = 16; cnt > 1; cnt >>= 1, o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < cnt / 2; ++i) {
+      const float send = upper ? v[i] : v[i + cnt / 2];
+      const float keep = upper ? v[i + cnt / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int o = 16 >> Log2<N>::value; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  return r;
+}
+
+template <int N>
+__device__ __forceinline__ int warp_reduce_index(int lane) {
+  int idx = 0;
+#pragma unroll
+  for (int s = 0; s < Log2<N>::value; ++s) idx = (idx << 1) | ((lane >> (4 - s)) & 1);
+  return idx;
+}
+
+template <int N>
+__device__ __forceinline__ bool warp_reduce_writer(int lane) {
+  return (lane & ((1 << (5 - Log2<N>::value)) - 1)) == 0;
+}
+
+// Block-wide sum of one float per thread; result valid in every thread.
+__device__ __forceinline__ float block_sum(float v, float *scratch) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kGemvWarps; ++w) t += scratch[w];
+  return t;
+}
+
+// ------------------------------------------------------------------ x staging
+// Writes x[m, k] into the two float4 planes xs[(m * 2 + plane) * KV + kv].
+template <int NB, int MODE>
+__device__ void stage_x(const GemvParams &p, float4 *xs, float *scratch) {
+  const int K = p.K, KV = K >> 3, tid = threadIdx.x;
+  for (int m = 0; m < NB; ++m) {
+    float4 *x0 = xs + (size_t)(m * 2) * KV;
+    float4 *x1 = x0 + KV;
+    const bool live = m < p.items;
+    if (!live) {
+      for (int kv = tid; kv < KV; kv += kGemvThreads) {
+        x0[kv] = make_float4(0.f, 0.f, 0.f, 0.f);
+        x1[kv] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      continue;
+    }
+    const int item = p.item0 + m;
+    if constexpr (MODE == GM_ENCODE) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(p.xb + (size_t)item * K);
+      for (int kv = tid; kv < KV; kv += kGemvThreads) {
+        const uint4 u = src[kv];
+        x0[kv] = make_float4(bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y));
+        x1[kv] = make_float4(bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w));
+      }
+    } else if constexpr (MODE == GM_O || MODE == GM_DOWN) {
+      const float4 *src = reinterpret_cast<const float4 *>(p.xf + (size_t)item * K);
+      for (int kv = tid; kv < KV; kv += kGemvThreads) {
+        x0[kv] = src[2 * kv];
+        x1[kv] = src[2 * kv + 1];
+      }
+    } else if constexpr (MODE == GM_GATEUP || MODE == GM_LMHEAD) {
+      // RMSNorm(x) * w over K = n_embd.
+      const float4 *src = reinterpret_cast<const float4 *>(p.xf + (size_t)item * K);
+      float ss = 0.f;
+      for (int kv = tid; kv < KV; kv += kGemvThreads) {
+        const float4 a = src[2 * kv], b = src[2 * kv + 1];
+        ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z +
+              b.w * b.w;
+      }
+      ss = block_sum(ss, scratch);
+      const float sc = rsqrtf(ss / (float)K + p.eps);
+      const uint4 *wn = reinterpret_cast<const uint4 *>(p.norm0);
+      for (int kv = tid; kv < KV; kv += kGemvThreads) {
+        const float4 a = src[2 * kv], b = src[2 * kv + 1];
+        const uint4 w = wn[kv];
+        x0[kv] = make_float4(a.x * sc * bf_lo(w.x), a.y * sc * bf_hi(w.x), a.z * sc * bf_lo(w.y),
+                             a.w * sc * bf_hi(w.y));
+        x1[kv] = make_float4(b.x * sc * bf_lo(w.z), b.y * sc * bf_hi(w.z), b.z * sc * bf_lo(w.w),
+                             b.w * sc * bf_hi(w.w));
+      }
+    } else if constexpr (MODE == GM_QKV) {
+      // [RMSNorm(embed(tok)) * w_in ; RMSNorm(g) * w_hid], K = 2 n.
+      const int n = p.n_embd, NV = n >> 3;
+      const PairItem it = resolve_pair(p.pairs, item, n);
+      int tok = it.tok;
+      if (tok < 0 || tok >= p.target_vocab) {
+        if (tid == 0) set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
+        tok = 0;
+      }
+      const uint4 *er = reinterpret_cast<const uint4 *>(p.embed + (size_t)tok * n);
+      const float4 *gr = reinterpret_cast<const float4 *>(it.g);
+      float se = 0.f, sg = 0.f;
+      for (int kv = tid; kv < NV; kv += kGemvThreads) {
+        const uint4 u = er[kv];
+        const float e[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
+                            bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) se += e[i] * e[i];
+        const float4 a = gr[2 * kv], b = gr[2 * kv + 1];
+        sg += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z +
+              b.w * b.w;
+      }
+      se = block_sum(se, scratch);
+      sg = block_sum(sg, scratch + kGemvWarps);
+      const float sce = rsqrtf(se / (float)n + p.eps);
+      const float scg = rsqrtf(sg / (float)n + p.eps);
+      const uint4 *wi = reinterpret_cast<const uint4 *>(p.norm0);
+      const uint4 *wh = reinterpret_cast<const uint4 *>(p.norm1);
+      for (int kv = tid; kv < NV; kv += kGemvThreads) {
+        const uint4 u = er[kv];
+        const uint4 w = wi[kv];
+        x0[kv] = make_float4(bf_lo(u.x) * sce * bf_lo(w.x), bf_hi(u.x) * sce * bf_hi(w.x),
+                             bf_lo(u.y) * sce * bf_lo(w.y), bf_hi(u.y) * sce * bf_hi(w.y));
+        x1[kv] = make_float4(bf_lo(u.z) * sce * bf_lo(w.z), bf_hi(u.z) * sce * bf_hi(w.z),
+                             bf_lo(u.w) * sce * bf_lo(w.w), bf_hi(u.w) * sce * bf_hi(w.w));
+        const float4 a = gr[2 * kv], b = gr[2 * kv + 1];
+        const uint4 h = wh[kv];
+        x0[NV + kv] = make_float4(a.x * scg * bf_lo(h.x), a.y * scg * bf_hi(h.x),
+                                  a.z * scg * bf_lo(h.y), a.w * scg * bf_hi(h.y));
+        x1[NV + kv] = make_float4(b.x * scg * bf_lo(h.z), b.y * scg * bf_hi(h.z),
+                                  b.z * scg * bf_lo(h.w), b.w * scg * bf_hi(h.w));
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- epilogues
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+
+template <int NB, int MODE>
+__device__ void epilogue(const GemvParams &p, const float *accs, int row0, int nrows) {
+  const int tid = threadIdx.x;
+  if constexpr (MODE == GM_ENCODE || MODE == GM_O || MODE == GM_DOWN) {
+    for (int idx = tid; idx < nrows * NB; idx += kGemvThreads) {
+      const int m = idx % NB, r = idx / NB;
+      if (m >= p.items) continue;
+      const int item = p.item0 + m, row = row0 + r;
+      float v = accs[r * NB + m];
+      if constexpr (MODE != GM_ENCODE) v += p.res[(size_t)item * p.rows + row];
+      p.out_f[(size_t)item * p.rows + row] = v;
+      if constexpr (MODE == GM_DOWN) {
+        if (p.dbg_f) p.dbg_f[(size_t)item * p.dbg_stride_b + p.dbg_off + row] = v;
+      }
+    }
+  } else if constexpr (MODE == GM_GATEUP) {
+    const int npairs = nrows >> 1;
+    for (int idx = tid; idx < npairs * NB; idx += kGemvThreads) {
+      const int m = idx % NB, pr = idx / NB;
+      if (m >= p.items) continue;
+      const int item = p.item0 + m;
+      const float gate = accs[(2 * pr) * NB + m], up = accs[(2 * pr + 1) * NB + m];
+      p.out_f[(size_t)item * p.n_ff + ((row0 >> 1) + pr)] = silu_f(gate) * up;
+    }
+  } else if constexpr (MODE == GM_QKV) {
+    const int d = p.head_dim, R = p.rope_dims, half = R >> 1;
+    const int qr = p.n_head * d, kr = p.n_head_kv * d;
+    const int npairs = nrows >> 1;
+    for (int idx = tid; idx < npairs * NB; idx += kGemvThreads) {
+      const int m = idx % NB, pr = idx / NB;
+      if (m >= p.items) continue;
+      const int item = p.item0 + m;
+      const int lr = p.row_base + row0 + 2 * pr;  // even logical row
+      float a = accs[(2 * pr) * NB + m], b = accs[(2 * pr + 1) * NB + m];
+      const PairItem it = resolve_pair(p.pairs, item, p.n_embd);
+      const int region = lr < qr ? 0 : (lr < qr + kr ? 1 : 2);
+      const int rr = region == 0 ? lr : (region == 1 ? lr - qr : lr - qr - kr);
+      const int head = rr / d, li = rr - head * d;
+      int dim0 = li, dim1 = li + 1;
+      if (region < 2 && li < R) {
+        dim0 = li >> 1;
+        dim1 = dim0 + half;
+        int pos = it.pos;
+        if (pos < 0 || pos >= p.max_cache_len) pos = 0;
+        const float2 cs = p.rope[(size_t)pos * half + dim0];
+        const float ra = a * cs.x - b * cs.y;
+        const float rb = b * cs.x + a * cs.y;
+        a = ra;
+        b = rb;
+      }
+      if (region == 0) {
+        float *q = p.out_f + (size_t)item * qr + (size_t)head * d;
+        q[dim0] = a;
+        q[dim1] = b;
+      } else if (it.write_kv) {
+        const int pos = it.pos;
+        if (pos < 0 || pos >= p.max_cache_len) {
+          set_status(p.status, EAGLE3_DEV_BAD_POSITION);
+          continue;
+        }
+        const int pg = p.page_table[(size_t)it.b * p.max_pages + pos / p.page_size];
+        if (pg < 0 || pg >= p.num_pages) {
+          set_status(p.status, EAGLE3_DEV_BAD_PAGE);
+          continue;
+        }
+        uint16_t *pool = region == 1 ? p.k_pool : p.v_pool;
+        uint16_t *dst = pool + (((size_t)pg * p.n_head_kv + head) * p.page_size + pos % p.page_size) * d;
+        dst[dim0] = f2bf(a);
+        dst[dim1] = f2bf(b);
+      }
+    }
+  } else if constexpr (MODE == GM_LMHEAD) {
+    // Per item: best (logit, lowest row) over this CTA's rows, then a global 64-bit
+    // atomicMax of (order key << 32 | ~row); the last CTA decodes and applies d2t.
+    __shared__ unsigned long long best_sh[kGemvWarps];
+    __shared__ int last_sh;
+    for (int m = 0; m < p.items; ++m) {
+      const int item = p.item0 + m;
+      unsigned long long best = 0ull;
+      for (int r = tid; r < nrows; r += kGemvThreads) {
+        const float v = accs[r * NB + m];
+        const int row = row0 + r;
+        if (p.dbg_f) p.dbg_f[(size_t)item * p.dbg_stride_b + p.dbg_off + row] = v;
+        const unsigned long long key =
+            ((unsigned long long)float_order_key(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);
+        best = key > best ? key : best;
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
+      }
+      if ((tid & 31) == 0) best_sh[tid >> 5] = best;
+      __syncthreads();
+      if (tid == 0) {
+        unsigned long long b = 0ull;
+        for (int w = 0; w < kGemvWarps; ++w) b = best_sh[w] > b ? best_sh[w] : b;
+        if (nrows > 0) atomicMax(p.am_slot + item, b);
+      }
+      __syncthreads();
+    }
+    if (tid == 0) {
+      __threadfence();
+      const unsigned prev = atomicAdd(p.am_count, 1u);
+      last_sh = (prev == gridDim.x - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (last_sh) {
+      __threadfence();
+      for (int m = tid; m < p.items; m += kGemvThreads) {
+        const int item = p.item0 + m;
+        const unsigned long long key = atomicExch(p.am_slot + item, 0ull);
+        uint32_t id = 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
+        if (id >= (uint32_t)p.draft_vocab) {
+          set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
+          id = 0;
+        }
+        long long tgt = (long long)id + p.d2t[id];
+        if (tgt < 0 || tgt >= p.target_vocab) {
+          set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
+          tgt = 0;
+        }
+        const bool valid = p.step < p.gamma_eff[item];
+        const size_t o = (size_t)item * p.gamma + p.step;
+        p.draft_tok[o] = valid ? (int32_t)tgt : -1;
+        if (p.draft_id) p.draft_id[o] = valid ? (int32_t)id : -1;
+        if (p.next_tok) p.next_tok[item] = (int32_t)tgt;
+      }
+      if (tid == 0) *p.am_count = 0u;
+    }
+  }
+}
+
+// -------------------------------------------------------------------- kernel
+template <int NB, int R, int U, int MODE>
+__global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int KV = p.K >> 3;
+  const int ngroups = (p.rows + R - 1) / R;
+  const int g_begin = (int)((long long)blockIdx.x * ngroups / gridDim.x);
+  const int g_end = (int)((long long)(blockIdx.x + 1) * ngroups / gridDim.x);
+  constexpr int TILE_KV = kGemvThreads * U;
+  const int n_kc = (KV + TILE_KV - 1) / TILE_KV;
+  const int ntiles = (g_end - g_begin) * n_kc;
+  const int row0 = g_begin * R;
+  const int nrows = min(g_end * R, p.rows) - row0;
+
+  float4 *xs = reinterpret_cast<float4 *>(smem);
+  float *red = reinterpret_cast<float *>(xs + (size_t)NB * 2 * KV);  // [2][warps][R * NB]
+  float *scratch = red + 2 * kGemvWarps * R * NB;                     // [2 * warps]
+  float *accs = scratch + 2 * kGemvWarps;                             // [nrows][NB]
+
+  auto load_tile = [&](int t, uint4 (&buf)[R][U]) {
+    const int g = g_begin + t / n_kc, kc = t - (t / n_kc) * n_kc;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int lrow = g * R + r;
+      const bool rv = lrow < p.rows;
+      const uint16_t *wp = row_ptr<MODE>(p, p.row_base + (rv ? lrow : 0));
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int kv = kc * TILE_KV + u * kGemvThreads + tid;
+        if (rv && kv < KV)
+          buf[r][u] = ldg_stream(wp + (size_t)kv * 8);
+        else
+          buf[r][u] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  };
+
+  float acc[R][NB];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int m = 0; m < NB; ++m) acc[r][m] = 0.f;
+  int parity = 0;
+
+  auto compute_tile = [&](int t, const uint4 (&buf)[R][U]) {
+    const int gi = t / n_kc, kc = t - gi * n_kc;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int kv = kc * TILE_KV + u * kGemvThreads + tid;
+      if (kv < KV) {
+        float wf[R][8];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const uint4 w = buf[r][u];
+          wf[r][0] = bf_lo(w.x); wf[r][1] = bf_hi(w.x);
+          wf[r][2] = bf_lo(w.y); wf[r][3] = bf_hi(w.y);
+          wf[r][4] = bf_lo(w.z); wf[r][5] = bf_hi(w.z);
+          wf[r][6] = bf_lo(w.w); wf[r][7] = bf_hi(w.w);
+        }
+#pragma unroll
+        for (int m = 0; m < NB; ++m) {
+          const float4 a = xs[(size_t)(m * 2) * KV + kv];
+          const float4 b = xs[(size_t)(m * 2 + 1) * KV + kv];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            float s = acc[r][m];
+            s = fmaf(wf[r][0], a.x, s); s = fmaf(wf[r][1], a.y, s);
+            s = fmaf(wf[r][2], a.z, s); s = fmaf(wf[r][3], a.w, s);
+            s = fmaf(wf[r][4], b.x, s); s = fmaf(wf[r][5], b.y, s);
+            s = fmaf(wf[r][6], b.z, s); s = fmaf(wf[r][7], b.w, s);
+            acc[r][m] = s;
+          }
+        }
+      }
+    }
+    if (kc == n_kc - 1) {
+      constexpr int N = R * NB;
+      float v[N];
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < NB; ++m) {
+          v[r * NB + m] = acc[r][m];
+          acc[r][m] = 0.f;
+        }
+      const float tot = warp_reduce_multi<N>(v, lane);
+      float *rb = red + parity * kGemvWarps * N;
+      if (warp_reduce_writer<N>(lane)) rb[warp * N + warp_reduce_index<N>(lane)] = tot;
+      __syncthreads();
+      if (tid < N) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kGemvWarps; ++w) s += rb[w * N + tid];
+        const int r = tid / NB, m = tid - r * NB;
+        const int lrow = gi * R + r;  // relative to row0
+        if (lrow < nrows) accs[lrow * NB + m] = s;
+      }
+      parity ^= 1;
+    }
+  };
+
+  // Pre-dependency part: only weights are touched.
+  uint4 wa[R][U], wb[R][U];
+  if (ntiles > 0) load_tile(0, wa);
+  {
+    // Ask L2 for the next rows of this CTA as well.
+    const int pf_rows = min(nrows, 2 * R);
+    for (int r = 1 + warp; r < pf_rows; r += kGemvWarps) {
+      if (lane == 0) {
+        const uint16_t *wp = row_ptr<MODE>(p, p.row_base + row0 + r);
+        const uint32_t bytes = (uint32_t)p.K * 2u;
+        for (uint32_t off = 0; off < bytes; off += 32768u)
+          prefetch_l2(reinterpret_cast<const char *>(wp) + off, min(32768u, bytes - off));
+      }
+    }
+  }
+  pdl_trigger();
+  pdl_wait();
+
+  stage_x<NB, MODE>(p, xs, scratch);
+  __syncthreads();
+
+  for (int t = 0; t < ntiles; t += 2) {
+    if (t + 1 < ntiles) load_tile(t + 1, wb);
+    compute_tile(t, wa);
+    if (t + 1 < ntiles) {
+      if (t + 2 < ntiles) load_tile(t + 2, wa);
+      compute_tile(t + 1, wb);
+    }
+  }
+  __syncthreads();
+  epilogue<NB, MODE>(p, accs, row0, nrows);
+}
+
+// ------------------------------------------------------------------ launcher
+template <int NB, int R, int U, int MODE>
+static cudaError_t launch_one(const GemvParams &p, int grid, cudaStream_t st, bool pdl) {
+  const int ngroups = (p.rows + R - 1) / R;
+  if (grid > ngroups) grid = ngroups;
+  if (grid < 1) grid = 1;
+  const int max_rows = ((ngroups + grid - 1) / grid) * R;
+  const size_t smem = (size_t)NB * p.K * 4 + (size_t)2 * kGemvWarps * R * NB * 4 +
+                      (size_t)2 * kGemvWarps * 4 + (size_t)max_rows * NB * 4;
+  if (smem > kGemvSmemLimit) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemvThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, R, U, MODE>, p);
+}
+
+template <int MODE>
+static cudaError_t dispatch_nb(const GemvParams &p, int nb, int grid, cudaStream_t st, bool pdl) {
+  switch (nb) {
+    case 1: return launch_one<1, 4, 2, MODE>(p, grid, st, pdl);
+    case 2: return launch_one<2, 4, 2, MODE>(p, grid, st, pdl);
+    case 4: return launch_one<4, 2, 2, MODE>(p, grid, st, pdl);
+    case 8: return launch_one<8, 2, 2, MODE>(p, grid, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int NB, int R, int U, int MODE>
+static cudaError_t prepare_one() {
+  return cudaFuncSetAttribute(gemv_kernel<NB, R, U, MODE>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmemLimit);
+}
+
+template <int MODE>
+static cudaError_t prepare_mode() {
+  cudaError_t e = prepare_one<1, 4, 2, MODE>();
+  if (e == cudaSuccess) e = prepare_one<2, 4, 2, MODE>();
+  if (e == cudaSuccess) e = prepare_one<4, 2, 2, MODE>();
+  if (e == cudaSuccess) e = prepare_one<8, 2, 2, MODE>();
+  return e;
+}
+
+// Raise every instantiation's dynamic shared memory limit once, outside any capture.
+cudaError_t gemv_prepare() {
+  cudaError_t e = prepare_mode<GM_ENCODE>();
+  if (e == cudaSuccess) e = prepare_mode<GM_QKV>();
+  if (e == cudaSuccess) e = prepare_mode<GM_O>();
+  if (e == cudaSuccess) e = prepare_mode<GM_GATEUP>();
+  if (e == cudaSuccess) e = prepare_mode<GM_DOWN>();
+  if (e == cudaSuccess) e = prepare_mode<GM_LMHEAD>();
+  return e;
+}
+
+int gemv_items_per_launch(int K, int items) {
+  // x of one launch lives in shared memory: NB * K * 4 bytes <= kGemvMaxXBytes.
+  int nb = 8;
+  while (nb > 1 && (size_t)nb * K * 4 > kGemvMaxXBytes) nb >>= 1;
+  while (nb > 1 && nb / 2 >= items) nb >>= 1;
+  return nb;
+}
+
+cudaError_t gemv_launch(const GemvParams &p, int grid, cudaStream_t st, bool pdl) {
+  const int nb = gemv_items_per_launch(p.K, p.items);
+  if (p.items > nb || p.items < 1) return cudaErrorInvalidValue;
+  switch (p.mode) {
+    case GM_ENCODE: return dispatch_nb<GM_ENCODE>(p, nb, grid, st, pdl);
+    case GM_QKV: return dispatch_nb<GM_QKV>(p, nb, grid, st, pdl);
+    case GM_O: return dispatch_nb<GM_O>(p, nb, grid, st, pdl);
+    case GM_GATEUP: return dispatch_nb<GM_GATEUP>(p, nb, grid, st, pdl);
+    case GM_DOWN: return dispatch_nb<GM_DOWN>(p, nb, grid, st, pdl);
+    case GM_LMHEAD: return dispatch_nb<GM_LMHEAD>(p, nb, grid, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace e3

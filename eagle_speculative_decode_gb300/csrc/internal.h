@@ -1,0 +1,43 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace e3 {
+
+// Largest float32 activation block (items * K * 4 bytes) one GEMV launch keeps in
+// shared memory.
+constexpr size_t kGemvMaxXBytes = 96 * 1024;
+// Dynamic shared memory ceiling of a GEMV CTA (x + reduction buffers + row sums).
+constexpr size_t kGemvSmemLimit = 200 * 1024;
+
+cudaError_t gemv_prepare();
+int gemv_items_per_launch(int K, int items);
+cudaError_t gemv_launch(const GemvParams &p, int grid, cudaStream_t st, bool pdl);
+
+bool attn_supported(int head_dim, int group);
+cudaError_t attn_launch(const AttnParams &p, int B, cudaStream_t st, bool pdl);
+
+// Small bookkeeping kernels (small.cu).
+cudaError_t launch_chain_begin(int B, int gamma, unsigned flags, int max_cache_len,
+                               const int32_t *kv_len, int32_t *round_start, int32_t *geff,
+                               int32_t *geff_out, int *status, cudaStream_t st, bool pdl);
+cudaError_t launch_chain_end(int B, int32_t *kv_len, const int32_t *round_start,
+                             const int32_t *geff, cudaStream_t st, bool pdl);
+cudaError_t launch_rewind(int B, int32_t *kv_len, const int32_t *round_start, cudaStream_t st);
+cudaError_t launch_accept(int B, int gamma, const int32_t *draft_tok, const int32_t *target_pred,
+                          const int32_t *gamma_eff, int32_t *n_acc, int32_t *bonus,
+                          cudaStream_t st);
+cudaError_t launch_rebuild_finish(int B, int gamma, int n_embd, const float *enc_g,
+                                  const int32_t *n_acc, const int32_t *bonus, float *bnd_g,
+                                  int32_t *bnd_tok, int32_t *kv_len, int max_cache_len,
+                                  int *status, cudaStream_t st);
+cudaError_t launch_prefill_finish(int b, int n_embd, int kv_len_value, const float *enc_last,
+                                  const int32_t *next_tok, float *bnd_g, int32_t *bnd_tok,
+                                  int32_t *kv_len, cudaStream_t st);
+
+}  // namespace e3

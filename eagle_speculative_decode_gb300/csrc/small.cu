@@ -1,0 +1,157 @@
+// Bookkeeping kernels of a speculative round: chain begin/end, rewind, the greedy accept
+// walk and the boundary updates of rebuild and prefill.  All integer work except two
+// row copies of the boundary feature.
+#include "common.cuh"
+#include "internal.h"
+
+namespace e3 {
+
+static cudaLaunchConfig_t small_cfg(int grid, int block, cudaStream_t st, bool pdl,
+                                    cudaLaunchAttribute *attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cfg;
+}
+
+// Records the round start and the per-sequence chain length.  gamma_eff follows the
+// capacity rule: kv_len + gamma_eff + 1 <= max_cache_len.
+__global__ void chain_begin_kernel(int B, int gamma, unsigned flags, int max_cache_len,
+                                   const int32_t *kv_len, int32_t *round_start, int32_t *geff,
+                                   int32_t *geff_out, int *status) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int L = kv_len[b];
+  int ge = gamma;
+  if (L < 0 || L + gamma + 1 > max_cache_len) {
+    if ((flags & EAGLE3_SHRINK_GAMMA) && L >= 0 && max_cache_len - L - 1 >= 1) {
+      ge = max_cache_len - L - 1;
+    } else {
+      ge = 0;
+      set_status(status, EAGLE3_DEV_BAD_LENGTH);
+    }
+  }
+  round_start[b] = L < 0 ? 0 : L;
+  geff[b] = ge;
+  if (geff_out) geff_out[b] = ge;
+}
+
+__global__ void chain_end_kernel(int B, int32_t *kv_len, const int32_t *round_start,
+                                 const int32_t *geff) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) kv_len[b] = round_start[b] + geff[b];
+}
+
+__global__ void rewind_kernel(int B, int32_t *kv_len, const int32_t *round_start) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) kv_len[b] = round_start[b];
+}
+
+// n = leading matches of target_pred[b, i] with draft_tok[b, i]; bonus = target_pred[b, n].
+__global__ void accept_kernel(int B, int gamma, const int32_t *draft_tok, const int32_t *target_pred,
+                              const int32_t *gamma_eff, int32_t *n_acc, int32_t *bonus) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  int ge = gamma_eff ? gamma_eff[b] : gamma;
+  ge = ge < 0 ? 0 : (ge > gamma ? gamma : ge);
+  const int32_t *d = draft_tok + (size_t)b * gamma;
+  const int32_t *y = target_pred + (size_t)b * (gamma + 1);
+  int n = 0;
+  while (n < ge && y[n] == d[n]) ++n;
+  n_acc[b] = n;
+  bonus[b] = y[n];
+}
+
+// New boundary (fc v_n, bonus) and kv_len += n + 1.
+__global__ void rebuild_finish_kernel(int B, int gamma, int n_embd, const float *enc_g,
+                                      const int32_t *n_acc, const int32_t *bonus, float *bnd_g,
+                                      int32_t *bnd_tok, int32_t *kv_len, int max_cache_len,
+                                      int *status) {
+  const int b = blockIdx.y;
+  int n = n_acc[b];
+  if (n < 0 || n > gamma) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, EAGLE3_DEV_BAD_LENGTH);
+    n = n < 0 ? 0 : gamma;
+  }
+  const float *src = enc_g + ((size_t)b * (gamma + 1) + n) * n_embd;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_embd; i += gridDim.x * blockDim.x)
+    bnd_g[(size_t)b * n_embd + i] = src[i];
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    bnd_tok[b] = bonus[b];
+    int L = kv_len[b] + n + 1;
+    if (L > max_cache_len) {
+      set_status(status, EAGLE3_DEV_BAD_LENGTH);
+      L = max_cache_len;
+    }
+    kv_len[b] = L;
+  }
+}
+
+__global__ void prefill_finish_kernel(int b, int n_embd, int kv_len_value, const float *enc_last,
+                                      const int32_t *next_tok, float *bnd_g, int32_t *bnd_tok,
+                                      int32_t *kv_len) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_embd; i += gridDim.x * blockDim.x)
+    bnd_g[(size_t)b * n_embd + i] = enc_last[i];
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    bnd_tok[b] = next_tok[b];
+    kv_len[b] = kv_len_value;
+  }
+}
+
+cudaError_t launch_chain_begin(int B, int gamma, unsigned flags, int max_cache_len,
+                               const int32_t *kv_len, int32_t *round_start, int32_t *geff,
+                               int32_t *geff_out, int *status, cudaStream_t st, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = small_cfg((B + 127) / 128, 128, st, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, chain_begin_kernel, B, gamma, flags, max_cache_len, kv_len,
+                            round_start, geff, geff_out, status);
+}
+
+cudaError_t launch_chain_end(int B, int32_t *kv_len, const int32_t *round_start,
+                             const int32_t *geff, cudaStream_t st, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = small_cfg((B + 127) / 128, 128, st, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, chain_end_kernel, B, kv_len, round_start, geff);
+}
+
+cudaError_t launch_rewind(int B, int32_t *kv_len, const int32_t *round_start, cudaStream_t st) {
+  rewind_kernel<<<(B + 127) / 128, 128, 0, st>>>(B, kv_len, round_start);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_accept(int B, int gamma, const int32_t *draft_tok, const int32_t *target_pred,
+                          const int32_t *gamma_eff, int32_t *n_acc, int32_t *bonus,
+                          cudaStream_t st) {
+  accept_kernel<<<(B + 127) / 128, 128, 0, st>>>(B, gamma, draft_tok, target_pred, gamma_eff,
+                                                 n_acc, bonus);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rebuild_finish(int B, int gamma, int n_embd, const float *enc_g,
+                                  const int32_t *n_acc, const int32_t *bonus, float *bnd_g,
+                                  int32_t *bnd_tok, int32_t *kv_len, int max_cache_len,
+                                  int *status, cudaStream_t st) {
+  dim3 grid((n_embd + 1023) / 1024, B);
+  rebuild_finish_kernel<<<grid, 256, 0, st>>>(B, gamma, n_embd, enc_g, n_acc, bonus, bnd_g,
+                                              bnd_tok, kv_len, max_cache_len, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_finish(int b, int n_embd, int kv_len_value, const float *enc_last,
+                                  const int32_t *next_tok, float *bnd_g, int32_t *bnd_tok,
+                                  int32_t *kv_len, cudaStream_t st) {
+  prefill_finish_kernel<<<(n_embd + 1023) / 1024, 256, 0, st>>>(b, n_embd, kv_len_value, enc_last,
+                                                                next_tok, bnd_g, bnd_tok, kv_len);
+  return cudaGetLastError();
+}
+
+}  // namespace e3

@@ -1,0 +1,225 @@
+/*
+ * eagle3.h -- C ABI of the EAGLE-3 drafter draft round for greedy speculative decoding,
+ * GB300 (sm_103a).  Library: libeagle3.so (eagle_speculative_decode_gb300/).
+ *
+ * What the library computes (sources are cited as page title + section):
+ *   - "memra_engine/eagle.rs" (docs.rs source page), module doc "Op-sequence": the fc
+ *     encode g = fc . [aux_1; aux_15; aux_28] and one draft step: embed, RMSNorm of the
+ *     embedding and of g, the 2*n_embd concat, q/k/v projections, partial NeoX RoPE,
+ *     GQA attention over the drafter KV cache, o_proj + residual (pre-norm g),
+ *     post-attention RMSNorm, SwiGLU MLP, fused-add residual (gsum, fed back as the next
+ *     g), final RMSNorm, lm_head, argmax and target_id = draft_id + d2t[draft_id]
+ *     (``d2t_map``); ``generate_spec_eagle`` steps 2 and 4: the chain of gamma steps and
+ *     the greedy accept-prefix walk.
+ *   - "feat(eagle3): Qwen3 EAGLE-3 drafter forward pass (single-step + chain rollout)",
+ *     PR body: prefill_prompt / prefill_batched, draft_chain, chain_round (rewind leaves
+ *     a round side-effect free), rebuild_after_verify; review comment: the k + 1
+ *     capacity rule (start 97, k 3, max 100 must be refused or k shrunk).
+ *   - "Add the Eagle3Speculator module for speculative decoding", PR body: the drafter
+ *     pairs target hidden state t with token t + 1; after verify the draft cache is
+ *     reseeded from verify's features paired with the corrected token.
+ *
+ * State of one sequence (committed tokens t_0..t_N, target features a_0..a_{N-1}):
+ *   drafter KV holds pairs (fc a_p, t_{p+1}) at positions p = 0..N-2, kv_len = N - 1, and
+ *   the boundary is (g = fc a_{N-1} as float32 [n_embd], tok = t_N).
+ *
+ * Conventions, all entry points:
+ *   - Every buffer is caller-owned.  Weights, KV pools, page tables, boundary and output
+ *     buffers are DEVICE pointers; arguments named *_host are HOST pointers.  bf16 data is
+ *     passed as uint16_t bit patterns.  Device pointers must be 16-byte aligned.
+ *   - Calls are asynchronous on the given stream and make no host<->device
+ *     synchronisation, except eagle3_init (one upload of the RoPE table and a check of
+ *     d2t) and eagle3_get_status.
+ *   - Return 0 (EAGLE3_OK) or a negative error code.  On an error return nothing has
+ *     been enqueued and no state has changed, except EAGLE3_ERR_CUDA where a launch
+ *     failed part-way.
+ *   - Device-side range checks (token ids, page ids, positions) never fault: the access
+ *     is skipped and a bit is set in a device status word read by eagle3_get_status.
+ *   - A context is used from one host thread at a time.
+ */
+#ifndef EAGLE3_H
+#define EAGLE3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *eagle3_stream_t;
+
+#define EAGLE3_OK 0
+#define EAGLE3_ERR_INVALID_ARG (-1) /* null/misaligned pointer, bad shape, gamma out of range, bad d2t */
+#define EAGLE3_ERR_CAPACITY (-2)    /* kv_len + gamma + 1 > max_cache_len without EAGLE3_SHRINK_GAMMA */
+#define EAGLE3_ERR_STATE (-3)       /* call out of order: chain while a round is open, rebuild before rewind */
+#define EAGLE3_ERR_CUDA (-4)        /* a CUDA call or launch failed */
+#define EAGLE3_ERR_DEVICE (-5)      /* the device status word is non-zero (eagle3_get_status) */
+#define EAGLE3_ERR_UNSUPPORTED (-6) /* geometry outside what the kernels are built for */
+
+/* Device status bits (eagle3_get_status). */
+#define EAGLE3_DEV_BAD_TOKEN 1      /* token id outside [0, target_vocab) */
+#define EAGLE3_DEV_BAD_PAGE 2       /* page id outside [0, num_pages) */
+#define EAGLE3_DEV_BAD_POSITION 4   /* KV position outside [0, max_cache_len) */
+#define EAGLE3_DEV_BAD_LENGTH 8     /* kv_len or prompt length out of range */
+
+/* eagle3_draft_chain flags. */
+#define EAGLE3_SHRINK_GAMMA 1u      /* shrink gamma per sequence to max_cache_len - kv_len - 1 */
+
+/* Drafter geometry and capacity limits.
+ * Kernels are built for head_dim in {64, 128, 256}, n_head / n_head_kv in {1, 2, 4, 8},
+ * n_embd, n_ff multiples of 8 and rope_dims even, <= head_dim. */
+typedef struct {
+  int n_embd;          /* hidden size n                                     (4096)   */
+  int n_head;          /* query heads H                                     (16)     */
+  int n_head_kv;       /* key/value heads H_kv                              (4)      */
+  int head_dim;        /* d                                                 (256)    */
+  int rope_dims;       /* leading dims of each head that RoPE rotates       (64)     */
+  float rope_theta;    /* RoPE base                                         (1e7)    */
+  float rms_eps;       /* RMSNorm epsilon                                   (1e-6)   */
+  int n_ff;            /* MLP width F                                       (12288)  */
+  int draft_vocab;     /* lm_head rows V_d                                  (32000)  */
+  int target_vocab;    /* embedding rows V_t, range of d2t-mapped ids       (248320) */
+  int max_batch;       /* largest B of any call                                      */
+  int max_gamma;       /* largest chain length                                       */
+  int max_cache_len;   /* KV positions per sequence (0 .. max_cache_len - 1)         */
+  int page_size;       /* KV positions per page                                      */
+} eagle3_config;
+
+/* Drafter weights: bf16, PyTorch Linear layout [out, in] row-major, device memory,
+ * owned by the caller and left unchanged.  Shapes: fc [n, 3n]; q [H d, 2n];
+ * k, v [H_kv d, 2n]; o [n, H d]; gate, up [F, n]; down [n, F]; lm_head [V_d, n];
+ * embed [V_t, n] (the target's token embedding, indexed by target id); the four
+ * RMSNorm gains [n].  d2t: int64 [V_d], target_id = draft_id + d2t[draft_id]. */
+typedef struct {
+  const uint16_t *fc, *in_norm, *hidden_norm, *q, *k, *v, *o, *post_norm, *gate, *up, *down,
+      *final_norm, *lm_head, *embed;
+  const int64_t *d2t;
+} eagle3_weights;
+
+/* Paged drafter KV cache, device memory owned by the caller.
+ *   k_pool, v_pool: bf16 [num_pages, n_head_kv, page_size, head_dim] each.
+ *   page_table:     int32 [B, max_pages_per_seq]; position p of sequence b lives in page
+ *                   page_table[b, p / page_size] at slot p % page_size.  The caller
+ *                   reserves max_cache_len positions per sequence up front.
+ *   kv_len:         int32 [B], committed length of each sequence (device copy). */
+typedef struct {
+  uint16_t *k_pool, *v_pool;
+  const int32_t *page_table;
+  int num_pages;
+  int max_pages_per_seq;
+  int32_t *kv_len;
+} eagle3_kv;
+
+/* Boundary of each sequence: g float32 [B, n] (= fc a_{N-1}) and tok int32 [B] (= t_N). */
+typedef struct {
+  float *g;
+  int32_t *tok;
+} eagle3_boundary;
+
+typedef struct eagle3_ctx eagle3_ctx;
+
+/* Library version, (major << 16) | minor. */
+int eagle3_version(void);
+
+/* Static description of an error code. */
+const char *eagle3_error_string(int code);
+
+/* Device workspace a context needs for cfg, in bytes; 0 if cfg is invalid or
+ * unsupported.  Host-only arithmetic. */
+size_t eagle3_workspace_bytes(const eagle3_config *cfg);
+
+/* Capacity rule ("feat(eagle3) ...", review comment on rebuild_after_verify committing
+ * k + 1 entries): a chain of gamma drafts at committed length kv_len needs
+ * kv_len + gamma + 1 <= max_cache_len.  Writes the allowed chain length to *gamma_eff and
+ * returns EAGLE3_OK, or returns EAGLE3_ERR_CAPACITY (with EAGLE3_SHRINK_GAMMA in flags the
+ * chain shrinks to max_cache_len - kv_len - 1, refused below 1), or EAGLE3_ERR_INVALID_ARG
+ * for gamma < 1 or kv_len < 0.  Host-only arithmetic. */
+int eagle3_plan_gamma(int kv_len, int gamma, int max_cache_len, unsigned flags, int *gamma_eff);
+
+/* Create a context.  workspace: device buffer of eagle3_workspace_bytes(cfg) bytes,
+ * 256-byte aligned, owned by the caller and used by this context only until
+ * eagle3_destroy.  Validates cfg and the weight pointers, checks on the host that d2t
+ * maps every draft id to a distinct target id in [0, target_vocab) (a blocking copy of
+ * d2t), and uploads the RoPE table (angles in double, stored as float32 cos/sin).  The
+ * context object itself lives in host memory and is freed by eagle3_destroy. */
+int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspace,
+                size_t workspace_bytes, eagle3_stream_t stream, eagle3_ctx **out);
+
+/* Release the host context (the workspace stays the caller's). */
+int eagle3_destroy(eagle3_ctx *ctx);
+
+/* Encode ("memra_engine/eagle.rs", Eagle3Draft::encode): g[m] = fc . concat(aux[m, 0],
+ * aux[m, 1], aux[m, 2]) for m < M.  aux: bf16 [M, 3, n] device; g: float32 [M, n] device.
+ * M >= 0 (M = 0 does nothing). */
+int eagle3_encode(eagle3_ctx *ctx, const uint16_t *aux, int M, float *g, eagle3_stream_t stream);
+
+/* Teacher-forced prefill ("feat(eagle3) ...", PR body: prefill_prompt / prefill_batched).
+ * For each sequence b with prompt t_0..t_{P-1} (P = prompt_len_host[b], 1 <= P <= P_max),
+ * target features a_0..a_{P-1} and the target's greedy next token t_P:
+ * writes the KV pairs (fc a_p, t_{p+1}) at positions p = 0..P-2, sets kv_len[b] = P - 1
+ * and the boundary (fc a_{P-1}, t_P).
+ *   tokens:   int32 [B, P_max] device, row b holds t_0..t_{P-1}
+ *   next_tok: int32 [B] device, t_P
+ *   aux:      bf16 [B, P_max, 3, n] device
+ *   prompt_len_host: int32 [B] host; P <= max_cache_len is required. */
+int eagle3_prefill(eagle3_ctx *ctx, int B, const int32_t *tokens, int P_max,
+                   const int32_t *next_tok, const int32_t *prompt_len_host, const uint16_t *aux,
+                   const eagle3_kv *kv, eagle3_boundary *bnd, eagle3_stream_t stream);
+
+/* Draft chain ("memra_engine/eagle.rs", generate_spec_eagle step 2; "feat(eagle3) ...",
+ * PR body: draft_chain): gamma draft steps from the boundary of each sequence at
+ * positions kv_len[b] + j.  Step 0 embeds bnd->tok with g = bnd->g; step j > 0 embeds the
+ * previous step's target id with the previous step's gsum.  Opens a round: the
+ * speculative KV entries are written at kv_len .. kv_len + gamma_eff - 1 and kv_len
+ * advances by gamma_eff; eagle3_rewind closes the round.  The boundary is not modified.
+ *   kv_len_host: int32 [B] host mirror of kv_len, used for the capacity check.
+ *   draft_tok:   int32 [B, gamma] device, target ids d_1..d_gamma (-1 past gamma_eff).
+ *   draft_id, gamma_eff, logits_dbg (float32 [B, gamma, V_d]), g_dbg (float32
+ *   [B, gamma, n]): optional device outputs, NULL to skip.
+ * Refused with EAGLE3_ERR_CAPACITY unless kv_len + gamma + 1 <= max_cache_len for every
+ * sequence, or EAGLE3_SHRINK_GAMMA is set (then gamma_eff = max_cache_len - kv_len - 1). */
+int eagle3_draft_chain(eagle3_ctx *ctx, int B, int gamma, unsigned flags,
+                       const int32_t *kv_len_host, const eagle3_kv *kv,
+                       const eagle3_boundary *bnd, int32_t *draft_tok, int32_t *draft_id,
+                       int32_t *gamma_eff, float *logits_dbg, float *g_dbg,
+                       eagle3_stream_t stream);
+
+/* Rewind ("feat(eagle3) ...", PR body: chain_round rewinds the speculative KV): restore
+ * kv_len[b] to its value at the start of the open round.  Committed entries, the page
+ * table and the boundary are untouched.  EAGLE3_ERR_STATE if no round is open. */
+int eagle3_rewind(eagle3_ctx *ctx, int B, const eagle3_kv *kv, eagle3_stream_t stream);
+
+/* Greedy accept walk ("memra_engine/eagle.rs", generate_spec_eagle step 4):
+ * n_acc[b] = number of leading i with target_pred[b, i] == draft_tok[b, i] (i < gamma_eff),
+ * bonus[b] = target_pred[b, n_acc[b]].  target_pred: int32 [B, gamma + 1] device, the
+ * target's greedy token after each verify position; gamma_eff may be NULL (= gamma). */
+int eagle3_accept(eagle3_ctx *ctx, int B, int gamma, const int32_t *draft_tok,
+                  const int32_t *target_pred, const int32_t *gamma_eff, int32_t *n_acc,
+                  int32_t *bonus, eagle3_stream_t stream);
+
+/* Rebuild after verify ("feat(eagle3) ...", PR body: rebuild_after_verify; "Add the
+ * Eagle3Speculator module", PR body): with verify features v_i (target features at the
+ * verify positions N + i, bf16 [B, gamma + 1, 3, n] device) writes the pairs at
+ * kv_len + i for i = 0..n_acc[b]: pair 0 = (old boundary g, old boundary tok), pair i >= 1
+ * = (fc v_{i-1}, draft_tok[b, i-1]); then kv_len += n_acc + 1 and the boundary becomes
+ * (fc v_{n_acc}, bonus).  Requires the round to be rewound first (EAGLE3_ERR_STATE).
+ * n_acc, draft_tok, bonus: device int32 from the chain and eagle3_accept. */
+int eagle3_rebuild_after_verify(eagle3_ctx *ctx, int B, int gamma, const int32_t *n_acc,
+                                const int32_t *draft_tok, const int32_t *bonus,
+                                const uint16_t *verify_aux, const eagle3_kv *kv,
+                                eagle3_boundary *bnd, eagle3_stream_t stream);
+
+/* Synchronise the context's last stream and read the device status word (0 = clean);
+ * returns EAGLE3_ERR_DEVICE when it is non-zero.  Clears the word.  Not for hot loops. */
+int eagle3_get_status(eagle3_ctx *ctx, int *device_status);
+
+/* Launch mode of eagle3_draft_chain: 1 (default) replays a CUDA graph of the gamma
+ * steps captured per (B, gamma, flags, buffer set); 0 launches the kernels directly. */
+int eagle3_set_graph_mode(eagle3_ctx *ctx, int enabled);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EAGLE3_H */
