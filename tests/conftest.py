@@ -11,3 +11,11 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA device (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running case")
+
+
+@pytest.fixture(scope="session")
+def built_lib():
+    """Build (or reuse) libeagle3.so for sm_103a and load it."""
+    from eagle_speculative_decode_gb300 import binding, build
+    build.build()
+    return binding.load()

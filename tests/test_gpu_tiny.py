@@ -1,0 +1,249 @@
+"""GPU parity of the whole round on the small drafter (n_embd 256, 4:1 GQA, head 64,
+RoPE 16/64, draft vocab 1024 -> 4096), through the C ABI, against the CPU oracle:
+prefill, chain, rewind, accept and rebuild, element by element, over several rounds,
+ragged batches, non-contiguous pages and the capacity boundary."""
+import numpy as np
+import pytest
+import torch
+
+from eagle_speculative_decode_gb300 import binding as Bd
+from eagle_speculative_decode_gb300 import synth
+from eagle_speculative_decode_gb300.runtime import DraftModel
+from oracle import eagle3_oracle as O
+from parity import assert_close, bf16_bits_to_f64, oracle_chain_following
+
+pytestmark = pytest.mark.gpu
+G = synth.TINY
+
+
+@pytest.fixture(scope="module")
+def tiny(built_lib):
+    wts = synth.make_weights(G, seed=0)
+    model = DraftModel(wts, max_batch=8, max_gamma=8, max_cache_len=100, page_size=16)
+    dr = O.Drafter(G, wts.bits, wts.d2t)
+    yield wts, model, dr
+    model.close()
+
+
+def _prompt(batch, lens, seed, P_max=None):
+    P_max = P_max or int(max(lens))
+    toks = synth.make_tokens((batch, P_max + 1), G, seed)
+    aux = synth.make_aux((batch, P_max), G, seed)
+    return toks, aux, P_max
+
+
+def _upload(model, toks, aux, lens):
+    dev = model.device
+    P_max = aux.shape[1]
+    t = torch.from_numpy(np.ascontiguousarray(toks[:, :P_max])).to(dev)
+    nxt = torch.from_numpy(np.ascontiguousarray(toks[np.arange(len(lens)), lens])).to(dev)
+    a = torch.from_numpy(aux.view(np.int16)).to(dev)
+    return t, nxt, a
+
+
+def _oracle_prefill(dr, toks, aux, lens):
+    return [O.prefill(dr, toks[b, :lens[b]], int(toks[b, lens[b]]), aux[b, :lens[b]])
+            for b in range(len(lens))]
+
+
+def _check_state(seq, states, what):
+    kv_len = seq.kv_len.cpu().numpy()
+    g = seq.g.cpu().numpy()
+    tok = seq.tok.cpu().numpy()
+    for b, st in enumerate(states):
+        assert kv_len[b] == st.kv_len, f"{what}: kv_len[{b}]"
+        assert tok[b] == st.tok, f"{what}: tok[{b}]"
+        assert_close(g[b], st.g, f"{what}: boundary g[{b}]", max_abs=1e-3, rel_l2=1e-5)
+        if st.kv_len:
+            k, v = seq.kv_entries(b, 0, st.kv_len)
+            assert_close(bf16_bits_to_f64(k), st.k, f"{what}: K[{b}]")
+            assert_close(bf16_bits_to_f64(v), st.v, f"{what}: V[{b}]")
+
+
+def _round(model, dr, seq, states, gamma, n_imposed, seed, flags=0):
+    """One full round on GPU and oracle; returns (new states, draft outputs)."""
+    Bn = seq.B
+    out = seq.draft_chain(gamma, flags=flags, debug=True)
+    torch.cuda.synchronize()
+    dt = out["draft_tok"].cpu().numpy()
+    di = out["draft_id"].cpu().numpy()
+    ge = out["gamma_eff"].cpu().numpy()
+    logits = out["logits"].cpu().numpy()
+    gdbg = out["g"].cpu().numpy()
+    L = np.array([st.kv_len for st in states])
+    assert np.array_equal(seq.kv_len.cpu().numpy(), L + ge)
+    for b, st in enumerate(states):
+        g_eff = O.plan_gamma(st.kv_len, gamma, model.max_cache_len, bool(flags & Bd.EAGLE3_SHRINK_GAMMA))
+        assert ge[b] == g_eff
+        ch, _ = oracle_chain_following(dr, st, g_eff, di[b, :g_eff], dt[b, :g_eff])
+        assert np.all(dt[b, g_eff:] == -1)
+        for j in range(g_eff):
+            assert_close(logits[b, j], ch.logits[j], f"logits b{b} j{j}", max_abs=2e-2, rel_l2=1e-2)
+            assert_close(gdbg[b, j], ch.g[j], f"g b{b} j{j}")
+        k, v = seq.kv_entries(b, st.kv_len, st.kv_len + g_eff)
+        assert_close(bf16_bits_to_f64(k), ch.spec_k, f"spec K b{b}")
+        assert_close(bf16_bits_to_f64(v), ch.spec_v, f"spec V b{b}")
+    # rewind: kv_len back, committed bytes and boundary untouched
+    snap_k = [seq.kv_entries(b, 0, st.kv_len) for b, st in enumerate(states)]
+    g_snap, tok_snap = seq.g.clone(), seq.tok.clone()
+    seq.rewind()
+    torch.cuda.synchronize()
+    assert np.array_equal(seq.kv_len.cpu().numpy(), L)
+    for b, st in enumerate(states):
+        k, v = seq.kv_entries(b, 0, st.kv_len)
+        assert np.array_equal(k, snap_k[b][0]) and np.array_equal(v, snap_k[b][1])
+    assert torch.equal(seq.g, g_snap) and torch.equal(seq.tok, tok_snap)
+    # accept against imposed target predictions
+    y = synth.impose_target_predictions(np.where(dt < 0, 0, dt), np.minimum(n_imposed, ge), G, seed)
+    dev = model.device
+    n_acc, bonus = seq.accept(out["draft_tok"], torch.from_numpy(y).to(dev), out["gamma_eff"])
+    torch.cuda.synchronize()
+    na, bo = n_acc.cpu().numpy(), bonus.cpu().numpy()
+    for b in range(Bn):
+        want = O.accept(dt[b], y[b], int(ge[b]))
+        assert (na[b], bo[b]) == want
+    # rebuild with verify features
+    vaux = synth.make_aux((Bn, gamma + 1), G, seed, stream=9)
+    seq.rebuild_after_verify(n_acc, out["draft_tok"], bonus, torch.from_numpy(vaux.view(np.int16)).to(dev))
+    torch.cuda.synchronize()
+    new_states = [O.rebuild_after_verify(dr, st, int(na[b]), dt[b], int(bo[b]), vaux[b])
+                  for b, st in enumerate(states)]
+    _check_state(seq, new_states, "rebuild")
+    assert seq.model.status() == 0
+    return new_states
+
+
+def test_single_sequence_rounds(tiny):
+    wts, model, dr = tiny
+    lens = np.array([32])
+    toks, aux, _ = _prompt(1, lens, seed=1)
+    seq = model.new_state(1)
+    seq.prefill(*_upload(model, toks, aux, lens), lens)
+    torch.cuda.synchronize()
+    states = _oracle_prefill(dr, toks, aux, lens)
+    _check_state(seq, states, "prefill")
+    for r, n in enumerate([2, 0, 3]):
+        states = _round(model, dr, seq, states, 3, np.array([n]), seed=10 + r)
+
+
+def test_ragged_batch_random_pages(tiny):
+    wts, model, dr = tiny
+    lens = np.array([5, 32, 17, 1])
+    toks, aux, _ = _prompt(4, lens, seed=2)
+    pages_per_seq = (model.max_cache_len + model.page_size - 1) // model.page_size
+    pt = synth.page_table(4, pages_per_seq, seed=3)
+    seq = model.new_state(4, page_table=pt)
+    seq.prefill(*_upload(model, toks, aux, lens), lens)
+    torch.cuda.synchronize()
+    states = _oracle_prefill(dr, toks, aux, lens)
+    _check_state(seq, states, "prefill")
+    for r in range(3):
+        n = synth.imposed_accept_lengths(4, 4, seed=20 + r)
+        states = _round(model, dr, seq, states, 4, n, seed=20 + r)
+
+
+def test_capacity_boundary_start_97_gamma_3_max_100(tiny):
+    """The review's worked case: start 97, k 3, max 100 must be refused, or drafted with
+    k shrunk to 2, after which an all-accepted rebuild ends exactly at 100."""
+    wts, model, dr = tiny
+    lens = np.array([98])
+    toks, aux, _ = _prompt(1, lens, seed=4)
+    seq = model.new_state(1)
+    seq.prefill(*_upload(model, toks, aux, lens), lens)
+    torch.cuda.synchronize()
+    states = _oracle_prefill(dr, toks, aux, lens)
+    assert states[0].kv_len == 97
+    with pytest.raises(Bd.Eagle3Error) as ei:
+        seq.draft_chain(3)
+    assert ei.value.code == Bd.EAGLE3_ERR_CAPACITY
+    assert seq.kv_len.cpu().item() == 97          # refused: nothing enqueued
+    states = _round(model, dr, seq, states, 3, np.array([3]), seed=5, flags=Bd.EAGLE3_SHRINK_GAMMA)
+    assert states[0].kv_len == 100 and seq.kv_len.cpu().item() == 100
+
+
+def test_graph_and_direct_launch_agree(tiny):
+    wts, model, dr = tiny
+    lens = np.array([20, 9])
+    toks, aux, _ = _prompt(2, lens, seed=6)
+    outs = []
+    for graph in (True, False, True):
+        model.set_graph_mode(graph)
+        seq = model.new_state(2)
+        seq.prefill(*_upload(model, toks, aux, lens), lens)
+        o = seq.draft_chain(5, debug=True)
+        torch.cuda.synchronize()
+        outs.append({k: v.cpu().numpy() for k, v in o.items()})
+        seq.rewind()
+    model.set_graph_mode(True)
+    for o in outs[1:]:
+        for k in outs[0]:
+            assert np.array_equal(outs[0][k], o[k]), k
+
+
+def test_encode_exact_integer_case(tiny):
+    """fc in {-1, 0, 1} * 2^-4 and integer features: every partial sum is exact in
+    float32, so the GPU must equal the oracle bit for bit."""
+    wts, model, dr = tiny
+    rng = np.random.default_rng(7)
+    fc = (rng.integers(-1, 2, size=(G.n_embd, 3 * G.n_embd)) * 2.0 ** -4).astype(np.float32)
+    aux = rng.integers(-8, 9, size=(5, 3, G.n_embd)).astype(np.float32)
+    fc_bits = (fc.view(np.uint32) >> 16).astype(np.uint16)
+    aux_bits = (aux.view(np.uint32) >> 16).astype(np.uint16)
+    bits = dict(wts.bits)
+    bits["fc"] = fc_bits
+    m2 = DraftModel(synth.DrafterWeights(G, bits, wts.d2t), max_batch=2, max_gamma=2,
+                    max_cache_len=16, page_size=16)
+    try:
+        got = m2.encode(torch.from_numpy(aux_bits.view(np.int16)).to(m2.device)).cpu().numpy()
+    finally:
+        m2.close()
+    want = O.encode(O.Drafter(G, bits, wts.d2t), aux_bits)
+    assert np.array_equal(got.astype(np.float64), want)
+
+
+def test_state_machine_and_argument_errors(tiny):
+    wts, model, dr = tiny
+    lens = np.array([10])
+    toks, aux, _ = _prompt(1, lens, seed=8)
+    seq = model.new_state(1)
+    seq.prefill(*_upload(model, toks, aux, lens), lens)
+    dev = model.device
+    dummy = torch.zeros(1, 4, dtype=torch.int32, device=dev)
+    vaux = torch.zeros(1, 4, 3, G.n_embd, dtype=torch.int16, device=dev)
+    with pytest.raises(Bd.Eagle3Error) as ei:            # no round open
+        seq.rewind()
+    assert ei.value.code == Bd.EAGLE3_ERR_STATE
+    with pytest.raises(Bd.Eagle3Error) as ei:            # rebuild before any chain/rewind
+        seq.rebuild_after_verify(dummy[:, 0], dummy[:, :3], dummy[:, 0], vaux, n_acc_host=[0])
+    assert ei.value.code == Bd.EAGLE3_ERR_STATE
+    with pytest.raises(Bd.Eagle3Error) as ei:            # gamma above max_gamma
+        seq.draft_chain(9)
+    assert ei.value.code == Bd.EAGLE3_ERR_INVALID_ARG
+    out = seq.draft_chain(3)
+    with pytest.raises(Bd.Eagle3Error) as ei:            # a round is already open
+        seq.draft_chain(3)
+    assert ei.value.code == Bd.EAGLE3_ERR_STATE
+    with pytest.raises(Bd.Eagle3Error) as ei:            # rebuild before rewind
+        seq.rebuild_after_verify(dummy[:, 0], out["draft_tok"], dummy[:, 0], vaux, n_acc_host=[0])
+    assert ei.value.code == Bd.EAGLE3_ERR_STATE
+    seq.rewind()
+    with pytest.raises(Bd.Eagle3Error) as ei:            # null verify features
+        Bd.eagle3_rebuild_after_verify(model.ctx, 1, 3, dummy.data_ptr(), out["draft_tok"].data_ptr(),
+                                       dummy.data_ptr(), 0, seq.kv, seq.bnd)
+    assert ei.value.code == Bd.EAGLE3_ERR_INVALID_ARG
+    assert model.status() == 0
+
+
+def test_out_of_range_token_sets_status_without_fault(tiny):
+    wts, model, dr = tiny
+    lens = np.array([6])
+    toks, aux, _ = _prompt(1, lens, seed=9)
+    seq = model.new_state(1)
+    seq.prefill(*_upload(model, toks, aux, lens), lens)
+    seq.tok.fill_(G.target_vocab + 5)
+    seq.draft_chain(2)
+    torch.cuda.synchronize()
+    st = model.status()
+    assert st & Bd.EAGLE3_DEV_BAD_TOKEN
+    assert model.status() == 0                            # reading clears the word
+    seq.rewind()
