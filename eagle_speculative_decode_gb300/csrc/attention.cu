@@ -67,16 +67,25 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
     for (int i = 0; i < 8; ++i) acc[g][i] = 0.f;
   }
 
+  // The whole warp walks the key blocks together (the score reduction shuffles across
+  // the lanes of a key group with a full mask); lane groups past the end or on a bad page
+  // take part in the shuffles but do not update their state.
   const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
-  for (int key = k0 + warp * KPW + grp; key < k1; key += NP) {
-    const int pg = pt[key / p.page_size];
-    if (pg < 0 || pg >= p.num_pages) {
-      set_status(p.status, EAGLE3_DEV_BAD_PAGE);
-      continue;
+  for (int base = k0 + warp * KPW; base < k1; base += NP) {
+    const int key = base + grp;
+    bool valid = key < k1;
+    uint4 ku = make_uint4(0u, 0u, 0u, 0u), vu = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) {
+      const int pg = pt[key / p.page_size];
+      if (pg < 0 || pg >= p.num_pages) {
+        set_status(p.status, EAGLE3_DEV_BAD_PAGE);
+        valid = false;
+      } else {
+        const size_t off = (((size_t)pg * Hkv + kvh) * p.page_size + key % p.page_size) * D + li * 8;
+        ku = *reinterpret_cast<const uint4 *>(p.k_pool + off);
+        vu = *reinterpret_cast<const uint4 *>(p.v_pool + off);
+      }
     }
-    const size_t off = (((size_t)pg * Hkv + kvh) * p.page_size + key % p.page_size) * D + li * 8;
-    const uint4 ku = *reinterpret_cast<const uint4 *>(p.k_pool + off);
-    const uint4 vu = *reinterpret_cast<const uint4 *>(p.v_pool + off);
     const float kf[8] = {bf_lo(ku.x), bf_hi(ku.x), bf_lo(ku.y), bf_hi(ku.y),
                          bf_lo(ku.z), bf_hi(ku.z), bf_lo(ku.w), bf_hi(ku.w)};
     const float vf[8] = {bf_lo(vu.x), bf_hi(vu.x), bf_lo(vu.y), bf_hi(vu.y),
@@ -88,13 +97,15 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
       for (int i = 0; i < 8; ++i) sc = fmaf(qv[g][i], kf[i], sc);
 #pragma unroll
       for (int o = LPK / 2; o >= 1; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o, LPK);
-      const float mn = fmaxf(mx[g], sc);
-      const float corr = exp2f(mx[g] - mn);
-      const float pr = exp2f(sc - mn);
-      sum[g] = sum[g] * corr + pr;
+      if (valid) {
+        const float mn = fmaxf(mx[g], sc);
+        const float corr = exp2f(mx[g] - mn);
+        const float pr = exp2f(sc - mn);
+        sum[g] = sum[g] * corr + pr;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[g][i] = fmaf(pr, vf[i], acc[g][i] * corr);
-      mx[g] = mn;
+        for (int i = 0; i < 8; ++i) acc[g][i] = fmaf(pr, vf[i], acc[g][i] * corr);
+        mx[g] = mn;
+      }
     }
   }
 
