@@ -32,7 +32,8 @@ EXPORTED = (
     "eagle3_version", "eagle3_error_string", "eagle3_workspace_bytes", "eagle3_plan_gamma",
     "eagle3_init", "eagle3_destroy", "eagle3_encode", "eagle3_prefill", "eagle3_draft_chain",
     "eagle3_rewind", "eagle3_accept", "eagle3_rebuild_after_verify", "eagle3_get_status",
-    "eagle3_set_graph_mode",
+    "eagle3_set_graph_mode", "eagle3_launch_count", "eagle3_set_phase_events",
+    "eagle3_phase_event_count", "eagle3_phase_event_label",
 )
 
 
@@ -99,6 +100,10 @@ def load() -> ctypes.CDLL:
         "eagle3_rebuild_after_verify": (ci, [vp, ci, ci, vp, vp, vp, vp, P(KV), P(Boundary), vp]),
         "eagle3_get_status": (ci, [vp, P(ci)]),
         "eagle3_set_graph_mode": (ci, [vp, ci]),
+        "eagle3_launch_count": (ctypes.c_ulonglong, [vp]),
+        "eagle3_set_phase_events": (ci, [vp, P(vp), ci]),
+        "eagle3_phase_event_count": (ci, [vp]),
+        "eagle3_phase_event_label": (ci, [vp, ci]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -204,3 +209,23 @@ def eagle3_get_status(ctx: int) -> int:
     if rc not in (EAGLE3_OK, EAGLE3_ERR_DEVICE):
         raise Eagle3Error(rc, "eagle3_get_status")
     return s.value
+
+
+def eagle3_launch_count(ctx: int) -> int:
+    return int(load().eagle3_launch_count(ctx))
+
+
+def eagle3_set_phase_events(ctx: int, event_handles) -> object:
+    """event_handles: list of cudaEvent_t handles (ints).  Returns the ctypes array, which
+    the caller must keep alive while recording is on."""
+    arr = (ctypes.c_void_p * max(1, len(event_handles)))(*event_handles)
+    _check(load().eagle3_set_phase_events(ctx, arr, len(event_handles)), "eagle3_set_phase_events")
+    return arr
+
+
+def eagle3_phase_event_count(ctx: int) -> int:
+    return int(load().eagle3_phase_event_count(ctx))
+
+
+def eagle3_phase_event_label(ctx: int, i: int) -> int:
+    return int(load().eagle3_phase_event_label(ctx, int(i)))

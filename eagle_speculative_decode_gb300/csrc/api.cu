@@ -99,6 +99,7 @@ struct GraphEntry {
   GraphKey key;
   cudaGraphExec_t exec;
   unsigned long long last_use;
+  unsigned long long kernels;
 };
 
 }  // namespace
@@ -125,6 +126,12 @@ struct eagle3_ctx {
   cudaStream_t cap_stream;
   std::vector<GraphEntry> graphs;
   unsigned long long use_clock;
+  // measurement: kernels launched (graph replays count their kernels) and optional
+  // events recorded after each kernel of a direct-mode chain
+  unsigned long long launches;
+  cudaEvent_t *ev;
+  int ev_cap, ev_used;
+  std::vector<int> ev_label;
 };
 
 namespace {
@@ -168,13 +175,47 @@ void set_kv(GemvParams &p, const eagle3_kv *kv) {
   p.max_pages = kv->max_pages_per_seq;
 }
 
+// Phase labels of the measurement events (eagle3_phase_event_label).
+enum PhaseLabel : int {
+  PH_START = 0, PH_QKV = 1, PH_ATTN = 2, PH_O = 3, PH_GATEUP = 4, PH_DOWN = 5, PH_LMHEAD = 6,
+  PH_ENCODE = 7, PH_KV = 8, PH_SMALL = 9,
+};
+
+int gemv_label(int mode) {
+  switch (mode) {
+    case GM_ENCODE: return PH_ENCODE;
+    case GM_QKV: return PH_QKV;
+    case GM_O: return PH_O;
+    case GM_GATEUP: return PH_GATEUP;
+    case GM_DOWN: return PH_DOWN;
+    default: return PH_LMHEAD;
+  }
+}
+
+void record_event(eagle3_ctx *ctx, cudaStream_t st, int label) {
+  if (ctx->ev && ctx->ev_used < ctx->ev_cap) {
+    cudaEventRecord(ctx->ev[ctx->ev_used], st);
+    ctx->ev_label[ctx->ev_used++] = label;
+  }
+}
+
+// Book-keeping after every kernel launch.
+cudaError_t launched(eagle3_ctx *ctx, cudaStream_t st, cudaError_t e, int label) {
+  if (e == cudaSuccess) {
+    ++ctx->launches;
+    record_event(ctx, st, label);
+  }
+  return e;
+}
+
 // Launch a GEMV over `items` activation rows in as many launches as shared memory needs.
 cudaError_t gemv_items(eagle3_ctx *ctx, GemvParams p, int items, cudaStream_t st, bool pdl) {
   const int nb = gemv_items_per_launch(p.K, items);
+  const int label = (p.mode == GM_QKV && p.row_base > 0) ? PH_KV : gemv_label(p.mode);
   for (int i0 = 0; i0 < items; i0 += nb) {
     p.item0 = i0;
     p.items = std::min(nb, items - i0);
-    cudaError_t e = gemv_launch(p, ctx->num_sms, st, pdl);
+    cudaError_t e = launched(ctx, st, gemv_launch(p, ctx->num_sms, st, pdl), label);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -233,9 +274,12 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
   const eagle3_config &c = ctx->c;
   const int n = c.n_embd, qr = c.n_head * c.head_dim, kr = c.n_head_kv * c.head_dim;
   const bool pdl = true;
-  cudaError_t e = launch_chain_begin(a.B, a.gamma, a.flags, c.max_cache_len, a.kv->kv_len,
-                                     ctx->round_start, ctx->geff, a.gamma_eff, ctx->status, st,
-                                     false);
+  record_event(ctx, st, PH_START);
+  cudaError_t e = launched(ctx, st,
+                           launch_chain_begin(a.B, a.gamma, a.flags, c.max_cache_len, a.kv->kv_len,
+                                              ctx->round_start, ctx->geff, a.gamma_eff,
+                                              ctx->status, st, false),
+                           PH_SMALL);
   if (e != cudaSuccess) return e;
   for (int j = 0; j < a.gamma; ++j) {
     // q/k/v + RoPE + KV append
@@ -285,7 +329,7 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     ap.part_ml = ctx->part_ml;
     ap.count = ctx->attn_cnt;
     ap.status = ctx->status;
-    if ((e = attn_launch(ap, a.B, st, pdl)) != cudaSuccess) return e;
+    if ((e = launched(ctx, st, attn_launch(ap, a.B, st, pdl), PH_ATTN)) != cudaSuccess) return e;
 
     // o_proj + residual (pre-norm g of this step)
     p = base_params(ctx);
@@ -346,7 +390,8 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     p.dbg_off = j * c.draft_vocab;
     if ((e = gemv_items(ctx, p, a.B, st, pdl)) != cudaSuccess) return e;
   }
-  return launch_chain_end(a.B, a.kv->kv_len, ctx->round_start, ctx->geff, st, pdl);
+  return launched(ctx, st, launch_chain_end(a.B, a.kv->kv_len, ctx->round_start, ctx->geff, st, pdl),
+                  PH_SMALL);
 }
 
 GraphKey chain_key(const ChainArgs &a) {
@@ -370,7 +415,9 @@ cudaError_t run_chain_graph(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st
   for (auto &g : ctx->graphs) {
     if (g.key == key) {
       g.last_use = ++ctx->use_clock;
-      return cudaGraphLaunch(g.exec, st);
+      const cudaError_t e = cudaGraphLaunch(g.exec, st);
+      if (e == cudaSuccess) ctx->launches += g.kernels;
+      return e;
     }
   }
   if (!ctx->cap_stream) {
@@ -379,7 +426,13 @@ cudaError_t run_chain_graph(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st
   }
   cudaError_t e = cudaStreamBeginCapture(ctx->cap_stream, cudaStreamCaptureModeThreadLocal);
   if (e != cudaSuccess) return e;
+  const unsigned long long before = ctx->launches;
+  cudaEvent_t *ev_saved = ctx->ev;
+  ctx->ev = nullptr;  // no measurement events inside a graph
   const cudaError_t e_enq = enqueue_chain(ctx, a, ctx->cap_stream);
+  ctx->ev = ev_saved;
+  const unsigned long long kernels = ctx->launches - before;
+  ctx->launches = before;
   cudaGraph_t graph = nullptr;
   e = cudaStreamEndCapture(ctx->cap_stream, &graph);
   if (e_enq != cudaSuccess) {
@@ -397,8 +450,10 @@ cudaError_t run_chain_graph(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st
     cudaGraphExecDestroy(old->exec);
     ctx->graphs.erase(old);
   }
-  ctx->graphs.push_back(GraphEntry{key, exec, ++ctx->use_clock});
-  return cudaGraphLaunch(exec, st);
+  ctx->graphs.push_back(GraphEntry{key, exec, ++ctx->use_clock, kernels});
+  e = cudaGraphLaunch(exec, st);
+  if (e == cudaSuccess) ctx->launches += kernels;
+  return e;
 }
 
 }  // namespace
@@ -596,8 +651,10 @@ int eagle3_prefill(eagle3_ctx *ctx, int B, const int32_t *tokens, int P_max,
         if (e != cudaSuccess) break;
       }
       if (p0 + cnt == P)
-        e = launch_prefill_finish(b, n, P - 1, ctx->genc + (size_t)(P - 1 - p0) * n, next_tok,
-                                  bnd->g, bnd->tok, kv->kv_len, st);
+        e = launched(ctx, st,
+                     launch_prefill_finish(b, n, P - 1, ctx->genc + (size_t)(P - 1 - p0) * n,
+                                           next_tok, bnd->g, bnd->tok, kv->kv_len, st),
+                     PH_SMALL);
     }
   }
   ctx->rebuild_ok = 0;
@@ -653,7 +710,7 @@ int eagle3_rewind(eagle3_ctx *ctx, int B, const eagle3_kv *kv, eagle3_stream_t s
   if (B != ctx->open_B) return EAGLE3_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   ctx->last_stream = st;
-  const cudaError_t e = launch_rewind(B, kv->kv_len, ctx->round_start, st);
+  const cudaError_t e = launched(ctx, st, launch_rewind(B, kv->kv_len, ctx->round_start, st), PH_SMALL);
   if (e != cudaSuccess) return EAGLE3_ERR_CUDA;
   ctx->round_open = 0;
   ctx->rebuild_ok = 1;
@@ -668,7 +725,9 @@ int eagle3_accept(eagle3_ctx *ctx, int B, int gamma, const int32_t *draft_tok,
   if (!draft_tok || !target_pred || !n_acc || !bonus) return EAGLE3_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   ctx->last_stream = st;
-  return cuda_err(launch_accept(B, gamma, draft_tok, target_pred, gamma_eff, n_acc, bonus, st));
+  return cuda_err(launched(ctx, st,
+                           launch_accept(B, gamma, draft_tok, target_pred, gamma_eff, n_acc, bonus, st),
+                           PH_SMALL));
 }
 
 int eagle3_rebuild_after_verify(eagle3_ctx *ctx, int B, int gamma, const int32_t *n_acc,
@@ -699,11 +758,31 @@ int eagle3_rebuild_after_verify(eagle3_ctx *ctx, int B, int gamma, const int32_t
     e = gemv_items(ctx, p, M, st, true);
   }
   if (e == cudaSuccess)
-    e = launch_rebuild_finish(B, gamma, n, ctx->genc, n_acc, bonus, bnd->g, bnd->tok, kv->kv_len,
-                              ctx->c.max_cache_len, ctx->status, st);
+    e = launched(ctx, st,
+                 launch_rebuild_finish(B, gamma, n, ctx->genc, n_acc, bonus, bnd->g, bnd->tok,
+                                       kv->kv_len, ctx->c.max_cache_len, ctx->status, st),
+                 PH_SMALL);
   if (e != cudaSuccess) return EAGLE3_ERR_CUDA;
   ctx->rebuild_ok = 0;
   return EAGLE3_OK;
+}
+
+unsigned long long eagle3_launch_count(const eagle3_ctx *ctx) { return ctx ? ctx->launches : 0ull; }
+
+int eagle3_set_phase_events(eagle3_ctx *ctx, void *const *events, int count) {
+  if (!ctx || count < 0 || (count > 0 && !events)) return EAGLE3_ERR_INVALID_ARG;
+  ctx->ev = count > 0 ? reinterpret_cast<cudaEvent_t *>(const_cast<void **>(events)) : nullptr;
+  ctx->ev_cap = count;
+  ctx->ev_used = 0;
+  ctx->ev_label.assign(count, -1);
+  return EAGLE3_OK;
+}
+
+int eagle3_phase_event_count(const eagle3_ctx *ctx) { return ctx ? ctx->ev_used : 0; }
+
+int eagle3_phase_event_label(const eagle3_ctx *ctx, int i) {
+  if (!ctx || i < 0 || i >= ctx->ev_used) return -1;
+  return ctx->ev_label[i];
 }
 
 int eagle3_get_status(eagle3_ctx *ctx, int *device_status) {

@@ -219,6 +219,28 @@ int eagle3_get_status(eagle3_ctx *ctx, int *device_status);
  * steps captured per (B, gamma, flags, buffer set); 0 launches the kernels directly. */
 int eagle3_set_graph_mode(eagle3_ctx *ctx, int enabled);
 
+/* ---- measurement (no counterpart on the pages; used by the benchmark) ----------------- */
+
+/* Number of kernels this context has launched since eagle3_init (a graph replay counts
+ * every kernel in the graph).  Host-only. */
+unsigned long long eagle3_launch_count(const eagle3_ctx *ctx);
+
+/* Phase events: events[0..count) are cudaEvent_t handles owned by the caller.  While
+ * set, every directly launched call (graph mode off) records events[i] on its stream
+ * after each of its kernels (eagle3_draft_chain also records one before its first kernel),
+ * until count events are used; eagle3_set_phase_events again resets the cursor.  A recorded
+ * event sits between two kernels, so it removes their launch overlap: time kernels with it,
+ * not whole rounds.  count = 0 switches recording off. */
+int eagle3_set_phase_events(eagle3_ctx *ctx, void *const *events, int count);
+
+/* Events recorded since the last eagle3_set_phase_events. */
+int eagle3_phase_event_count(const eagle3_ctx *ctx);
+
+/* Kernel that precedes event i: 0 = start marker, 1 = q/k/v GEMV, 2 = attention,
+ * 3 = o_proj GEMV, 4 = gate/up GEMV, 5 = down GEMV, 6 = lm_head GEMV + argmax, 7 = encode
+ * GEMV, 8 = k/v-only GEMV (prefill, rebuild), 9 = bookkeeping kernel; -1 if out of range. */
+int eagle3_phase_event_label(const eagle3_ctx *ctx, int i);
+
 #ifdef __cplusplus
 }
 #endif
