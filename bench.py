@@ -347,26 +347,18 @@ def run_mine(args, cfg):
     # ---- per-kernel durations (direct launches with events between kernels)
     model.set_graph_mode(False)
     n_ev = 4 * (2 + 8 * gamma * max(1, (B + 1) // 2) + 16)
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-    handles = [e.cuda_event for e in evs]
     per_label = {}
     for _ in range(args.phase_rounds):
-        keep = Bd.eagle3_set_phase_events(model.ctx, handles)
+        Bd.eagle3_profile_begin(model.ctx, n_ev)
         seq.draft_chain(gamma, out=out)
-        cnt = Bd.eagle3_phase_event_count(model.ctx)
-        labels = [Bd.eagle3_phase_event_label(model.ctx, i) for i in range(cnt)]
-        Bd.eagle3_set_phase_events(model.ctx, [])
-        del keep
-        torch.cuda.synchronize()
-        for i in range(1, cnt):
-            per_label.setdefault(labels[i], []).append(evs[i - 1].elapsed_time(evs[i]) * 1e3)
+        for lab, ms in Bd.eagle3_profile_end(model.ctx):
+            per_label.setdefault(lab, []).append(ms * 1e3)
         seq.rewind()
-        one_round_tail = n_imp_host[r]
         d = out["draft_tok"]
         ext = torch.cat([d, ((d[:, -1:] + 7) % geo.target_vocab)], dim=1)
         torch.where(ar[None, :] < n_imp[r][:, None], ext, (ext + 1) % geo.target_vocab, out=y)
         seq.accept(d, y, out["gamma_eff"], n_acc=n_acc, bonus=bonus)
-        seq.rebuild_after_verify(n_acc, d, bonus, vaux[r], n_acc_host=one_round_tail)
+        seq.rebuild_after_verify(n_acc, d, bonus, vaux[r], n_acc_host=n_imp_host[r])
         r += 1
     torch.cuda.synchronize()
     model.set_graph_mode(True)

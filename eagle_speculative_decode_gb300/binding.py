@@ -32,8 +32,8 @@ EXPORTED = (
     "eagle3_version", "eagle3_error_string", "eagle3_workspace_bytes", "eagle3_plan_gamma",
     "eagle3_init", "eagle3_destroy", "eagle3_encode", "eagle3_prefill", "eagle3_draft_chain",
     "eagle3_rewind", "eagle3_accept", "eagle3_rebuild_after_verify", "eagle3_get_status",
-    "eagle3_set_graph_mode", "eagle3_launch_count", "eagle3_set_phase_events",
-    "eagle3_phase_event_count", "eagle3_phase_event_label",
+    "eagle3_set_graph_mode", "eagle3_launch_count", "eagle3_profile_begin",
+    "eagle3_profile_end", "eagle3_profile_interval",
 )
 
 
@@ -101,9 +101,9 @@ def load() -> ctypes.CDLL:
         "eagle3_get_status": (ci, [vp, P(ci)]),
         "eagle3_set_graph_mode": (ci, [vp, ci]),
         "eagle3_launch_count": (ctypes.c_ulonglong, [vp]),
-        "eagle3_set_phase_events": (ci, [vp, P(vp), ci]),
-        "eagle3_phase_event_count": (ci, [vp]),
-        "eagle3_phase_event_label": (ci, [vp, ci]),
+        "eagle3_profile_begin": (ci, [vp, ci]),
+        "eagle3_profile_end": (ci, [vp, P(ci)]),
+        "eagle3_profile_interval": (ci, [vp, ci, P(ci), P(ctypes.c_float)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -215,17 +215,18 @@ def eagle3_launch_count(ctx: int) -> int:
     return int(load().eagle3_launch_count(ctx))
 
 
-def eagle3_set_phase_events(ctx: int, event_handles) -> object:
-    """event_handles: list of cudaEvent_t handles (ints).  Returns the ctypes array, which
-    the caller must keep alive while recording is on."""
-    arr = (ctypes.c_void_p * max(1, len(event_handles)))(*event_handles)
-    _check(load().eagle3_set_phase_events(ctx, arr, len(event_handles)), "eagle3_set_phase_events")
-    return arr
+def eagle3_profile_begin(ctx: int, max_events: int) -> None:
+    _check(load().eagle3_profile_begin(ctx, int(max_events)), "eagle3_profile_begin")
 
 
-def eagle3_phase_event_count(ctx: int) -> int:
-    return int(load().eagle3_phase_event_count(ctx))
-
-
-def eagle3_phase_event_label(ctx: int, i: int) -> int:
-    return int(load().eagle3_phase_event_label(ctx, int(i)))
+def eagle3_profile_end(ctx: int) -> list[tuple[int, float]]:
+    """Stops recording; returns [(label, milliseconds)] for every recorded interval."""
+    n = ctypes.c_int(0)
+    _check(load().eagle3_profile_end(ctx, ctypes.byref(n)), "eagle3_profile_end")
+    out = []
+    lab, ms = ctypes.c_int(0), ctypes.c_float(0.0)
+    for i in range(1, n.value):
+        _check(load().eagle3_profile_interval(ctx, i, ctypes.byref(lab), ctypes.byref(ms)),
+               "eagle3_profile_interval")
+        out.append((lab.value, ms.value))
+    return out

@@ -132,6 +132,7 @@ struct eagle3_ctx {
   cudaEvent_t *ev;
   int ev_cap, ev_used;
   std::vector<int> ev_label;
+  std::vector<cudaEvent_t> ev_pool;
 };
 
 namespace {
@@ -594,6 +595,7 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
 int eagle3_destroy(eagle3_ctx *ctx) {
   if (!ctx) return EAGLE3_ERR_INVALID_ARG;
   for (auto &g : ctx->graphs) cudaGraphExecDestroy(g.exec);
+  for (cudaEvent_t e : ctx->ev_pool) cudaEventDestroy(e);
   if (ctx->cap_stream) cudaStreamDestroy(ctx->cap_stream);
   delete ctx;
   return EAGLE3_OK;
@@ -769,20 +771,39 @@ int eagle3_rebuild_after_verify(eagle3_ctx *ctx, int B, int gamma, const int32_t
 
 unsigned long long eagle3_launch_count(const eagle3_ctx *ctx) { return ctx ? ctx->launches : 0ull; }
 
-int eagle3_set_phase_events(eagle3_ctx *ctx, void *const *events, int count) {
-  if (!ctx || count < 0 || (count > 0 && !events)) return EAGLE3_ERR_INVALID_ARG;
-  ctx->ev = count > 0 ? reinterpret_cast<cudaEvent_t *>(const_cast<void **>(events)) : nullptr;
-  ctx->ev_cap = count;
+int eagle3_profile_begin(eagle3_ctx *ctx, int max_events) {
+  if (!ctx || max_events < 2 || max_events > (1 << 16)) return EAGLE3_ERR_INVALID_ARG;
+  for (cudaEvent_t e : ctx->ev_pool) cudaEventDestroy(e);
+  ctx->ev_pool.assign(max_events, nullptr);
+  for (int i = 0; i < max_events; ++i)
+    if (cudaEventCreate(&ctx->ev_pool[i]) != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(ctx->ev_pool[j]);
+      ctx->ev_pool.clear();
+      ctx->ev = nullptr;
+      return EAGLE3_ERR_CUDA;
+    }
+  ctx->ev = ctx->ev_pool.data();
+  ctx->ev_cap = max_events;
   ctx->ev_used = 0;
-  ctx->ev_label.assign(count, -1);
+  ctx->ev_label.assign(max_events, -1);
   return EAGLE3_OK;
 }
 
-int eagle3_phase_event_count(const eagle3_ctx *ctx) { return ctx ? ctx->ev_used : 0; }
+int eagle3_profile_end(eagle3_ctx *ctx, int *n_events) {
+  if (!ctx || !n_events) return EAGLE3_ERR_INVALID_ARG;
+  *n_events = ctx->ev_used;
+  ctx->ev = nullptr;
+  if (ctx->ev_used > 0 && cudaEventSynchronize(ctx->ev_pool[ctx->ev_used - 1]) != cudaSuccess)
+    return EAGLE3_ERR_CUDA;
+  return EAGLE3_OK;
+}
 
-int eagle3_phase_event_label(const eagle3_ctx *ctx, int i) {
-  if (!ctx || i < 0 || i >= ctx->ev_used) return -1;
-  return ctx->ev_label[i];
+int eagle3_profile_interval(const eagle3_ctx *ctx, int i, int *label, float *ms) {
+  if (!ctx || !label || !ms || i < 1 || i >= ctx->ev_used) return EAGLE3_ERR_INVALID_ARG;
+  *label = ctx->ev_label[i];
+  if (cudaEventElapsedTime(ms, ctx->ev_pool[i - 1], ctx->ev_pool[i]) != cudaSuccess)
+    return EAGLE3_ERR_CUDA;
+  return EAGLE3_OK;
 }
 
 int eagle3_get_status(eagle3_ctx *ctx, int *device_status) {

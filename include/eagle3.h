@@ -225,21 +225,21 @@ int eagle3_set_graph_mode(eagle3_ctx *ctx, int enabled);
  * every kernel in the graph).  Host-only. */
 unsigned long long eagle3_launch_count(const eagle3_ctx *ctx);
 
-/* Phase events: events[0..count) are cudaEvent_t handles owned by the caller.  While
- * set, every directly launched call (graph mode off) records events[i] on its stream
- * after each of its kernels (eagle3_draft_chain also records one before its first kernel),
- * until count events are used; eagle3_set_phase_events again resets the cursor.  A recorded
- * event sits between two kernels, so it removes their launch overlap: time kernels with it,
- * not whole rounds.  count = 0 switches recording off. */
-int eagle3_set_phase_events(eagle3_ctx *ctx, void *const *events, int count);
+/* Kernel timing.  eagle3_profile_begin creates max_events CUDA events (host calls, no
+ * device memory) and from then on every directly launched call (graph mode off) records
+ * one event on its stream after each of its kernels (eagle3_draft_chain also records one
+ * before its first kernel), until max_events are used.  An event between two kernels
+ * removes their launch overlap, so use this to time kernels, not whole rounds. */
+int eagle3_profile_begin(eagle3_ctx *ctx, int max_events);
 
-/* Events recorded since the last eagle3_set_phase_events. */
-int eagle3_phase_event_count(const eagle3_ctx *ctx);
+/* Stop recording, wait for the last recorded event, and return how many were recorded. */
+int eagle3_profile_end(eagle3_ctx *ctx, int *n_events);
 
-/* Kernel that precedes event i: 0 = start marker, 1 = q/k/v GEMV, 2 = attention,
- * 3 = o_proj GEMV, 4 = gate/up GEMV, 5 = down GEMV, 6 = lm_head GEMV + argmax, 7 = encode
- * GEMV, 8 = k/v-only GEMV (prefill, rebuild), 9 = bookkeeping kernel; -1 if out of range. */
-int eagle3_phase_event_label(const eagle3_ctx *ctx, int i);
+/* For recorded event i >= 1: *ms = time from event i-1 to event i, and *label = the kernel
+ * launched between them: 0 = start marker, 1 = q/k/v GEMV, 2 = attention, 3 = o_proj
+ * GEMV, 4 = gate/up GEMV, 5 = down GEMV, 6 = lm_head GEMV + argmax, 7 = encode GEMV,
+ * 8 = k/v-only GEMV (prefill, rebuild), 9 = bookkeeping kernel. */
+int eagle3_profile_interval(const eagle3_ctx *ctx, int i, int *label, float *ms);
 
 #ifdef __cplusplus
 }

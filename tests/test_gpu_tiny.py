@@ -41,6 +41,11 @@ def _upload(model, toks, aux, lens):
     return t, nxt, a
 
 
+def _prefill(seq, model, toks, aux, lens):
+    t, nxt, a = _upload(model, toks, aux, lens)
+    seq.prefill(t, nxt, lens, a)
+
+
 def _oracle_prefill(dr, toks, aux, lens):
     return [O.prefill(dr, toks[b, :lens[b]], int(toks[b, lens[b]]), aux[b, :lens[b]])
             for b in range(len(lens))]
@@ -118,7 +123,7 @@ def test_single_sequence_rounds(tiny):
     lens = np.array([32])
     toks, aux, _ = _prompt(1, lens, seed=1)
     seq = model.new_state(1)
-    seq.prefill(*_upload(model, toks, aux, lens), lens)
+    _prefill(seq, model, toks, aux, lens)
     torch.cuda.synchronize()
     states = _oracle_prefill(dr, toks, aux, lens)
     _check_state(seq, states, "prefill")
@@ -133,7 +138,7 @@ def test_ragged_batch_random_pages(tiny):
     pages_per_seq = (model.max_cache_len + model.page_size - 1) // model.page_size
     pt = synth.page_table(4, pages_per_seq, seed=3)
     seq = model.new_state(4, page_table=pt)
-    seq.prefill(*_upload(model, toks, aux, lens), lens)
+    _prefill(seq, model, toks, aux, lens)
     torch.cuda.synchronize()
     states = _oracle_prefill(dr, toks, aux, lens)
     _check_state(seq, states, "prefill")
@@ -149,7 +154,7 @@ def test_capacity_boundary_start_97_gamma_3_max_100(tiny):
     lens = np.array([98])
     toks, aux, _ = _prompt(1, lens, seed=4)
     seq = model.new_state(1)
-    seq.prefill(*_upload(model, toks, aux, lens), lens)
+    _prefill(seq, model, toks, aux, lens)
     torch.cuda.synchronize()
     states = _oracle_prefill(dr, toks, aux, lens)
     assert states[0].kv_len == 97
@@ -169,7 +174,7 @@ def test_graph_and_direct_launch_agree(tiny):
     for graph in (True, False, True):
         model.set_graph_mode(graph)
         seq = model.new_state(2)
-        seq.prefill(*_upload(model, toks, aux, lens), lens)
+        _prefill(seq, model, toks, aux, lens)
         o = seq.draft_chain(5, debug=True)
         torch.cuda.synchronize()
         outs.append({k: v.cpu().numpy() for k, v in o.items()})
@@ -206,7 +211,7 @@ def test_state_machine_and_argument_errors(tiny):
     lens = np.array([10])
     toks, aux, _ = _prompt(1, lens, seed=8)
     seq = model.new_state(1)
-    seq.prefill(*_upload(model, toks, aux, lens), lens)
+    _prefill(seq, model, toks, aux, lens)
     dev = model.device
     dummy = torch.zeros(1, 4, dtype=torch.int32, device=dev)
     vaux = torch.zeros(1, 4, 3, G.n_embd, dtype=torch.int16, device=dev)
@@ -239,7 +244,7 @@ def test_out_of_range_token_sets_status_without_fault(tiny):
     lens = np.array([6])
     toks, aux, _ = _prompt(1, lens, seed=9)
     seq = model.new_state(1)
-    seq.prefill(*_upload(model, toks, aux, lens), lens)
+    _prefill(seq, model, toks, aux, lens)
     seq.tok.fill_(G.target_vocab + 5)
     seq.draft_chain(2)
     torch.cuda.synchronize()
