@@ -27,6 +27,7 @@ EAGLE3_DEV_BAD_TOKEN = 1
 EAGLE3_DEV_BAD_PAGE = 2
 EAGLE3_DEV_BAD_POSITION = 4
 EAGLE3_DEV_BAD_LENGTH = 8
+EAGLE3_DEV_TIMEOUT = 16
 
 EXPORTED = (
     "eagle3_version", "eagle3_error_string", "eagle3_workspace_bytes", "eagle3_plan_gamma",

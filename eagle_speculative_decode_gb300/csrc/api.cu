@@ -39,6 +39,7 @@ bool cfg_valid(const eagle3_config *c) {
   if (c->rope_dims < 0 || c->rope_dims % 2 || c->rope_dims > c->head_dim) return false;
   if (!(c->rope_theta > 0.f) || !(c->rms_eps >= 0.f)) return false;
   if (c->n_ff <= 0 || c->n_ff % 8) return false;
+  if (c->draft_vocab % 2 || (c->head_dim * c->n_head_kv) % 2) return false;  // GEMV row pairs
   if (c->draft_vocab <= 0 || c->target_vocab <= 0) return false;
   if (c->max_batch <= 0 || c->max_gamma <= 0 || c->max_gamma > 64) return false;
   if (c->max_cache_len <= 1 || c->page_size <= 0) return false;
@@ -249,17 +250,18 @@ void kv_only_params(const eagle3_ctx *ctx, const eagle3_kv *kv, GemvParams &p) {
   p.norm1 = ctx->w.hidden_norm;
 }
 
+// Splits of the attention key range: about four CTAs per SM over all (sequence, kv head)
+// pairs, at least ~32 keys per split (rounded to a power of two so that a growing
+// context re-captures the chain graph rarely).
 int choose_splits(const eagle3_ctx *ctx, int B, int max_len) {
   const int per = B * ctx->c.n_head_kv;
-  int s = std::max(1, (2 * ctx->num_sms + per - 1) / per);
+  int s = std::max(1, (4 * ctx->num_sms + per - 1) / per);
   s = std::min(s, kMaxSplits);
   s = std::min(s, std::max(1, kSplitSlots / per));
-  // at least ~64 keys per split
-  const int by_len = std::max(1, (max_len + 63) / 64);
-  s = std::min(s, by_len);
+  const int by_len = std::max(1, (max_len + 31) / 32);
   int p2 = 1;
-  while (p2 * 2 <= s) p2 *= 2;
-  return p2;
+  while (p2 * 2 <= by_len) p2 *= 2;
+  return std::max(1, std::min(s, p2));
 }
 
 struct ChainArgs {

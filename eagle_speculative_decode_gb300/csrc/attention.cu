@@ -67,45 +67,71 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
     for (int i = 0; i < 8; ++i) acc[g][i] = 0.f;
   }
 
-  // The whole warp walks the key blocks together (the score reduction shuffles across
-  // the lanes of a key group with a full mask); lane groups past the end or on a bad page
-  // take part in the shuffles but do not update their state.
+  // The whole warp walks blocks of UNR * KPW keys together (the score reduction shuffles
+  // across the lanes of a key group with a full mask); the K/V loads of a block are all
+  // issued before any score is computed, so each lane keeps 2 * UNR 16-byte loads in
+  // flight.  Lane groups past the end or on a bad page take part in the shuffles but do
+  // not update their state.
+  constexpr int UNR = (G >= 8 || D < 128) ? 4 : 8;
   const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
-  for (int base = k0 + warp * KPW; base < k1; base += NP) {
-    const int key = base + grp;
-    bool valid = key < k1;
-    uint4 ku = make_uint4(0u, 0u, 0u, 0u), vu = make_uint4(0u, 0u, 0u, 0u);
-    if (valid) {
-      const int pg = pt[key / p.page_size];
-      if (pg < 0 || pg >= p.num_pages) {
-        set_status(p.status, EAGLE3_DEV_BAD_PAGE);
-        valid = false;
-      } else {
-        const size_t off = (((size_t)pg * Hkv + kvh) * p.page_size + key % p.page_size) * D + li * 8;
-        ku = *reinterpret_cast<const uint4 *>(p.k_pool + off);
-        vu = *reinterpret_cast<const uint4 *>(p.v_pool + off);
+  for (int base = k0 + warp * KPW * UNR; base < k1; base += NP * UNR) {
+    bool valid[UNR];
+    uint4 ku[UNR], vu[UNR];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int key = base + u * KPW + grp;
+      valid[u] = key < k1;
+      ku[u] = make_uint4(0u, 0u, 0u, 0u);
+      vu[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (valid[u]) {
+        const int pg = pt[key / p.page_size];
+        if (pg < 0 || pg >= p.num_pages) {
+          set_status(p.status, EAGLE3_DEV_BAD_PAGE);
+          valid[u] = false;
+        } else {
+          const size_t off = (((size_t)pg * Hkv + kvh) * p.page_size + key % p.page_size) * D + li * 8;
+          ku[u] = *reinterpret_cast<const uint4 *>(p.k_pool + off);
+          vu[u] = *reinterpret_cast<const uint4 *>(p.v_pool + off);
+        }
       }
     }
-    const float kf[8] = {bf_lo(ku.x), bf_hi(ku.x), bf_lo(ku.y), bf_hi(ku.y),
-                         bf_lo(ku.z), bf_hi(ku.z), bf_lo(ku.w), bf_hi(ku.w)};
-    const float vf[8] = {bf_lo(vu.x), bf_hi(vu.x), bf_lo(vu.y), bf_hi(vu.y),
-                         bf_lo(vu.z), bf_hi(vu.z), bf_lo(vu.w), bf_hi(vu.w)};
+    float sc[UNR][G];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const float kf[8] = {bf_lo(ku[u].x), bf_hi(ku[u].x), bf_lo(ku[u].y), bf_hi(ku[u].y),
+                           bf_lo(ku[u].z), bf_hi(ku[u].z), bf_lo(ku[u].w), bf_hi(ku[u].w)};
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float d = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) d = fmaf(qv[g][i], kf[i], d);
+#pragma unroll
+        for (int o = LPK / 2; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o, LPK);
+        sc[u][g] = valid[u] ? d : -INFINITY;
+      }
+    }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      float sc = 0.f;
+      float mb = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sc = fmaf(qv[g][i], kf[i], sc);
+      for (int u = 0; u < UNR; ++u) mb = fmaxf(mb, sc[u][g]);
+      if (mb == -INFINITY) continue;  // no valid key of this lane group in the block
+      const float mn = fmaxf(mx[g], mb);
+      const float corr = exp2f(mx[g] - mn);
+      float l = sum[g] * corr;
 #pragma unroll
-      for (int o = LPK / 2; o >= 1; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o, LPK);
-      if (valid) {
-        const float mn = fmaxf(mx[g], sc);
-        const float corr = exp2f(mx[g] - mn);
-        const float pr = exp2f(sc - mn);
-        sum[g] = sum[g] * corr + pr;
+      for (int i = 0; i < 8; ++i) acc[g][i] *= corr;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[g][i] = fmaf(pr, vf[i], acc[g][i] * corr);
-        mx[g] = mn;
+      for (int u = 0; u < UNR; ++u) {
+        const float pr = exp2f(sc[u][g] - mn);  // 0 for invalid keys
+        l += pr;
+        const float vf[8] = {bf_lo(vu[u].x), bf_hi(vu[u].x), bf_lo(vu[u].y), bf_hi(vu[u].y),
+                             bf_lo(vu[u].z), bf_hi(vu[u].z), bf_lo(vu[u].w), bf_hi(vu[u].w)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[g][i] = fmaf(pr, vf[i], acc[g][i]);
       }
+      sum[g] = l;
+      mx[g] = mn;
     }
   }
 

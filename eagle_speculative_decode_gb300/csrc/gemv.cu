@@ -6,16 +6,17 @@
 // consumes y (partial RoPE + bf16 KV append, residual adds, SwiGLU, argmax + d2t).
 // Ops follow "memra_engine/eagle.rs", module doc "Op-sequence".
 //
-// Work split: the logical rows are cut into groups of R rows; every CTA owns a
-// contiguous, balanced range of groups and streams those rows with 16-byte
-// non-allocating loads, 256 threads side by side along K (so every warp moves 512
-// contiguous bytes per load).  Loads of the next tile are issued before the FMAs of the
-// current one (register double buffer) and the first tile is requested before the
-// kernel waits on its predecessor (PDL), so weight streaming overlaps the previous
-// kernel's tail.  x lives in shared memory as float32, split into two float4 planes
-// (elements 0-3 and 4-7 of each 8-element vector) so that each warp's LDS.128 is
-// conflict free.  Per-group partial sums are reduced across the CTA into a per-row
-// accumulator array in shared memory; the epilogue runs once all groups are done.
+// Data movement (one CTA per SM): the CTA owns a contiguous, balanced range of row
+// pairs.  A producer warp streams those rows, SR whole rows per stage (<= 32 KB), with
+// bulk copies (cp.async.bulk, TMA) into an NSTAGE-deep shared-memory ring guarded by
+// mbarriers.  It starts before the kernel waits on its predecessor (programmatic
+// dependent launch), so the next weights are already in flight while the previous
+// kernel drains.  Eight consumer warps stage x (normalised where the op says so) in
+// shared memory as float32 in two float4 planes (elements 0-3 and 4-7 of each 8-element
+// vector: conflict-free LDS.128), then, per stage, each thread takes 16-byte vectors
+// k = 8 * (warp * 32 + lane + 256 j) of all SR rows, so every x vector it loads serves
+// SR rows.  A stage's per-row sums are reduced within the warp and kept per warp; the
+// eight warp partials are added in a fixed order before the epilogue (deterministic).
 #include <math.h>
 
 #include "common.cuh"
@@ -90,9 +91,9 @@ __device__ __forceinline__ float block_sum(float v, float *scratch) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
+  consumer_sync();
   if (lane == 0) scratch[warp] = v;
-  __syncthreads();
+  consumer_sync();
   float t = 0.f;
 #pragma unroll
   for (int w = 0; w < kGemvWarps; ++w) t += scratch[w];
@@ -155,7 +156,8 @@ __device__ void stage_x(const GemvParams &p, float4 *xs, float *scratch) {
       const PairItem it = resolve_pair(p.pairs, item, n);
       int tok = it.tok;
       if (tok < 0 || tok >= p.target_vocab) {
-        if (tid == 0) set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
+        // only rows whose K/V are kept (or the chain's q) may report a bad token
+        if (tid == 0 && (it.write_kv || p.row_base == 0)) set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
         tok = 0;
       }
       const uint4 *er = reinterpret_cast<const uint4 *>(p.embed + (size_t)tok * n);
@@ -291,20 +293,20 @@ __device__ void epilogue(const GemvParams &p, const float *accs, int row0, int n
         best = other > best ? other : best;
       }
       if ((tid & 31) == 0) best_sh[tid >> 5] = best;
-      __syncthreads();
+      consumer_sync();
       if (tid == 0) {
         unsigned long long b = 0ull;
         for (int w = 0; w < kGemvWarps; ++w) b = best_sh[w] > b ? best_sh[w] : b;
         if (nrows > 0) atomicMax(p.am_slot + item, b);
       }
-      __syncthreads();
+      consumer_sync();
     }
     if (tid == 0) {
       __threadfence();
       const unsigned prev = atomicAdd(p.am_count, 1u);
       last_sh = (prev == gridDim.x - 1) ? 1 : 0;
     }
-    __syncthreads();
+    consumer_sync();
     if (last_sh) {
       __threadfence();
       for (int m = tid; m < p.items; m += kGemvThreads) {
@@ -332,186 +334,231 @@ __device__ void epilogue(const GemvParams &p, const float *accs, int row0, int n
 }
 
 // -------------------------------------------------------------------- kernel
-template <int NB, int R, int U, int MODE>
-__global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams p) {
-  extern __shared__ __align__(16) unsigned char smem[];
+constexpr int kStageBytes = 32 * 1024;
+constexpr int kGemvCtaThreads = kGemvThreads + 32;  // 8 consumer warps + 1 producer warp
+
+struct GemvSmem {
+  int x_bytes, ring_off, stage_bytes, part_off, accs_off, scratch_off, bar_off, flag_off, total;
+};
+
+__host__ __device__ inline GemvSmem gemv_smem_layout(int NB, int SR, int K, int nstage, int max_rows) {
+  GemvSmem L;
+  L.x_bytes = NB * K * 4;
+  L.stage_bytes = SR * K * 2;
+  L.ring_off = L.x_bytes;
+  L.part_off = L.ring_off + nstage * L.stage_bytes;
+  L.accs_off = L.part_off + max_rows * kGemvWarps * NB * 4;
+  L.scratch_off = L.accs_off + max_rows * NB * 4;
+  L.bar_off = (L.scratch_off + 2 * kGemvWarps * 4 + 15) / 16 * 16;
+  L.flag_off = L.bar_off + 2 * nstage * 8;
+  L.total = L.flag_off + 16;
+  return L;
+}
+
+template <int NB, int SR, int MODE>
+__global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int KV = p.K >> 3;
-  const int ngroups = (p.rows + R - 1) / R;
-  const int g_begin = (int)((long long)blockIdx.x * ngroups / gridDim.x);
-  const int g_end = (int)((long long)(blockIdx.x + 1) * ngroups / gridDim.x);
-  constexpr int TILE_KV = kGemvThreads * U;
-  const int n_kc = (KV + TILE_KV - 1) / TILE_KV;
-  const int ntiles = (g_end - g_begin) * n_kc;
-  const int row0 = g_begin * R;
-  const int nrows = min(g_end * R, p.rows) - row0;
+  const int K = p.K, KV = K >> 3;
+  const int npairs = p.rows >> 1;
+  const int pb = (int)((long long)blockIdx.x * npairs / gridDim.x);
+  const int pe = (int)((long long)(blockIdx.x + 1) * npairs / gridDim.x);
+  const int row0 = 2 * pb, nrows = 2 * (pe - pb);
+  const int max_rows = 2 * ((npairs + gridDim.x - 1) / gridDim.x);
+  const int nst = p.nstage;
+  const GemvSmem L = gemv_smem_layout(NB, SR, K, nst, max_rows);
+  const int n_stages = (nrows + SR - 1) / SR;
 
   float4 *xs = reinterpret_cast<float4 *>(smem);
-  float *red = reinterpret_cast<float *>(xs + (size_t)NB * 2 * KV);  // [2][warps][R * NB]
-  float *scratch = red + 2 * kGemvWarps * R * NB;                     // [2 * warps]
-  float *accs = scratch + 2 * kGemvWarps;                             // [nrows][NB]
+  unsigned char *ring = smem + L.ring_off;
+  float *part = reinterpret_cast<float *>(smem + L.part_off);     // [max_rows][warps][NB]
+  float *accs = reinterpret_cast<float *>(smem + L.accs_off);     // [max_rows][NB]
+  float *scratch = reinterpret_cast<float *>(smem + L.scratch_off);
+  const uint32_t full0 = smem_addr(smem + L.bar_off);
+  const uint32_t empty0 = full0 + 8 * nst;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
 
-  auto load_tile = [&](int t, uint4 (&buf)[R][U]) {
-    const int g = g_begin + t / n_kc, kc = t - (t / n_kc) * n_kc;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int lrow = g * R + r;
-      const bool rv = lrow < p.rows;
-      const uint16_t *wp = row_ptr<MODE>(p, p.row_base + (rv ? lrow : 0));
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int kv = kc * TILE_KV + u * kGemvThreads + tid;
-        if (rv && kv < KV)
-          buf[r][u] = ldg_stream(wp + (size_t)kv * 8);
-        else
-          buf[r][u] = make_uint4(0u, 0u, 0u, 0u);
-      }
+  if (tid == 0) {
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, kGemvWarps);
     }
-  };
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  pdl_trigger();
 
-  float acc[R][NB];
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int m = 0; m < NB; ++m) acc[r][m] = 0.f;
-  int parity = 0;
+  if (warp == kGemvWarps) {
+    // ------------------------------------------------------------ producer warp
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      const uint32_t row_bytes = (uint32_t)K * 2u;
+      int issued = 0;
+      for (int st = 0; st < n_stages; ++st) {
+        const int slot = st % nst;
+        if (st >= nst && !mbar_wait(empty0 + 8 * slot, ((st / nst) - 1) & 1, abort_flag, p.status))
+          break;
+        const int rows_here = min(SR, nrows - st * SR);
+        mbar_expect_tx(full0 + 8 * slot, (uint32_t)rows_here * row_bytes);
+        const uint32_t dst = smem_addr(ring + (size_t)slot * L.stage_bytes);
+        for (int r = 0; r < rows_here; ++r)
+          bulk_g2s(dst + r * row_bytes, row_ptr<MODE>(p, p.row_base + row0 + st * SR + r), row_bytes,
+                   full0 + 8 * slot, pol);
+        issued = st + 1;
+      }
+      // Never leave copies in flight into shared memory: wait for the last stages issued.
+      for (int st = max(0, issued - nst); st < issued; ++st)
+        mbar_wait(full0 + 8 * (st % nst), (st / nst) & 1, abort_flag, p.status);
+    }
+    return;
+  }
 
-  auto compute_tile = [&](int t, const uint4 (&buf)[R][U]) {
-    const int gi = t / n_kc, kc = t - gi * n_kc;
+  // ------------------------------------------------------------ consumer warps
+  pdl_wait();
+  stage_x<NB, MODE>(p, xs, scratch);
+  consumer_sync();
+
+  for (int st = 0; st < n_stages; ++st) {
+    const int slot = st % nst;
+    const bool ok = mbar_wait(full0 + 8 * slot, (st / nst) & 1, abort_flag, p.status);
+    float acc[SR][NB];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int kv = kc * TILE_KV + u * kGemvThreads + tid;
-      if (kv < KV) {
-        float wf[R][8];
+    for (int r = 0; r < SR; ++r)
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const uint4 w = buf[r][u];
-          wf[r][0] = bf_lo(w.x); wf[r][1] = bf_hi(w.x);
-          wf[r][2] = bf_lo(w.y); wf[r][3] = bf_hi(w.y);
-          wf[r][4] = bf_lo(w.z); wf[r][5] = bf_hi(w.z);
-          wf[r][6] = bf_lo(w.w); wf[r][7] = bf_hi(w.w);
-        }
+      for (int m = 0; m < NB; ++m) acc[r][m] = 0.f;
+    if (ok) {
+      const unsigned char *stage = ring + (size_t)slot * L.stage_bytes;
+      const int rows_here = min(SR, nrows - st * SR);
+      for (int kv = warp * 32 + lane; kv < KV; kv += kGemvThreads) {
+        float4 xa[NB], xb[NB];
 #pragma unroll
         for (int m = 0; m < NB; ++m) {
-          const float4 a = xs[(size_t)(m * 2) * KV + kv];
-          const float4 b = xs[(size_t)(m * 2 + 1) * KV + kv];
+          xa[m] = xs[(size_t)(m * 2) * KV + kv];
+          xb[m] = xs[(size_t)(m * 2 + 1) * KV + kv];
+        }
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            float s = acc[r][m];
-            s = fmaf(wf[r][0], a.x, s); s = fmaf(wf[r][1], a.y, s);
-            s = fmaf(wf[r][2], a.z, s); s = fmaf(wf[r][3], a.w, s);
-            s = fmaf(wf[r][4], b.x, s); s = fmaf(wf[r][5], b.y, s);
-            s = fmaf(wf[r][6], b.z, s); s = fmaf(wf[r][7], b.w, s);
-            acc[r][m] = s;
+        for (int r = 0; r < SR; ++r) {
+          if (r < rows_here) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(stage + ((size_t)r * K + (size_t)kv * 8) * 2);
+            const float w0 = bf_lo(w.x), w1 = bf_hi(w.x), w2 = bf_lo(w.y), w3 = bf_hi(w.y);
+            const float w4 = bf_lo(w.z), w5 = bf_hi(w.z), w6 = bf_lo(w.w), w7 = bf_hi(w.w);
+#pragma unroll
+            for (int m = 0; m < NB; ++m) {
+              float a = acc[r][m];
+              a = fmaf(w0, xa[m].x, a); a = fmaf(w1, xa[m].y, a);
+              a = fmaf(w2, xa[m].z, a); a = fmaf(w3, xa[m].w, a);
+              a = fmaf(w4, xb[m].x, a); a = fmaf(w5, xb[m].y, a);
+              a = fmaf(w6, xb[m].z, a); a = fmaf(w7, xb[m].w, a);
+              acc[r][m] = a;
+            }
           }
         }
       }
     }
-    if (kc == n_kc - 1) {
-      constexpr int N = R * NB;
-      float v[N];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+    // per-warp partial of every (row, item) of this stage
+    constexpr int N = SR * NB;
+    float v[N];
 #pragma unroll
-      for (int r = 0; r < R; ++r)
+    for (int r = 0; r < SR; ++r)
 #pragma unroll
-        for (int m = 0; m < NB; ++m) {
-          v[r * NB + m] = acc[r][m];
-          acc[r][m] = 0.f;
-        }
-      const float tot = warp_reduce_multi<N>(v, lane);
-      float *rb = red + parity * kGemvWarps * N;
-      if (warp_reduce_writer<N>(lane)) rb[warp * N + warp_reduce_index<N>(lane)] = tot;
-      __syncthreads();
-      if (tid < N) {
-        float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < kGemvWarps; ++w) s += rb[w * N + tid];
-        const int r = tid / NB, m = tid - r * NB;
-        const int lrow = gi * R + r;  // relative to row0
-        if (lrow < nrows) accs[lrow * NB + m] = s;
-      }
-      parity ^= 1;
-    }
-  };
-
-  // Pre-dependency part: only weights are touched.
-  uint4 wa[R][U], wb[R][U];
-  if (ntiles > 0) load_tile(0, wa);
-  {
-    // Ask L2 for the next rows of this CTA as well.
-    const int pf_rows = min(nrows, 2 * R);
-    for (int r = 1 + warp; r < pf_rows; r += kGemvWarps) {
-      if (lane == 0) {
-        const uint16_t *wp = row_ptr<MODE>(p, p.row_base + row0 + r);
-        const uint32_t bytes = (uint32_t)p.K * 2u;
-        for (uint32_t off = 0; off < bytes; off += 32768u)
-          prefetch_l2(reinterpret_cast<const char *>(wp) + off, min(32768u, bytes - off));
-      }
+      for (int m = 0; m < NB; ++m) v[r * NB + m] = acc[r][m];
+    const float tot = warp_reduce_multi<N>(v, lane);
+    if (warp_reduce_writer<N>(lane)) {
+      const int idx = warp_reduce_index<N>(lane);
+      const int r = idx / NB, m = idx - r * NB;
+      const int lrow = st * SR + r;
+      if (lrow < nrows) part[((size_t)lrow * kGemvWarps + warp) * NB + m] = tot;
     }
   }
-  pdl_trigger();
-  pdl_wait();
-
-  stage_x<NB, MODE>(p, xs, scratch);
-  __syncthreads();
-
-  for (int t = 0; t < ntiles; t += 2) {
-    if (t + 1 < ntiles) load_tile(t + 1, wb);
-    compute_tile(t, wa);
-    if (t + 1 < ntiles) {
-      if (t + 2 < ntiles) load_tile(t + 2, wa);
-      compute_tile(t + 1, wb);
-    }
+  consumer_sync();
+  for (int e = tid; e < nrows * NB; e += kGemvThreads) {
+    const int r = e / NB, m = e - r * NB;
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kGemvWarps; ++w) sum += part[((size_t)r * kGemvWarps + w) * NB + m];
+    accs[e] = sum;
   }
-  __syncthreads();
+  consumer_sync();
   epilogue<NB, MODE>(p, accs, row0, nrows);
 }
 
 // ------------------------------------------------------------------ launcher
-template <int NB, int R, int U, int MODE>
-static cudaError_t launch_one(const GemvParams &p, int grid, cudaStream_t st, bool pdl) {
-  const int ngroups = (p.rows + R - 1) / R;
-  if (grid > ngroups) grid = ngroups;
+static int stage_rows(int K) {
+  int sr = kStageBytes / (2 * K);
+  if (sr < 1) sr = 1;
+  if (sr > 8) sr = 8;
+  int p2 = 1;
+  while (p2 * 2 <= sr) p2 *= 2;
+  return p2;
+}
+
+template <int NB, int SR, int MODE>
+static cudaError_t launch_one(GemvParams p, int grid, cudaStream_t st, bool pdl) {
+  const int npairs = p.rows / 2;
+  if (grid > npairs) grid = npairs;
   if (grid < 1) grid = 1;
-  const int max_rows = ((ngroups + grid - 1) / grid) * R;
-  const size_t smem = (size_t)NB * p.K * 4 + (size_t)2 * kGemvWarps * R * NB * 4 +
-                      (size_t)2 * kGemvWarps * 4 + (size_t)max_rows * NB * 4;
-  if (smem > kGemvSmemLimit) return cudaErrorInvalidValue;
+  const int max_rows = 2 * ((npairs + grid - 1) / grid);
+  const GemvSmem L0 = gemv_smem_layout(NB, SR, p.K, 0, max_rows);
+  const long long room = (long long)kGemvSmemLimit - L0.total - 64;
+  int nst = (int)(room / (SR * p.K * 2 + 16));
+  if (nst > 8) nst = 8;
+  if (nst < 2) return cudaErrorInvalidValue;
+  p.nstage = nst;
+  const GemvSmem L = gemv_smem_layout(NB, SR, p.K, nst, max_rows);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kGemvThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.blockDim = dim3(kGemvCtaThreads);
+  cfg.dynamicSmemBytes = (size_t)L.total;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, R, U, MODE>, p);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, SR, MODE>, p);
+}
+
+template <int NB, int MODE>
+static cudaError_t dispatch_sr(const GemvParams &p, int grid, cudaStream_t st, bool pdl) {
+  switch (stage_rows(p.K)) {
+    case 1: return launch_one<NB, 1, MODE>(p, grid, st, pdl);
+    case 2: return launch_one<NB, 2, MODE>(p, grid, st, pdl);
+    case 4: return launch_one<NB, 4, MODE>(p, grid, st, pdl);
+    default: return launch_one<NB, 8, MODE>(p, grid, st, pdl);
+  }
 }
 
 template <int MODE>
 static cudaError_t dispatch_nb(const GemvParams &p, int nb, int grid, cudaStream_t st, bool pdl) {
   switch (nb) {
-    case 1: return launch_one<1, 4, 2, MODE>(p, grid, st, pdl);
-    case 2: return launch_one<2, 4, 2, MODE>(p, grid, st, pdl);
-    case 4: return launch_one<4, 2, 2, MODE>(p, grid, st, pdl);
-    case 8: return launch_one<8, 2, 2, MODE>(p, grid, st, pdl);
+    case 1: return dispatch_sr<1, MODE>(p, grid, st, pdl);
+    case 2: return dispatch_sr<2, MODE>(p, grid, st, pdl);
+    case 4: return dispatch_sr<4, MODE>(p, grid, st, pdl);
+    case 8: return dispatch_sr<8, MODE>(p, grid, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <int NB, int R, int U, int MODE>
-static cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(gemv_kernel<NB, R, U, MODE>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmemLimit);
+template <int NB, int MODE>
+static cudaError_t prepare_nb() {
+  cudaError_t e = cudaSuccess;
+  const int lim = (int)kGemvSmemLimit;
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<NB, 1, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<NB, 2, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<NB, 4, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<NB, 8, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  return e;
 }
 
 template <int MODE>
 static cudaError_t prepare_mode() {
-  cudaError_t e = prepare_one<1, 4, 2, MODE>();
-  if (e == cudaSuccess) e = prepare_one<2, 4, 2, MODE>();
-  if (e == cudaSuccess) e = prepare_one<4, 2, 2, MODE>();
-  if (e == cudaSuccess) e = prepare_one<8, 2, 2, MODE>();
+  cudaError_t e = prepare_nb<1, MODE>();
+  if (e == cudaSuccess) e = prepare_nb<2, MODE>();
+  if (e == cudaSuccess) e = prepare_nb<4, MODE>();
+  if (e == cudaSuccess) e = prepare_nb<8, MODE>();
   return e;
 }
 

@@ -11,9 +11,9 @@ namespace e3 {
 
 // Largest float32 activation block (items * K * 4 bytes) one GEMV launch keeps in
 // shared memory.
-constexpr size_t kGemvMaxXBytes = 96 * 1024;
-// Dynamic shared memory ceiling of a GEMV CTA (x + reduction buffers + row sums).
-constexpr size_t kGemvSmemLimit = 200 * 1024;
+constexpr size_t kGemvMaxXBytes = 128 * 1024;
+// Dynamic shared memory ceiling of a GEMV CTA (x + weight ring + row sums + barriers).
+constexpr size_t kGemvSmemLimit = 224 * 1024;
 
 cudaError_t gemv_prepare();
 int gemv_items_per_launch(int K, int items);

@@ -63,6 +63,7 @@ typedef struct CUstream_st *eagle3_stream_t;
 #define EAGLE3_DEV_BAD_PAGE 2       /* page id outside [0, num_pages) */
 #define EAGLE3_DEV_BAD_POSITION 4   /* KV position outside [0, max_cache_len) */
 #define EAGLE3_DEV_BAD_LENGTH 8     /* kv_len or prompt length out of range */
+#define EAGLE3_DEV_TIMEOUT 16       /* a bounded on-chip wait gave up (the kernel returned) */
 
 /* eagle3_draft_chain flags. */
 #define EAGLE3_SHRINK_GAMMA 1u      /* shrink gamma per sequence to max_cache_len - kv_len - 1 */
