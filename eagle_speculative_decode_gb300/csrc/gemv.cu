@@ -57,6 +57,7 @@ struct Log2 {
 // lanes whose low (5-S) bits are zero are the designated writers.
 template <int N>
 __device__ __forceinline__ float warp_reduce_multi(float (&v)[N], int lane) {
+  static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "1..32 values, a power of two");
 #pragma unroll
   for (int cnt = N, o = 16; cnt > 1; cnt >>= 1, o >>= 1) {
     const bool upper = (lane & o) != 0;
@@ -486,10 +487,13 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
 }
 
 // ------------------------------------------------------------------ launcher
-static int stage_rows(int K) {
+// Rows per ring stage: whole rows up to kStageBytes, at most 8, and at most 32 / NB so
+// that a stage's (row, item) sums fit one warp reduction.
+static int stage_rows(int K, int NB) {
   int sr = kStageBytes / (2 * K);
   if (sr < 1) sr = 1;
   if (sr > 8) sr = 8;
+  if (sr > 32 / NB) sr = 32 / NB;
   int p2 = 1;
   while (p2 * 2 <= sr) p2 *= 2;
   return p2;
@@ -523,11 +527,11 @@ static cudaError_t launch_one(GemvParams p, int grid, cudaStream_t st, bool pdl)
 
 template <int NB, int MODE>
 static cudaError_t dispatch_sr(const GemvParams &p, int grid, cudaStream_t st, bool pdl) {
-  switch (stage_rows(p.K)) {
+  switch (stage_rows(p.K, NB)) {
     case 1: return launch_one<NB, 1, MODE>(p, grid, st, pdl);
     case 2: return launch_one<NB, 2, MODE>(p, grid, st, pdl);
     case 4: return launch_one<NB, 4, MODE>(p, grid, st, pdl);
-    default: return launch_one<NB, 8, MODE>(p, grid, st, pdl);
+    default: return launch_one<NB, (NB <= 4 ? 8 : 4), MODE>(p, grid, st, pdl);
   }
 }
 
@@ -549,7 +553,8 @@ static cudaError_t prepare_nb() {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<NB, 1, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<NB, 2, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<NB, 4, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<NB, 8, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (NB <= 4 && e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemv_kernel<NB, (NB <= 4 ? 8 : 4), MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
   return e;
 }
 
