@@ -18,6 +18,7 @@
 namespace e3 {
 
 constexpr int kAttnWarps = 4;
+constexpr int kMaxAttnSplits = 64;
 constexpr int kAttnThreads = kAttnWarps * 32;
 
 template <int D, int G>
@@ -178,20 +179,54 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
   __syncthreads();
   if (!last_sh) return;
   __threadfence();
+  // Merge the splits: weights w[q][g] = exp2(m_q - M_g) / L_g first (all splits loaded in
+  // parallel), then every thread sums float4 slices over the splits with independent loads.
+  __shared__ float2 ml_all[kMaxAttnSplits][G];
+  __shared__ float wsm[kMaxAttnSplits][G];
+  __shared__ float2 ML[G];
   const size_t slot0 = ((size_t)b * Hkv + kvh) * p.splits;
-  for (int e = tid; e < G * D; e += kAttnThreads) {
-    const int g = e / D, dim = e - g * D;
+  for (int i = tid; i < p.splits * G; i += kAttnThreads)
+    ml_all[i / G][i % G] = __ldcg(&p.part_ml[slot0 * G + i]);
+  __syncthreads();
+  if (tid < G) {
     float M = -INFINITY;
-    for (int q = 0; q < p.splits; ++q) M = fmaxf(M, __ldcg(&p.part_ml[(slot0 + q) * G + g]).x);
-    float Ls = 0.f, O = 0.f;
-    for (int q = 0; q < p.splits; ++q) {
-      const float2 ml = __ldcg(&p.part_ml[(slot0 + q) * G + g]);
-      if (ml.x == -INFINITY) continue;
-      const float w = exp2f(ml.x - M);
-      Ls += ml.y * w;
-      O += __ldcg(&p.part_o[((slot0 + q) * G + g) * D + dim]) * w;
+    for (int q = 0; q < p.splits; ++q) M = fmaxf(M, ml_all[q][tid].x);
+    float Ls = 0.f;
+    for (int q = 0; q < p.splits; ++q)
+      if (ml_all[q][tid].x != -INFINITY) Ls += ml_all[q][tid].y * exp2f(ml_all[q][tid].x - M);
+    ML[tid] = make_float2(M, 1.0f / Ls);
+  }
+  __syncthreads();
+  for (int i = tid; i < p.splits * G; i += kAttnThreads) {
+    const int q = i / G, g = i % G;
+    const float2 ml = ml_all[q][g];
+    wsm[q][g] = ml.x == -INFINITY ? 0.f : exp2f(ml.x - ML[g].x) * ML[g].y;
+  }
+  __syncthreads();
+  const float4 *po = reinterpret_cast<const float4 *>(p.part_o) + slot0 * (G * D / 4);
+  float4 *out4 = reinterpret_cast<float4 *>(p.out + (size_t)b * H * D + (size_t)kvh * G * D);
+  for (int f = tid; f < G * D / 4; f += kAttnThreads) {
+    const int g = (f * 4) / D;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    int q = 0;
+    for (; q + 4 <= p.splits; q += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcg(po + (size_t)(q + u) * (G * D / 4) + f);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float w = wsm[q + u][g];
+        o.x = fmaf(w, v[u].x, o.x); o.y = fmaf(w, v[u].y, o.y);
+        o.z = fmaf(w, v[u].z, o.z); o.w = fmaf(w, v[u].w, o.w);
+      }
     }
-    p.out[(size_t)b * H * D + (size_t)(kvh * G + g) * D + dim] = O / Ls;
+    for (; q < p.splits; ++q) {
+      const float4 v = __ldcg(po + (size_t)q * (G * D / 4) + f);
+      const float w = wsm[q][g];
+      o.x = fmaf(w, v.x, o.x); o.y = fmaf(w, v.y, o.y);
+      o.z = fmaf(w, v.z, o.z); o.w = fmaf(w, v.w, o.w);
+    }
+    out4[f] = o;
   }
   if (tid == 0) p.count[(size_t)b * Hkv + kvh] = 0u;
 }

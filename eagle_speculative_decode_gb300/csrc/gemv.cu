@@ -336,6 +336,9 @@ __device__ void epilogue(const GemvParams &p, const float *accs, int row0, int n
 
 // -------------------------------------------------------------------- kernel
 constexpr int kStageBytes = 32 * 1024;
+// Single-item launches with K <= 6 * 256 * 8 = 12288 keep x in registers: 6 vectors of 8
+// floats per thread (larger K reads x from shared memory).
+constexpr int kXRegVecs = 6;
 constexpr int kGemvCtaThreads = kGemvThreads + 32;  // 8 consumer warps + 1 producer warp
 
 struct GemvSmem {
@@ -361,11 +364,13 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.K, KV = K >> 3;
-  const int npairs = p.rows >> 1;
-  const int pb = (int)((long long)blockIdx.x * npairs / gridDim.x);
-  const int pe = (int)((long long)(blockIdx.x + 1) * npairs / gridDim.x);
-  const int row0 = 2 * pb, nrows = 2 * (pe - pb);
-  const int max_rows = 2 * ((npairs + gridDim.x - 1) / gridDim.x);
+  // rows are handed out in units of 2 where the epilogue pairs rows (RoPE, SwiGLU)
+  constexpr int UNIT = (MODE == GM_QKV || MODE == GM_GATEUP) ? 2 : 1;
+  const int nunits = p.rows / UNIT;
+  const int ub = (int)((long long)blockIdx.x * nunits / gridDim.x);
+  const int ue = (int)((long long)(blockIdx.x + 1) * nunits / gridDim.x);
+  const int row0 = UNIT * ub, nrows = UNIT * (ue - ub);
+  const int max_rows = UNIT * ((nunits + gridDim.x - 1) / gridDim.x);
   const int nst = p.nstage;
   const GemvSmem L = gemv_smem_layout(NB, SR, K, nst, max_rows);
   const int n_stages = (nrows + SR - 1) / SR;
@@ -419,6 +424,18 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
   pdl_wait();
   stage_x<NB, MODE>(p, xs, scratch);
   consumer_sync();
+  float xr[NB == 1 ? kXRegVecs : 1][8];
+  const bool xreg = (NB == 1) && (KV <= kXRegVecs * kGemvThreads);
+  if (xreg) {
+#pragma unroll
+    for (int j = 0; j < (NB == 1 ? kXRegVecs : 0); ++j) {
+      const int kv = tid + j * kGemvThreads;
+      const float4 a = kv < KV ? xs[kv] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 c = kv < KV ? xs[KV + kv] : make_float4(0.f, 0.f, 0.f, 0.f);
+      xr[j][0] = a.x; xr[j][1] = a.y; xr[j][2] = a.z; xr[j][3] = a.w;
+      xr[j][4] = c.x; xr[j][5] = c.y; xr[j][6] = c.z; xr[j][7] = c.w;
+    }
+  }
 
   for (int st = 0; st < n_stages; ++st) {
     const int slot = st % nst;
@@ -431,27 +448,49 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
     if (ok) {
       const unsigned char *stage = ring + (size_t)slot * L.stage_bytes;
       const int rows_here = min(SR, nrows - st * SR);
-      for (int kv = warp * 32 + lane; kv < KV; kv += kGemvThreads) {
-        float4 xa[NB], xb[NB];
+      if (xreg) {
+        // x of this thread's vectors is held in registers across all stages
 #pragma unroll
-        for (int m = 0; m < NB; ++m) {
-          xa[m] = xs[(size_t)(m * 2) * KV + kv];
-          xb[m] = xs[(size_t)(m * 2 + 1) * KV + kv];
+        for (int j = 0; j < (NB == 1 ? kXRegVecs : 0); ++j) {
+          const int kv = tid + j * kGemvThreads;
+          if (kv < KV) {
+#pragma unroll
+            for (int r = 0; r < SR; ++r) {
+              if (r < rows_here) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(stage + ((size_t)r * K + (size_t)kv * 8) * 2);
+                float a = acc[r][0];
+                a = fmaf(bf_lo(w.x), xr[j][0], a); a = fmaf(bf_hi(w.x), xr[j][1], a);
+                a = fmaf(bf_lo(w.y), xr[j][2], a); a = fmaf(bf_hi(w.y), xr[j][3], a);
+                a = fmaf(bf_lo(w.z), xr[j][4], a); a = fmaf(bf_hi(w.z), xr[j][5], a);
+                a = fmaf(bf_lo(w.w), xr[j][6], a); a = fmaf(bf_hi(w.w), xr[j][7], a);
+                acc[r][0] = a;
+              }
+            }
+          }
         }
+      } else {
+        for (int kv = tid; kv < KV; kv += kGemvThreads) {
+          float4 xa[NB], xb[NB];
 #pragma unroll
-        for (int r = 0; r < SR; ++r) {
-          if (r < rows_here) {
-            const uint4 w = *reinterpret_cast<const uint4 *>(stage + ((size_t)r * K + (size_t)kv * 8) * 2);
-            const float w0 = bf_lo(w.x), w1 = bf_hi(w.x), w2 = bf_lo(w.y), w3 = bf_hi(w.y);
-            const float w4 = bf_lo(w.z), w5 = bf_hi(w.z), w6 = bf_lo(w.w), w7 = bf_hi(w.w);
+          for (int m = 0; m < NB; ++m) {
+            xa[m] = xs[(size_t)(m * 2) * KV + kv];
+            xb[m] = xs[(size_t)(m * 2 + 1) * KV + kv];
+          }
 #pragma unroll
-            for (int m = 0; m < NB; ++m) {
-              float a = acc[r][m];
-              a = fmaf(w0, xa[m].x, a); a = fmaf(w1, xa[m].y, a);
-              a = fmaf(w2, xa[m].z, a); a = fmaf(w3, xa[m].w, a);
-              a = fmaf(w4, xb[m].x, a); a = fmaf(w5, xb[m].y, a);
-              a = fmaf(w6, xb[m].z, a); a = fmaf(w7, xb[m].w, a);
-              acc[r][m] = a;
+          for (int r = 0; r < SR; ++r) {
+            if (r < rows_here) {
+              const uint4 w = *reinterpret_cast<const uint4 *>(stage + ((size_t)r * K + (size_t)kv * 8) * 2);
+              const float w0 = bf_lo(w.x), w1 = bf_hi(w.x), w2 = bf_lo(w.y), w3 = bf_hi(w.y);
+              const float w4 = bf_lo(w.z), w5 = bf_hi(w.z), w6 = bf_lo(w.w), w7 = bf_hi(w.w);
+#pragma unroll
+              for (int m = 0; m < NB; ++m) {
+                float a = acc[r][m];
+                a = fmaf(w0, xa[m].x, a); a = fmaf(w1, xa[m].y, a);
+                a = fmaf(w2, xa[m].z, a); a = fmaf(w3, xa[m].w, a);
+                a = fmaf(w4, xb[m].x, a); a = fmaf(w5, xb[m].y, a);
+                a = fmaf(w6, xb[m].z, a); a = fmaf(w7, xb[m].w, a);
+                acc[r][m] = a;
+              }
             }
           }
         }
@@ -501,10 +540,11 @@ static int stage_rows(int K, int NB) {
 
 template <int NB, int SR, int MODE>
 static cudaError_t launch_one(GemvParams p, int grid, cudaStream_t st, bool pdl) {
-  const int npairs = p.rows / 2;
-  if (grid > npairs) grid = npairs;
+  constexpr int UNIT = (MODE == GM_QKV || MODE == GM_GATEUP) ? 2 : 1;
+  const int nunits = p.rows / UNIT;
+  if (grid > nunits) grid = nunits;
   if (grid < 1) grid = 1;
-  const int max_rows = 2 * ((npairs + grid - 1) / grid);
+  const int max_rows = UNIT * ((nunits + grid - 1) / grid);
   const GemvSmem L0 = gemv_smem_layout(NB, SR, p.K, 0, max_rows);
   const long long room = (long long)kGemvSmemLimit - L0.total - 64;
   int nst = (int)(room / (SR * p.K * 2 + 16));
