@@ -212,7 +212,7 @@ cudaError_t launched(eagle3_ctx *ctx, cudaStream_t st, cudaError_t e, int label)
 
 // Launch a GEMV over `items` activation rows in as many launches as shared memory needs.
 cudaError_t gemv_items(eagle3_ctx *ctx, GemvParams p, int items, cudaStream_t st, bool pdl) {
-  const int nb = gemv_items_per_launch(p.K, items);
+  const int nb = gemv_items_per_launch(p.mode, p.K, items);
   const int label = (p.mode == GM_QKV && p.row_base > 0) ? PH_KV : gemv_label(p.mode);
   for (int i0 = 0; i0 < items; i0 += nb) {
     p.item0 = i0;
@@ -251,14 +251,14 @@ void kv_only_params(const eagle3_ctx *ctx, const eagle3_kv *kv, GemvParams &p) {
 }
 
 // Splits of the attention key range: about four CTAs per SM over all (sequence, kv head)
-// pairs, at least ~32 keys per split (rounded to a power of two so that a growing
+// pairs, at least ~64 keys per split (rounded to a power of two so that a growing
 // context re-captures the chain graph rarely).
 int choose_splits(const eagle3_ctx *ctx, int B, int max_len) {
   const int per = B * ctx->c.n_head_kv;
   int s = std::max(1, (4 * ctx->num_sms + per - 1) / per);
   s = std::min(s, kMaxSplits);
   s = std::min(s, std::max(1, kSplitSlots / per));
-  const int by_len = std::max(1, (max_len + 31) / 32);
+  const int by_len = std::max(1, (max_len + 63) / 64);
   int p2 = 1;
   while (p2 * 2 <= by_len) p2 *= 2;
   return std::max(1, std::min(s, p2));

@@ -209,12 +209,12 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
     const int g = (f * 4) / D;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     int q = 0;
-    for (; q + 4 <= p.splits; q += 4) {
-      float4 v[4];
+    for (; q + 8 <= p.splits; q += 8) {
+      float4 v[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __ldcg(po + (size_t)(q + u) * (G * D / 4) + f);
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(po + (size_t)(q + u) * (G * D / 4) + f);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const float w = wsm[q + u][g];
         o.x = fmaf(w, v[u].x, o.x); o.y = fmaf(w, v[u].y, o.y);
         o.z = fmaf(w, v[u].z, o.z); o.w = fmaf(w, v[u].w, o.w);

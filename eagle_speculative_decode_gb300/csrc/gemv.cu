@@ -12,11 +12,15 @@
 // mbarriers.  It starts before the kernel waits on its predecessor (programmatic
 // dependent launch), so the next weights are already in flight while the previous
 // kernel drains.  Eight consumer warps stage x (normalised where the op says so) in
-// shared memory as float32 in two float4 planes (elements 0-3 and 4-7 of each 8-element
-// vector: conflict-free LDS.128), then, per stage, each thread takes 16-byte vectors
-// k = 8 * (warp * 32 + lane + 256 j) of all SR rows, so every x vector it loads serves
-// SR rows.  A stage's per-row sums are reduced within the warp and kept per warp; the
-// eight warp partials are added in a fixed order before the epilogue (deterministic).
+// shared memory (float32 in two float4 planes -- elements 0-3 and 4-7 of each 8-element
+// vector, conflict-free LDS.128 -- or as the caller's bf16 for the encode), then, per
+// stage, each thread takes 16-byte vectors k = 8 * (tid + 256 j) of all SR rows, so every
+// x vector it loads serves SR rows; single-item launches keep their x vectors in
+// registers.  RMSNorm is applied after the dot product: the GEMV runs on x * w_norm and
+// the per-item scale 1 / sqrt(mean(x^2) + eps), reduced while x is staged, multiplies the
+// row sums, so no block-wide reduction stands between the dependency wait and the first
+// FMA.  A stage's per-row sums are reduced within the warp and kept per warp; the eight
+// warp partials are added in a fixed order before the epilogue (deterministic).
 #include <math.h>
 
 #include "common.cuh"
@@ -87,29 +91,44 @@ __device__ __forceinline__ bool warp_reduce_writer(int lane) {
   return (lane & ((1 << (5 - Log2<N>::value)) - 1)) == 0;
 }
 
-// Block-wide sum of one float per thread; result valid in every thread.
-__device__ __forceinline__ float block_sum(float v, float *scratch) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  consumer_sync();
-  if (lane == 0) scratch[warp] = v;
-  consumer_sync();
-  float t = 0.f;
-#pragma unroll
-  for (int w = 0; w < kGemvWarps; ++w) t += scratch[w];
-  return t;
+// ------------------------------------------------------------------ x staging
+template <int MODE>
+struct ModeTraits {
+  static constexpr bool kBf16X = MODE == GM_ENCODE;  // x kept as the caller's bf16
+  static constexpr int kHalves = MODE == GM_QKV ? 2 : 1;  // separately normalised K halves
+  static constexpr bool kNorm = MODE == GM_QKV || MODE == GM_GATEUP || MODE == GM_LMHEAD;
+  static constexpr int kUnit = (MODE == GM_QKV || MODE == GM_GATEUP) ? 2 : 1;  // row pairing
+};
+
+__device__ __forceinline__ float sq8(float4 a, float4 b) {
+  return a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z +
+         b.w * b.w;
+}
+__device__ __forceinline__ float4 mul4(float4 a, float w0, float w1, float w2, float w3) {
+  return make_float4(a.x * w0, a.y * w1, a.z * w2, a.w * w3);
 }
 
-// ------------------------------------------------------------------ x staging
-// Writes x[m, k] into the two float4 planes xs[(m * 2 + plane) * KV + kv].
+// Writes x[m, k] (times the norm gain where the op normalises) into shared memory and
+// accumulates this thread's share of sum(x^2) per item and K half into ss.
 template <int NB, int MODE>
-__device__ void stage_x(const GemvParams &p, float4 *xs, float *scratch) {
+__device__ void stage_x(const GemvParams &p, unsigned char *xmem, float (&ss)[NB][ModeTraits<MODE>::kHalves]) {
+  using T = ModeTraits<MODE>;
   const int K = p.K, KV = K >> 3, tid = threadIdx.x;
+#pragma unroll
+  for (int m = 0; m < NB; ++m)
+#pragma unroll
+    for (int h = 0; h < T::kHalves; ++h) ss[m][h] = 0.f;
   for (int m = 0; m < NB; ++m) {
-    float4 *x0 = xs + (size_t)(m * 2) * KV;
-    float4 *x1 = x0 + KV;
     const bool live = m < p.items;
+    const int item = p.item0 + m;
+    if constexpr (T::kBf16X) {
+      uint4 *xb = reinterpret_cast<uint4 *>(xmem) + (size_t)m * KV;
+      const uint4 *src = reinterpret_cast<const uint4 *>(p.xb + (size_t)item * K);
+      for (int kv = tid; kv < KV; kv += kGemvThreads) xb[kv] = live ? src[kv] : make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    float4 *x0 = reinterpret_cast<float4 *>(xmem) + (size_t)(m * 2) * KV;
+    float4 *x1 = x0 + KV;
     if (!live) {
       for (int kv = tid; kv < KV; kv += kGemvThreads) {
         x0[kv] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -117,42 +136,24 @@ __device__ void stage_x(const GemvParams &p, float4 *xs, float *scratch) {
       }
       continue;
     }
-    const int item = p.item0 + m;
-    if constexpr (MODE == GM_ENCODE) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(p.xb + (size_t)item * K);
-      for (int kv = tid; kv < KV; kv += kGemvThreads) {
-        const uint4 u = src[kv];
-        x0[kv] = make_float4(bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y));
-        x1[kv] = make_float4(bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w));
-      }
-    } else if constexpr (MODE == GM_O || MODE == GM_DOWN) {
+    if constexpr (MODE == GM_O || MODE == GM_DOWN) {
       const float4 *src = reinterpret_cast<const float4 *>(p.xf + (size_t)item * K);
       for (int kv = tid; kv < KV; kv += kGemvThreads) {
         x0[kv] = src[2 * kv];
         x1[kv] = src[2 * kv + 1];
       }
     } else if constexpr (MODE == GM_GATEUP || MODE == GM_LMHEAD) {
-      // RMSNorm(x) * w over K = n_embd.
       const float4 *src = reinterpret_cast<const float4 *>(p.xf + (size_t)item * K);
-      float ss = 0.f;
-      for (int kv = tid; kv < KV; kv += kGemvThreads) {
-        const float4 a = src[2 * kv], b = src[2 * kv + 1];
-        ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z +
-              b.w * b.w;
-      }
-      ss = block_sum(ss, scratch);
-      const float sc = rsqrtf(ss / (float)K + p.eps);
       const uint4 *wn = reinterpret_cast<const uint4 *>(p.norm0);
       for (int kv = tid; kv < KV; kv += kGemvThreads) {
         const float4 a = src[2 * kv], b = src[2 * kv + 1];
         const uint4 w = wn[kv];
-        x0[kv] = make_float4(a.x * sc * bf_lo(w.x), a.y * sc * bf_hi(w.x), a.z * sc * bf_lo(w.y),
-                             a.w * sc * bf_hi(w.y));
-        x1[kv] = make_float4(b.x * sc * bf_lo(w.z), b.y * sc * bf_hi(w.z), b.z * sc * bf_lo(w.w),
-                             b.w * sc * bf_hi(w.w));
+        ss[m][0] += sq8(a, b);
+        x0[kv] = mul4(a, bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+        x1[kv] = mul4(b, bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w));
       }
     } else if constexpr (MODE == GM_QKV) {
-      // [RMSNorm(embed(tok)) * w_in ; RMSNorm(g) * w_hid], K = 2 n.
+      // [embed(tok) * w_in ; g * w_hid]; the two RMSNorm scales come later
       const int n = p.n_embd, NV = n >> 3;
       const PairItem it = resolve_pair(p.pairs, item, n);
       int tok = it.tok;
@@ -163,39 +164,47 @@ __device__ void stage_x(const GemvParams &p, float4 *xs, float *scratch) {
       }
       const uint4 *er = reinterpret_cast<const uint4 *>(p.embed + (size_t)tok * n);
       const float4 *gr = reinterpret_cast<const float4 *>(it.g);
-      float se = 0.f, sg = 0.f;
-      for (int kv = tid; kv < NV; kv += kGemvThreads) {
-        const uint4 u = er[kv];
-        const float e[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
-                            bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) se += e[i] * e[i];
-        const float4 a = gr[2 * kv], b = gr[2 * kv + 1];
-        sg += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z +
-              b.w * b.w;
-      }
-      se = block_sum(se, scratch);
-      sg = block_sum(sg, scratch + kGemvWarps);
-      const float sce = rsqrtf(se / (float)n + p.eps);
-      const float scg = rsqrtf(sg / (float)n + p.eps);
       const uint4 *wi = reinterpret_cast<const uint4 *>(p.norm0);
       const uint4 *wh = reinterpret_cast<const uint4 *>(p.norm1);
       for (int kv = tid; kv < NV; kv += kGemvThreads) {
         const uint4 u = er[kv];
+        const float4 ea = make_float4(bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y));
+        const float4 eb = make_float4(bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w));
         const uint4 w = wi[kv];
-        x0[kv] = make_float4(bf_lo(u.x) * sce * bf_lo(w.x), bf_hi(u.x) * sce * bf_hi(w.x),
-                             bf_lo(u.y) * sce * bf_lo(w.y), bf_hi(u.y) * sce * bf_hi(w.y));
-        x1[kv] = make_float4(bf_lo(u.z) * sce * bf_lo(w.z), bf_hi(u.z) * sce * bf_hi(w.z),
-                             bf_lo(u.w) * sce * bf_lo(w.w), bf_hi(u.w) * sce * bf_hi(w.w));
+        ss[m][0] += sq8(ea, eb);
+        x0[kv] = mul4(ea, bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+        x1[kv] = mul4(eb, bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w));
         const float4 a = gr[2 * kv], b = gr[2 * kv + 1];
-        const uint4 h = wh[kv];
-        x0[NV + kv] = make_float4(a.x * scg * bf_lo(h.x), a.y * scg * bf_hi(h.x),
-                                  a.z * scg * bf_lo(h.y), a.w * scg * bf_hi(h.y));
-        x1[NV + kv] = make_float4(b.x * scg * bf_lo(h.z), b.y * scg * bf_hi(h.z),
-                                  b.z * scg * bf_lo(h.w), b.w * scg * bf_hi(h.w));
+        const uint4 hw = wh[kv];
+        ss[m][T::kHalves - 1] += sq8(a, b);
+        x0[NV + kv] = mul4(a, bf_lo(hw.x), bf_hi(hw.x), bf_lo(hw.y), bf_hi(hw.y));
+        x1[NV + kv] = mul4(b, bf_lo(hw.z), bf_hi(hw.z), bf_lo(hw.w), bf_hi(hw.w));
       }
     }
   }
+}
+
+// x vector kv of item m as 8 floats.
+template <int MODE>
+__device__ __forceinline__ void load_x8(const unsigned char *xmem, int KV, int m, int kv, float (&x)[8]) {
+  if constexpr (ModeTraits<MODE>::kBf16X) {
+    const uint4 u = reinterpret_cast<const uint4 *>(xmem)[(size_t)m * KV + kv];
+    x[0] = bf_lo(u.x); x[1] = bf_hi(u.x); x[2] = bf_lo(u.y); x[3] = bf_hi(u.y);
+    x[4] = bf_lo(u.z); x[5] = bf_hi(u.z); x[6] = bf_lo(u.w); x[7] = bf_hi(u.w);
+  } else {
+    const float4 *xs = reinterpret_cast<const float4 *>(xmem);
+    const float4 a = xs[(size_t)(m * 2) * KV + kv], b = xs[(size_t)(m * 2 + 1) * KV + kv];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+}
+
+__device__ __forceinline__ float dot8(const uint4 w, const float (&x)[8], float a) {
+  a = fmaf(bf_lo(w.x), x[0], a); a = fmaf(bf_hi(w.x), x[1], a);
+  a = fmaf(bf_lo(w.y), x[2], a); a = fmaf(bf_hi(w.y), x[3], a);
+  a = fmaf(bf_lo(w.z), x[4], a); a = fmaf(bf_hi(w.z), x[5], a);
+  a = fmaf(bf_lo(w.w), x[6], a); a = fmaf(bf_hi(w.w), x[7], a);
+  return a;
 }
 
 // ---------------------------------------------------------------- epilogues
@@ -342,18 +351,21 @@ constexpr int kXRegVecs = 6;
 constexpr int kGemvCtaThreads = kGemvThreads + 32;  // 8 consumer warps + 1 producer warp
 
 struct GemvSmem {
-  int x_bytes, ring_off, stage_bytes, part_off, accs_off, scratch_off, bar_off, flag_off, total;
+  int x_bytes, ring_off, stage_bytes, part_off, accs_off, red_off, scale_off, bar_off, flag_off,
+      total;
 };
 
-__host__ __device__ inline GemvSmem gemv_smem_layout(int NB, int SR, int K, int nstage, int max_rows) {
+__host__ __device__ inline GemvSmem gemv_smem_layout(int NB, int SR, int H, int xbytes_per_elem,
+                                                     int K, int nstage, int max_rows) {
   GemvSmem L;
-  L.x_bytes = NB * K * 4;
+  L.x_bytes = NB * K * xbytes_per_elem;
   L.stage_bytes = SR * K * 2;
   L.ring_off = L.x_bytes;
   L.part_off = L.ring_off + nstage * L.stage_bytes;
-  L.accs_off = L.part_off + max_rows * kGemvWarps * NB * 4;
-  L.scratch_off = L.accs_off + max_rows * NB * 4;
-  L.bar_off = (L.scratch_off + 2 * kGemvWarps * 4 + 15) / 16 * 16;
+  L.accs_off = L.part_off + max_rows * kGemvWarps * H * NB * 4;
+  L.red_off = L.accs_off + max_rows * NB * 4;
+  L.scale_off = L.red_off + kGemvWarps * NB * H * 4;
+  L.bar_off = (L.scale_off + NB * H * 4 + 15) / 16 * 16;
   L.flag_off = L.bar_off + 2 * nstage * 8;
   L.total = L.flag_off + 16;
   return L;
@@ -361,25 +373,28 @@ __host__ __device__ inline GemvSmem gemv_smem_layout(int NB, int SR, int K, int 
 
 template <int NB, int SR, int MODE>
 __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvParams p) {
+  using T = ModeTraits<MODE>;
+  constexpr int H = T::kHalves;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.K, KV = K >> 3;
   // rows are handed out in units of 2 where the epilogue pairs rows (RoPE, SwiGLU)
-  constexpr int UNIT = (MODE == GM_QKV || MODE == GM_GATEUP) ? 2 : 1;
-  const int nunits = p.rows / UNIT;
+  const int nunits = p.rows / T::kUnit;
   const int ub = (int)((long long)blockIdx.x * nunits / gridDim.x);
   const int ue = (int)((long long)(blockIdx.x + 1) * nunits / gridDim.x);
-  const int row0 = UNIT * ub, nrows = UNIT * (ue - ub);
-  const int max_rows = UNIT * ((nunits + gridDim.x - 1) / gridDim.x);
+  const int row0 = T::kUnit * ub, nrows = T::kUnit * (ue - ub);
+  const int max_rows = T::kUnit * ((nunits + gridDim.x - 1) / gridDim.x);
   const int nst = p.nstage;
-  const GemvSmem L = gemv_smem_layout(NB, SR, K, nst, max_rows);
+  const GemvSmem L = gemv_smem_layout(NB, SR, H, T::kBf16X ? 2 : 4, K, nst, max_rows);
   const int n_stages = (nrows + SR - 1) / SR;
+  const int NVH = H == 2 ? (p.n_embd >> 3) : KV;  // first vector of the second K half
 
-  float4 *xs = reinterpret_cast<float4 *>(smem);
+  unsigned char *xmem = smem;
   unsigned char *ring = smem + L.ring_off;
-  float *part = reinterpret_cast<float *>(smem + L.part_off);     // [max_rows][warps][NB]
-  float *accs = reinterpret_cast<float *>(smem + L.accs_off);     // [max_rows][NB]
-  float *scratch = reinterpret_cast<float *>(smem + L.scratch_off);
+  float *part = reinterpret_cast<float *>(smem + L.part_off);  // [max_rows][warps][H][NB]
+  float *accs = reinterpret_cast<float *>(smem + L.accs_off);  // [max_rows][NB]
+  float *red = reinterpret_cast<float *>(smem + L.red_off);    // [warps][NB * H]
+  float *scale = reinterpret_cast<float *>(smem + L.scale_off);  // [NB * H]
   const uint32_t full0 = smem_addr(smem + L.bar_off);
   const uint32_t empty0 = full0 + 8 * nst;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
@@ -422,136 +437,157 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
 
   // ------------------------------------------------------------ consumer warps
   pdl_wait();
-  stage_x<NB, MODE>(p, xs, scratch);
+  float ss[NB][H];
+  stage_x<NB, MODE>(p, xmem, ss);
   consumer_sync();
-  float xr[NB == 1 ? kXRegVecs : 1][8];
   const bool xreg = (NB == 1) && (KV <= kXRegVecs * kGemvThreads);
+  float xr[NB == 1 ? kXRegVecs : 1][8];
   if (xreg) {
 #pragma unroll
     for (int j = 0; j < (NB == 1 ? kXRegVecs : 0); ++j) {
       const int kv = tid + j * kGemvThreads;
-      const float4 a = kv < KV ? xs[kv] : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 c = kv < KV ? xs[KV + kv] : make_float4(0.f, 0.f, 0.f, 0.f);
-      xr[j][0] = a.x; xr[j][1] = a.y; xr[j][2] = a.z; xr[j][3] = a.w;
-      xr[j][4] = c.x; xr[j][5] = c.y; xr[j][6] = c.z; xr[j][7] = c.w;
+      if (kv < KV) {
+        load_x8<MODE>(xmem, KV, 0, kv, xr[j]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xr[j][i] = 0.f;
+      }
     }
   }
 
   for (int st = 0; st < n_stages; ++st) {
     const int slot = st % nst;
     const bool ok = mbar_wait(full0 + 8 * slot, (st / nst) & 1, abort_flag, p.status);
-    float acc[SR][NB];
+    float acc[H][SR][NB];
 #pragma unroll
-    for (int r = 0; r < SR; ++r)
+    for (int h = 0; h < H; ++h)
 #pragma unroll
-      for (int m = 0; m < NB; ++m) acc[r][m] = 0.f;
+      for (int r = 0; r < SR; ++r)
+#pragma unroll
+        for (int m = 0; m < NB; ++m) acc[h][r][m] = 0.f;
     if (ok) {
       const unsigned char *stage = ring + (size_t)slot * L.stage_bytes;
       const int rows_here = min(SR, nrows - st * SR);
+      auto fma_rows = [&](int kv, const float (&x)[8], int m, float (&a)[SR][NB]) {
+#pragma unroll
+        for (int r = 0; r < SR; ++r)
+          if (r < rows_here) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(stage + ((size_t)r * K + (size_t)kv * 8) * 2);
+            a[r][m] = dot8(w, x, a[r][m]);
+          }
+      };
       if (xreg) {
-        // x of this thread's vectors is held in registers across all stages
 #pragma unroll
         for (int j = 0; j < (NB == 1 ? kXRegVecs : 0); ++j) {
           const int kv = tid + j * kGemvThreads;
           if (kv < KV) {
-#pragma unroll
-            for (int r = 0; r < SR; ++r) {
-              if (r < rows_here) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(stage + ((size_t)r * K + (size_t)kv * 8) * 2);
-                float a = acc[r][0];
-                a = fmaf(bf_lo(w.x), xr[j][0], a); a = fmaf(bf_hi(w.x), xr[j][1], a);
-                a = fmaf(bf_lo(w.y), xr[j][2], a); a = fmaf(bf_hi(w.y), xr[j][3], a);
-                a = fmaf(bf_lo(w.z), xr[j][4], a); a = fmaf(bf_hi(w.z), xr[j][5], a);
-                a = fmaf(bf_lo(w.w), xr[j][6], a); a = fmaf(bf_hi(w.w), xr[j][7], a);
-                acc[r][0] = a;
-              }
-            }
+            if (H == 1 || kv < NVH)
+              fma_rows(kv, xr[j], 0, acc[0]);
+            else
+              fma_rows(kv, xr[j], 0, acc[H - 1]);
           }
         }
       } else {
         for (int kv = tid; kv < KV; kv += kGemvThreads) {
-          float4 xa[NB], xb[NB];
 #pragma unroll
           for (int m = 0; m < NB; ++m) {
-            xa[m] = xs[(size_t)(m * 2) * KV + kv];
-            xb[m] = xs[(size_t)(m * 2 + 1) * KV + kv];
-          }
-#pragma unroll
-          for (int r = 0; r < SR; ++r) {
-            if (r < rows_here) {
-              const uint4 w = *reinterpret_cast<const uint4 *>(stage + ((size_t)r * K + (size_t)kv * 8) * 2);
-              const float w0 = bf_lo(w.x), w1 = bf_hi(w.x), w2 = bf_lo(w.y), w3 = bf_hi(w.y);
-              const float w4 = bf_lo(w.z), w5 = bf_hi(w.z), w6 = bf_lo(w.w), w7 = bf_hi(w.w);
-#pragma unroll
-              for (int m = 0; m < NB; ++m) {
-                float a = acc[r][m];
-                a = fmaf(w0, xa[m].x, a); a = fmaf(w1, xa[m].y, a);
-                a = fmaf(w2, xa[m].z, a); a = fmaf(w3, xa[m].w, a);
-                a = fmaf(w4, xb[m].x, a); a = fmaf(w5, xb[m].y, a);
-                a = fmaf(w6, xb[m].z, a); a = fmaf(w7, xb[m].w, a);
-                acc[r][m] = a;
-              }
-            }
+            float x[8];
+            load_x8<MODE>(xmem, KV, m, kv, x);
+            if (H == 1 || kv < NVH)
+              fma_rows(kv, x, m, acc[0]);
+            else
+              fma_rows(kv, x, m, acc[H - 1]);
           }
         }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-    // per-warp partial of every (row, item) of this stage
-    constexpr int N = SR * NB;
+    // per-warp partial of every (half, row, item) of this stage
+    constexpr int N = H * SR * NB;
     float v[N];
 #pragma unroll
-    for (int r = 0; r < SR; ++r)
+    for (int h = 0; h < H; ++h)
 #pragma unroll
-      for (int m = 0; m < NB; ++m) v[r * NB + m] = acc[r][m];
+      for (int r = 0; r < SR; ++r)
+#pragma unroll
+        for (int m = 0; m < NB; ++m) v[(h * SR + r) * NB + m] = acc[h][r][m];
     const float tot = warp_reduce_multi<N>(v, lane);
     if (warp_reduce_writer<N>(lane)) {
       const int idx = warp_reduce_index<N>(lane);
-      const int r = idx / NB, m = idx - r * NB;
+      const int m = idx % NB, r = (idx / NB) % SR, h = idx / (NB * SR);
       const int lrow = st * SR + r;
-      if (lrow < nrows) part[((size_t)lrow * kGemvWarps + warp) * NB + m] = tot;
+      if (lrow < nrows) part[(((size_t)lrow * kGemvWarps + warp) * H + h) * NB + m] = tot;
     }
   }
+  // RMSNorm scales 1 / sqrt(mean(x^2) + eps) per item and K half
+  if constexpr (T::kNorm) {
+    float v[NB * H];
+#pragma unroll
+    for (int m = 0; m < NB; ++m)
+#pragma unroll
+      for (int h = 0; h < H; ++h) v[m * H + h] = ss[m][h];
+    const float tot = warp_reduce_multi<NB * H>(v, lane);
+    if (warp_reduce_writer<NB * H>(lane)) red[warp * NB * H + warp_reduce_index<NB * H>(lane)] = tot;
+  }
   consumer_sync();
+  if constexpr (T::kNorm) {
+    if (tid < NB * H) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < kGemvWarps; ++w) t += red[w * NB * H + tid];
+      const float len = (float)(K / H);
+      scale[tid] = rsqrtf(t / len + p.eps);
+    }
+    consumer_sync();
+  }
   for (int e = tid; e < nrows * NB; e += kGemvThreads) {
     const int r = e / NB, m = e - r * NB;
-    float sum = 0.f;
+    float y = 0.f;
 #pragma unroll
-    for (int w = 0; w < kGemvWarps; ++w) sum += part[((size_t)r * kGemvWarps + w) * NB + m];
-    accs[e] = sum;
+    for (int h = 0; h < H; ++h) {
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kGemvWarps; ++w) sum += part[(((size_t)r * kGemvWarps + w) * H + h) * NB + m];
+      y += T::kNorm ? sum * scale[m * H + h] : sum;
+    }
+    accs[e] = y;
   }
   consumer_sync();
   epilogue<NB, MODE>(p, accs, row0, nrows);
 }
 
 // ------------------------------------------------------------------ launcher
-// Rows per ring stage: whole rows up to kStageBytes, at most 8, and at most 32 / NB so
-// that a stage's (row, item) sums fit one warp reduction.
-static int stage_rows(int K, int NB) {
+// Rows per ring stage: whole rows up to kStageBytes, at most 8, at most 32 / (NB * H) so
+// that a stage's sums fit one warp reduction, and fewer if that keeps >= 4 stages.
+template <int MODE>
+static int stage_rows(int K, int NB, int max_rows) {
+  using T = ModeTraits<MODE>;
   int sr = kStageBytes / (2 * K);
   if (sr < 1) sr = 1;
   if (sr > 8) sr = 8;
-  if (sr > 32 / NB) sr = 32 / NB;
+  if (sr > 32 / (NB * T::kHalves)) sr = 32 / (NB * T::kHalves);
   int p2 = 1;
   while (p2 * 2 <= sr) p2 *= 2;
+  while (p2 > 1) {
+    const GemvSmem L = gemv_smem_layout(NB, p2, T::kHalves, T::kBf16X ? 2 : 4, K, 0, max_rows);
+    const long long room = (long long)kGemvSmemLimit - L.total - 64;
+    if (room / (p2 * K * 2 + 16) >= 4) break;
+    p2 >>= 1;
+  }
   return p2;
 }
 
 template <int NB, int SR, int MODE>
-static cudaError_t launch_one(GemvParams p, int grid, cudaStream_t st, bool pdl) {
-  constexpr int UNIT = (MODE == GM_QKV || MODE == GM_GATEUP) ? 2 : 1;
-  const int nunits = p.rows / UNIT;
-  if (grid > nunits) grid = nunits;
-  if (grid < 1) grid = 1;
-  const int max_rows = UNIT * ((nunits + grid - 1) / grid);
-  const GemvSmem L0 = gemv_smem_layout(NB, SR, p.K, 0, max_rows);
+static cudaError_t launch_one(GemvParams p, int grid, int max_rows, cudaStream_t st, bool pdl) {
+  using T = ModeTraits<MODE>;
+  const GemvSmem L0 = gemv_smem_layout(NB, SR, T::kHalves, T::kBf16X ? 2 : 4, p.K, 0, max_rows);
   const long long room = (long long)kGemvSmemLimit - L0.total - 64;
   int nst = (int)(room / (SR * p.K * 2 + 16));
   if (nst > 8) nst = 8;
   if (nst < 2) return cudaErrorInvalidValue;
   p.nstage = nst;
-  const GemvSmem L = gemv_smem_layout(NB, SR, p.K, nst, max_rows);
+  const GemvSmem L = gemv_smem_layout(NB, SR, T::kHalves, T::kBf16X ? 2 : 4, p.K, nst, max_rows);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kGemvCtaThreads);
@@ -567,11 +603,17 @@ static cudaError_t launch_one(GemvParams p, int grid, cudaStream_t st, bool pdl)
 
 template <int NB, int MODE>
 static cudaError_t dispatch_sr(const GemvParams &p, int grid, cudaStream_t st, bool pdl) {
-  switch (stage_rows(p.K, NB)) {
-    case 1: return launch_one<NB, 1, MODE>(p, grid, st, pdl);
-    case 2: return launch_one<NB, 2, MODE>(p, grid, st, pdl);
-    case 4: return launch_one<NB, 4, MODE>(p, grid, st, pdl);
-    default: return launch_one<NB, (NB <= 4 ? 8 : 4), MODE>(p, grid, st, pdl);
+  using T = ModeTraits<MODE>;
+  const int nunits = p.rows / T::kUnit;
+  if (grid > nunits) grid = nunits;
+  if (grid < 1) grid = 1;
+  const int max_rows = T::kUnit * ((nunits + grid - 1) / grid);
+  constexpr int SRMAX = 32 / (NB * T::kHalves) >= 8 ? 8 : 32 / (NB * T::kHalves);
+  switch (stage_rows<MODE>(p.K, NB, max_rows)) {
+    case 1: return launch_one<NB, 1, MODE>(p, grid, max_rows, st, pdl);
+    case 2: return launch_one<NB, (SRMAX >= 2 ? 2 : 1), MODE>(p, grid, max_rows, st, pdl);
+    case 4: return launch_one<NB, (SRMAX >= 4 ? 4 : 1), MODE>(p, grid, max_rows, st, pdl);
+    default: return launch_one<NB, SRMAX, MODE>(p, grid, max_rows, st, pdl);
   }
 }
 
@@ -588,13 +630,16 @@ static cudaError_t dispatch_nb(const GemvParams &p, int nb, int grid, cudaStream
 
 template <int NB, int MODE>
 static cudaError_t prepare_nb() {
-  cudaError_t e = cudaSuccess;
+  using T = ModeTraits<MODE>;
+  constexpr int SRMAX = 32 / (NB * T::kHalves) >= 8 ? 8 : 32 / (NB * T::kHalves);
   const int lim = (int)kGemvSmemLimit;
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<NB, 1, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<NB, 2, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<NB, 4, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  if (NB <= 4 && e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemv_kernel<NB, (NB <= 4 ? 8 : 4), MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB, 1, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemv_kernel<NB, (SRMAX >= 2 ? 2 : 1), MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemv_kernel<NB, (SRMAX >= 4 ? 4 : 1), MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemv_kernel<NB, SRMAX, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
   return e;
 }
 
@@ -618,16 +663,17 @@ cudaError_t gemv_prepare() {
   return e;
 }
 
-int gemv_items_per_launch(int K, int items) {
-  // x of one launch lives in shared memory: NB * K * 4 bytes <= kGemvMaxXBytes.
+int gemv_items_per_launch(int mode, int K, int items) {
+  // x of one launch lives in shared memory: NB * K * (2 or 4) bytes <= kGemvMaxXBytes.
+  const size_t eb = mode == GM_ENCODE ? 2 : 4;
   int nb = 8;
-  while (nb > 1 && (size_t)nb * K * 4 > kGemvMaxXBytes) nb >>= 1;
+  while (nb > 1 && (size_t)nb * K * eb > kGemvMaxXBytes) nb >>= 1;
   while (nb > 1 && nb / 2 >= items) nb >>= 1;
   return nb;
 }
 
 cudaError_t gemv_launch(const GemvParams &p, int grid, cudaStream_t st, bool pdl) {
-  const int nb = gemv_items_per_launch(p.K, p.items);
+  const int nb = gemv_items_per_launch(p.mode, p.K, p.items);
   if (p.items > nb || p.items < 1) return cudaErrorInvalidValue;
   switch (p.mode) {
     case GM_ENCODE: return dispatch_nb<GM_ENCODE>(p, nb, grid, st, pdl);

@@ -16,7 +16,7 @@ constexpr size_t kGemvMaxXBytes = 128 * 1024;
 constexpr size_t kGemvSmemLimit = 224 * 1024;
 
 cudaError_t gemv_prepare();
-int gemv_items_per_launch(int K, int items);
+int gemv_items_per_launch(int mode, int K, int items);
 cudaError_t gemv_launch(const GemvParams &p, int grid, cudaStream_t st, bool pdl);
 
 bool attn_supported(int head_dim, int group);
