@@ -163,6 +163,22 @@ def kv_entry(dr: Drafter, tok: int, g: np.ndarray, pos: int):
     return round_bf16(k), round_bf16(v)
 
 
+def kv_entries(dr: Drafter, toks, gs: np.ndarray, positions):
+    """kv_entry for many pairs at once: the same definition with the projections of all
+    pairs done as one matrix product (rows are independent; a library matmul step)."""
+    geo = dr.geom
+    eps = geo.rms_eps
+    toks = np.asarray(toks)
+    e = np.stack([dr.embed(t) for t in toks])
+    cat = np.concatenate([rms_norm(e, dr.w["in_norm"], eps),
+                          rms_norm(np.asarray(gs, dtype=np.float64), dr.w["hidden_norm"], eps)], axis=1)
+    k = (cat @ dr.w["k"].T).reshape(len(toks), geo.n_head_kv, geo.head_dim)
+    v = (cat @ dr.w["v"].T).reshape(len(toks), geo.n_head_kv, geo.head_dim)
+    k = np.stack([rope_neox(k[i], int(p), geo.rope_dims, geo.rope_theta)
+                  for i, p in enumerate(positions)]) if len(toks) else k
+    return round_bf16(k), round_bf16(v)
+
+
 @dataclass
 class StepOut:
     logits: np.ndarray      # [draft_vocab]
@@ -240,14 +256,12 @@ def prefill(dr: Drafter, tokens, next_tok: int, aux_bits) -> SeqState:
     if n_prompt < 1:
         raise ValueError("empty prompt")
     genc = encode(dr, aux_bits)
-    ks, vs = [], []
-    for p in range(n_prompt - 1):
-        k, v = kv_entry(dr, int(tokens[p + 1]), genc[p], p)
-        ks.append(k)
-        vs.append(v)
     geo = dr.geom
-    k_arr = np.stack(ks) if ks else _empty_kv(geo)
-    v_arr = np.stack(vs) if vs else _empty_kv(geo)
+    if n_prompt > 1:
+        k_arr, v_arr = kv_entries(dr, tokens[1:n_prompt], genc[:n_prompt - 1],
+                                  np.arange(n_prompt - 1))
+    else:
+        k_arr, v_arr = _empty_kv(geo), _empty_kv(geo)
     return SeqState(k_arr, v_arr, genc[n_prompt - 1].copy(), int(next_tok))
 
 

@@ -9,7 +9,10 @@ and relative L2 1e-2.
 from __future__ import annotations
 
 import numpy as np
+import torch
 
+from eagle_speculative_decode_gb300 import binding as Bd
+from eagle_speculative_decode_gb300 import synth
 from oracle import eagle3_oracle as O
 
 MARGIN = 1e-2
@@ -64,3 +67,93 @@ def oracle_chain_following(dr, st, gamma, gpu_ids, gpu_toks):
     f = ChainFollower(dr, gpu_ids, gpu_toks)
     ch = O.draft_chain(dr, st, gamma, stepper=f)
     return ch, f
+
+
+# ----------------------------------------------------------------- round driver
+def upload_prompt(model, toks, aux, lens):
+    dev = model.device
+    P_max = aux.shape[1]
+    t = torch.from_numpy(np.ascontiguousarray(toks[:, :P_max])).to(dev)
+    nxt = torch.from_numpy(np.ascontiguousarray(toks[np.arange(len(lens)), lens])).to(dev)
+    a = torch.from_numpy(aux.view(np.int16)).to(dev)
+    return t, nxt, a
+
+
+def gpu_prefill(seq, model, toks, aux, lens):
+    t, nxt, a = upload_prompt(model, toks, aux, lens)
+    seq.prefill(t, nxt, lens, a)
+
+
+def oracle_prefill(dr, toks, aux, lens, which=None):
+    which = range(len(lens)) if which is None else which
+    return {b: O.prefill(dr, toks[b, :lens[b]], int(toks[b, lens[b]]), aux[b, :lens[b]]) for b in which}
+
+
+def check_state(seq, states: dict, what, kv_lo=0):
+    kv_len = seq.kv_len.cpu().numpy()
+    g = seq.g.cpu().numpy()
+    tok = seq.tok.cpu().numpy()
+    for b, st in states.items():
+        assert kv_len[b] == st.kv_len, f"{what}: kv_len[{b}] {kv_len[b]} vs {st.kv_len}"
+        assert tok[b] == st.tok, f"{what}: tok[{b}]"
+        assert_close(g[b], st.g, f"{what}: boundary g[{b}]", max_abs=1e-3, rel_l2=1e-5)
+        if st.kv_len > kv_lo:
+            k, v = seq.kv_entries(b, kv_lo, st.kv_len)
+            assert_close(bf16_bits_to_f64(k), st.k[kv_lo:], f"{what}: K[{b}]")
+            assert_close(bf16_bits_to_f64(v), st.v[kv_lo:], f"{what}: V[{b}]")
+
+
+def run_round(model, dr, seq, states: dict, gamma, n_imposed, seed, flags=0, kv_lo=0):
+    """One full round on the GPU and, for the sequences in `states`, the oracle: chain
+    (ids with the margin rule, logits, g, speculative KV), rewind (kv_len, committed
+    bytes, boundary), accept against imposed target predictions, rebuild."""
+    geo = model.geom
+    Bn = seq.B
+    out = seq.draft_chain(gamma, flags=flags, debug=True)
+    torch.cuda.synchronize()
+    dt = out["draft_tok"].cpu().numpy()
+    di = out["draft_id"].cpu().numpy()
+    ge = out["gamma_eff"].cpu().numpy()
+    L_all = seq._round_start_host.copy()
+    assert np.array_equal(seq.kv_len.cpu().numpy(), L_all + ge)
+    ties = 0
+    for b, st in states.items():
+        g_eff = O.plan_gamma(st.kv_len, gamma, model.max_cache_len, bool(flags & Bd.EAGLE3_SHRINK_GAMMA))
+        assert ge[b] == g_eff
+        ch, f = oracle_chain_following(dr, st, g_eff, di[b, :g_eff], dt[b, :g_eff])
+        ties += f.ties
+        assert np.all(dt[b, g_eff:] == -1)
+        logits = out["logits"][b, :g_eff].cpu().numpy()
+        gdbg = out["g"][b, :g_eff].cpu().numpy()
+        for j in range(g_eff):
+            assert_close(logits[j], ch.logits[j], f"logits b{b} j{j}")
+            assert_close(gdbg[j], ch.g[j], f"g b{b} j{j}")
+        k, v = seq.kv_entries(b, st.kv_len, st.kv_len + g_eff)
+        assert_close(bf16_bits_to_f64(k), ch.spec_k, f"spec K b{b}")
+        assert_close(bf16_bits_to_f64(v), ch.spec_v, f"spec V b{b}")
+    # rewind: kv_len back, committed bytes and boundary untouched
+    snap = {b: seq.kv_entries(b, max(0, st.kv_len - 64), st.kv_len) for b, st in states.items()}
+    g_snap, tok_snap = seq.g.clone(), seq.tok.clone()
+    seq.rewind()
+    torch.cuda.synchronize()
+    assert np.array_equal(seq.kv_len.cpu().numpy(), L_all)
+    for b, st in states.items():
+        k, v = seq.kv_entries(b, max(0, st.kv_len - 64), st.kv_len)
+        assert np.array_equal(k, snap[b][0]) and np.array_equal(v, snap[b][1])
+    assert torch.equal(seq.g, g_snap) and torch.equal(seq.tok, tok_snap)
+    # accept against imposed target predictions
+    y = synth.impose_target_predictions(np.where(dt < 0, 0, dt), np.minimum(n_imposed, ge), geo, seed)
+    dev = model.device
+    n_acc, bonus = seq.accept(out["draft_tok"], torch.from_numpy(y).to(dev), out["gamma_eff"])
+    torch.cuda.synchronize()
+    na, bo = n_acc.cpu().numpy(), bonus.cpu().numpy()
+    for b in range(Bn):
+        assert (na[b], bo[b]) == O.accept(dt[b], y[b], int(ge[b]))
+    vaux = synth.make_aux((Bn, gamma + 1), geo, seed, stream=9)
+    seq.rebuild_after_verify(n_acc, out["draft_tok"], bonus, torch.from_numpy(vaux.view(np.int16)).to(dev))
+    torch.cuda.synchronize()
+    new_states = {b: O.rebuild_after_verify(dr, st, int(na[b]), dt[b], int(bo[b]), vaux[b])
+                  for b, st in states.items()}
+    check_state(seq, new_states, "rebuild", kv_lo=kv_lo)
+    assert seq.model.status() == 0
+    return new_states, out, na, bo, vaux, ties

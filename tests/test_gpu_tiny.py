@@ -10,7 +10,7 @@ from eagle_speculative_decode_gb300 import binding as Bd
 from eagle_speculative_decode_gb300 import synth
 from eagle_speculative_decode_gb300.runtime import DraftModel
 from oracle import eagle3_oracle as O
-from parity import assert_close, bf16_bits_to_f64, oracle_chain_following
+from parity import check_state, gpu_prefill, oracle_prefill, run_round
 
 pytestmark = pytest.mark.gpu
 G = synth.TINY
@@ -32,90 +32,8 @@ def _prompt(batch, lens, seed, P_max=None):
     return toks, aux, P_max
 
 
-def _upload(model, toks, aux, lens):
-    dev = model.device
-    P_max = aux.shape[1]
-    t = torch.from_numpy(np.ascontiguousarray(toks[:, :P_max])).to(dev)
-    nxt = torch.from_numpy(np.ascontiguousarray(toks[np.arange(len(lens)), lens])).to(dev)
-    a = torch.from_numpy(aux.view(np.int16)).to(dev)
-    return t, nxt, a
-
-
-def _prefill(seq, model, toks, aux, lens):
-    t, nxt, a = _upload(model, toks, aux, lens)
-    seq.prefill(t, nxt, lens, a)
-
-
-def _oracle_prefill(dr, toks, aux, lens):
-    return [O.prefill(dr, toks[b, :lens[b]], int(toks[b, lens[b]]), aux[b, :lens[b]])
-            for b in range(len(lens))]
-
-
-def _check_state(seq, states, what):
-    kv_len = seq.kv_len.cpu().numpy()
-    g = seq.g.cpu().numpy()
-    tok = seq.tok.cpu().numpy()
-    for b, st in enumerate(states):
-        assert kv_len[b] == st.kv_len, f"{what}: kv_len[{b}]"
-        assert tok[b] == st.tok, f"{what}: tok[{b}]"
-        assert_close(g[b], st.g, f"{what}: boundary g[{b}]", max_abs=1e-3, rel_l2=1e-5)
-        if st.kv_len:
-            k, v = seq.kv_entries(b, 0, st.kv_len)
-            assert_close(bf16_bits_to_f64(k), st.k, f"{what}: K[{b}]")
-            assert_close(bf16_bits_to_f64(v), st.v, f"{what}: V[{b}]")
-
-
 def _round(model, dr, seq, states, gamma, n_imposed, seed, flags=0):
-    """One full round on GPU and oracle; returns (new states, draft outputs)."""
-    Bn = seq.B
-    out = seq.draft_chain(gamma, flags=flags, debug=True)
-    torch.cuda.synchronize()
-    dt = out["draft_tok"].cpu().numpy()
-    di = out["draft_id"].cpu().numpy()
-    ge = out["gamma_eff"].cpu().numpy()
-    logits = out["logits"].cpu().numpy()
-    gdbg = out["g"].cpu().numpy()
-    L = np.array([st.kv_len for st in states])
-    assert np.array_equal(seq.kv_len.cpu().numpy(), L + ge)
-    for b, st in enumerate(states):
-        g_eff = O.plan_gamma(st.kv_len, gamma, model.max_cache_len, bool(flags & Bd.EAGLE3_SHRINK_GAMMA))
-        assert ge[b] == g_eff
-        ch, _ = oracle_chain_following(dr, st, g_eff, di[b, :g_eff], dt[b, :g_eff])
-        assert np.all(dt[b, g_eff:] == -1)
-        for j in range(g_eff):
-            assert_close(logits[b, j], ch.logits[j], f"logits b{b} j{j}", max_abs=2e-2, rel_l2=1e-2)
-            assert_close(gdbg[b, j], ch.g[j], f"g b{b} j{j}")
-        k, v = seq.kv_entries(b, st.kv_len, st.kv_len + g_eff)
-        assert_close(bf16_bits_to_f64(k), ch.spec_k, f"spec K b{b}")
-        assert_close(bf16_bits_to_f64(v), ch.spec_v, f"spec V b{b}")
-    # rewind: kv_len back, committed bytes and boundary untouched
-    snap_k = [seq.kv_entries(b, 0, st.kv_len) for b, st in enumerate(states)]
-    g_snap, tok_snap = seq.g.clone(), seq.tok.clone()
-    seq.rewind()
-    torch.cuda.synchronize()
-    assert np.array_equal(seq.kv_len.cpu().numpy(), L)
-    for b, st in enumerate(states):
-        k, v = seq.kv_entries(b, 0, st.kv_len)
-        assert np.array_equal(k, snap_k[b][0]) and np.array_equal(v, snap_k[b][1])
-    assert torch.equal(seq.g, g_snap) and torch.equal(seq.tok, tok_snap)
-    # accept against imposed target predictions
-    y = synth.impose_target_predictions(np.where(dt < 0, 0, dt), np.minimum(n_imposed, ge), G, seed)
-    dev = model.device
-    n_acc, bonus = seq.accept(out["draft_tok"], torch.from_numpy(y).to(dev), out["gamma_eff"])
-    torch.cuda.synchronize()
-    na, bo = n_acc.cpu().numpy(), bonus.cpu().numpy()
-    for b in range(Bn):
-        want = O.accept(dt[b], y[b], int(ge[b]))
-        assert (na[b], bo[b]) == want
-    # rebuild with verify features
-    vaux = synth.make_aux((Bn, gamma + 1), G, seed, stream=9)
-    seq.rebuild_after_verify(n_acc, out["draft_tok"], bonus, torch.from_numpy(vaux.view(np.int16)).to(dev))
-    torch.cuda.synchronize()
-    new_states = [O.rebuild_after_verify(dr, st, int(na[b]), dt[b], int(bo[b]), vaux[b])
-                  for b, st in enumerate(states)]
-    _check_state(seq, new_states, "rebuild")
-    assert seq.model.status() == 0
-    return new_states
+    return run_round(model, dr, seq, states, gamma, n_imposed, seed, flags)[0]
 
 
 def test_single_sequence_rounds(tiny):
@@ -123,10 +41,10 @@ def test_single_sequence_rounds(tiny):
     lens = np.array([32])
     toks, aux, _ = _prompt(1, lens, seed=1)
     seq = model.new_state(1)
-    _prefill(seq, model, toks, aux, lens)
+    gpu_prefill(seq, model, toks, aux, lens)
     torch.cuda.synchronize()
-    states = _oracle_prefill(dr, toks, aux, lens)
-    _check_state(seq, states, "prefill")
+    states = oracle_prefill(dr, toks, aux, lens)
+    check_state(seq, states, "prefill")
     for r, n in enumerate([2, 0, 3]):
         states = _round(model, dr, seq, states, 3, np.array([n]), seed=10 + r)
 
@@ -138,10 +56,10 @@ def test_ragged_batch_random_pages(tiny):
     pages_per_seq = (model.max_cache_len + model.page_size - 1) // model.page_size
     pt = synth.page_table(4, pages_per_seq, seed=3)
     seq = model.new_state(4, page_table=pt)
-    _prefill(seq, model, toks, aux, lens)
+    gpu_prefill(seq, model, toks, aux, lens)
     torch.cuda.synchronize()
-    states = _oracle_prefill(dr, toks, aux, lens)
-    _check_state(seq, states, "prefill")
+    states = oracle_prefill(dr, toks, aux, lens)
+    check_state(seq, states, "prefill")
     for r in range(3):
         n = synth.imposed_accept_lengths(4, 4, seed=20 + r)
         states = _round(model, dr, seq, states, 4, n, seed=20 + r)
@@ -154,9 +72,9 @@ def test_capacity_boundary_start_97_gamma_3_max_100(tiny):
     lens = np.array([98])
     toks, aux, _ = _prompt(1, lens, seed=4)
     seq = model.new_state(1)
-    _prefill(seq, model, toks, aux, lens)
+    gpu_prefill(seq, model, toks, aux, lens)
     torch.cuda.synchronize()
-    states = _oracle_prefill(dr, toks, aux, lens)
+    states = oracle_prefill(dr, toks, aux, lens)
     assert states[0].kv_len == 97
     with pytest.raises(Bd.Eagle3Error) as ei:
         seq.draft_chain(3)
@@ -174,7 +92,7 @@ def test_graph_and_direct_launch_agree(tiny):
     for graph in (True, False, True):
         model.set_graph_mode(graph)
         seq = model.new_state(2)
-        _prefill(seq, model, toks, aux, lens)
+        gpu_prefill(seq, model, toks, aux, lens)
         o = seq.draft_chain(5, debug=True)
         torch.cuda.synchronize()
         outs.append({k: v.cpu().numpy() for k, v in o.items()})
@@ -211,7 +129,7 @@ def test_state_machine_and_argument_errors(tiny):
     lens = np.array([10])
     toks, aux, _ = _prompt(1, lens, seed=8)
     seq = model.new_state(1)
-    _prefill(seq, model, toks, aux, lens)
+    gpu_prefill(seq, model, toks, aux, lens)
     dev = model.device
     dummy = torch.zeros(1, 4, dtype=torch.int32, device=dev)
     vaux = torch.zeros(1, 4, 3, G.n_embd, dtype=torch.int16, device=dev)
@@ -244,7 +162,7 @@ def test_out_of_range_token_sets_status_without_fault(tiny):
     lens = np.array([6])
     toks, aux, _ = _prompt(1, lens, seed=9)
     seq = model.new_state(1)
-    _prefill(seq, model, toks, aux, lens)
+    gpu_prefill(seq, model, toks, aux, lens)
     seq.tok.fill_(G.target_vocab + 5)
     seq.draft_chain(2)
     torch.cuda.synchronize()

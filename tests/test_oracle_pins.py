@@ -501,3 +501,15 @@ def test_speculative_loop_reproduces_target_greedy_stream():
     out = hist[len(prompt):]
     assert out == greedy[:len(out)]
     assert accepted > 0
+
+
+def test_batched_kv_entries_equal_one_by_one():
+    wts, dr = random_tiny(seed=8)
+    toks = synth.make_tokens((9,), dr.geom, 30)
+    gs = O.encode(dr, synth.make_aux((9,), dr.geom, 30))
+    pos = np.array([0, 1, 5, 17, 18, 40, 41, 90, 99])
+    kb, vb = O.kv_entries(dr, toks, gs, pos)
+    for i in range(9):
+        k1, v1 = O.kv_entry(dr, int(toks[i]), gs[i], int(pos[i]))
+        assert np.max(np.abs(kb[i] - k1)) <= 2.0 ** -8 * np.max(np.abs(k1))
+        assert np.max(np.abs(vb[i] - v1)) <= 2.0 ** -8 * np.max(np.abs(v1))
