@@ -558,7 +558,7 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      gemv_prepare() != cudaSuccess) {
+      gemv_prepare() != cudaSuccess || attn_prepare() != cudaSuccess) {
     delete ctx;
     return EAGLE3_ERR_CUDA;
   }

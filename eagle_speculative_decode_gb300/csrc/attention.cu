@@ -4,12 +4,16 @@
 // the keys 0..len-1 of (q . k) / sqrt(d), then sum of p * v ("memra_engine/eagle.rs",
 // ``attn``: fa_decode with scale 1/sqrt(head_dim); the new key is appended first).
 //
-// One CTA per (split, kv head, sequence): the G query heads that share a kv head are
-// served from one read of each K/V vector.  A key of d = 256 dims is spread over the 32
-// lanes of a warp (8 dims = 16 bytes per lane); smaller heads put several keys in a warp.
-// Each lane group keeps an online softmax (running max in the log2 domain, running sum,
-// running weighted V).  The CTA merges its warps in shared memory; with more than one
-// split the last CTA of a (sequence, kv head) to finish merges the splits' partials.
+// One CTA of 8 warps per (split, kv head, sequence): the G query heads that share a kv
+// head are served from one read of each K/V vector.  A key of d = 256 dims is spread over
+// the 32 lanes of a warp (8 dims = 16 bytes per lane); smaller heads put several keys in
+// a warp.  The warp walks blocks of UNR keys per lane group and issues all of a block's
+// K/V loads before computing, keeping an online softmax per lane group (running max in
+// the log2 domain, running sum, running weighted V).  Keys below the committed length
+// were written before the chain started, so the first block of those is loaded before
+// the kernel waits on its predecessor (programmatic dependent launch).  The CTA merges
+// its lane groups in shared memory; with more than one split the last CTA of a
+// (sequence, kv head) to finish merges the splits' partials.
 #include <math.h>
 
 #include "common.cuh"
@@ -17,39 +21,80 @@
 
 namespace e3 {
 
-constexpr int kAttnWarps = 4;
-constexpr int kMaxAttnSplits = 64;
+constexpr int kAttnWarps = 8;
 constexpr int kAttnThreads = kAttnWarps * 32;
+constexpr int kMaxAttnSplits = 64;
 
 template <int D, int G>
-__global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnParams p) {
-  constexpr int LPK = D / 8;        // lanes per key
-  constexpr int KPW = 32 / LPK;     // keys per warp pass
-  constexpr int NP = kAttnWarps * KPW;
+struct AttnShape {
+  static constexpr int LPK = D / 8;             // lanes per key
+  static constexpr int KPW = 32 / LPK;          // keys per warp pass
+  static constexpr int NP = kAttnWarps * KPW;   // lane groups per CTA
+  static constexpr int UNR = (G >= 8 || D < 128) ? 4 : 8;
+  static constexpr size_t kSmem = (size_t)NP * G * D * 4;  // lane-group partial V sums
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const AttnParams p) {
+  using S = AttnShape<D, G>;
+  constexpr int LPK = S::LPK, KPW = S::KPW, NP = S::NP, UNR = S::UNR;
+  extern __shared__ __align__(16) float sm_acc[];  // [NP][G][D]
   __shared__ float2 sm_ml[NP][G];
-  __shared__ __align__(16) float sm_acc[NP][G][D];
   __shared__ int last_sh;
 
   const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grp = lane / LPK, li = lane - grp * LPK;
   const int H = p.n_head, Hkv = p.n_head_kv;
+  const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
+
+  // ---- before the dependency wait: committed keys only (positions < L)
+  const int L = p.kv_len[b];
+  int len = L + p.step + 1;
+  if (len > p.max_cache_len) len = p.max_cache_len;
+  if (len < 1) len = 1;
+  const int chunk = (len + p.splits - 1) / p.splits;
+  const int k0 = s * chunk;
+  int k1 = min(len, k0 + chunk);
+
+  bool valid[UNR];
+  uint4 ku[UNR], vu[UNR];
+  const int base0 = k0 + warp * KPW * UNR;
+  auto load_key = [&](int u, int key) {
+    const int pg = pt[key / p.page_size];
+    if (pg < 0 || pg >= p.num_pages) {
+      set_status(p.status, EAGLE3_DEV_BAD_PAGE);
+      valid[u] = false;
+      return;
+    }
+    const size_t off = (((size_t)pg * Hkv + kvh) * p.page_size + key % p.page_size) * D + li * 8;
+    ku[u] = *reinterpret_cast<const uint4 *>(p.k_pool + off);
+    vu[u] = *reinterpret_cast<const uint4 *>(p.v_pool + off);
+    valid[u] = true;
+  };
+  bool pre[UNR];
+#pragma unroll
+  for (int u = 0; u < UNR; ++u) {
+    const int key = base0 + u * KPW + grp;
+    ku[u] = make_uint4(0u, 0u, 0u, 0u);
+    vu[u] = make_uint4(0u, 0u, 0u, 0u);
+    valid[u] = false;
+    pre[u] = L >= 0 && key < k1 && key < L;
+    if (pre[u]) load_key(u, key);
+  }
 
   pdl_trigger();
   pdl_wait();
 
-  const int L = p.kv_len[b];
+  // ---- after the wait: this step's length (gamma_eff is written by the chain start)
   const int ge = p.gamma_eff ? p.gamma_eff[b] : p.step + 1;
-  int len = L + min(p.step, max(ge - 1, 0)) + 1;
-  if (L < 0 || len > p.max_cache_len) {
+  int len2 = L + min(p.step, max(ge - 1, 0)) + 1;
+  if (L < 0 || len2 > p.max_cache_len) {
     if (tid == 0 && s == 0 && kvh == 0) set_status(p.status, EAGLE3_DEV_BAD_LENGTH);
-    len = min(max(len, 1), p.max_cache_len);
+    len2 = min(max(len2, 1), p.max_cache_len);
   }
-  const int chunk = (len + p.splits - 1) / p.splits;
-  const int k0 = s * chunk;
-  const int k1 = min(len, k0 + chunk);
+  k1 = min(k1, len2);
 
-  // q of the G heads, pre-scaled so that scores are in the log2 domain.
   const float qscale = rsqrtf((float)D) * 1.4426950408889634f;
   float qv[G][8];
 #pragma unroll
@@ -69,32 +114,20 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
   }
 
   // The whole warp walks blocks of UNR * KPW keys together (the score reduction shuffles
-  // across the lanes of a key group with a full mask); the K/V loads of a block are all
-  // issued before any score is computed, so each lane keeps 2 * UNR 16-byte loads in
-  // flight.  Lane groups past the end or on a bad page take part in the shuffles but do
-  // not update their state.
-  constexpr int UNR = (G >= 8 || D < 128) ? 4 : 8;
-  const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
-  for (int base = k0 + warp * KPW * UNR; base < k1; base += NP * UNR) {
-    bool valid[UNR];
-    uint4 ku[UNR], vu[UNR];
+  // across the lanes of a key group with a full mask).  Lane groups past the end or on a
+  // bad page take part in the shuffles but do not update their state.
+  for (int base = base0; base < k1; base += NP * UNR) {
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       const int key = base + u * KPW + grp;
-      valid[u] = key < k1;
+      if (base == base0 && pre[u]) {
+        valid[u] = valid[u] && key < k1;
+        continue;
+      }
+      valid[u] = false;
       ku[u] = make_uint4(0u, 0u, 0u, 0u);
       vu[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (valid[u]) {
-        const int pg = pt[key / p.page_size];
-        if (pg < 0 || pg >= p.num_pages) {
-          set_status(p.status, EAGLE3_DEV_BAD_PAGE);
-          valid[u] = false;
-        } else {
-          const size_t off = (((size_t)pg * Hkv + kvh) * p.page_size + key % p.page_size) * D + li * 8;
-          ku[u] = *reinterpret_cast<const uint4 *>(p.k_pool + off);
-          vu[u] = *reinterpret_cast<const uint4 *>(p.v_pool + off);
-        }
-      }
+      if (key < k1) load_key(u, key);
     }
     float sc[UNR][G];
 #pragma unroll
@@ -141,7 +174,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
   for (int g = 0; g < G; ++g) {
     if (li == 0) sm_ml[part][g] = make_float2(mx[g], sum[g]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sm_acc[part][g][li * 8 + i] = acc[g][i];
+    for (int i = 0; i < 8; ++i) sm_acc[((size_t)part * G + g) * D + li * 8 + i] = acc[g][i];
   }
   __syncthreads();
 
@@ -158,7 +191,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
         const float2 ml = sm_ml[q][g];
         const float w = exp2f(ml.x - M);
         Ls += ml.y * w;
-        O += sm_acc[q][g][dim] * w;
+        O += sm_acc[((size_t)q * G + g) * D + dim] * w;
       }
     }
     if (p.splits == 1) {
@@ -180,7 +213,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
   if (!last_sh) return;
   __threadfence();
   // Merge the splits: weights w[q][g] = exp2(m_q - M_g) / L_g first (all splits loaded in
-  // parallel), then every thread sums float4 slices over the splits with independent loads.
+  // parallel), then every thread sums float4 slices over the splits, 8 loads at a time.
   __shared__ float2 ml_all[kMaxAttnSplits][G];
   __shared__ float wsm[kMaxAttnSplits][G];
   __shared__ float2 ML[G];
@@ -236,7 +269,7 @@ static cudaError_t attn_launch_dg(const AttnParams &p, int B, cudaStream_t st, b
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.splits, p.n_head_kv, B);
   cfg.blockDim = dim3(kAttnThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = AttnShape<D, G>::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -246,18 +279,35 @@ static cudaError_t attn_launch_dg(const AttnParams &p, int B, cudaStream_t st, b
   return cudaLaunchKernelEx(&cfg, attn_decode_kernel<D, G>, p);
 }
 
+template <int D, int G>
+static cudaError_t attn_prepare_dg() {
+  return cudaFuncSetAttribute(attn_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)AttnShape<D, G>::kSmem);
+}
+
 bool attn_supported(int head_dim, int group) {
   return (head_dim == 64 || head_dim == 128 || head_dim == 256) &&
          (group == 1 || group == 2 || group == 4 || group == 8);
 }
 
+#define E3_ATTN_ALL(X) \
+  X(64, 1) X(64, 2) X(64, 4) X(64, 8) X(128, 1) X(128, 2) X(128, 4) X(128, 8) X(256, 1) X(256, 2) X(256, 4) X(256, 8)
+
+cudaError_t attn_prepare() {
+  cudaError_t e = cudaSuccess;
+#define E3_PREP(DD, GG) \
+  if (e == cudaSuccess) e = attn_prepare_dg<DD, GG>();
+  E3_ATTN_ALL(E3_PREP)
+#undef E3_PREP
+  return e;
+}
+
 cudaError_t attn_launch(const AttnParams &p, int B, cudaStream_t st, bool pdl) {
   const int G = p.n_head / p.n_head_kv;
+  if (p.splits < 1 || p.splits > kMaxAttnSplits) return cudaErrorInvalidValue;
 #define E3_ATTN_CASE(DD, GG) \
   if (p.head_dim == DD && G == GG) return attn_launch_dg<DD, GG>(p, B, st, pdl);
-  E3_ATTN_CASE(64, 1) E3_ATTN_CASE(64, 2) E3_ATTN_CASE(64, 4) E3_ATTN_CASE(64, 8)
-  E3_ATTN_CASE(128, 1) E3_ATTN_CASE(128, 2) E3_ATTN_CASE(128, 4) E3_ATTN_CASE(128, 8)
-  E3_ATTN_CASE(256, 1) E3_ATTN_CASE(256, 2) E3_ATTN_CASE(256, 4) E3_ATTN_CASE(256, 8)
+  E3_ATTN_ALL(E3_ATTN_CASE)
 #undef E3_ATTN_CASE
   return cudaErrorInvalidValue;
 }

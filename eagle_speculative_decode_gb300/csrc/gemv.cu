@@ -488,15 +488,32 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
           }
         }
       } else {
+        // several items: each weight vector is loaded and widened once, then used for
+        // every item
         for (int kv = tid; kv < KV; kv += kGemvThreads) {
+          float wf[SR][8];
+#pragma unroll
+          for (int r = 0; r < SR; ++r) {
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows_here) w = *reinterpret_cast<const uint4 *>(stage + ((size_t)r * K + (size_t)kv * 8) * 2);
+            wf[r][0] = bf_lo(w.x); wf[r][1] = bf_hi(w.x); wf[r][2] = bf_lo(w.y); wf[r][3] = bf_hi(w.y);
+            wf[r][4] = bf_lo(w.z); wf[r][5] = bf_hi(w.z); wf[r][6] = bf_lo(w.w); wf[r][7] = bf_hi(w.w);
+          }
+          const int h = (H == 1 || kv < NVH) ? 0 : H - 1;
 #pragma unroll
           for (int m = 0; m < NB; ++m) {
             float x[8];
             load_x8<MODE>(xmem, KV, m, kv, x);
-            if (H == 1 || kv < NVH)
-              fma_rows(kv, x, m, acc[0]);
-            else
-              fma_rows(kv, x, m, acc[H - 1]);
+#pragma unroll
+            for (int r = 0; r < SR; ++r) {
+              float a0 = 0.f;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) a0 = fmaf(wf[r][i], x[i], a0);
+              if (h == 0)
+                acc[0][r][m] += a0;
+              else
+                acc[H - 1][r][m] += a0;
+            }
           }
         }
       }

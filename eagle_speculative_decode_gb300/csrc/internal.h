@@ -20,6 +20,7 @@ int gemv_items_per_launch(int mode, int K, int items);
 cudaError_t gemv_launch(const GemvParams &p, int grid, cudaStream_t st, bool pdl);
 
 bool attn_supported(int head_dim, int group);
+cudaError_t attn_prepare();
 cudaError_t attn_launch(const AttnParams &p, int B, cudaStream_t st, bool pdl);
 
 // Small bookkeeping kernels (small.cu).

@@ -16,8 +16,8 @@ import torch
 from eagle_speculative_decode_gb300 import synth
 from eagle_speculative_decode_gb300.runtime import DraftModel
 from oracle import eagle3_oracle as O
-from parity import (assert_close, bf16_bits_to_f64, check_state, gpu_prefill, oracle_prefill,
-                    run_round)
+from parity import (assert_close, assert_close_bf16, bf16_bits_to_f64, check_state, gpu_prefill,
+                    oracle_prefill, run_round)
 
 pytestmark = pytest.mark.gpu
 G = synth.FULL
@@ -97,8 +97,8 @@ def test_batch64_context2048_sampled(full):
             g_p = O.encode(dr, aux[b, p])
             k, v = O.kv_entry(dr, int(toks[b, p + 1]), g_p, int(p))
             kg, vg = seq.kv_entries(int(b), int(p), int(p) + 1)
-            assert_close(bf16_bits_to_f64(kg[0]), k, f"prefill K b{b} p{p}")
-            assert_close(bf16_bits_to_f64(vg[0]), v, f"prefill V b{b} p{p}")
+            assert_close_bf16(bf16_bits_to_f64(kg[0]), k, f"prefill K b{b} p{p}")
+            assert_close_bf16(bf16_bits_to_f64(vg[0]), v, f"prefill V b{b} p{p}")
         # boundary of every sequence
         g_all = seq.g.cpu().numpy()
         want = O.encode(dr, aux[np.arange(B), lens - 1])
@@ -126,8 +126,8 @@ def test_batch64_context2048_sampled(full):
             kg, vg = seq.kv_entries(b, int(L[b]), int(L[b]) + len(pairs))
             for i, (t, gg) in enumerate(pairs):
                 k, v = O.kv_entry(dr, t, gg, int(L[b]) + i)
-                assert_close(bf16_bits_to_f64(kg[i]), k, f"rebuilt K b{b} i{i}")
-                assert_close(bf16_bits_to_f64(vg[i]), v, f"rebuilt V b{b} i{i}")
+                assert_close_bf16(bf16_bits_to_f64(kg[i]), k, f"rebuilt K b{b} i{i}")
+                assert_close_bf16(bf16_bits_to_f64(vg[i]), v, f"rebuilt V b{b} i{i}")
             assert_close(seq.g[b].cpu().numpy(), venc[b, int(na[b])], f"new boundary b{b}",
                          max_abs=1e-3, rel_l2=1e-5)
             assert int(seq.tok[b].item()) == int(bo[b])
