@@ -34,7 +34,7 @@ EXPORTED = (
     "eagle3_init", "eagle3_destroy", "eagle3_encode", "eagle3_prefill", "eagle3_draft_chain",
     "eagle3_rewind", "eagle3_accept", "eagle3_rebuild_after_verify", "eagle3_get_status",
     "eagle3_set_graph_mode", "eagle3_launch_count", "eagle3_profile_begin",
-    "eagle3_profile_end", "eagle3_profile_interval",
+    "eagle3_profile_end", "eagle3_profile_interval", "eagle3_lmhead_argmax_noalloc",
 )
 
 
@@ -105,6 +105,8 @@ def load() -> ctypes.CDLL:
         "eagle3_profile_begin": (ci, [vp, ci]),
         "eagle3_profile_end": (ci, [vp, P(ci)]),
         "eagle3_profile_interval": (ci, [vp, ci, P(ci), P(ctypes.c_float)]),
+        "eagle3_lmhead_argmax_noalloc": (ci, [vp, vp, vp, vp, ci, ci, ci, ci, ctypes.c_float,
+                                              vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -231,3 +233,13 @@ def eagle3_profile_end(ctx: int) -> list[tuple[int, float]]:
                "eagle3_profile_interval")
         out.append((lab.value, ms.value))
     return out
+
+
+def eagle3_lmhead_argmax_noalloc(lm_head: int, final_norm: int, d2t: int, x: int, rows: int,
+                                 n_embd: int, draft_vocab: int, target_vocab: int, rms_eps: float,
+                                 draft_id: int | None, target_id: int, logits: int | None = None,
+                                 stream: int = 0) -> None:
+    _check(load().eagle3_lmhead_argmax_noalloc(lm_head, final_norm, d2t, x, int(rows), int(n_embd),
+                                               int(draft_vocab), int(target_vocab), float(rms_eps),
+                                               draft_id, target_id, logits, stream),
+           "eagle3_lmhead_argmax_noalloc")

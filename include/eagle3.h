@@ -242,6 +242,33 @@ int eagle3_profile_end(eagle3_ctx *ctx, int *n_events);
  * 8 = k/v-only GEMV (prefill, rebuild), 9 = bookkeeping kernel. */
 int eagle3_profile_interval(const eagle3_ctx *ctx, int i, int *label, float *ms);
 
+/* ---- lm_head argmax without any allocation ------------------------------------------
+ * The pages have no counterpart: this entry point exists for callers that cannot allocate
+ * device memory when they need the result -- for example code that runs while a CUDA
+ * graph is being captured (cudaMalloc is not allowed there) or a runtime whose memory plan
+ * is fixed at start-up and that therefore cannot provide a context workspace.
+ *
+ * Computes, for each of `rows` float32 vectors x[r] (device, [rows, n_embd]), the draft
+ * chain's last kernel: logits = lm_head . (RMSNorm(x[r]) * final_norm), draft_id[r] = the
+ * argmax (lowest index on ties), target_id[r] = draft_id[r] + d2t[draft_id[r]].  Same
+ * weights and layouts as eagle3_weights; draft_id and logits ([rows, draft_vocab]) may be
+ * NULL; target_id is required.  Every buffer is caller-owned device memory.
+ *
+ * The kernel's scratch (one argmax slot per row and an arrival counter) lives in a static
+ * device array inside the library, so the call allocates nothing: it is limited to
+ * rows <= 64 (larger requests return EAGLE3_ERR_INVALID_ARG), and every GPU that loads the
+ * library holds that array (about 520 bytes) until the process exits.  The first call on a
+ * device looks the array's device address up; make that first call before any stream
+ * capture.  All calls share the array, which keeps the last call's contents (each call
+ * clears it on its stream before use): calls that overlap on the GPU -- on different
+ * streams, or on devices sharing this process -- race, so serialise them.
+ * Returns EAGLE3_OK, EAGLE3_ERR_INVALID_ARG or EAGLE3_ERR_CUDA. */
+int eagle3_lmhead_argmax_noalloc(const uint16_t *lm_head, const uint16_t *final_norm,
+                                 const int64_t *d2t, const float *x, int rows, int n_embd,
+                                 int draft_vocab, int target_vocab, float rms_eps,
+                                 int32_t *draft_id, int32_t *target_id, float *logits,
+                                 eagle3_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
