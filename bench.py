@@ -274,9 +274,15 @@ def run_mine(args, cfg):
     aux = torch.from_numpy(synth.make_aux((B, P_max), geo, seed + 3).view(np.int16)).to(dev)
     t_tok = torch.from_numpy(toks[:, :P_max].copy()).to(dev)
     t_next = torch.from_numpy(toks[np.arange(B), lens].astype(np.int32)).to(dev)
+    torch.cuda.synchronize()
+    pf0, pf1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pf0.record()
     seq.prefill(t_tok, t_next, lens, aux)
+    pf1.record()
     del aux
     torch.cuda.synchronize()
+    prefill_ms = pf0.elapsed_time(pf1)
+    prefill_positions = int(lens.sum())
 
     # per-round synthetic verifier inputs: verify features and imposed accept lengths
     n_rounds_max = rounds
@@ -437,6 +443,9 @@ def run_mine(args, cfg):
                      "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
                      "bytes_per_launch": dom_bytes, "us_per_launch": kern_us.get(dominant)},
         "kernel_us": kern_us,
+        "prefill": {"positions": prefill_positions, "ms": prefill_ms,
+                    "positions_per_s": prefill_positions / (prefill_ms * 1e-3),
+                    "note": "eagle3_prefill of the prompts (encode + k/v teacher forcing), timed once"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "draft tokens/s",
                 "h2d_bytes_per_step": int(vaux[0].numel() * 2),
