@@ -8,8 +8,10 @@
 // head are served from one read of each K/V vector.  A key of d = 256 dims is spread over
 // the 32 lanes of a warp (8 dims = 16 bytes per lane); smaller heads put several keys in
 // a warp.  The warp walks blocks of UNR keys per lane group and issues all of a block's
-// K/V loads before computing, keeping an online softmax per lane group (running max in
-// the log2 domain, running sum, running weighted V).  Keys below the committed length
+// K/V loads before computing.  The UNR x G partial scores of a block are reduced across
+// the lane group in one transposed reduction (each lane ends with one full score, takes
+// its exponential, and the probabilities are broadcast for the V update), keeping an
+// online softmax per head (running max in the log2 domain, running sum, weighted V).  Keys below the committed length
 // were written before the chain started, so the first block of those is loaded before
 // the kernel waits on its predecessor (programmatic dependent launch).  The CTA merges
 // its lane groups in shared memory; with more than one split the last CTA of a
@@ -25,19 +27,54 @@ constexpr int kAttnWarps = 8;
 constexpr int kAttnThreads = kAttnWarps * 32;
 constexpr int kMaxAttnSplits = 64;
 
+template <int X>
+struct ILog2 {
+  static constexpr int value = X <= 1 ? 0 : 1 + ILog2<X / 2>::value;
+};
+template <>
+struct ILog2<1> {
+  static constexpr int value = 0;
+};
+
 template <int D, int G>
 struct AttnShape {
-  static constexpr int LPK = D / 8;             // lanes per key
+  static constexpr int LPK = D / 8;             // lanes per key (a segment of the warp)
   static constexpr int KPW = 32 / LPK;          // keys per warp pass
   static constexpr int NP = kAttnWarps * KPW;   // lane groups per CTA
-  static constexpr int UNR = (G >= 8 || D < 128) ? 4 : 8;
+  // keys per lane group per block; UNR * G partial scores fit one segment reduction
+  static constexpr int UNR = (LPK / G) < 8 ? (LPK / G < 1 ? 1 : LPK / G) : 8;
+  static constexpr int N = UNR * G;
+  static constexpr int SH = ILog2<LPK>::value - ILog2<N>::value;  // lane bits below a score index
+  static constexpr int LOG_G = ILog2<G>::value;
   static constexpr size_t kSmem = (size_t)NP * G * D * 4;  // lane-group partial V sums
 };
+
+// Reduce N values held by each lane across a segment of LPK lanes (N <= LPK, both powers
+// of two).  Afterwards lane li of the segment holds the segment total of value index
+// li >> (log2 LPK - log2 N).
+template <int N, int LPK>
+__device__ __forceinline__ float seg_reduce_multi(float (&v)[N], int li) {
+#pragma unroll
+  for (int cnt = N, o = LPK / 2; cnt > 1; cnt >>= 1, o >>= 1) {
+    const bool upper = (li & o) != 0;
+#pragma unroll
+    for (int i = 0; i < cnt / 2; ++i) {
+      const float send = upper ? v[i] : v[i + cnt / 2];
+      const float keep = upper ? v[i + cnt / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o, LPK);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int o = LPK / (2 * N); o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o, LPK);
+  return r;
+}
 
 template <int D, int G>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const AttnParams p) {
   using S = AttnShape<D, G>;
-  constexpr int LPK = S::LPK, KPW = S::KPW, NP = S::NP, UNR = S::UNR;
+  constexpr int LPK = S::LPK, KPW = S::KPW, NP = S::NP, UNR = S::UNR, N = S::N, SH = S::SH;
+  constexpr int LOG_G = S::LOG_G;
   extern __shared__ __align__(16) float sm_acc[];  // [NP][G][D]
   __shared__ float2 sm_ml[NP][G];
   __shared__ int last_sh;
@@ -104,32 +141,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const Attn
     qv[g][0] = a.x * qscale; qv[g][1] = a.y * qscale; qv[g][2] = a.z * qscale; qv[g][3] = a.w * qscale;
     qv[g][4] = c.x * qscale; qv[g][5] = c.y * qscale; qv[g][6] = c.z * qscale; qv[g][7] = c.w * qscale;
   }
-  float mx[G], sum[G], acc[G][8];
+  // Score index of this lane after the segment reduction: (key u_me, head g_me).
+  const int idx_me = li >> SH;
+  const int g_me = idx_me & (G - 1), u_me = idx_me >> LOG_G;
+  float m_me = -INFINITY, l_me = 0.f;  // running max (log2 domain) and sum of head g_me
+  float acc[G][8];                     // running weighted V of this lane's 8 dims, every head
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    mx[g] = -INFINITY;
-    sum[g] = 0.f;
+  for (int g = 0; g < G; ++g)
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[g][i] = 0.f;
-  }
 
-  // The whole warp walks blocks of UNR * KPW keys together (the score reduction shuffles
-  // across the lanes of a key group with a full mask).  Lane groups past the end or on a
-  // bad page take part in the shuffles but do not update their state.
+  // The whole warp walks blocks of UNR keys per lane group together.  Each lane forms
+  // partial dot products of its 8 dims for all UNR x G (key, head) pairs; one segment
+  // reduction leaves every pair's full score in one lane, which also does that pair's
+  // exponential; the probabilities are then broadcast for the V update.  Lane groups
+  // past the end or on a bad page take part in every shuffle with their pairs masked.
   for (int base = base0; base < k1; base += NP * UNR) {
+    unsigned vmask = 0u;
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       const int key = base + u * KPW + grp;
       if (base == base0 && pre[u]) {
         valid[u] = valid[u] && key < k1;
-        continue;
+      } else {
+        valid[u] = false;
+        ku[u] = make_uint4(0u, 0u, 0u, 0u);
+        vu[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (key < k1) load_key(u, key);
       }
-      valid[u] = false;
-      ku[u] = make_uint4(0u, 0u, 0u, 0u);
-      vu[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (key < k1) load_key(u, key);
+      vmask |= valid[u] ? (1u << u) : 0u;
     }
-    float sc[UNR][G];
+    float part_s[N];
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       const float kf[8] = {bf_lo(ku[u].x), bf_hi(ku[u].x), bf_lo(ku[u].y), bf_hi(ku[u].y),
@@ -139,43 +181,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const Attn
         float d = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) d = fmaf(qv[g][i], kf[i], d);
-#pragma unroll
-        for (int o = LPK / 2; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o, LPK);
-        sc[u][g] = valid[u] ? d : -INFINITY;
+        part_s[u * G + g] = d;
       }
     }
+    const bool vld = (vmask >> u_me) & 1u;
+    const float red = seg_reduce_multi<N, LPK>(part_s, li);  // every lane takes part
+    const float sc = vld ? red : -INFINITY;
+    // block max and sum over the keys of head g_me (lanes differing in the key bits)
+    float bm = sc;
+#pragma unroll
+    for (int o = 1 << (SH + LOG_G); o < LPK; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o, LPK));
+    const float m_new = fmaxf(m_me, bm);
+    const float corr = m_new == -INFINITY ? 1.f : exp2f(m_me - m_new);
+    const float pr = vld ? exp2f(sc - m_new) : 0.f;
+    float ps = pr;
+#pragma unroll
+    for (int o = 1 << (SH + LOG_G); o < LPK; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o, LPK);
+    l_me = l_me * corr + ps;
+    m_me = m_new;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      float mb = -INFINITY;
+      const float c = __shfl_sync(0xffffffffu, corr, g << SH, LPK);
 #pragma unroll
-      for (int u = 0; u < UNR; ++u) mb = fmaxf(mb, sc[u][g]);
-      if (mb == -INFINITY) continue;  // no valid key of this lane group in the block
-      const float mn = fmaxf(mx[g], mb);
-      const float corr = exp2f(mx[g] - mn);
-      float l = sum[g] * corr;
+      for (int i = 0; i < 8; ++i) acc[g][i] *= c;
+    }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[g][i] *= corr;
+    for (int u = 0; u < UNR; ++u) {
+      const float vf[8] = {bf_lo(vu[u].x), bf_hi(vu[u].x), bf_lo(vu[u].y), bf_hi(vu[u].y),
+                           bf_lo(vu[u].z), bf_hi(vu[u].z), bf_lo(vu[u].w), bf_hi(vu[u].w)};
 #pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        const float pr = exp2f(sc[u][g] - mn);  // 0 for invalid keys
-        l += pr;
-        const float vf[8] = {bf_lo(vu[u].x), bf_hi(vu[u].x), bf_lo(vu[u].y), bf_hi(vu[u].y),
-                             bf_lo(vu[u].z), bf_hi(vu[u].z), bf_lo(vu[u].w), bf_hi(vu[u].w)};
+      for (int g = 0; g < G; ++g) {
+        const float pg = __shfl_sync(0xffffffffu, pr, (u * G + g) << SH, LPK);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[g][i] = fmaf(pr, vf[i], acc[g][i]);
+        for (int i = 0; i < 8; ++i) acc[g][i] = fmaf(pg, vf[i], acc[g][i]);
       }
-      sum[g] = l;
-      mx[g] = mn;
     }
   }
 
   const int part = warp * KPW + grp;
+  if (u_me == 0 && (li & ((1 << SH) - 1)) == 0) sm_ml[part][g_me] = make_float2(m_me, l_me);
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    if (li == 0) sm_ml[part][g] = make_float2(mx[g], sum[g]);
+  for (int g = 0; g < G; ++g)
 #pragma unroll
     for (int i = 0; i < 8; ++i) sm_acc[((size_t)part * G + g) * D + li * 8 + i] = acc[g][i];
-  }
   __syncthreads();
 
   const size_t slot = ((size_t)b * Hkv + kvh) * p.splits + s;
