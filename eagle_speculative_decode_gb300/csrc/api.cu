@@ -24,8 +24,13 @@ constexpr int kMaxGraphs = 16;
 
 struct Layout {
   size_t rope, q, attn_o, part_o, part_ml, attn_cnt, x1, act, gwork, tokwork, am_slot, am_cnt,
-      round_start, geff, status, genc, total;
+      round_start, geff, status, genc, xp0, xp1, xp2, sumsq, tc_part, tc_cnt, total;
+  size_t tc_items, tc_k, tc_part_elems;
 };
+
+constexpr int kTcMinItems = 3;       // batched projections use the tensor-core GEMM from here
+constexpr size_t kTcCounters = 4096;
+constexpr int kTcEncodeChunk = 2048;  // encode rows per tensor-core launch
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -77,6 +82,16 @@ Layout make_layout(const eagle3_config &c) {
   L.geff = take(B * 4);
   L.status = take(4);
   L.genc = take(std::max<size_t>(B * (c.max_gamma + 1), kPrefillChunk) * n * 4);
+  // tensor-core path: the three bf16 parts of x, norm sums, split-K partials and counters
+  L.tc_items = std::max<size_t>(B * (c.max_gamma + 1), kPrefillChunk);
+  L.tc_k = std::max(std::max<size_t>(2 * n, (size_t)c.n_ff), hd);
+  L.xp0 = take(L.tc_items * L.tc_k * 2);
+  L.xp1 = take(L.tc_items * L.tc_k * 2);
+  L.xp2 = take(L.tc_items * L.tc_k * 2);
+  L.sumsq = take(L.tc_items * 2 * 4);
+  L.tc_part_elems = (size_t)2 * 160 * 128 * 256;
+  L.tc_part = take(L.tc_part_elems * 4);
+  L.tc_cnt = take(kTcCounters * 4);
   L.total = align_up(off, 256);
   return L;
 }
@@ -134,6 +149,11 @@ struct eagle3_ctx {
   int ev_cap, ev_used;
   std::vector<int> ev_label;
   std::vector<cudaEvent_t> ev_pool;
+  // tensor-core path
+  int tc_ok, tc_min_items;
+  uint16_t *xp0, *xp1, *xp2;  // the three bf16 parts of x
+  float *sumsq, *tc_part;
+  unsigned *tc_cnt;
 };
 
 namespace {
@@ -210,8 +230,71 @@ cudaError_t launched(eagle3_ctx *ctx, cudaStream_t st, cudaError_t e, int label)
   return e;
 }
 
+// Tensor-core GEMM of one projection over `items` activation rows: x split into three bf16
+// parts (not for the encode, whose features are bf16 already), then the tcgen05 kernel.
+cudaError_t tc_items(eagle3_ctx *ctx, const GemvParams &p, int items, cudaStream_t st, bool pdl) {
+  const eagle3_config &c = ctx->c;
+  TcLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  L.p = p;
+  L.p.item0 = 0;
+  L.p.items = items;
+  L.M = items;
+  L.sumsq = ctx->sumsq;
+  L.part = ctx->tc_part;
+  L.part_elems = ctx->L.tc_part_elems;
+  L.tile_cnt = ctx->tc_cnt;
+  L.tile_cnt_elems = kTcCounters;
+  L.num_sms = ctx->num_sms;
+  const int n = c.n_embd, qr = c.n_head * c.head_dim, kr = c.n_head_kv * c.head_dim;
+  switch (p.mode) {
+    case GM_ENCODE: L.a0 = ctx->w.fc; L.a0_rows = n; break;
+    case GM_QKV:
+      L.a0 = ctx->w.q; L.a0_rows = qr;
+      L.a1 = ctx->w.k; L.a1_rows = kr;
+      L.a2 = ctx->w.v; L.a2_rows = kr;
+      break;
+    case GM_O: L.a0 = ctx->w.o; L.a0_rows = n; break;
+    case GM_GATEUP:
+      L.a0 = ctx->w.gate; L.a0_rows = c.n_ff;
+      L.a1 = ctx->w.up; L.a1_rows = c.n_ff;
+      break;
+    case GM_DOWN: L.a0 = ctx->w.down; L.a0_rows = n; break;
+    default: L.a0 = ctx->w.lm_head; L.a0_rows = c.draft_vocab; break;
+  }
+  const int label = (p.mode == GM_QKV && p.row_base > 0) ? PH_KV : gemv_label(p.mode);
+  if (p.mode == GM_ENCODE) {
+    // bf16 features straight from the caller's rows, in chunks of kTcEncodeChunk items
+    for (int i0 = 0; i0 < items; i0 += kTcEncodeChunk) {
+      L.M = std::min(kTcEncodeChunk, items - i0);
+      L.p.items = L.M;
+      L.p.out_f = p.out_f + (size_t)i0 * p.rows;
+      L.b0 = p.xb + (size_t)i0 * p.K;
+      cudaError_t e = launched(ctx, st, tc_launch(L, st, pdl), label);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  } else {
+    cudaError_t e = launched(
+        ctx, st, tc_prep_launch(p, items, ctx->xp0, ctx->xp1, ctx->xp2, ctx->sumsq, st, pdl), PH_SMALL);
+    if (e != cudaSuccess) return e;
+    L.b0 = ctx->xp0;
+    L.b1 = ctx->xp1;
+    L.b2 = ctx->xp2;
+  }
+  return launched(ctx, st, tc_launch(L, st, pdl), label);
+}
+
+bool use_tc(const eagle3_ctx *ctx, const GemvParams &p, int items) {
+  if (!ctx->tc_ok || items < ctx->tc_min_items) return false;
+  if (p.mode != GM_ENCODE && (size_t)items > ctx->L.tc_items) return false;
+  if (p.mode == GM_LMHEAD && items > tc_tile_items(items, p.mode)) return false;  // one item tile
+  return true;
+}
+
 // Launch a GEMV over `items` activation rows in as many launches as shared memory needs.
 cudaError_t gemv_items(eagle3_ctx *ctx, GemvParams p, int items, cudaStream_t st, bool pdl) {
+  if (use_tc(ctx, p, items)) return tc_items(ctx, p, items, st, pdl);
   const int nb = gemv_items_per_launch(p.mode, p.K, items);
   const int label = (p.mode == GM_QKV && p.row_base > 0) ? PH_KV : gemv_label(p.mode);
   for (int i0 = 0; i0 < items; i0 += nb) {
@@ -413,6 +496,14 @@ GraphKey chain_key(const ChainArgs &a) {
   return k;
 }
 
+// Forget every captured chain (after the work already enqueued on the last stream).
+void drop_graphs(eagle3_ctx *ctx) {
+  if (ctx->graphs.empty()) return;
+  cudaStreamSynchronize(ctx->last_stream);
+  for (auto &g : ctx->graphs) cudaGraphExecDestroy(g.exec);
+  ctx->graphs.clear();
+}
+
 cudaError_t run_chain_graph(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) {
   const GraphKey key = chain_key(a);
   for (auto &g : ctx->graphs) {
@@ -553,6 +644,12 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
   ctx->geff = reinterpret_cast<int32_t *>(b + L.geff);
   ctx->status = reinterpret_cast<int *>(b + L.status);
   ctx->genc = reinterpret_cast<float *>(b + L.genc);
+  ctx->xp0 = reinterpret_cast<uint16_t *>(b + L.xp0);
+  ctx->xp1 = reinterpret_cast<uint16_t *>(b + L.xp1);
+  ctx->xp2 = reinterpret_cast<uint16_t *>(b + L.xp2);
+  ctx->sumsq = reinterpret_cast<float *>(b + L.sumsq);
+  ctx->tc_part = reinterpret_cast<float *>(b + L.tc_part);
+  ctx->tc_cnt = reinterpret_cast<unsigned *>(b + L.tc_cnt);
   ctx->graph_mode = 1;
   ctx->last_stream = st;
   int dev = 0;
@@ -561,6 +658,17 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
       gemv_prepare() != cudaSuccess || attn_prepare() != cudaSuccess) {
     delete ctx;
     return EAGLE3_ERR_CUDA;
+  }
+
+  // The tensor-core path needs 64-aligned K dims, 128-row q / k / v blocks that hold whole
+  // heads (or whole heads that hold whole 128-row tiles) and a driver with tensor maps.
+  {
+    const int n = cfg->n_embd, d = cfg->head_dim;
+    const int qr = cfg->n_head * d, kr = cfg->n_head_kv * d;
+    const bool geo = n % 64 == 0 && cfg->n_ff % 64 == 0 && qr % 128 == 0 && kr % 128 == 0 &&
+                     qr % 64 == 0 && (d % 128 == 0 || 128 % d == 0) && cfg->n_ff % 64 == 0;
+    ctx->tc_ok = geo && tc_prepare() == cudaSuccess ? 1 : 0;
+    ctx->tc_min_items = kTcMinItems;
   }
 
   // RoPE table: angle p * theta^(-2i/R) in double, stored as float32 (cos, sin).
@@ -585,6 +693,7 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
   if (e == cudaSuccess) e = cudaMemsetAsync(b + L.am_slot, 0, (size_t)cfg->max_batch * 8, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(b + L.am_cnt, 0, 64 * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(b + L.status, 0, 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(b + L.tc_cnt, 0, kTcCounters * 4, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {
     delete ctx;
@@ -606,6 +715,16 @@ int eagle3_destroy(eagle3_ctx *ctx) {
 int eagle3_set_graph_mode(eagle3_ctx *ctx, int enabled) {
   if (!ctx) return EAGLE3_ERR_INVALID_ARG;
   ctx->graph_mode = enabled ? 1 : 0;
+  return EAGLE3_OK;
+}
+
+int eagle3_set_tc_min_items(eagle3_ctx *ctx, int min_items) {
+  if (!ctx || min_items < 0) return EAGLE3_ERR_INVALID_ARG;
+  const int v = min_items == 0 ? kTcMinItems : min_items;
+  if (v != ctx->tc_min_items) {
+    ctx->tc_min_items = v;
+    drop_graphs(ctx);
+  }
   return EAGLE3_OK;
 }
 

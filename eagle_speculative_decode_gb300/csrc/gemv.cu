@@ -24,324 +24,10 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace e3 {
-
-template <int MODE>
-__device__ __forceinline__ const uint16_t *row_ptr(const GemvParams &p, int lr) {
-  const size_t K = (size_t)p.K;
-  if constexpr (MODE == GM_GATEUP) {
-    return ((lr & 1) ? p.w1 : p.w0) + (size_t)(lr >> 1) * K;
-  } else if constexpr (MODE == GM_QKV) {
-    const int d = p.head_dim, R = p.rope_dims;
-    const int qr = p.n_head * d, kr = p.n_head_kv * d;
-    if (lr < qr + kr) {
-      const bool isq = lr < qr;
-      const uint16_t *base = isq ? p.w0 : p.w1;
-      const int rr = isq ? lr : lr - qr;
-      const int head = rr / d, li = rr - head * d;
-      // RoPE partners (i, i + R/2) sit on adjacent logical rows 2i, 2i + 1.
-      const int dim = li < R ? ((li & 1) ? (li >> 1) + (R >> 1) : (li >> 1)) : li;
-      return base + ((size_t)head * d + dim) * K;
-    }
-    return p.w2 + (size_t)(lr - qr - kr) * K;
-  } else {
-    return p.w0 + (size_t)lr * K;
-  }
-}
-
-template <int N>
-struct Log2 {
-  static constexpr int value = (N >= 32) ? 5 : (N >= 16) ? 4 : (N >= 8) ? 3 : (N >= 4) ? 2 : (N >= 2) ? 1 : 0;
-};
-
-// Reduce N = 2^S values held by every lane across the warp.  Afterwards lane l holds
-// the warp total of value index idx(l) = bits 4..(5-S) of l read as an S-bit number;
-// lanes whose low (5-S) bits are zero are the designated writers.
-template <int N>
-__device__ __forceinline__ float warp_reduce_multi(float (&v)[N], int lane) {
-  static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "1..32 values, a power of two");
-#pragma unroll
-  for (int cnt = N, o = 16; cnt > 1; cnt >>= 1, o >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < cnt / 2; ++i) {
-      const float send = upper ? v[i] : v[i + cnt / 2];
-      const float keep = upper ? v[i + cnt / 2] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-    }
-  }
-  float r = v[0];
-#pragma unroll
-  for (int o = 16 >> Log2<N>::value; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
-  return r;
-}
-
-template <int N>
-__device__ __forceinline__ int warp_reduce_index(int lane) {
-  int idx = 0;
-#pragma unroll
-  for (int s = 0; s < Log2<N>::value; ++s) idx = (idx << 1) | ((lane >> (4 - s)) & 1);
-  return idx;
-}
-
-template <int N>
-__device__ __forceinline__ bool warp_reduce_writer(int lane) {
-  return (lane & ((1 << (5 - Log2<N>::value)) - 1)) == 0;
-}
-
-// ------------------------------------------------------------------ x staging
-template <int MODE>
-struct ModeTraits {
-  static constexpr bool kBf16X = MODE == GM_ENCODE;  // x kept as the caller's bf16
-  static constexpr int kHalves = MODE == GM_QKV ? 2 : 1;  // separately normalised K halves
-  static constexpr bool kNorm = MODE == GM_QKV || MODE == GM_GATEUP || MODE == GM_LMHEAD;
-  static constexpr int kUnit = (MODE == GM_QKV || MODE == GM_GATEUP) ? 2 : 1;  // row pairing
-};
-
-__device__ __forceinline__ float sq8(float4 a, float4 b) {
-  return a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z +
-         b.w * b.w;
-}
-__device__ __forceinline__ float4 mul4(float4 a, float w0, float w1, float w2, float w3) {
-  return make_float4(a.x * w0, a.y * w1, a.z * w2, a.w * w3);
-}
-
-// Writes x[m, k] (times the norm gain where the op normalises) into shared memory and
-// accumulates this thread's share of sum(x^2) per item and K half into ss.
-template <int NB, int MODE>
-__device__ void stage_x(const GemvParams &p, unsigned char *xmem, float (&ss)[NB][ModeTraits<MODE>::kHalves]) {
-  using T = ModeTraits<MODE>;
-  const int K = p.K, KV = K >> 3, tid = threadIdx.x;
-#pragma unroll
-  for (int m = 0; m < NB; ++m)
-#pragma unroll
-    for (int h = 0; h < T::kHalves; ++h) ss[m][h] = 0.f;
-  for (int m = 0; m < NB; ++m) {
-    const bool live = m < p.items;
-    const int item = p.item0 + m;
-    if constexpr (T::kBf16X) {
-      uint4 *xb = reinterpret_cast<uint4 *>(xmem) + (size_t)m * KV;
-      const uint4 *src = reinterpret_cast<const uint4 *>(p.xb + (size_t)item * K);
-      for (int kv = tid; kv < KV; kv += kGemvThreads) xb[kv] = live ? src[kv] : make_uint4(0u, 0u, 0u, 0u);
-      continue;
-    }
-    float4 *x0 = reinterpret_cast<float4 *>(xmem) + (size_t)(m * 2) * KV;
-    float4 *x1 = x0 + KV;
-    if (!live) {
-      for (int kv = tid; kv < KV; kv += kGemvThreads) {
-        x0[kv] = make_float4(0.f, 0.f, 0.f, 0.f);
-        x1[kv] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      continue;
-    }
-    if constexpr (MODE == GM_O || MODE == GM_DOWN) {
-      const float4 *src = reinterpret_cast<const float4 *>(p.xf + (size_t)item * K);
-      for (int kv = tid; kv < KV; kv += kGemvThreads) {
-        x0[kv] = src[2 * kv];
-        x1[kv] = src[2 * kv + 1];
-      }
-    } else if constexpr (MODE == GM_GATEUP || MODE == GM_LMHEAD) {
-      const float4 *src = reinterpret_cast<const float4 *>(p.xf + (size_t)item * K);
-      const uint4 *wn = reinterpret_cast<const uint4 *>(p.norm0);
-      for (int kv = tid; kv < KV; kv += kGemvThreads) {
-        const float4 a = src[2 * kv], b = src[2 * kv + 1];
-        const uint4 w = wn[kv];
-        ss[m][0] += sq8(a, b);
-        x0[kv] = mul4(a, bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
-        x1[kv] = mul4(b, bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w));
-      }
-    } else if constexpr (MODE == GM_QKV) {
-      // [embed(tok) * w_in ; g * w_hid]; the two RMSNorm scales come later
-      const int n = p.n_embd, NV = n >> 3;
-      const PairItem it = resolve_pair(p.pairs, item, n);
-      int tok = it.tok;
-      if (tok < 0 || tok >= p.target_vocab) {
-        // only rows whose K/V are kept (or the chain's q) may report a bad token
-        if (tid == 0 && (it.write_kv || p.row_base == 0)) set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
-        tok = 0;
-      }
-      const uint4 *er = reinterpret_cast<const uint4 *>(p.embed + (size_t)tok * n);
-      const float4 *gr = reinterpret_cast<const float4 *>(it.g);
-      const uint4 *wi = reinterpret_cast<const uint4 *>(p.norm0);
-      const uint4 *wh = reinterpret_cast<const uint4 *>(p.norm1);
-      for (int kv = tid; kv < NV; kv += kGemvThreads) {
-        const uint4 u = er[kv];
-        const float4 ea = make_float4(bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y));
-        const float4 eb = make_float4(bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w));
-        const uint4 w = wi[kv];
-        ss[m][0] += sq8(ea, eb);
-        x0[kv] = mul4(ea, bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
-        x1[kv] = mul4(eb, bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w));
-        const float4 a = gr[2 * kv], b = gr[2 * kv + 1];
-        const uint4 hw = wh[kv];
-        ss[m][T::kHalves - 1] += sq8(a, b);
-        x0[NV + kv] = mul4(a, bf_lo(hw.x), bf_hi(hw.x), bf_lo(hw.y), bf_hi(hw.y));
-        x1[NV + kv] = mul4(b, bf_lo(hw.z), bf_hi(hw.z), bf_lo(hw.w), bf_hi(hw.w));
-      }
-    }
-  }
-}
-
-// x vector kv of item m as 8 floats.
-template <int MODE>
-__device__ __forceinline__ void load_x8(const unsigned char *xmem, int KV, int m, int kv, float (&x)[8]) {
-  if constexpr (ModeTraits<MODE>::kBf16X) {
-    const uint4 u = reinterpret_cast<const uint4 *>(xmem)[(size_t)m * KV + kv];
-    x[0] = bf_lo(u.x); x[1] = bf_hi(u.x); x[2] = bf_lo(u.y); x[3] = bf_hi(u.y);
-    x[4] = bf_lo(u.z); x[5] = bf_hi(u.z); x[6] = bf_lo(u.w); x[7] = bf_hi(u.w);
-  } else {
-    const float4 *xs = reinterpret_cast<const float4 *>(xmem);
-    const float4 a = xs[(size_t)(m * 2) * KV + kv], b = xs[(size_t)(m * 2 + 1) * KV + kv];
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-  }
-}
-
-__device__ __forceinline__ float dot8(const uint4 w, const float (&x)[8], float a) {
-  a = fmaf(bf_lo(w.x), x[0], a); a = fmaf(bf_hi(w.x), x[1], a);
-  a = fmaf(bf_lo(w.y), x[2], a); a = fmaf(bf_hi(w.y), x[3], a);
-  a = fmaf(bf_lo(w.z), x[4], a); a = fmaf(bf_hi(w.z), x[5], a);
-  a = fmaf(bf_lo(w.w), x[6], a); a = fmaf(bf_hi(w.w), x[7], a);
-  return a;
-}
-
-// ---------------------------------------------------------------- epilogues
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
-
-template <int NB, int MODE>
-__device__ void epilogue(const GemvParams &p, const float *accs, int row0, int nrows) {
-  const int tid = threadIdx.x;
-  if constexpr (MODE == GM_ENCODE || MODE == GM_O || MODE == GM_DOWN) {
-    for (int idx = tid; idx < nrows * NB; idx += kGemvThreads) {
-      const int m = idx % NB, r = idx / NB;
-      if (m >= p.items) continue;
-      const int item = p.item0 + m, row = row0 + r;
-      float v = accs[r * NB + m];
-      if constexpr (MODE != GM_ENCODE) v += p.res[(size_t)item * p.rows + row];
-      p.out_f[(size_t)item * p.rows + row] = v;
-      if constexpr (MODE == GM_DOWN) {
-        if (p.dbg_f) p.dbg_f[(size_t)item * p.dbg_stride_b + p.dbg_off + row] = v;
-      }
-    }
-  } else if constexpr (MODE == GM_GATEUP) {
-    const int npairs = nrows >> 1;
-    for (int idx = tid; idx < npairs * NB; idx += kGemvThreads) {
-      const int m = idx % NB, pr = idx / NB;
-      if (m >= p.items) continue;
-      const int item = p.item0 + m;
-      const float gate = accs[(2 * pr) * NB + m], up = accs[(2 * pr + 1) * NB + m];
-      p.out_f[(size_t)item * p.n_ff + ((row0 >> 1) + pr)] = silu_f(gate) * up;
-    }
-  } else if constexpr (MODE == GM_QKV) {
-    const int d = p.head_dim, R = p.rope_dims, half = R >> 1;
-    const int qr = p.n_head * d, kr = p.n_head_kv * d;
-    const int npairs = nrows >> 1;
-    for (int idx = tid; idx < npairs * NB; idx += kGemvThreads) {
-      const int m = idx % NB, pr = idx / NB;
-      if (m >= p.items) continue;
-      const int item = p.item0 + m;
-      const int lr = p.row_base + row0 + 2 * pr;  // even logical row
-      float a = accs[(2 * pr) * NB + m], b = accs[(2 * pr + 1) * NB + m];
-      const PairItem it = resolve_pair(p.pairs, item, p.n_embd);
-      const int region = lr < qr ? 0 : (lr < qr + kr ? 1 : 2);
-      const int rr = region == 0 ? lr : (region == 1 ? lr - qr : lr - qr - kr);
-      const int head = rr / d, li = rr - head * d;
-      int dim0 = li, dim1 = li + 1;
-      if (region < 2 && li < R) {
-        dim0 = li >> 1;
-        dim1 = dim0 + half;
-        int pos = it.pos;
-        if (pos < 0 || pos >= p.max_cache_len) pos = 0;
-        const float2 cs = p.rope[(size_t)pos * half + dim0];
-        const float ra = a * cs.x - b * cs.y;
-        const float rb = b * cs.x + a * cs.y;
-        a = ra;
-        b = rb;
-      }
-      if (region == 0) {
-        float *q = p.out_f + (size_t)item * qr + (size_t)head * d;
-        q[dim0] = a;
-        q[dim1] = b;
-      } else if (it.write_kv) {
-        const int pos = it.pos;
-        if (pos < 0 || pos >= p.max_cache_len) {
-          set_status(p.status, EAGLE3_DEV_BAD_POSITION);
-          continue;
-        }
-        const int pg = p.page_table[(size_t)it.b * p.max_pages + pos / p.page_size];
-        if (pg < 0 || pg >= p.num_pages) {
-          set_status(p.status, EAGLE3_DEV_BAD_PAGE);
-          continue;
-        }
-        uint16_t *pool = region == 1 ? p.k_pool : p.v_pool;
-        uint16_t *dst = pool + (((size_t)pg * p.n_head_kv + head) * p.page_size + pos % p.page_size) * d;
-        dst[dim0] = f2bf(a);
-        dst[dim1] = f2bf(b);
-      }
-    }
-  } else if constexpr (MODE == GM_LMHEAD) {
-    // Per item: best (logit, lowest row) over this CTA's rows, then a global 64-bit
-    // atomicMax of (order key << 32 | ~row); the last CTA decodes and applies d2t.
-    __shared__ unsigned long long best_sh[kGemvWarps];
-    __shared__ int last_sh;
-    for (int m = 0; m < p.items; ++m) {
-      const int item = p.item0 + m;
-      unsigned long long best = 0ull;
-      for (int r = tid; r < nrows; r += kGemvThreads) {
-        const float v = accs[r * NB + m];
-        const int row = row0 + r;
-        if (p.dbg_f) p.dbg_f[(size_t)item * p.dbg_stride_b + p.dbg_off + row] = v;
-        const unsigned long long key =
-            ((unsigned long long)float_order_key(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);
-        best = key > best ? key : best;
-      }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-        best = other > best ? other : best;
-      }
-      if ((tid & 31) == 0) best_sh[tid >> 5] = best;
-      consumer_sync();
-      if (tid == 0) {
-        unsigned long long b = 0ull;
-        for (int w = 0; w < kGemvWarps; ++w) b = best_sh[w] > b ? best_sh[w] : b;
-        if (nrows > 0) atomicMax(p.am_slot + item, b);
-      }
-      consumer_sync();
-    }
-    if (tid == 0) {
-      __threadfence();
-      const unsigned prev = atomicAdd(p.am_count, 1u);
-      last_sh = (prev == gridDim.x - 1) ? 1 : 0;
-    }
-    consumer_sync();
-    if (last_sh) {
-      __threadfence();
-      for (int m = tid; m < p.items; m += kGemvThreads) {
-        const int item = p.item0 + m;
-        const unsigned long long key = atomicExch(p.am_slot + item, 0ull);
-        uint32_t id = 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
-        if (id >= (uint32_t)p.draft_vocab) {
-          set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
-          id = 0;
-        }
-        long long tgt = (long long)id + p.d2t[id];
-        if (tgt < 0 || tgt >= p.target_vocab) {
-          set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
-          tgt = 0;
-        }
-        const bool valid = p.step < p.gamma_eff[item];
-        const size_t o = (size_t)item * p.gamma + p.step;
-        p.draft_tok[o] = valid ? (int32_t)tgt : -1;
-        if (p.draft_id) p.draft_id[o] = valid ? (int32_t)id : -1;
-        if (p.next_tok) p.next_tok[item] = (int32_t)tgt;
-      }
-      if (tid == 0) *p.am_count = 0u;
-    }
-  }
-}
 
 // -------------------------------------------------------------------- kernel
 constexpr int kStageBytes = 32 * 1024;

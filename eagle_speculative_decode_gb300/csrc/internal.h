@@ -19,6 +19,27 @@ cudaError_t gemv_prepare();
 int gemv_items_per_launch(int mode, int K, int items);
 cudaError_t gemv_launch(const GemvParams &p, int grid, cudaStream_t st, bool pdl);
 
+// Tensor-core GEMM (gemm_tc.cu): weights [rows, K] against M activation rows.
+constexpr size_t kTcSmemLimit = 220 * 1024;
+struct TcLaunch {
+  GemvParams p;                 // mode, rows, row_base, K and the epilogue's parameters
+  int M;                        // activation rows (items)
+  const void *a0, *a1, *a2;     // weight matrices of the mode (see gemm_tc.cu)
+  int a0_rows, a1_rows, a2_rows;
+  const uint16_t *b0, *b1, *b2; // activations bf16 [M, K]: one part (encode) or three
+  const float *sumsq;           // [M][halves] (norm modes)
+  float *part;                  // split-K partials
+  size_t part_elems;
+  unsigned *tile_cnt;           // split-K counters (zero between launches)
+  size_t tile_cnt_elems;
+  int num_sms;
+};
+cudaError_t tc_prepare();
+int tc_tile_items(int M, int mode);
+cudaError_t tc_launch(const TcLaunch &L, cudaStream_t st, bool pdl);
+cudaError_t tc_prep_launch(const GemvParams &p, int M, uint16_t *x0, uint16_t *x1, uint16_t *x2,
+                           float *sumsq, cudaStream_t st, bool pdl);
+
 bool attn_supported(int head_dim, int group);
 cudaError_t attn_prepare();
 cudaError_t attn_launch(const AttnParams &p, int B, cudaStream_t st, bool pdl);

@@ -77,6 +77,10 @@ class DraftModel:
     def set_graph_mode(self, on: bool):
         B.eagle3_set_graph_mode(self.ctx, on)
 
+    def set_tc_min_items(self, min_items: int):
+        """Items from which projections use the tensor cores (0: the default)."""
+        B.eagle3_set_tc_min_items(self.ctx, min_items)
+
     def status(self) -> int:
         return B.eagle3_get_status(self.ctx)
 

@@ -58,7 +58,13 @@ FULL = Geometry(n_embd=4096, n_head=16, n_head_kv=4, head_dim=256, rope_dims=64,
                 rope_theta=1e7, rms_eps=1e-6, n_ff=12288, draft_vocab=32000,
                 target_vocab=248320)
 
-GEOMETRIES = {"tiny": TINY, "full": FULL}
+# Small drafter whose q / k / v blocks are whole 128-row tiles (8:2 GQA of 64-wide
+# heads), so that batched projections take the tensor-core GEMM at test sizes.
+SMALL = Geometry(n_embd=256, n_head=8, n_head_kv=2, head_dim=64, rope_dims=16,
+                 rope_theta=1e7, rms_eps=1e-6, n_ff=768, draft_vocab=1024,
+                 target_vocab=4096)
+
+GEOMETRIES = {"tiny": TINY, "small": SMALL, "full": FULL}
 
 # Tensor order fixes the per-tensor sub-seed.
 WEIGHT_NAMES = ("fc", "in_norm", "hidden_norm", "q", "k", "v", "o", "post_norm",

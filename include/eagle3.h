@@ -220,6 +220,15 @@ int eagle3_get_status(eagle3_ctx *ctx, int *device_status);
  * steps captured per (B, gamma, flags, buffer set); 0 launches the kernels directly. */
 int eagle3_set_graph_mode(eagle3_ctx *ctx, int enabled);
 
+/* Smallest number of activation rows (items) for which a projection runs on the tensor
+ * cores (tcgen05, the weights read once for up to 128 items per tile) instead of the
+ * CUDA-core weight-streaming GEMV.  0 restores the default (3); a value above every batch
+ * keeps all projections on the GEMV.  The tensor-core path needs a geometry whose K dims
+ * are multiples of 64 and whose q / k / v blocks are whole 128-row tiles; otherwise the
+ * GEMV is used whatever the threshold.  Takes effect for later calls (a captured chain
+ * graph is re-captured).  Returns EAGLE3_ERR_INVALID_ARG for a negative value. */
+int eagle3_set_tc_min_items(eagle3_ctx *ctx, int min_items);
+
 /* ---- measurement (no counterpart on the pages; used by the benchmark) ----------------- */
 
 /* Number of kernels this context has launched since eagle3_init (a graph replay counts
