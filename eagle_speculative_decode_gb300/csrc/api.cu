@@ -288,7 +288,6 @@ cudaError_t tc_items(eagle3_ctx *ctx, const GemvParams &p, int items, cudaStream
 bool use_tc(const eagle3_ctx *ctx, const GemvParams &p, int items) {
   if (!ctx->tc_ok || items < ctx->tc_min_items) return false;
   if (p.mode != GM_ENCODE && (size_t)items > ctx->L.tc_items) return false;
-  if (p.mode == GM_LMHEAD && items > tc_tile_items(items, p.mode)) return false;  // one item tile
   return true;
 }
 

@@ -191,6 +191,31 @@ __device__ __forceinline__ float dot8(const uint4 w, const float (&x)[8], float 
 // ---------------------------------------------------------------- epilogues
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
+// Last CTA of an lm_head launch: decode each item's winning (logit, row) key, map the
+// draft id through d2t and write the step's tokens; the slots are left at zero.
+__device__ __forceinline__ void lmhead_finalize(const GemvParams &p, int item0, int items, int tid,
+                                                int nthreads) {
+  for (int m = tid; m < items; m += nthreads) {
+    const int item = item0 + m;
+    const unsigned long long key = atomicExch(p.am_slot + item, 0ull);
+    uint32_t id = 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
+    if (id >= (uint32_t)p.draft_vocab) {
+      set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
+      id = 0;
+    }
+    long long tgt = (long long)id + p.d2t[id];
+    if (tgt < 0 || tgt >= p.target_vocab) {
+      set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
+      tgt = 0;
+    }
+    const bool valid = p.step < p.gamma_eff[item];
+    const size_t o = (size_t)item * p.gamma + p.step;
+    p.draft_tok[o] = valid ? (int32_t)tgt : -1;
+    if (p.draft_id) p.draft_id[o] = valid ? (int32_t)id : -1;
+    if (p.next_tok) p.next_tok[item] = (int32_t)tgt;
+  }
+}
+
 // Row stride (floats) of the accumulator tile accs[row][item].  Wide tiles (the tensor-core
 // GEMM) pad it to an odd stride so that walking rows hits distinct banks; they also walk
 // rows fastest so that the global writes of one item are contiguous.
@@ -345,25 +370,7 @@ __device__ void epilogue(const GemvParams &p, const float *accs, int row0, int n
     consumer_sync();
     if (last_sh) {
       __threadfence();
-      for (int m = tid; m < p.items; m += kGemvThreads) {
-        const int item = p.item0 + m;
-        const unsigned long long key = atomicExch(p.am_slot + item, 0ull);
-        uint32_t id = 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
-        if (id >= (uint32_t)p.draft_vocab) {
-          set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
-          id = 0;
-        }
-        long long tgt = (long long)id + p.d2t[id];
-        if (tgt < 0 || tgt >= p.target_vocab) {
-          set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
-          tgt = 0;
-        }
-        const bool valid = p.step < p.gamma_eff[item];
-        const size_t o = (size_t)item * p.gamma + p.step;
-        p.draft_tok[o] = valid ? (int32_t)tgt : -1;
-        if (p.draft_id) p.draft_id[o] = valid ? (int32_t)id : -1;
-        if (p.next_tok) p.next_tok[item] = (int32_t)tgt;
-      }
+      lmhead_finalize(p, p.item0, p.items, tid, kGemvThreads);
       if (tid == 0) *p.am_count = 0u;
     }
   }

@@ -3,20 +3,28 @@
 // from HBM once for the whole batch.
 //
 // y[item, row] = sum_k W[row, k] * x[item, k].  The MMA's M side is 128 weight rows, its N
-// side the items (16..256), K in 64-element stages ("swap AB": the weights are the A
+// side the items (16..128), K in 64-element k-tiles ("swap AB": the weights are the A
 // operand, the activations the B operand; both K-major in shared memory, 128-byte
 // swizzled, loaded by TMA).  float32 activations are split into three bf16 parts
 // x = x0 + x1 + x2 (exact to float32's 24 bits) and every part is multiplied; bf16
-// features (the encode) are one part.  The products of x0 rotate over up to four TMEM
-// accumulators and those of x1 and x2 (2^-8 smaller) share one more, so that no float32
-// accumulator takes more than a quarter of the K slices; the epilogue adds them in a
-// fixed order.  Accumulators are read back with tcgen05.ld for the same fused epilogues
-// as the CUDA-core GEMV (epilogue.cuh).  Matrices with few 128-row tiles split K across
-// CTAs; the last CTA of a tile adds the splits in a fixed order.
+// features (the encode) are one part.
 //
-// Warp roles (320 threads): warps 0-7 epilogue (two per TMEM lane quadrant), warp 8 TMA
-// producer, warp 9 MMA issuer (one elected thread) and TMEM owner.  Every mbarrier wait
-// is bounded (EAGLE3_DEV_TIMEOUT), and no copy is left in flight when the CTA finishes.
+// Persistent stream-K schedule: one CTA per SM walks an equal share of all
+// (tile, k-tile) units, tile by tile, so no SM idles in a tail wave.  A tile that two or
+// more CTAs share is finished by the last of them, which adds the others' float32
+// partial sums in CTA order.
+//
+// The three parts sit on consecutive rows of the B tile, so one MMA of width 3N multiplies
+// them all (the x0, x1, x2 products land in adjacent TMEM column blocks).  Precision: a
+// TMEM accumulator takes at most kTcChunk k-tiles (4 * kTcChunk MMAs), then the epilogue
+// warps add the chunk into float32 registers; two TMEM buffers alternate, so the MMAs do
+// not wait for the drain.
+//
+// Warp roles (352 threads): warps 0-7 drain TMEM and run the fused epilogues (two warps
+// per TMEM lane quadrant), warp 8 streams the weight tiles (deep ring: the HBM stream),
+// warp 9 issues the MMAs (one thread) and owns TMEM, warp 10 streams the activation
+// tiles (shallow ring: they come from L2).  Every mbarrier wait is bounded
+// (EAGLE3_DEV_TIMEOUT), and no copy is left in flight when the CTA finishes.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -29,10 +37,10 @@
 namespace e3 {
 
 constexpr int kTcM = 128;          // MMA M (weight rows per tile)
-constexpr int kTcK = 64;           // K per stage: one 128-byte swizzle row of bf16
-constexpr int kTcThreads = 320;
-constexpr int kTcProducerWarp = 8;
-constexpr int kTcMmaWarp = 9;
+constexpr int kTcK = 64;           // k-tile: one 128-byte swizzle row of bf16
+constexpr int kTcAWarp = 8, kTcMmaWarp = 9, kTcBWarp = 10;
+constexpr int kTcThreads = 352;
+constexpr int kTcChunk = 8;        // k-tiles per TMEM accumulation chunk
 
 struct TcArgs {
   CUtensorMap a0;   // weight matrix of the tile (q / fc / o / gate / down / lm_head)
@@ -41,14 +49,13 @@ struct TcArgs {
   CUtensorMap b0;   // activations [M, K] bf16: the bf16 features, or x0 of the split
   CUtensorMap b1;   // x1 of the split
   CUtensorMap b2;   // x2 of the split
-  GemvParams p;     // epilogue parameters; p.items / p.item0 set per item tile in-kernel
+  GemvParams p;     // epilogue parameters (p.items = M, p.item0 = 0)
   const float *sumsq;  // [M][halves] sum of squares of the staged x (norm modes)
-  float *part;         // split-K partials [ksplit][halves][item_tiles * N][rows]
-  unsigned *tile_cnt;  // split-K arrival counters [row_tiles * item_tiles]
+  float *part;         // stream-K partials [grid][2][halves][N][128]
+  unsigned *tile_cnt;  // stream-K arrival counters [tiles], zero between launches
   int M;               // items in total
-  int ksplit, kper;    // K splits and K columns per split (a multiple of 64)
-  int item_tiles, row_tiles;
-  int nstage;
+  int item_tiles, row_tiles, ktiles;
+  int units;           // tiles * ktiles
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -103,8 +110,8 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 16 consecutive float32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+// 16 consecutive float32 columns of this thread's TMEM lane, added into acc.
+__device__ __forceinline__ void tmem_add16(uint32_t taddr, float *acc) {
   uint32_t r[16];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -114,98 +121,426 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(r[i]);
 }
 
-// ------------------------------------------------------------------ row maps
-// Logical row (relative to the tile) of physical A-tile row r: the tile's rows follow the
-// weight matrix; the epilogues expect RoPE partners (i, i + R/2) and gate/up on adjacent
-// logical rows.
+// ------------------------------------------------------------------ shapes
 template <int MODE>
-__device__ __forceinline__ int tc_logical_row(const GemvParams &p, int lrow0, int r) {
-  if constexpr (MODE == GM_GATEUP) {
-    return r < 64 ? 2 * r : 2 * (r - 64) + 1;
+struct TcMode {
+  static constexpr int H = ModeTraits<MODE>::kHalves;
+  static constexpr int P = MODE == GM_ENCODE ? 1 : 3;  // bf16 parts of x
+  static constexpr int kMaxN = MODE == GM_ENCODE ? 128 : 64;
+  static constexpr bool kStaging = MODE == GM_QKV || MODE == GM_GATEUP;  // row exchange
+};
+
+template <int N, int MODE>
+struct TcShape {
+  using T = TcMode<MODE>;
+  static constexpr int H = T::H, P = T::P;
+  static constexpr int kA = kTcM * kTcK * 2;            // 16 KB weight tile
+  static constexpr int kB = N * kTcK * 2;               // one activation part
+  static constexpr int kBStage = P * kB;
+  // TMEM: two chunk buffers of [P][N] columns (a chunk lies in one K half)
+  static constexpr int NP = P * N;                      // MMA width: the parts stacked
+  static_assert(NP % 16 == 0 && NP <= 256, "MMA N of kind::f16 with M = 128");
+  static constexpr int kCols = 2 * NP;
+  static_assert(kCols <= 512, "accumulators fit in TMEM");
+  static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
+  static constexpr int NCH = N >= 32 ? N / 32 : 1;      // 16-column chunks per epilogue thread
+  static constexpr int kStageBytes = T::kStaging ? kTcM * (N + 1) * 4 : 0;
+  // lm_head: per-quad best keys of a tile [4][N] and the CTA's running best [N] (u64)
+  static constexpr int kLmBytes = MODE == GM_LMHEAD ? 5 * N * 8 : 0;
+  static constexpr int kAux = 3072;                      // barriers and per-item tables
+  // activation ring: shallow (L2 hits); the weight ring (HBM) takes the rest
+  static constexpr int kNB = kBStage <= 12 * 1024 ? 4 : 3;
+  static constexpr int kFixed = 1024 /*alignment*/ + kAux + kStageBytes + kLmBytes + kNB * kBStage;
+  static constexpr int kFitA = (int)((kTcSmemLimit - kFixed) / kA);
+  static constexpr int kNA = kFitA > 12 ? 12 : kFitA;   // weight ring stages
+  static_assert(kNA >= 4 && kNA >= kNB, "a weight ring of four stages, no shallower than the activation ring");
+  static constexpr int kSmem = kFixed + kNA * kA;
+  static __device__ __forceinline__ uint32_t buf_col(int b) { return (uint32_t)(b * NP); }
+};
+
+// The stream-K partition: CTA c owns units [start(c), start(c + 1)) of the flattened
+// (tile, k-tile) space, tiles ordered row tile major, item tile minor.
+struct TcSched {
+  int units, grid;
+  __host__ __device__ int start(int c) const { return (int)(((long long)units * c) / grid); }
+  __host__ __device__ int cta_of(int u) const {
+    int c = (int)(((long long)u * grid) / units);
+    while (c + 1 < grid && start(c + 1) <= u) ++c;
+    while (c > 0 && start(c) > u) --c;
+    return c;
+  }
+};
+
+// One contiguous run of k-tiles [kt0, kt1) of tile t inside a CTA's share.
+struct TcSeg {
+  int t, kt0, kt1;
+};
+
+__device__ __forceinline__ TcSeg tc_seg(int u, int uend, int ktiles) {
+  TcSeg s;
+  s.t = u / ktiles;
+  s.kt0 = u - s.t * ktiles;
+  s.kt1 = min(ktiles, s.kt0 + (uend - u));
+  return s;
+}
+
+// K half (q/k/v: [embed ; g], normalised separately) of k-tile kt.
+template <int H>
+__device__ __forceinline__ int tc_half(int kt, int n_embd) {
+  return (H == 2 && kt * kTcK >= n_embd) ? 1 : 0;
+}
+
+// End of the accumulation chunk that starts at k-tile cb inside a segment ending at kt1:
+// chunks end at multiples of kTcChunk and at the K half boundary (nh_tiles), so each
+// chunk lies in one half.
+template <int H>
+__device__ __forceinline__ int tc_chunk_end(int cb, int kt1, int nh_tiles) {
+  int ce = min(kt1, (cb / kTcChunk + 1) * kTcChunk);
+  if (H == 2 && cb < nh_tiles && ce > nh_tiles) ce = nh_tiles;
+  return ce;
+}
+
+// One lane of the (converged) warp, the same lane every time for the same mask.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.u32 %0, 1, 0, P;\n}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// mbar_wait on every lane of the warp; true only when all lanes saw the phase, so the warp
+// leaves converged.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status) {
+  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;  // the usual case: already there
+  const bool ok = mbar_wait(bar, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// Wait without the CTA's abort shortcut (still bounded): used to drain copies and MMAs
+// that are in flight before the CTA releases its shared memory and TMEM.
+__device__ __forceinline__ void tc_drain_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if (i > 64) __nanosleep(64);
+  }
+}
+
+// ------------------------------------------------------------------ tile epilogues
+// Thread (quad, chalf, lane) holds TMEM lane r = 32 * quad + lane (row r of the tile) and
+// the 16-column chunks c0(j) = (2 j + chalf) * 16 < N (items item0 + c0(j) + i).
+template <int N>
+__device__ __forceinline__ int tc_c0(int j, int chalf) {
+  return N >= 32 ? (2 * j + chalf) * 16 : 0;
+}
+template <int N>
+__device__ __forceinline__ bool tc_has(int j, int chalf) {
+  return N >= 32 ? true : chalf == 0;
+}
+
+struct TcTables {
+  float *scale;  // [N][H] RMSNorm scales of the tile's items
+  int *pos;      // [N] q/k/v: position, sequence and keep flag of each item
+  int *seq;
+  int *keep;
+  float *stage;  // [128][N + 1] row exchange (q/k/v RoPE partners, gate/up)
+  unsigned long long *quad_best;  // lm_head [4][N]
+  unsigned long long *run_best;   // lm_head [N]: this CTA's best so far, item tile run_it
+};
+
+// Max of NV 64-bit keys per lane across the warp, transposed: afterwards lane l holds the
+// maximum of value index warp_reduce_index<NV>(l) (writers: warp_reduce_writer<NV>(l)).
+template <int NV>
+__device__ __forceinline__ unsigned long long warp_max_multi(unsigned long long (&v)[NV], int lane) {
+  static_assert(NV >= 1 && NV <= 32 && (NV & (NV - 1)) == 0, "1..32 values, a power of two");
+#pragma unroll
+  for (int cnt = NV, o = 16; cnt > 1; cnt >>= 1, o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < cnt / 2; ++i) {
+      const unsigned long long send = upper ? v[i] : v[i + cnt / 2];
+      const unsigned long long keep = upper ? v[i + cnt / 2] : v[i];
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = keep > other ? keep : other;
+    }
+  }
+  unsigned long long r = v[0];
+#pragma unroll
+  for (int o = 16 >> Log2<NV>::value; o >= 1; o >>= 1) {
+    const unsigned long long other = __shfl_xor_sync(0xffffffffu, r, o);
+    r = other > r ? other : r;
+  }
+  return r;
+}
+
+// lm_head: push the CTA's running best keys (item tile it) to the global argmax slots.
+template <int N>
+__device__ __forceinline__ void tc_lm_flush(const TcArgs &A, const TcTables &tb, int it) {
+  const int tid = threadIdx.x;
+  if (tid < N) {
+    const unsigned long long k = tb.run_best[tid];
+    const int item = it * N + tid;
+    if (k != 0ull && item < A.M) atomicMax(A.p.am_slot + item, k);
+    tb.run_best[tid] = 0ull;
+  }
+}
+
+template <int N, int MODE>
+__device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>::H][TcShape<N, MODE>::NCH][16],
+                                 int rt, int it, const TcTables &tb) {
+  using S = TcShape<N, MODE>;
+  constexpr int H = S::H, NCH = S::NCH, SP = N + 1;
+  const GemvParams &p = A.p;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int quad = warp & 3, chalf = warp >> 2, r = quad * 32 + lane;
+  const int item0 = it * N;
+
+  // per-item tables of this tile
+  if constexpr (ModeTraits<MODE>::kNorm) {
+    for (int i = tid; i < N * H; i += kGemvThreads) {
+      const int c = i / H, h = i - c * H, item = item0 + c;
+      tb.scale[i] = item < A.M ? rsqrtf(A.sumsq[(size_t)item * H + h] / (float)(p.K / H) + p.eps) : 0.f;
+    }
+  }
+  if constexpr (MODE == GM_QKV) {
+    for (int c = tid; c < N; c += kGemvThreads) {
+      const int item = item0 + c;
+      if (item < A.M) {
+        const PairItem pi = resolve_pair(p.pairs, item, p.n_embd);
+        tb.pos[c] = pi.pos;
+        tb.seq[c] = pi.b;
+        tb.keep[c] = pi.write_kv ? 1 : 0;
+      } else {
+        tb.pos[c] = 0;
+        tb.seq[c] = 0;
+        tb.keep[c] = 0;
+      }
+    }
+  }
+  consumer_sync();
+
+  // y = sum over K halves of (raw sum) * (norm scale), in place in acc[0]
+#pragma unroll
+  for (int j = 0; j < NCH; ++j)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = tc_c0<N>(j, chalf) + i;
+      float v = 0.f;
+#pragma unroll
+      for (int h = 0; h < H; ++h)
+        v += ModeTraits<MODE>::kNorm ? acc[h][j][i] * tb.scale[(c < N ? c : 0) * H + h] : acc[h][j][i];
+      acc[0][j][i] = v;
+    }
+  float(&y)[NCH][16] = acc[0];
+
+  if constexpr (MODE == GM_ENCODE || MODE == GM_O || MODE == GM_DOWN) {
+    const int row = rt * kTcM + r;
+    if (row < p.rows) {
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        if (!tc_has<N>(j, chalf)) continue;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int item = item0 + tc_c0<N>(j, chalf) + i;
+          if (item >= A.M) continue;
+          float v = y[j][i];
+          if constexpr (MODE != GM_ENCODE) v += p.res[(size_t)item * p.rows + row];
+          p.out_f[(size_t)item * p.rows + row] = v;
+          if constexpr (MODE == GM_DOWN) {
+            if (p.dbg_f) p.dbg_f[(size_t)item * p.dbg_stride_b + p.dbg_off + row] = v;
+          }
+        }
+      }
+    }
+  } else if constexpr (MODE == GM_LMHEAD) {
+    // per item: best (logit, lowest row) of the warp's 32 rows by a transposed shuffle
+    // reduction, then of the 4 lane quadrants in shared memory, folded into the CTA's
+    // running best (pushed to the global slots once per item tile).
+    constexpr int NV = NCH * 16;
+    const int row = rt * kTcM + r;
+    const bool vrow = row < p.rows;
+    if (tc_has<N>(0, chalf)) {
+      unsigned long long keys[NV];
+#pragma unroll
+      for (int j = 0; j < NCH; ++j)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int item = item0 + tc_c0<N>(j, chalf) + i;
+          const float v = y[j][i];
+          if (vrow && item < A.M && p.dbg_f) p.dbg_f[(size_t)item * p.dbg_stride_b + p.dbg_off + row] = v;
+          keys[j * 16 + i] = vrow ? (((unsigned long long)float_order_key(v) << 32) |
+                                     (unsigned long long)(0xFFFFFFFFu - (uint32_t)row))
+                                  : 0ull;
+        }
+      const unsigned long long best = warp_max_multi<NV>(keys, lane);
+      if (warp_reduce_writer<NV>(lane)) {
+        const int vi = warp_reduce_index<NV>(lane);
+        tb.quad_best[quad * N + tc_c0<N>(vi / 16, chalf) + (vi % 16)] = best;
+      }
+    }
+    consumer_sync();
+    if (tid < N) {
+      unsigned long long b = tb.run_best[tid];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) b = tb.quad_best[q * N + tid] > b ? tb.quad_best[q * N + tid] : b;
+      tb.run_best[tid] = b;
+    }
+    consumer_sync();
+    if (A.item_tiles > 1) {  // the next tile may belong to another item tile
+      tc_lm_flush<N>(A, tb, it);
+      consumer_sync();
+    }
+  } else if constexpr (MODE == GM_GATEUP) {
+    // tile rt: gate rows rt*64 + i in tile rows i < 64, the matching up rows in 64 + i
+    if (r >= 64) {
+#pragma unroll
+      for (int j = 0; j < NCH; ++j)
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (tc_has<N>(j, chalf)) tb.stage[(r - 64) * SP + tc_c0<N>(j, chalf) + i] = y[j][i];
+    }
+    consumer_sync();
+    const int row = rt * 64 + r;
+    if (r < 64 && row < p.n_ff) {
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        if (!tc_has<N>(j, chalf)) continue;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = tc_c0<N>(j, chalf) + i, item = item0 + c;
+          if (item >= A.M) continue;
+          p.out_f[(size_t)item * p.n_ff + row] = silu_f(y[j][i]) * tb.stage[r * SP + c];
+        }
+      }
+    }
+    consumer_sync();  // the staging area is free again
   } else if constexpr (MODE == GM_QKV) {
     const int d = p.head_dim, R = p.rope_dims, half = R >> 1;
     const int qr = p.n_head * d, kr = p.n_head_kv * d;
-    const int lr = p.row_base + lrow0 + r;  // physical == logical set within a tile
-    if (lr >= qr + kr) return r;            // v rows are not rotated
-    const int rr = lr < qr ? lr : lr - qr;
-    const int hr = rr % d;
-    if (hr >= R) return r;
-    const int lh = hr < half ? 2 * hr : 2 * (hr - half) + 1;
-    return r - hr + lh;
-  } else {
-    return r;
+    const int lr0 = p.row_base + rt * kTcM;  // row of [q; k; v] at tile row 0
+    const int region = lr0 < qr ? 0 : (lr0 < qr + kr ? 1 : 2);
+    const int rr = lr0 + r - (region == 0 ? 0 : (region == 1 ? qr : qr + kr));
+    const int head = rr / d, hr = rr - head * d;
+    const bool rope = region < 2 && hr < R;
+    const int rp = r + (hr < half ? half : -half);  // RoPE partner (same tile)
+    const bool vrow = lr0 + r < qr + 2 * kr;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j)
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (tc_has<N>(j, chalf)) tb.stage[r * SP + tc_c0<N>(j, chalf) + i] = y[j][i];
+    consumer_sync();
+    if (vrow) {
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        if (!tc_has<N>(j, chalf)) continue;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = tc_c0<N>(j, chalf) + i, item = item0 + c;
+          if (item >= A.M) continue;
+          float v = y[j][i];
+          const int pos = tb.pos[c];
+          if (rope) {
+            const float pv = tb.stage[rp * SP + c];
+            const int pr = (pos < 0 || pos >= p.max_cache_len) ? 0 : pos;
+            const float2 cs = p.rope[(size_t)pr * half + (hr < half ? hr : hr - half)];
+            v = hr < half ? v * cs.x - pv * cs.y : v * cs.x + pv * cs.y;
+          }
+          if (region == 0) {
+            p.out_f[(size_t)item * qr + rr] = v;
+          } else if (tb.keep[c]) {
+            if (pos < 0 || pos >= p.max_cache_len) {
+              set_status(p.status, EAGLE3_DEV_BAD_POSITION);
+              continue;
+            }
+            const int pg = p.page_table[(size_t)tb.seq[c] * p.max_pages + pos / p.page_size];
+            if (pg < 0 || pg >= p.num_pages) {
+              set_status(p.status, EAGLE3_DEV_BAD_PAGE);
+              continue;
+            }
+            uint16_t *pool = region == 1 ? p.k_pool : p.v_pool;
+            pool[(((size_t)pg * p.n_head_kv + head) * p.page_size + pos % p.page_size) * d + hr] = f2bf(v);
+          }
+        }
+      }
+    }
+    consumer_sync();  // the staging area is free again
   }
 }
 
 // ------------------------------------------------------------------ kernel
 template <int N, int MODE>
-struct TcShape {
-  static constexpr int H = ModeTraits<MODE>::kHalves;
-  static constexpr int P = MODE == GM_ENCODE ? 1 : 3;  // bf16 parts of x
-  static constexpr int kA = kTcM * kTcK * 2;            // 16 KB
-  static constexpr int kB = N * kTcK * 2;               // per part
-  static constexpr int kStage = kA + P * kB;
-  static constexpr int kLo = P > 1 ? 1 : 0;             // accumulator of the x1, x2 products
-  static constexpr int kFit = 512 / (H * N) - kLo;
-  static constexpr int kAccHi = kFit > 4 ? 4 : (kFit < 1 ? 1 : kFit);  // rotating x0 accumulators
-  static constexpr int kAcc = kAccHi + kLo;
-  static constexpr int kCols = kAcc * H * N;
-  static_assert(kCols <= 512, "accumulators fit in TMEM");
-  static constexpr int kFitStages = (int)((kTcSmemLimit - 1024 - 64) / kStage);
-  static constexpr int kNst = kFitStages > 8 ? 8 : kFitStages;  // ring stages
-  static_assert(kNst >= 2, "two stages fit in shared memory");
-  static_assert(kTcM * AccStride<N>::value * 4 <= kNst * kStage, "accumulator tile fits the ring");
-  static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
-  // TMEM column of accumulator a (0..kAccHi-1: x0 products; kAccHi: the rest) of half h
-  static __device__ __forceinline__ uint32_t col(int a, int h) { return (uint32_t)((a * H + h) * N); }
-};
-
-template <int N, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ TcArgs args) {
   using S = TcShape<N, MODE>;
-  constexpr int H = S::H;
+  constexpr int H = S::H, P = S::P, NA = S::kNA, NB = S::kNB, NCH = S::NCH;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // 1024-byte alignment for the swizzled tiles
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  const int nst = args.nstage;
-  const uint32_t full0 = smem_addr(smem + (size_t)nst * S::kStage);
-  const uint32_t empty0 = full0 + 8 * nst;
-  const uint32_t done_bar = empty0 + 8 * nst;
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + (size_t)nst * S::kStage + 16 * nst + 8);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + (size_t)nst * S::kStage + 16 * nst + 16);
-  __shared__ float scale_sm[N * 2];
-  __shared__ int last_sh;
+  // [A ring NA x 16 KB][B ring NB x P parts][staging][barriers, flags, per-item tables]
+  unsigned char *aring = smem;
+  unsigned char *bring = aring + (size_t)NA * S::kA;
+  float *stage = reinterpret_cast<float *>(bring + (size_t)NB * S::kBStage);
+  unsigned char *lmb = reinterpret_cast<unsigned char *>(stage) + S::kStageBytes;
+  unsigned char *aux = lmb + S::kLmBytes;
+  const uint32_t fullA = smem_addr(aux), emptyA = fullA + 8 * NA;
+  const uint32_t fullB = emptyA + 8 * NA;
+  const uint32_t hi_full = fullB + 8 * NB, hi_free = hi_full + 16;
+  const uint32_t mma_done = hi_free + 16;
+  unsigned char *aux2 = aux + 8 * (2 * NA + 2 * NB + 7);
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(aux2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(aux2 + 4);
+  int *last_sh = reinterpret_cast<int *>(aux2 + 8);
+  TcTables tb;
+  tb.scale = reinterpret_cast<float *>(aux2 + 16);
+  tb.pos = reinterpret_cast<int *>(tb.scale + N * H);
+  tb.seq = tb.pos + N;
+  tb.keep = tb.seq + N;
+  tb.stage = stage;
+  tb.quad_best = reinterpret_cast<unsigned long long *>(lmb);
+  tb.run_best = tb.quad_best + 4 * N;
+  static_assert(8 * (2 * S::kNA + 2 * S::kNB + 7) + 16 + 4 * (N * S::H + 3 * N) <= S::kAux, "aux area");
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const GemvParams &pc = args.p;
-  // item tiles of one row tile are adjacent in launch order, so they share its weights in L2
-  const int row_tiles = args.row_tiles;
-  const int it = blockIdx.x % args.item_tiles;
-  const int rt = (blockIdx.x / args.item_tiles) % row_tiles;
-  const int ks = blockIdx.x / (args.item_tiles * row_tiles);
-  const int lrow0 = rt * kTcM;                      // logical row of the tile (rel. row_base)
-  const int item0 = it * N;
-  const int k_begin = ks * args.kper;
-  const int k_end = min(pc.K, k_begin + args.kper);
-  const int n_stages = (k_end - k_begin + kTcK - 1) / kTcK;
+  const int ktiles = args.ktiles, item_tiles = args.item_tiles;
+  TcSched sched;
+  sched.units = args.units;
+  sched.grid = gridDim.x;
+  const int cta = blockIdx.x;
+  const int u_begin = sched.start(cta), u_end = sched.start(cta + 1);
 
   if (warp == kTcMmaWarp) {
-    // TMEM for H accumulators of N columns
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_holder)),
                  "r"(S::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    for (int i = 0; i < nst; ++i) {
-      mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, 1);
+    for (int i = 0; i < NA; ++i) {
+      mbar_init(fullA + 8 * i, 1);
+      mbar_init(emptyA + 8 * i, 1);
     }
-    mbar_init(done_bar, 1);
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(fullB + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(hi_full + 8 * i, 1);
+      mbar_init(hi_free + 8 * i, 8);  // one arrival per epilogue warp
+    }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -215,22 +550,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   const uint32_t tmem = *tmem_holder;
   pdl_trigger();
 
-  if (warp == kTcProducerWarp) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+  // Producer and MMA warps run their loops with all 32 lanes converged (waits on every
+  // lane, operands warp-uniform); one elected lane issues the copies, MMAs and commits.
+  if (warp == kTcAWarp) {
+    // ------------------------------------------------------------ weight tiles (HBM)
+    const bool leader = elect_one();
+    if (leader) {
       tma_prefetch_map(&args.a0);
-      tma_prefetch_map(&args.b0);
-      const uint64_t pol_w = l2_evict_first_policy();
-      uint64_t pol_x;
-      asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
-      // which matrix and physical rows hold this tile
+      if (MODE == GM_QKV || MODE == GM_GATEUP) tma_prefetch_map(&args.a1);
+      if (MODE == GM_QKV) tma_prefetch_map(&args.a2);
+    }
+    const uint64_t pol_w = l2_evict_first_policy();
+    const uint32_t abase = smem_addr(aring);
+    int g = 0;
+    bool ok = true;
+    for (int u = u_begin; u < u_end && ok;) {
+      const TcSeg sg = tc_seg(u, u_end, ktiles);
+      const int rt = sg.t / item_tiles;
       const CUtensorMap *amap = &args.a0;
-      int arow = lrow0;
+      int arow = rt * kTcM;
       if constexpr (MODE == GM_QKV) {
         const int qr = pc.n_head * pc.head_dim, kr = pc.n_head_kv * pc.head_dim;
-        const int lr = pc.row_base + lrow0;
+        const int lr = pc.row_base + rt * kTcM;
         if (lr < qr) {
-          amap = &args.a0;
           arow = lr;
         } else if (lr < qr + kr) {
           amap = &args.a1;
@@ -240,179 +582,224 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           arow = lr - qr - kr;
         }
       } else if constexpr (MODE == GM_GATEUP) {
-        arow = lrow0 / 2;
+        arow = rt * 64;
       }
-      bool waited = false;
-      int issued = 0;
-      for (int st = 0; st < n_stages; ++st) {
-        const int slot = st % nst;
-        if (st >= nst && !mbar_wait(empty0 + 8 * slot, ((st / nst) - 1) & 1, abort_flag, pc.status)) break;
-        const int kx = k_begin + st * kTcK;
-        const uint32_t sa = smem_addr(smem + (size_t)slot * S::kStage);
-        const uint32_t sb = sa + S::kA;
-        mbar_expect_tx(full0 + 8 * slot, (uint32_t)S::kStage);
-        if constexpr (MODE == GM_GATEUP) {
-          tma_load_2d(sa, &args.a0, kx, arow, full0 + 8 * slot, pol_w);
-          tma_load_2d(sa + S::kA / 2, &args.a1, kx, arow, full0 + 8 * slot, pol_w);
-        } else {
-          tma_load_2d(sa, amap, kx, arow, full0 + 8 * slot, pol_w);
+      for (int kt = sg.kt0; kt < sg.kt1; ++kt, ++g) {
+        const int s = g % NA;
+        if (g >= NA && !warp_wait(emptyA + 8 * s, ((g / NA) - 1) & 1, abort_flag, pc.status)) {
+          ok = false;
+          break;
         }
-        if (!waited) {  // the activations come from the previous kernel
-          pdl_wait();
-          waited = true;
+        if (leader) {
+          const uint32_t dst = abase + (uint32_t)(s * S::kA);
+          mbar_expect_tx(fullA + 8 * s, (uint32_t)S::kA);
+          if constexpr (MODE == GM_GATEUP) {
+            tma_load_2d(dst, &args.a0, kt * kTcK, arow, fullA + 8 * s, pol_w);
+            tma_load_2d(dst + S::kA / 2, &args.a1, kt * kTcK, arow, fullA + 8 * s, pol_w);
+          } else {
+            tma_load_2d(dst, amap, kt * kTcK, arow, fullA + 8 * s, pol_w);
+          }
         }
-        tma_load_2d(sb, &args.b0, kx, item0, full0 + 8 * slot, pol_x);
-        if constexpr (S::P > 1) {
-          tma_load_2d(sb + S::kB, &args.b1, kx, item0, full0 + 8 * slot, pol_x);
-          tma_load_2d(sb + 2 * S::kB, &args.b2, kx, item0, full0 + 8 * slot, pol_x);
-        }
-        issued = st + 1;
+        __syncwarp();
       }
-      for (int st = max(0, issued - nst); st < issued; ++st)
-        mbar_wait(full0 + 8 * (st % nst), (st / nst) & 1, abort_flag, pc.status);
-      if (!waited) pdl_wait();
+      u += sg.kt1 - sg.kt0;
     }
+    for (int q = max(0, g - NA); q < g; ++q) tc_drain_wait(fullA + 8 * (q % NA), (q / NA) & 1);
+    __syncwarp();
+  } else if (warp == kTcBWarp) {
+    // ------------------------------------------------------------ activation tiles (L2)
+    const bool leader = elect_one();
+    if (leader) tma_prefetch_map(&args.b0);
+    uint64_t pol_x;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
+    const uint32_t bbase = smem_addr(bring);
+    pdl_wait();  // the activations come from the previous kernel
+    int g = 0;
+    bool ok = true;
+    for (int u = u_begin; u < u_end && ok;) {
+      const TcSeg sg = tc_seg(u, u_end, ktiles);
+      const int ycoord = (sg.t % item_tiles) * N;
+      for (int kt = sg.kt0; kt < sg.kt1; ++kt, ++g) {
+        const int s = g % NB;
+        // slot s last held stage g - NB: free once that stage's MMAs finished, which the
+        // weight ring's empty barrier of that stage records
+        if (g >= NB && !warp_wait(emptyA + 8 * ((g - NB) % NA), ((g - NB) / NA) & 1, abort_flag, pc.status)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
+          const uint32_t dst = bbase + (uint32_t)(s * S::kBStage);
+          mbar_expect_tx(fullB + 8 * s, (uint32_t)S::kBStage);
+          tma_load_2d(dst, &args.b0, kt * kTcK, ycoord, fullB + 8 * s, pol_x);
+          if constexpr (P > 1) {
+            tma_load_2d(dst + S::kB, &args.b1, kt * kTcK, ycoord, fullB + 8 * s, pol_x);
+            tma_load_2d(dst + 2 * S::kB, &args.b2, kt * kTcK, ycoord, fullB + 8 * s, pol_x);
+          }
+        }
+        __syncwarp();
+      }
+      u += sg.kt1 - sg.kt0;
+    }
+    for (int q = max(0, g - NB); q < g; ++q) tc_drain_wait(fullB + 8 * (q % NB), (q / NB) & 1);
+    __syncwarp();
   } else if (warp == kTcMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = tc_idesc(kTcM, N);
-      const int nh = pc.n_embd;  // K of the first half (q/k/v: [embed ; g])
-      uint32_t started = 0u;  // bit a * H + h: accumulator (a, h) holds a product
-      int t = 0;              // K slice index within this split
-      for (int st = 0; st < n_stages; ++st) {
-        const int slot = st % nst;
-        if (!mbar_wait(full0 + 8 * slot, (st / nst) & 1, abort_flag, pc.status)) break;
-        tc_fence_after();
-        const int kx = k_begin + st * kTcK;
-        const int h = (H == 2 && kx >= nh) ? 1 : 0;
-        const uint32_t sa = smem_addr(smem + (size_t)slot * S::kStage);
-        const uint32_t sb = sa + S::kA;
-        const int kcols = min(kTcK, k_end - kx);  // a multiple of 16 (K is a multiple of 64)
-#pragma unroll
-        for (int kk = 0; kk < kTcK / 16; ++kk, ++t) {
-          if (kk * 16 >= kcols) break;
-          const uint64_t ad = smem_desc_sw128(sa + kk * 32);
-          const int a = t % S::kAccHi;
-          const int bit = a * H + h;
-          tc_mma(tmem + S::col(a, h), ad, smem_desc_sw128(sb + kk * 32), idesc, (started >> bit) & 1u);
-          started |= 1u << bit;
-          if constexpr (S::P > 1) {
-            const int lb = S::kAccHi * H + h;
-            tc_mma(tmem + S::col(S::kAccHi, h), ad, smem_desc_sw128(sb + S::kB + kk * 32), idesc,
-                   (started >> lb) & 1u);
-            started |= 1u << lb;
-            tc_mma(tmem + S::col(S::kAccHi, h), ad, smem_desc_sw128(sb + 2 * S::kB + kk * 32), idesc, 1u);
-          }
+    const bool leader = elect_one();
+    constexpr uint32_t idesc = tc_idesc(kTcM, S::NP);
+    const int nh_tiles = pc.n_embd / kTcK;
+    // descriptors of ring slot 0; slot s and K slice kk add (offset >> 4) to the start field
+    const uint64_t adesc0 = smem_desc_sw128(smem_addr(aring));
+    const uint64_t bdesc0 = smem_desc_sw128(smem_addr(bring));
+    int g = 0, ch = 0;
+    bool ok = true;
+    for (int u = u_begin; u < u_end && ok;) {
+      const TcSeg sg = tc_seg(u, u_end, ktiles);
+      for (int cb = sg.kt0; cb < sg.kt1 && ok; ++ch) {
+        const int ce = tc_chunk_end<H>(cb, sg.kt1, nh_tiles);
+        const int hb = ch & 1;
+        if (ch >= 2 && !warp_wait(hi_free + 8 * hb, ((ch >> 1) - 1) & 1, abort_flag, pc.status)) {
+          ok = false;
+          break;
         }
-        tc_commit(empty0 + 8 * slot);  // the stage's smem is free once these MMAs finish
+        const uint32_t dt = tmem + S::buf_col(hb);
+        for (int kt = cb; kt < ce; ++kt, ++g) {
+          const int sa = g % NA, sb = g % NB;
+          if (!warp_wait(fullA + 8 * sa, (g / NA) & 1, abort_flag, pc.status) ||
+              !warp_wait(fullB + 8 * sb, (g / NB) & 1, abort_flag, pc.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad0 = adesc0 + (uint64_t)((sa * S::kA) >> 4);
+          const uint64_t bd0 = bdesc0 + (uint64_t)((sb * S::kBStage) >> 4);
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < kTcK / 16; ++kk)  // 32 bytes further along K per slice
+              tc_mma(dt, ad0 + (uint64_t)(kk * 2), bd0 + (uint64_t)(kk * 2), idesc, (kt > cb || kk > 0) ? 1u : 0u);
+            tc_commit(emptyA + 8 * sa);  // both rings' slots are free once these MMAs finish
+          }
+          __syncwarp();
+        }
+        if (ok) {
+          if (leader) tc_commit(hi_full + 8 * hb);
+          __syncwarp();
+        }
+        cb = ce;
       }
-      tc_commit(done_bar);
+      u += sg.kt1 - sg.kt0;
     }
+    // every MMA of this CTA has finished before TMEM is released
+    if (leader) tc_commit(mma_done);
+    __syncwarp();
+    tc_drain_wait(mma_done, 0);
+    __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue warps
-    pdl_wait();  // the norm sums and the outputs' other readers belong to earlier kernels
-    const bool ok = mbar_wait(done_bar, 0, abort_flag, pc.status);
-    tc_fence_after();
-    // The K slices of a (split, half) pair come in runs of at least four consecutive
-    // slices, so every accumulator of a half that this split touches received a product;
-    // a half it does not touch is zero.
-    bool has_h[H];
-#pragma unroll
-    for (int h = 0; h < H; ++h)
-      has_h[h] = H == 1 ? (k_end > k_begin) : (h == 0 ? k_begin < pc.n_embd : k_end > pc.n_embd);
-    const int quad = warp & 3, chalf = warp >> 2;
-    const int r = quad * 32 + lane;  // physical row of the tile (TMEM lane)
-    GemvParams p = pc;
-    p.item0 = item0;
-    p.items = min(N, args.M - item0);
-    // RMSNorm scales of the tile's items (norm modes)
-    if constexpr (ModeTraits<MODE>::kNorm) {
-      for (int i = tid; i < N * H; i += kGemvThreads) {
-        const int m = i / H, h = i % H;
-        float s = 0.f;
-        if (item0 + m < args.M) s = args.sumsq[(size_t)(item0 + m) * H + h];
-        scale_sm[i] = rsqrtf(s / (float)(pc.K / H) + pc.eps);
-      }
+    // ------------------------------------------------------------ drain + epilogues
+    pdl_wait();  // norm sums, residuals and the outputs' earlier readers
+    const int quad = warp & 3, chalf = warp >> 2, r = quad * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const int nh_tiles = pc.n_embd / kTcK;
+    int ch = 0;
+    if constexpr (MODE == GM_LMHEAD) {
+      if (tid < N) tb.run_best[tid] = 0ull;  // published by the first tile's consumer_sync
     }
-    consumer_sync();
-    constexpr int AS = AccStride<N>::value;
-    float *accs = reinterpret_cast<float *>(smem);  // the ring is idle now: [128][AS]
-    const int lr = tc_logical_row<MODE>(pc, lrow0, r);
-    const int ncol = N / 2;  // columns per warp in the split-K reduction
-    // TMEM is read in 16-column chunks; the two warps of a lane quadrant take alternate
-    // chunks.  sum16 adds the accumulators of half h in a fixed order.
-    auto sum16 = [&](int h, int c0, float (&y)[16]) {
+    float acc[H][NCH][16];
+    for (int u = u_begin; u < u_end;) {
+      const TcSeg sg = tc_seg(u, u_end, ktiles);
+      u += sg.kt1 - sg.kt0;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = 0.f;
+      for (int h = 0; h < H; ++h)
 #pragma unroll
-      for (int a = 0; a < S::kAcc; ++a) {
-        float v[16];
-        tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + S::col(a, h) + (uint32_t)c0, v);
+        for (int j = 0; j < NCH; ++j)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] += v[i];
-      }
-    };
-    if (args.ksplit == 1) {
-      for (int c0 = chalf * 16; c0 < N; c0 += 32) {
-        float y[16];
+          for (int i = 0; i < 16; ++i) acc[h][j][i] = 0.f;
+      for (int cb = sg.kt0; cb < sg.kt1; ++ch) {
+        const int ce = tc_chunk_end<H>(cb, sg.kt1, nh_tiles);
+        const int h = tc_half<H>(cb, pc.n_embd);
+        const int hb = ch & 1;
+        const bool ok = mbar_wait(hi_full + 8 * hb, (ch >> 1) & 1, abort_flag, pc.status);
+        tc_fence_after();
+        if (ok) {
+          // x0, then x1 and x2 products of this chunk, added in that order
 #pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] = 0.f;
+          for (int j = 0; j < NCH; ++j) {
+            if (!tc_has<N>(j, chalf)) continue;
+            const uint32_t col = tmem + lane_base + S::buf_col(hb) + (uint32_t)tc_c0<N>(j, chalf);
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
-          float v[16];
-          sum16(h, c0, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a = has_h[h] ? v[i] : 0.f;
-            y[i] += ModeTraits<MODE>::kNorm ? a * scale_sm[(c0 + i) * H + h] : a;
+            for (int q = 0; q < P; ++q) {
+              if (H == 2 && h == 1) tmem_add16(col + (uint32_t)(q * N), acc[H - 1][j]);
+              else tmem_add16(col + (uint32_t)(q * N), acc[0][j]);
+            }
           }
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) accs[(size_t)lr * AS + c0 + i] = ok ? y[i] : 0.f;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(hi_free + 8 * hb);
+        cb = ce;
       }
-    } else {
-      // split K: publish this split's raw sums, the last split of the tile reduces
-      const size_t rows_pad = (size_t)row_tiles * kTcM;
-      const size_t cols_pad = (size_t)args.item_tiles * N;
-      for (int c0 = chalf * 16; c0 < N; c0 += 32) {
+      const int rt = sg.t / item_tiles, it = sg.t % item_tiles;
+      if (!(sg.kt0 == 0 && sg.kt1 == ktiles)) {
+        // a shared tile: publish this CTA's raw sums; the last contributor adds them all
+        const int t0 = sg.t * ktiles;
+        const int c_first = sched.cta_of(t0), c_last = sched.cta_of(t0 + ktiles - 1);
+        // slot 0: the CTA's first segment; slot 1: a later (its last) segment
+        const int my_slot = sched.start(cta) >= t0 ? 0 : 1;
+        float *mine = args.part + ((size_t)cta * 2 + my_slot) * H * N * kTcM;
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
-          float v[16];
-          sum16(h, c0, v);
+        for (int h = 0; h < H; ++h)
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            args.part[(((size_t)ks * H + h) * cols_pad + item0 + c0 + i) * rows_pad + lrow0 + r] =
-                (ok && has_h[h]) ? v[i] : 0.f;
+          for (int j = 0; j < NCH; ++j)
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (tc_has<N>(j, chalf)) mine[((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM + r] = acc[h][j][i];
+        __threadfence();
+        consumer_sync();
+        if (tid == 0) {
+          const unsigned prev = atomicAdd(args.tile_cnt + sg.t, 1u);
+          *last_sh = prev == (unsigned)(c_last - c_first) ? 1 : 0;
         }
+        consumer_sync();
+        if (!*last_sh) continue;
+        __threadfence();
+        // fixed order: the published sums of contributors c_first .. c_last (this CTA's
+        // own included), one contributor's tile at a time
+#pragma unroll
+        for (int h = 0; h < H; ++h)
+#pragma unroll
+          for (int j = 0; j < NCH; ++j)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[h][j][i] = 0.f;
+        for (int c2 = c_first; c2 <= c_last; ++c2) {
+          // a contributor's segment is its first one (slot 0) unless it began earlier
+          const int slot2 = sched.start(c2) >= t0 ? 0 : 1;
+          const float *src = args.part + ((size_t)c2 * 2 + slot2) * H * N * kTcM + r;
+#pragma unroll
+          for (int h = 0; h < H; ++h)
+#pragma unroll
+            for (int j = 0; j < NCH; ++j)
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (tc_has<N>(j, chalf)) acc[h][j][i] += __ldcg(src + ((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM);
+        }
+        if (tid == 0) args.tile_cnt[sg.t] = 0u;
       }
+      tc_tile_epilogue<N, MODE>(args, acc, rt, it, tb);
+    }
+    if constexpr (MODE == GM_LMHEAD) {
+      // the last CTA to finish decodes every item's argmax
+      if (args.item_tiles == 1) tc_lm_flush<N>(args, tb, 0);
       __threadfence();
       consumer_sync();
       if (tid == 0) {
-        const unsigned prev = atomicAdd(args.tile_cnt + (size_t)it * row_tiles + rt, 1u);
-        last_sh = (prev == (unsigned)args.ksplit - 1) ? 1 : 0;
+        const unsigned prev = atomicAdd(pc.am_count, 1u);
+        *last_sh = prev == gridDim.x - 1 ? 1 : 0;
       }
       consumer_sync();
-      if (last_sh) {
+      if (*last_sh) {
         __threadfence();
-        for (int c0 = chalf * ncol; c0 < (chalf + 1) * ncol; ++c0) {
-          float y = 0.f;
-#pragma unroll
-          for (int h = 0; h < H; ++h) {
-            float sum = 0.f;
-            for (int q = 0; q < args.ksplit; ++q)
-              sum += __ldcg(&args.part[(((size_t)q * H + h) * cols_pad + item0 + c0) * rows_pad + lrow0 + r]);
-            y += ModeTraits<MODE>::kNorm ? sum * scale_sm[c0 * H + h] : sum;
-          }
-          accs[(size_t)lr * AS + c0] = y;
-        }
-        if (tid == 0) args.tile_cnt[(size_t)it * row_tiles + rt] = 0u;
+        lmhead_finalize(pc, 0, args.M, tid, kGemvThreads);
+        if (tid == 0) *pc.am_count = 0u;
       }
-    }
-    tc_fence_before();
-    consumer_sync();
-    if (args.ksplit == 1 || last_sh) {
-      const int nrows = min(kTcM, pc.rows - lrow0);
-      epilogue<N, MODE>(p, accs, lrow0, nrows);
     }
   }
   __syncthreads();
@@ -457,11 +844,14 @@ static cudaError_t tc_launch_n(const TcLaunch &L, cudaStream_t st, bool pdl) {
   TcArgs a;
   memset(&a, 0, sizeof(a));
   a.p = L.p;
+  a.p.item0 = 0;
+  a.p.items = L.M;
   a.M = L.M;
   a.sumsq = L.sumsq;
   a.part = L.part;
   a.tile_cnt = L.tile_cnt;
   const int K = L.p.K;
+  if (K % kTcK || L.p.rows % (MODE == GM_GATEUP ? 128 : 1)) return cudaErrorInvalidValue;
   const int box_a = MODE == GM_GATEUP ? 64 : kTcM;
   if (!tc_make_map(&a.a0, L.a0, L.a0_rows, K, box_a)) return cudaErrorInvalidValue;
   if (L.a1 && !tc_make_map(&a.a1, L.a1, L.a1_rows, K, box_a)) return cudaErrorInvalidValue;
@@ -469,34 +859,20 @@ static cudaError_t tc_launch_n(const TcLaunch &L, cudaStream_t st, bool pdl) {
   if (!tc_make_map(&a.b0, L.b0, L.M, K, N)) return cudaErrorInvalidValue;
   if (S::P > 1 && (!tc_make_map(&a.b1, L.b1, L.M, K, N) || !tc_make_map(&a.b2, L.b2, L.M, K, N)))
     return cudaErrorInvalidValue;
-  const int row_tiles = (L.p.rows + kTcM - 1) / kTcM;
-  const int item_tiles = (L.M + N - 1) / N;
-  // the lm_head's argmax counts one CTA per row tile of a single item tile
-  if (MODE == GM_LMHEAD && item_tiles != 1) return cudaErrorInvalidValue;
-  // split K until the grid covers the SMs (K ranges stay multiples of 64, >= 512 wide)
-  int ksplit = 1;
-  const int ktiles = K / kTcK;
-  while (MODE != GM_LMHEAD && ksplit < 16 && row_tiles * item_tiles * (ksplit + 1) <= L.num_sms &&
-         ktiles / (ksplit + 1) >= 8)
-    ++ksplit;
-  if (ksplit > 1 && (!L.part || (size_t)ksplit * S::H * row_tiles * kTcM * item_tiles * N > L.part_elems ||
-                     (size_t)row_tiles * item_tiles > L.tile_cnt_elems))
-    ksplit = 1;
-  // equal K ranges of whole 64-column tiles; no split is left empty
-  const int tiles_per = (ktiles + ksplit - 1) / ksplit;
-  ksplit = (ktiles + tiles_per - 1) / tiles_per;
-  a.ksplit = ksplit;
-  a.kper = tiles_per * kTcK;
-  a.item_tiles = item_tiles;
-  a.row_tiles = row_tiles;
-  const size_t base = (size_t)S::kStage;
-  const int nst = S::kNst;
-  a.nstage = nst;
-  const size_t smem = 1024 + (size_t)nst * base + 16 * nst + 32;
+  a.row_tiles = (L.p.rows + kTcM - 1) / kTcM;
+  a.item_tiles = (L.M + N - 1) / N;
+  a.ktiles = K / kTcK;
+  const long long tiles = (long long)a.row_tiles * a.item_tiles;
+  const long long units = tiles * a.ktiles;
+  if (units > (1ll << 30) || tiles > (long long)L.tile_cnt_elems) return cudaErrorInvalidValue;
+  a.units = (int)units;
+  const int grid = (int)std::min<long long>(L.num_sms, units);
+  // stream-K partials: two slots per CTA
+  if ((size_t)grid * 2 * S::H * N * kTcM > L.part_elems) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(item_tiles * row_tiles * ksplit);
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = S::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -506,27 +882,25 @@ static cudaError_t tc_launch_n(const TcLaunch &L, cudaStream_t st, bool pdl) {
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<N, MODE>, a);
 }
 
+// Items per tile: the smallest of 16, 32, 64 (128 for the one-part encode) that holds M;
+// more items take several item tiles.
+int tc_tile_items(int M, int mode) {
+  const int cap = mode == GM_ENCODE ? TcMode<GM_ENCODE>::kMaxN : TcMode<GM_QKV>::kMaxN;
+  int n = 16;
+  while (n < M && n < cap) n *= 2;
+  return n;
+}
+
 template <int MODE>
 static cudaError_t tc_launch_mode(const TcLaunch &L, cudaStream_t st, bool pdl) {
   switch (tc_tile_items(L.M, MODE)) {
     case 16: return tc_launch_n<16, MODE>(L, st, pdl);
     case 32: return tc_launch_n<32, MODE>(L, st, pdl);
     case 64: return tc_launch_n<64, MODE>(L, st, pdl);
-    case 128: return tc_launch_n<128, MODE>(L, st, pdl);
     default:
-      if constexpr (MODE == GM_ENCODE) return tc_launch_n<256, MODE>(L, st, pdl);
+      if constexpr (TcMode<MODE>::kMaxN >= 128) return tc_launch_n<128, MODE>(L, st, pdl);
       return cudaErrorInvalidValue;
   }
-}
-
-// Items per tile: the smallest of 16..128 that holds M; the encode (one bf16 part, so a
-// smaller stage) goes up to 256.
-int tc_tile_items(int M, int mode) {
-  if (M <= 16) return 16;
-  if (M <= 32) return 32;
-  if (M <= 64) return 64;
-  if (M <= 128 || mode != GM_ENCODE) return 128;
-  return 256;
 }
 
 cudaError_t tc_launch(const TcLaunch &L, cudaStream_t st, bool pdl) {
@@ -544,7 +918,7 @@ cudaError_t tc_launch(const TcLaunch &L, cudaStream_t st, bool pdl) {
 template <int N, int MODE>
 static cudaError_t tc_prepare_n() {
   return cudaFuncSetAttribute(gemm_tc_kernel<N, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)kTcSmemLimit);
+                              TcShape<N, MODE>::kSmem);
 }
 
 template <int MODE>
@@ -552,9 +926,8 @@ static cudaError_t tc_prepare_mode() {
   cudaError_t e = tc_prepare_n<16, MODE>();
   if (e == cudaSuccess) e = tc_prepare_n<32, MODE>();
   if (e == cudaSuccess) e = tc_prepare_n<64, MODE>();
-  if (e == cudaSuccess) e = tc_prepare_n<128, MODE>();
-  if constexpr (MODE == GM_ENCODE)
-    if (e == cudaSuccess) e = tc_prepare_n<256, MODE>();
+  if constexpr (TcMode<MODE>::kMaxN >= 128)
+    if (e == cudaSuccess) e = tc_prepare_n<128, MODE>();
   return e;
 }
 
