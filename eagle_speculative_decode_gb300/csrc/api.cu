@@ -31,6 +31,7 @@ struct Layout {
 constexpr int kTcMinItems = 3;       // batched projections use the tensor-core GEMM from here
 constexpr size_t kTcCounters = 4096;
 constexpr int kTcEncodeChunk = 2048;  // encode rows per tensor-core launch
+constexpr int kTcPrepMaxK = 16384;    // widest float32 input the activation split handles
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -288,6 +289,7 @@ cudaError_t tc_items(eagle3_ctx *ctx, const GemvParams &p, int items, cudaStream
 bool use_tc(const eagle3_ctx *ctx, const GemvParams &p, int items) {
   if (!ctx->tc_ok || items < ctx->tc_min_items) return false;
   if (p.mode != GM_ENCODE && (size_t)items > ctx->L.tc_items) return false;
+  if (p.mode != GM_ENCODE && p.K > kTcPrepMaxK) return false;  // the activation split's limit
   return true;
 }
 

@@ -256,6 +256,7 @@ struct TcTables {
   int *pos;      // [N] q/k/v: position, sequence and keep flag of each item
   int *seq;
   int *keep;
+  int *page;     // [N] q/k/v: physical KV page of each kept item's position (-1: none)
   float *stage;  // [128][N + 1] row exchange (q/k/v RoPE partners, gate/up)
   unsigned long long *quad_best;  // lm_head [4][N]
   unsigned long long *run_best;   // lm_head [N]: this CTA's best so far, item tile run_it
@@ -316,18 +317,32 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
     }
   }
   if constexpr (MODE == GM_QKV) {
+    // k / v tiles also look up each kept item's KV page here, once per item
+    const bool kv_tile = p.row_base + rt * kTcM >= p.n_head * p.head_dim;
     for (int c = tid; c < N; c += kGemvThreads) {
       const int item = item0 + c;
+      int pos = 0, seq = 0, keep = 0, page = -1;
       if (item < A.M) {
         const PairItem pi = resolve_pair(p.pairs, item, p.n_embd);
-        tb.pos[c] = pi.pos;
-        tb.seq[c] = pi.b;
-        tb.keep[c] = pi.write_kv ? 1 : 0;
-      } else {
-        tb.pos[c] = 0;
-        tb.seq[c] = 0;
-        tb.keep[c] = 0;
+        pos = pi.pos;
+        seq = pi.b;
+        keep = pi.write_kv ? 1 : 0;
+        if (kv_tile && keep) {
+          if (pos < 0 || pos >= p.max_cache_len) {
+            set_status(p.status, EAGLE3_DEV_BAD_POSITION);
+          } else {
+            page = p.page_table[(size_t)seq * p.max_pages + pos / p.page_size];
+            if (page < 0 || page >= p.num_pages) {
+              set_status(p.status, EAGLE3_DEV_BAD_PAGE);
+              page = -1;
+            }
+          }
+        }
       }
+      tb.pos[c] = pos;
+      tb.seq[c] = seq;
+      tb.keep[c] = keep;
+      tb.page[c] = page;
     }
   }
   consumer_sync();
@@ -349,6 +364,18 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
   if constexpr (MODE == GM_ENCODE || MODE == GM_O || MODE == GM_DOWN) {
     const int row = rt * kTcM + r;
     if (row < p.rows) {
+      // all residual loads first (independent, in flight together), then the stores
+      if constexpr (MODE != GM_ENCODE) {
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          if (!tc_has<N>(j, chalf)) continue;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int item = item0 + tc_c0<N>(j, chalf) + i;
+            if (item < A.M) y[j][i] += __ldcg(p.res + (size_t)item * p.rows + row);
+          }
+        }
+      }
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
         if (!tc_has<N>(j, chalf)) continue;
@@ -356,11 +383,9 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
         for (int i = 0; i < 16; ++i) {
           const int item = item0 + tc_c0<N>(j, chalf) + i;
           if (item >= A.M) continue;
-          float v = y[j][i];
-          if constexpr (MODE != GM_ENCODE) v += p.res[(size_t)item * p.rows + row];
-          p.out_f[(size_t)item * p.rows + row] = v;
+          p.out_f[(size_t)item * p.rows + row] = y[j][i];
           if constexpr (MODE == GM_DOWN) {
-            if (p.dbg_f) p.dbg_f[(size_t)item * p.dbg_stride_b + p.dbg_off + row] = v;
+            if (p.dbg_f) p.dbg_f[(size_t)item * p.dbg_stride_b + p.dbg_off + row] = y[j][i];
           }
         }
       }
@@ -444,6 +469,24 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
         if (tc_has<N>(j, chalf)) tb.stage[r * SP + tc_c0<N>(j, chalf) + i] = y[j][i];
     consumer_sync();
     if (vrow) {
+      // RoPE in registers first (partner from the staging area, angles from the table),
+      // then the stores
+      if (rope) {
+        const int i0 = hr < half ? hr : hr - half;
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          if (!tc_has<N>(j, chalf)) continue;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = tc_c0<N>(j, chalf) + i;
+            const int pos = tb.pos[c];
+            const int pr = (pos < 0 || pos >= p.max_cache_len) ? 0 : pos;
+            const float2 cs = __ldg(p.rope + (size_t)pr * half + i0);
+            const float pv = tb.stage[rp * SP + c];
+            y[j][i] = hr < half ? y[j][i] * cs.x - pv * cs.y : y[j][i] * cs.x + pv * cs.y;
+          }
+        }
+      }
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
         if (!tc_has<N>(j, chalf)) continue;
@@ -451,28 +494,14 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
         for (int i = 0; i < 16; ++i) {
           const int c = tc_c0<N>(j, chalf) + i, item = item0 + c;
           if (item >= A.M) continue;
-          float v = y[j][i];
-          const int pos = tb.pos[c];
-          if (rope) {
-            const float pv = tb.stage[rp * SP + c];
-            const int pr = (pos < 0 || pos >= p.max_cache_len) ? 0 : pos;
-            const float2 cs = p.rope[(size_t)pr * half + (hr < half ? hr : hr - half)];
-            v = hr < half ? v * cs.x - pv * cs.y : v * cs.x + pv * cs.y;
-          }
           if (region == 0) {
-            p.out_f[(size_t)item * qr + rr] = v;
-          } else if (tb.keep[c]) {
-            if (pos < 0 || pos >= p.max_cache_len) {
-              set_status(p.status, EAGLE3_DEV_BAD_POSITION);
-              continue;
-            }
-            const int pg = p.page_table[(size_t)tb.seq[c] * p.max_pages + pos / p.page_size];
-            if (pg < 0 || pg >= p.num_pages) {
-              set_status(p.status, EAGLE3_DEV_BAD_PAGE);
-              continue;
-            }
+            p.out_f[(size_t)item * qr + rr] = y[j][i];
+          } else {
+            const int pg = tb.page[c];
+            if (pg < 0) continue;
+            const int pos = tb.pos[c];
             uint16_t *pool = region == 1 ? p.k_pool : p.v_pool;
-            pool[(((size_t)pg * p.n_head_kv + head) * p.page_size + pos % p.page_size) * d + hr] = f2bf(v);
+            pool[(((size_t)pg * p.n_head_kv + head) * p.page_size + pos % p.page_size) * d + hr] = f2bf(y[j][i]);
           }
         }
       }
@@ -508,10 +537,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   tb.pos = reinterpret_cast<int *>(tb.scale + N * H);
   tb.seq = tb.pos + N;
   tb.keep = tb.seq + N;
+  tb.page = tb.keep + N;
   tb.stage = stage;
   tb.quad_best = reinterpret_cast<unsigned long long *>(lmb);
   tb.run_best = tb.quad_best + 4 * N;
-  static_assert(8 * (2 * S::kNA + 2 * S::kNB + 7) + 16 + 4 * (N * S::H + 3 * N) <= S::kAux, "aux area");
+  static_assert(8 * (2 * S::kNA + 2 * S::kNB + 7) + 16 + 4 * (N * S::H + 4 * N) <= S::kAux, "aux area");
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const GemvParams &pc = args.p;
@@ -769,17 +799,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           for (int j = 0; j < NCH; ++j)
 #pragma unroll
             for (int i = 0; i < 16; ++i) acc[h][j][i] = 0.f;
-        for (int c2 = c_first; c2 <= c_last; ++c2) {
+        // two contributors per pass: both tiles' loads in flight together, added in order
+        for (int c2 = c_first; c2 <= c_last; c2 += 2) {
           // a contributor's segment is its first one (slot 0) unless it began earlier
-          const int slot2 = sched.start(c2) >= t0 ? 0 : 1;
-          const float *src = args.part + ((size_t)c2 * 2 + slot2) * H * N * kTcM + r;
+          const bool two = c2 + 1 <= c_last;
+          const float *src0 = args.part + ((size_t)c2 * 2 + (sched.start(c2) >= t0 ? 0 : 1)) * H * N * kTcM + r;
+          const float *src1 = two ? args.part + ((size_t)(c2 + 1) * 2 + (sched.start(c2 + 1) >= t0 ? 0 : 1)) * H * N * kTcM + r
+                                  : src0;
 #pragma unroll
           for (int h = 0; h < H; ++h)
 #pragma unroll
-            for (int j = 0; j < NCH; ++j)
+            for (int j = 0; j < NCH; ++j) {
+              if (!tc_has<N>(j, chalf)) continue;
+              float v0[16], v1[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                if (tc_has<N>(j, chalf)) acc[h][j][i] += __ldcg(src + ((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM);
+              for (int i = 0; i < 16; ++i) {
+                const size_t off = ((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM;
+                v0[i] = __ldcg(src0 + off);
+                v1[i] = two ? __ldcg(src1 + off) : 0.f;
+              }
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                acc[h][j][i] += v0[i];
+                if (two) acc[h][j][i] += v1[i];
+              }
+            }
         }
         if (tid == 0) args.tile_cnt[sg.t] = 0u;
       }
@@ -943,6 +987,7 @@ cudaError_t tc_prepare() {
 }
 
 // ------------------------------------------------------------------ activation prep
+constexpr int kPrepIters = 8;  // 8-element vectors per thread: K up to 8 * 256 * 8 = 16384
 // x (times the norm gain where the op normalises) split into three bf16 parts
 // x0 = bf16(x), x1 = bf16(x - x0), x2 = bf16(x - x0 - x1) -- both differences are exact
 // in float32 and x0 + x1 + x2 carries x's 24 significant bits -- and the sum of squares
@@ -992,8 +1037,26 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const GemvParams p, uint16
     const float4 *gr = reinterpret_cast<const float4 *>(itm.g);
     const uint4 *wi = reinterpret_cast<const uint4 *>(p.norm0);
     const uint4 *wh = reinterpret_cast<const uint4 *>(p.norm1);
-    for (int kv = tid; kv < NV; kv += 256) {
-      const uint4 u = er[kv], w = wi[kv];
+    // every load of this thread first (all in flight together), then convert and store
+    constexpr int kIt = kPrepIters / 2;
+    uint4 ue[kIt], uw[kIt], uh[kIt];
+    float4 ga[kIt], gb[kIt];
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+      const int kv = tid + it * 256;
+      if (kv < NV) {
+        ue[it] = __ldg(er + kv);
+        uw[it] = __ldg(wi + kv);
+        uh[it] = __ldg(wh + kv);
+        ga[it] = __ldcg(gr + 2 * kv);
+        gb[it] = __ldcg(gr + 2 * kv + 1);
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+      const int kv = tid + it * 256;
+      if (kv >= NV) break;
+      const uint4 u = ue[it], w = uw[it];
       const float e[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y), bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
       const float wf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y), bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
       float x[8];
@@ -1003,8 +1066,8 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const GemvParams p, uint16
         x[i] = e[i] * wf[i];
       }
       put(kv, x);
-      const float4 a = gr[2 * kv], b = gr[2 * kv + 1];
-      const uint4 hw = wh[kv];
+      const float4 a = ga[it], b = gb[it];
+      const uint4 hw = uh[it];
       const float g[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
       const float hf[8] = {bf_lo(hw.x), bf_hi(hw.x), bf_lo(hw.y), bf_hi(hw.y), bf_lo(hw.z), bf_hi(hw.z), bf_lo(hw.w), bf_hi(hw.w)};
 #pragma unroll
@@ -1017,11 +1080,26 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const GemvParams p, uint16
   } else {
     const float4 *src = reinterpret_cast<const float4 *>(p.xf + (size_t)item * K);
     const uint4 *wn = reinterpret_cast<const uint4 *>(p.norm0);
-    for (int kv = tid; kv < KV; kv += 256) {
-      const float4 a = src[2 * kv], b = src[2 * kv + 1];
+    // every load of this thread first (all in flight together), then convert and store
+    float4 va[kPrepIters], vb[kPrepIters];
+    uint4 vw[kPrepIters];
+#pragma unroll
+    for (int it = 0; it < kPrepIters; ++it) {
+      const int kv = tid + it * 256;
+      if (kv < KV) {
+        va[it] = __ldcg(src + 2 * kv);
+        vb[it] = __ldcg(src + 2 * kv + 1);
+        if constexpr (T::kNorm) vw[it] = __ldg(wn + kv);
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < kPrepIters; ++it) {
+      const int kv = tid + it * 256;
+      if (kv >= KV) break;
+      const float4 a = va[it], b = vb[it];
       float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
       if constexpr (T::kNorm) {
-        const uint4 w = wn[kv];
+        const uint4 w = vw[it];
         const float wf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y), bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -1051,6 +1129,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const GemvParams p, uint16
 
 cudaError_t tc_prep_launch(const GemvParams &p, int M, uint16_t *x0, uint16_t *x1, uint16_t *x2,
                            float *sumsq, cudaStream_t st, bool pdl) {
+  if (p.K > kPrepIters * 256 * 8 || p.K % 8) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(M);
   cfg.blockDim = dim3(256);
