@@ -18,13 +18,12 @@ using namespace e3;
 namespace {
 
 constexpr int kPrefillChunk = 512;   // prompt positions encoded per prefill chunk
-constexpr int kMaxSplits = 64;       // split-KV partitions per (sequence, kv head)
-constexpr int kSplitSlots = 4096;    // (sequence, kv head, split) partial slots
+constexpr int kSplitSlots = 4096;    // attention partial slots (two per CTA) and pair counters
 constexpr int kMaxGraphs = 16;
 
 struct Layout {
   size_t rope, q, attn_o, part_o, part_ml, attn_cnt, x1, act, gwork, tokwork, am_slot, am_cnt,
-      round_start, geff, status, genc, xp0, xp1, xp2, sumsq, tc_part, tc_cnt, total;
+      round_start, geff, status, genc, xp0, xp1, xp2, sumsq, tc_part, tc_cnt, attn_plan, total;
   size_t tc_items, tc_k, tc_part_elems;
 };
 
@@ -93,6 +92,7 @@ Layout make_layout(const eagle3_config &c) {
   L.tc_part_elems = (size_t)2 * 160 * 128 * 256;
   L.tc_part = take(L.tc_part_elems * 4);
   L.tc_cnt = take(kTcCounters * 4);
+  L.attn_plan = take((size_t)c.max_gamma * (B + 1) * 4);  // attention unit prefix per step
   L.total = align_up(off, 256);
   return L;
 }
@@ -152,6 +152,9 @@ struct eagle3_ctx {
   std::vector<cudaEvent_t> ev_pool;
   // tensor-core path
   int tc_ok, tc_min_items;
+  // attention work units (keys per unit) and the round's unit prefix tables
+  int unit_keys;
+  int32_t *attn_plan;
   uint16_t *xp0, *xp1, *xp2;  // the three bf16 parts of x
   float *sumsq, *tc_part;
   unsigned *tc_cnt;
@@ -334,20 +337,6 @@ void kv_only_params(const eagle3_ctx *ctx, const eagle3_kv *kv, GemvParams &p) {
   p.norm1 = ctx->w.hidden_norm;
 }
 
-// Splits of the attention key range: about four CTAs per SM over all (sequence, kv head)
-// pairs, at least ~64 keys per split (rounded to a power of two so that a growing
-// context re-captures the chain graph rarely).
-int choose_splits(const eagle3_ctx *ctx, int B, int max_len) {
-  const int per = B * ctx->c.n_head_kv;
-  int s = std::max(1, (4 * ctx->num_sms + per - 1) / per);
-  s = std::min(s, kMaxSplits);
-  s = std::min(s, std::max(1, kSplitSlots / per));
-  const int by_len = std::max(1, (max_len + 63) / 64);
-  int p2 = 1;
-  while (p2 * 2 <= by_len) p2 *= 2;
-  return std::max(1, std::min(s, p2));
-}
-
 struct ChainArgs {
   int B, gamma, splits;
   unsigned flags;
@@ -367,6 +356,12 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
                                               ctx->round_start, ctx->geff, a.gamma_eff,
                                               ctx->status, st, false),
                            PH_SMALL);
+  if (e != cudaSuccess) return e;
+  // the attention's unit partition of every step; the round's later kernels start after it
+  e = launched(ctx, st,
+               attn_plan_launch(a.B, a.gamma, a.kv->kv_len, c.max_cache_len, ctx->unit_keys,
+                                ctx->attn_plan, st),
+               PH_SMALL);
   if (e != cudaSuccess) return e;
   for (int j = 0; j < a.gamma; ++j) {
     // q/k/v + RoPE + KV append
@@ -411,12 +406,14 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     ap.n_head = c.n_head;
     ap.n_head_kv = c.n_head_kv;
     ap.head_dim = c.head_dim;
-    ap.splits = a.splits;
+    ap.batch = a.B;
+    ap.unit_keys = ctx->unit_keys;
+    ap.unit_pre = ctx->attn_plan + (size_t)j * (a.B + 1);
     ap.part_o = ctx->part_o;
     ap.part_ml = ctx->part_ml;
     ap.count = ctx->attn_cnt;
     ap.status = ctx->status;
-    if ((e = launched(ctx, st, attn_launch(ap, a.B, st, pdl), PH_ATTN)) != cudaSuccess) return e;
+    if ((e = launched(ctx, st, attn_launch(ap, ctx->num_sms, st, pdl), PH_ATTN)) != cudaSuccess) return e;
 
     // o_proj + residual (pre-norm g of this step)
     p = base_params(ctx);
@@ -645,6 +642,8 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
   ctx->geff = reinterpret_cast<int32_t *>(b + L.geff);
   ctx->status = reinterpret_cast<int *>(b + L.status);
   ctx->genc = reinterpret_cast<float *>(b + L.genc);
+  ctx->attn_plan = reinterpret_cast<int32_t *>(b + L.attn_plan);
+  ctx->unit_keys = attn_unit_keys(cfg->head_dim, cfg->n_head / cfg->n_head_kv, cfg->page_size);
   ctx->xp0 = reinterpret_cast<uint16_t *>(b + L.xp0);
   ctx->xp1 = reinterpret_cast<uint16_t *>(b + L.xp1);
   ctx->xp2 = reinterpret_cast<uint16_t *>(b + L.xp2);
@@ -798,13 +797,11 @@ int eagle3_draft_chain(eagle3_ctx *ctx, int B, int gamma, unsigned flags,
     return EAGLE3_ERR_INVALID_ARG;
   if (flags & ~EAGLE3_SHRINK_GAMMA) return EAGLE3_ERR_INVALID_ARG;
   if (ctx->round_open) return EAGLE3_ERR_STATE;
-  int max_len = 0;
   for (int b = 0; b < B; ++b) {
     int ge = 0;
     const int r = eagle3_plan_gamma(kv_len_host[b], gamma, ctx->c.max_cache_len, flags, &ge);
     if (r == EAGLE3_ERR_INVALID_ARG) return EAGLE3_ERR_INVALID_ARG;
     if (r != EAGLE3_OK) return EAGLE3_ERR_CAPACITY;
-    max_len = std::max(max_len, kv_len_host[b] + ge);
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   ctx->last_stream = st;
@@ -812,7 +809,7 @@ int eagle3_draft_chain(eagle3_ctx *ctx, int B, int gamma, unsigned flags,
   a.B = B;
   a.gamma = gamma;
   a.flags = flags;
-  a.splits = choose_splits(ctx, B, max_len);
+  a.splits = 1;  // the attention's partition is planned on the device each round
   a.kv = kv;
   a.bnd = bnd;
   a.draft_tok = draft_tok;

@@ -1,23 +1,28 @@
-// Split-KV GQA decode attention over the paged bf16 drafter KV cache.
+// GQA decode attention over the paged bf16 drafter KV cache.
 //
 // For each sequence b and q head h (kv head h / G, G = n_head / n_head_kv): softmax over
 // the keys 0..len-1 of (q . k) / sqrt(d), then sum of p * v ("memra_engine/eagle.rs",
 // ``attn``: fa_decode with scale 1/sqrt(head_dim); the new key is appended first).
 //
-// One CTA per (split, kv head, sequence): the G query heads that share a kv head are
-// served from one read of each K/V vector.  A producer warp streams the split's keys in
-// runs of up to 64 consecutive positions inside one page -- the K rows and the V rows of
-// a run are contiguous in the paged pool -- with bulk copies (TMA) into a 3-stage
-// shared-memory ring guarded by mbarriers.  Runs below the committed length were written
-// before the chain started, so they are requested before the kernel waits on its
-// predecessor (programmatic dependent launch).  Eight consumer warps take UNR keys per
-// lane group of each run (a key of d = 256 dims spans a warp, 8 dims = 16 bytes per
-// lane; smaller heads put several keys in a warp).  The UNR x G partial scores are
-// reduced across the lane group in one transposed reduction: each lane ends with one full
-// score and takes its exponential, and the probabilities are broadcast for the V update.
-// An online softmax per head keeps the running max (log2 domain), sum and weighted V.
-// The CTA merges its lane groups in shared memory; with more than one split the last CTA
-// of a (sequence, kv head) to finish merges the splits' partials.
+// Persistent stream-K schedule: the keys of every (sequence, kv head) pair are cut into
+// units of U consecutive positions inside one page (U = min(64-ish run, the largest power
+// of two dividing the page size)), and one CTA per SM takes an equal share of all units in
+// (sequence, kv head, unit) order, so ragged lengths and any batch fill the GPU evenly.
+// Inside a CTA, a producer warp streams the K rows and V rows of each unit -- contiguous
+// in the paged pool -- with bulk copies (TMA) into a 3-stage shared-memory ring guarded by
+// mbarriers, across pair boundaries without a pause.  Units below the committed length
+// were written before the chain started, so they are requested before the kernel waits
+// on its predecessor (programmatic dependent launch).
+//
+// Eight consumer warps take UNR keys per lane group of each unit (a key of d = 256 dims
+// spans a warp, 8 dims = 16 bytes per lane; smaller heads put several keys in a warp).
+// The UNR x G partial scores are reduced across the lane group in one transposed
+// reduction: each lane ends with one full score and takes its exponential, and the
+// probabilities are broadcast for the V update.  An online softmax per head keeps the
+// running max (log2 domain), sum and weighted V.  At the end of a pair's run of units the
+// CTA merges its lane groups in shared memory; a pair whose units all fall to this CTA is
+// written out at once, otherwise its (max, sum, weighted V) is published and the last
+// contributing CTA merges the contributions in CTA order.
 #include <math.h>
 
 #include "common.cuh"
@@ -28,7 +33,6 @@ namespace e3 {
 constexpr int kAttnWarps = 8;                          // consumer warps
 constexpr int kAttnThreads = kAttnWarps * 32;
 constexpr int kAttnCtaThreads = kAttnThreads + 32;     // + one producer warp
-constexpr int kMaxAttnSplits = 64;
 constexpr int kAttnStages = 3;
 
 template <int X>
@@ -45,16 +49,20 @@ struct AttnShape {
   static constexpr int LPK = D / 8;             // lanes per key (a segment of the warp)
   static constexpr int KPW = 32 / LPK;          // keys per warp pass
   static constexpr int NP = kAttnWarps * KPW;   // lane groups per CTA
-  // keys per lane group per block; UNR * G partial scores fit one segment reduction
+  // keys per lane group per unit; UNR * G partial scores fit one segment reduction
   static constexpr int UNR = (LPK / G) < 8 ? (LPK / G < 1 ? 1 : LPK / G) : 8;
   static constexpr int N = UNR * G;
   static constexpr int SH = ILog2<LPK>::value - ILog2<N>::value;  // lane bits below a score index
   static constexpr int LOG_G = ILog2<G>::value;
-  static constexpr int CH = NP * UNR;                     // keys per run (one pass of all warps)
-  static constexpr size_t kStage = (size_t)2 * CH * D * 2;  // K and V rows of a run, bf16
+  static constexpr int CH = NP * UNR;                     // keys per unit at most (one pass of all warps)
+  static constexpr size_t kStage = (size_t)2 * CH * D * 2;  // K and V rows of a unit, bf16
   static constexpr size_t kAcc = (size_t)NP * G * D * 4;    // lane-group partial V sums
   static constexpr size_t kRing = kAttnStages * kStage;
-  static constexpr size_t kSmem = (kRing > kAcc ? kRing : kAcc) + 2 * kAttnStages * 8 + 16;
+  static constexpr size_t kBar = kRing + kAcc;              // mbarriers and flags
+  static constexpr size_t kSmem = kBar + 2 * kAttnStages * 8 + 16;
+  static_assert(kSmem <= 227 * 1024, "attention shared memory");
+  // merge scratch in the lane-group area: (max, sum), weight and slot per contributor
+  static constexpr int kMaxContrib = (int)((kAcc - 64) / (G * 12 + 4));
 };
 
 // Reduce N values held by each lane across a segment of LPK lanes (N <= LPK, both powers
@@ -78,36 +86,76 @@ __device__ __forceinline__ float seg_reduce_multi(float (&v)[N], int li) {
   return r;
 }
 
+// The unit partition of one launch: pre[b] = units of one kv head of sequences < b (a
+// table the round's planning kernel wrote for this step);
+// CTA c owns units [start(c), start(c + 1)) of the Hkv * pre[B] units in (sequence,
+// kv head, unit) order.
+struct AttnSched {
+  const int *pre;
+  int B, Hkv, grid;
+  long long total;
+  __device__ long long start(int c) const { return total * c / grid; }
+  __device__ int cta_of(long long u) const {
+    int c = (int)(u * grid / total);
+    while (c + 1 < grid && start(c + 1) <= u) ++c;
+    while (c > 0 && start(c) > u) --c;
+    return c;
+  }
+  // sequence b whose units hold u: the largest b with Hkv * pre[b] <= u
+  __device__ int seq_of(long long u) const {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((long long)Hkv * pre[mid] <= u) lo = mid;
+      else hi = mid - 1;
+    }
+    return lo;
+  }
+};
+
+// A run of units [r0, r1) of pair (b, kvh) inside one CTA's share; pair units nu.
+struct AttnSeg {
+  int b, kvh, r0, r1, nu;
+  long long pair_u0;  // first unit of the pair
+};
+
+__device__ __forceinline__ AttnSeg attn_seg(const AttnSched &S, long long u, long long u_end) {
+  AttnSeg s;
+  s.b = S.seq_of(u);
+  s.nu = S.pre[s.b + 1] - S.pre[s.b];
+  const long long off = u - (long long)S.Hkv * S.pre[s.b];
+  s.kvh = (int)(off / s.nu);
+  s.r0 = (int)(off - (long long)s.kvh * s.nu);
+  s.pair_u0 = u - s.r0;
+  s.r1 = (int)min((long long)s.nu, (long long)s.r0 + (u_end - u));
+  return s;
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const AttnParams p) {
   using S = AttnShape<D, G>;
   constexpr int LPK = S::LPK, KPW = S::KPW, NP = S::NP, UNR = S::UNR, N = S::N, SH = S::SH;
   constexpr int LOG_G = S::LOG_G, CH = S::CH;
   extern __shared__ __align__(128) unsigned char smem[];
-  // ring of runs; after the last run the same memory holds the lane-group partials
-  float *sm_acc = reinterpret_cast<float *>(smem);  // [NP][G][D]
-  const size_t bar_off = (S::kRing > S::kAcc ? S::kRing : S::kAcc);
-  const uint32_t full0 = smem_addr(smem + bar_off);
+  float *sm_acc = reinterpret_cast<float *>(smem + S::kRing);  // [NP][G][D] lane-group partials
+  const uint32_t full0 = smem_addr(smem + S::kBar);
   const uint32_t empty0 = full0 + 8 * kAttnStages;
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + bar_off + 2 * kAttnStages * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kBar + 2 * kAttnStages * 8);
   __shared__ float2 sm_ml[NP][G];
   __shared__ int last_sh;
 
-  const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grp = lane / LPK, li = lane - grp * LPK;
-  const int H = p.n_head, Hkv = p.n_head_kv, ps = p.page_size;
-  const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
-
-  // Key range of this split, from the length before gamma_eff is known (committed + step).
-  const int L = p.kv_len[b];
-  int len = L + p.step + 1;
-  if (len > p.max_cache_len) len = p.max_cache_len;
-  if (len < 1) len = 1;
-  const int chunk = (len + p.splits - 1) / p.splits;
-  const int k0 = min(s * chunk, len);
-  const int k1_est = min(len, k0 + chunk);
-  const int run_max = min(CH, ps);  // a run never crosses a page
+  const int H = p.n_head, Hkv = p.n_head_kv, ps = p.page_size, U = p.unit_keys;
+  AttnSched sch;
+  sch.pre = p.unit_pre;
+  sch.B = p.batch;
+  sch.Hkv = Hkv;
+  sch.total = (long long)Hkv * sch.pre[p.batch];
+  // every active CTA owns at least one unit (a CTA beyond the unit count has none)
+  sch.grid = (int)min((long long)gridDim.x, sch.total);
+  const int cta = blockIdx.x;
+  const long long u_begin = cta < sch.grid ? sch.start(cta) : 0, u_end = cta < sch.grid ? sch.start(cta + 1) : 0;
 
   if (tid == 0) {
     for (int i = 0; i < kAttnStages; ++i) {
@@ -119,14 +167,25 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
   }
   __syncthreads();
   pdl_trigger();
+  if (u_begin >= u_end) {  // a CTA beyond the unit count: nothing to do
+    pdl_wait();
+    return;
+  }
 
-  // run boundaries: [pos, pos + n), n = min(run_max, page end - pos, k1 - pos)
-  auto run_len = [&](int pos, int k1) { return min(min(run_max, (pos / ps + 1) * ps - pos), k1 - pos); };
-  auto final_k1 = [&]() {
+  // keys of sequence b: the estimate before gamma_eff is read (committed + step + 1) fixes
+  // the unit partition; the final length (after the wait) trims the last unit.
+  auto est_len = [&](int b) {
+    const int L = p.kv_len[b];
+    int len = L + p.step + 1;
+    if (len > p.max_cache_len) len = p.max_cache_len;
+    return len < 1 ? 1 : len;
+  };
+  auto final_len = [&](int b) {
+    const int L = p.kv_len[b];
     const int ge = p.gamma_eff ? p.gamma_eff[b] : p.step + 1;
     int len2 = L + min(p.step, max(ge - 1, 0)) + 1;
     if (L < 0 || len2 > p.max_cache_len) len2 = min(max(len2, 1), p.max_cache_len);
-    return min(k1_est, len2);
+    return min(est_len(b), len2);
   };
 
   if (warp == kAttnWarps) {
@@ -134,90 +193,116 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       bool waited = false;
-      int k1 = k1_est, r = 0;
-      for (int pos = k0; pos < k1; ++r) {
-        int n = run_len(pos, k1);
-        if (!waited && (pos + n > L || L < 0)) {  // this run holds keys written by the chain
-          pdl_wait();
-          waited = true;
-          k1 = final_k1();
-          if (pos >= k1) break;
-          n = run_len(pos, k1);
+      int g = 0;  // ring stage counter
+      bool ok = true;
+      for (long long u = u_begin; u < u_end && ok;) {
+        const AttnSeg sg = attn_seg(sch, u, u_end);
+        u += sg.r1 - sg.r0;
+        const int L = p.kv_len[sg.b], est = est_len(sg.b);
+        const int32_t *pt = p.page_table + (size_t)sg.b * p.max_pages;
+        int fin = est;
+        for (int r = sg.r0; r < sg.r1; ++r) {
+          const int k0 = r * U;
+          int k1 = min(k0 + U, est);
+          if (k1 > L) {  // this unit holds keys written by the chain: wait for them
+            if (!waited) {
+              pdl_wait();
+              waited = true;
+            }
+            fin = final_len(sg.b);
+            k1 = min(k1, fin);
+          }
+          if (k1 <= k0) continue;  // trimmed away: the consumers skip it too
+          const int slot = g % kAttnStages;
+          if (g >= kAttnStages && !mbar_wait(empty0 + 8 * slot, ((g / kAttnStages) - 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const int pg = pt[k0 / ps];
+          const uint32_t bytes = (uint32_t)(k1 - k0) * D * 2u;
+          mbar_expect_tx(full0 + 8 * slot, 2u * bytes);
+          if (pg < 0 || pg >= p.num_pages) {
+            // keep the ring in step: complete the stage without data (consumers skip it)
+            set_status(p.status, EAGLE3_DEV_BAD_PAGE);
+            asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * slot), "r"(2u * bytes) : "memory");
+          } else {
+            const size_t off = (((size_t)pg * Hkv + sg.kvh) * ps + k0 % ps) * D;
+            const uint32_t dst = smem_addr(smem + (size_t)slot * S::kStage);
+            bulk_g2s(dst, p.k_pool + off, bytes, full0 + 8 * slot, pol);
+            bulk_g2s(dst + (uint32_t)(CH * D * 2), p.v_pool + off, bytes, full0 + 8 * slot, pol);
+          }
+          ++g;
         }
-        const int slot = r % kAttnStages;
-        if (r >= kAttnStages && !mbar_wait(empty0 + 8 * slot, ((r / kAttnStages) - 1) & 1, abort_flag, p.status))
-          break;
-        const int pg = pt[pos / ps];
-        const uint32_t bytes = (uint32_t)n * D * 2u;
-        mbar_expect_tx(full0 + 8 * slot, 2u * bytes);
-        if (pg < 0 || pg >= p.num_pages) {
-          // keep the ring in step: complete the stage without data (consumers skip it)
-          set_status(p.status, EAGLE3_DEV_BAD_PAGE);
-          asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * slot), "r"(2u * bytes) : "memory");
-        } else {
-          const size_t off = (((size_t)pg * Hkv + kvh) * ps + pos % ps) * D;
-          const uint32_t dst = smem_addr(smem + (size_t)slot * S::kStage);
-          bulk_g2s(dst, p.k_pool + off, bytes, full0 + 8 * slot, pol);
-          bulk_g2s(dst + (uint32_t)(CH * D * 2), p.v_pool + off, bytes, full0 + 8 * slot, pol);
-        }
-        pos += n;
       }
       // no copy may still be in flight when the CTA moves on
-      for (int i = max(0, r - kAttnStages); i < r; ++i)
+      for (int i = max(0, g - kAttnStages); i < g; ++i)
         mbar_wait(full0 + 8 * (i % kAttnStages), (i / kAttnStages) & 1, abort_flag, p.status);
       if (!waited) pdl_wait();
     }
     __syncwarp();
-  } else {
-    // ---------------------------------------------------------- consumer warps
-    pdl_wait();
-    const int k1 = final_k1();
-    const float qscale = rsqrtf((float)D) * 1.4426950408889634f;
+    return;
+  }
+
+  // ------------------------------------------------------------ consumer warps
+  pdl_wait();
+  const float qscale = rsqrtf((float)D) * 1.4426950408889634f;
+  // Score index of this lane after the segment reduction: (key u_me, head g_me).
+  const int idx_me = li >> SH;
+  const int g_me = idx_me & (G - 1), u_me = idx_me >> LOG_G;
+  const int part = warp * KPW + grp;
+  int g = 0;
+  for (long long u = u_begin; u < u_end;) {
+    const AttnSeg sg = attn_seg(sch, u, u_end);
+    u += sg.r1 - sg.r0;
+    const int b = sg.b, kvh = sg.kvh;
+    const int est = est_len(b), fin = final_len(b), L = p.kv_len[b];
+    const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
     float qv[G][8];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float4 *qp = reinterpret_cast<const float4 *>(p.q + (size_t)b * H * D + (size_t)(kvh * G + g) * D + li * 8);
-      const float4 a = qp[0], c = qp[1];
-      qv[g][0] = a.x * qscale; qv[g][1] = a.y * qscale; qv[g][2] = a.z * qscale; qv[g][3] = a.w * qscale;
-      qv[g][4] = c.x * qscale; qv[g][5] = c.y * qscale; qv[g][6] = c.z * qscale; qv[g][7] = c.w * qscale;
+    for (int gg = 0; gg < G; ++gg) {
+      const float4 *qp = reinterpret_cast<const float4 *>(p.q + (size_t)b * H * D + (size_t)(kvh * G + gg) * D + li * 8);
+      const float4 a = __ldcg(qp), c = __ldcg(qp + 1);
+      qv[gg][0] = a.x * qscale; qv[gg][1] = a.y * qscale; qv[gg][2] = a.z * qscale; qv[gg][3] = a.w * qscale;
+      qv[gg][4] = c.x * qscale; qv[gg][5] = c.y * qscale; qv[gg][6] = c.z * qscale; qv[gg][7] = c.w * qscale;
     }
-    // Score index of this lane after the segment reduction: (key u_me, head g_me).
-    const int idx_me = li >> SH;
-    const int g_me = idx_me & (G - 1), u_me = idx_me >> LOG_G;
     float m_me = -INFINITY, l_me = 0.f;  // running max (log2 domain) and sum of head g_me
     float acc[G][8];                     // running weighted V of this lane's 8 dims, every head
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+    for (int gg = 0; gg < G; ++gg)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[g][i] = 0.f;
+      for (int i = 0; i < 8; ++i) acc[gg][i] = 0.f;
 
-    int r = 0;
-    for (int pos = k0; pos < k1; ++r) {
-      const int n = run_len(pos, k1);
-      const int slot = r % kAttnStages;
-      const bool ok = mbar_wait(full0 + 8 * slot, (r / kAttnStages) & 1, abort_flag, p.status);
-      const int pg = pt[pos / ps];
+    for (int r = sg.r0; r < sg.r1; ++r) {
+      const int k0 = r * U;
+      int k1 = min(k0 + U, est);
+      if (k1 > L) k1 = min(k1, fin);
+      if (k1 <= k0) continue;
+      const int n = k1 - k0;
+      const int slot = g % kAttnStages;
+      const bool ok = mbar_wait(full0 + 8 * slot, (g / kAttnStages) & 1, abort_flag, p.status);
+      ++g;
+      const int pg = pt[k0 / ps];
       const bool have = ok && pg >= 0 && pg < p.num_pages;
       const unsigned char *kst = smem + (size_t)slot * S::kStage;
       const unsigned char *vst = kst + (size_t)CH * D * 2;
-      // keys of this lane group: kk = warp * KPW * UNR + u * KPW + grp
+      // keys of this lane group: kk = warp * KPW * UNR + uu * KPW + grp
       unsigned vmask = 0u;
       float part_s[N];
 #pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        const int kk = warp * KPW * UNR + u * KPW + grp;
+      for (int uu = 0; uu < UNR; ++uu) {
+        const int kk = warp * KPW * UNR + uu * KPW + grp;
         const bool v = have && kk < n;
-        vmask |= v ? (1u << u) : 0u;
+        vmask |= v ? (1u << uu) : 0u;
         uint4 ku = make_uint4(0u, 0u, 0u, 0u);
         if (v) ku = *reinterpret_cast<const uint4 *>(kst + ((size_t)kk * D + li * 8) * 2);
         const float kf[8] = {bf_lo(ku.x), bf_hi(ku.x), bf_lo(ku.y), bf_hi(ku.y),
                              bf_lo(ku.z), bf_hi(ku.z), bf_lo(ku.w), bf_hi(ku.w)};
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int gg = 0; gg < G; ++gg) {
           float d = 0.f;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) d = fmaf(qv[g][i], kf[i], d);
-          part_s[u * G + g] = d;
+          for (int i = 0; i < 8; ++i) d = fmaf(qv[gg][i], kf[i], d);
+          part_s[uu * G + gg] = d;
         }
       }
       const bool vld = (vmask >> u_me) & 1u;
@@ -236,130 +321,153 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
       l_me = l_me * corr + psum;
       m_me = m_new;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float c = __shfl_sync(0xffffffffu, corr, g << SH, LPK);
+      for (int gg = 0; gg < G; ++gg) {
+        const float c = __shfl_sync(0xffffffffu, corr, gg << SH, LPK);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[g][i] *= c;
+        for (int i = 0; i < 8; ++i) acc[gg][i] *= c;
       }
 #pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        const int kk = warp * KPW * UNR + u * KPW + grp;
+      for (int uu = 0; uu < UNR; ++uu) {
+        const int kk = warp * KPW * UNR + uu * KPW + grp;
         uint4 vu = make_uint4(0u, 0u, 0u, 0u);
-        if ((vmask >> u) & 1u) vu = *reinterpret_cast<const uint4 *>(vst + ((size_t)kk * D + li * 8) * 2);
+        if ((vmask >> uu) & 1u) vu = *reinterpret_cast<const uint4 *>(vst + ((size_t)kk * D + li * 8) * 2);
         const float vf[8] = {bf_lo(vu.x), bf_hi(vu.x), bf_lo(vu.y), bf_hi(vu.y),
                              bf_lo(vu.z), bf_hi(vu.z), bf_lo(vu.w), bf_hi(vu.w)};
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float pg2 = __shfl_sync(0xffffffffu, pr, (u * G + g) << SH, LPK);
+        for (int gg = 0; gg < G; ++gg) {
+          const float pg2 = __shfl_sync(0xffffffffu, pr, (uu * G + gg) << SH, LPK);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[g][i] = fmaf(pg2, vf[i], acc[g][i]);
+          for (int i = 0; i < 8; ++i) acc[gg][i] = fmaf(pg2, vf[i], acc[gg][i]);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-      pos += n;
     }
-    // the ring is reused for the partials only after every warp is done with it
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    const int part = warp * KPW + grp;
+
+    // ---- end of this CTA's units of pair (b, kvh): merge the lane groups
+    asm volatile("bar.sync 1, 256;" ::: "memory");  // the previous pair's reads of sm_acc are done
     if (u_me == 0 && (li & ((1 << SH) - 1)) == 0) sm_ml[part][g_me] = make_float2(m_me, l_me);
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+    for (int gg = 0; gg < G; ++gg)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sm_acc[((size_t)part * G + g) * D + li * 8 + i] = acc[g][i];
-  }
-  __syncthreads();
-
-  const size_t slot = ((size_t)b * Hkv + kvh) * p.splits + s;
-  for (int e = tid; e < G * D; e += kAttnCtaThreads) {
-    const int g = e / D, dim = e - g * D;
-    float M = -INFINITY;
+      for (int i = 0; i < 8; ++i) sm_acc[((size_t)part * G + gg) * D + li * 8 + i] = acc[gg][i];
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    const bool whole = sg.r0 == 0 && sg.r1 == sg.nu;
+    float *out = p.out + (size_t)b * H * D + (size_t)kvh * G * D;
+    // this CTA's (max, sum, weighted V) of the pair: in place in sm_acc lane group 0 and
+    // sm_ml, or written out when no other CTA holds units of the pair
+    const int mine = cta * 2 + (sch.start(cta) >= sg.pair_u0 ? 0 : 1);  // partial slot
+    for (int e = tid; e < G * D; e += kAttnThreads) {
+      const int gg = e / D, dim = e - gg * D;
+      float M = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < NP; ++q) M = fmaxf(M, sm_ml[q][g].x);
-    float Ls = 0.f, O = 0.f;
-    if (M != -INFINITY) {
+      for (int q = 0; q < NP; ++q) M = fmaxf(M, sm_ml[q][gg].x);
+      float Ls = 0.f, O = 0.f;
+      if (M != -INFINITY) {
 #pragma unroll
-      for (int q = 0; q < NP; ++q) {
-        const float2 ml = sm_ml[q][g];
-        const float w = exp2f(ml.x - M);
-        Ls += ml.y * w;
-        O += sm_acc[((size_t)q * G + g) * D + dim] * w;
+        for (int q = 0; q < NP; ++q) {
+          const float2 ml = sm_ml[q][gg];
+          const float w = exp2f(ml.x - M);
+          Ls += ml.y * w;
+          O += sm_acc[((size_t)q * G + gg) * D + dim] * w;
+        }
+      }
+      if (whole) {
+        out[e] = O / Ls;
+      } else {
+        p.part_o[(size_t)mine * G * D + e] = O;
+        if (dim == 0) p.part_ml[(size_t)mine * G + gg] = make_float2(M, Ls);
       }
     }
-    if (p.splits == 1) {
-      p.out[(size_t)b * H * D + (size_t)(kvh * G + g) * D + dim] = O / Ls;
-    } else {
-      p.part_o[(slot * G + g) * D + dim] = O;
-      if (dim == 0) p.part_ml[slot * G + g] = make_float2(M, Ls);
-    }
-  }
-  if (p.splits == 1) return;
+    if (whole) continue;
 
-  __syncthreads();
-  if (tid == 0) {
+    // ---- a pair shared with other CTAs: the last of them merges, in CTA order
+    const int pair = b * Hkv + kvh;
+    const long long pu0 = sg.pair_u0, pu1 = sg.pair_u0 + sg.nu;
+    const int c_first = sch.cta_of(pu0), c_last = sch.cta_of(pu1 - 1);
     __threadfence();
-    const unsigned prev = atomicAdd(p.count + (size_t)b * Hkv + kvh, 1u);
-    last_sh = (prev == (unsigned)p.splits - 1) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!last_sh) return;
-  __threadfence();
-  // Merge the splits: weights w[q][g] = exp2(m_q - M_g) / L_g first (all splits loaded in
-  // parallel), then every thread sums float4 slices over the splits, 8 loads at a time.
-  __shared__ float2 ml_all[kMaxAttnSplits][G];
-  __shared__ float wsm[kMaxAttnSplits][G];
-  __shared__ float2 ML[G];
-  const size_t slot0 = ((size_t)b * Hkv + kvh) * p.splits;
-  for (int i = tid; i < p.splits * G; i += kAttnCtaThreads)
-    ml_all[i / G][i % G] = __ldcg(&p.part_ml[slot0 * G + i]);
-  __syncthreads();
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int q = 0; q < p.splits; ++q) M = fmaxf(M, ml_all[q][tid].x);
-    float Ls = 0.f;
-    for (int q = 0; q < p.splits; ++q)
-      if (ml_all[q][tid].x != -INFINITY) Ls += ml_all[q][tid].y * exp2f(ml_all[q][tid].x - M);
-    ML[tid] = make_float2(M, 1.0f / Ls);
-  }
-  __syncthreads();
-  for (int i = tid; i < p.splits * G; i += kAttnCtaThreads) {
-    const int q = i / G, g = i % G;
-    const float2 ml = ml_all[q][g];
-    wsm[q][g] = ml.x == -INFINITY ? 0.f : exp2f(ml.x - ML[g].x) * ML[g].y;
-  }
-  __syncthreads();
-  const float4 *po = reinterpret_cast<const float4 *>(p.part_o) + slot0 * (G * D / 4);
-  float4 *out4 = reinterpret_cast<float4 *>(p.out + (size_t)b * H * D + (size_t)kvh * G * D);
-  for (int f = tid; f < G * D / 4; f += kAttnCtaThreads) {
-    const int g = (f * 4) / D;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    int q = 0;
-    for (; q + 8 <= p.splits; q += 8) {
-      float4 v[8];
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (tid == 0) {
+      const unsigned prev = atomicAdd(p.count + pair, 1u);
+      last_sh = prev == (unsigned)(c_last - c_first) ? 1 : 0;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (!last_sh) continue;
+    __threadfence();
+    // Weights first: every contributor's (max, sum) and slot into shared memory (the lane-
+    // group area is free now), w = exp2(m - M) / L per (contributor, head); then each
+    // thread sums float4 slices over the contributors, 8 loads at a time.
+    const int nc = c_last - c_first + 1;
+    float2 *ml_s = reinterpret_cast<float2 *>(sm_acc);   // [nc][G]
+    float *w_s = reinterpret_cast<float *>(ml_s + nc * G); // [nc][G]
+    int *slot_s = reinterpret_cast<int *>(w_s + nc * G);   // [nc]
+    float2 *ML = reinterpret_cast<float2 *>((reinterpret_cast<uintptr_t>(slot_s + nc) + 7) & ~(uintptr_t)7);  // [G]
+    for (int i = tid; i < nc; i += kAttnThreads) {
+      const int c2 = c_first + i;
+      slot_s[i] = c2 * 2 + (sch.start(c2) >= pu0 ? 0 : 1);
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    for (int i = tid; i < nc * G; i += kAttnThreads) ml_s[i] = __ldcg(&p.part_ml[(size_t)slot_s[i / G] * G + i % G]);
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (tid < G) {
+      float M = -INFINITY;
+      for (int q = 0; q < nc; ++q) M = fmaxf(M, ml_s[q * G + tid].x);
+      float Ls = 0.f;
+      for (int q = 0; q < nc; ++q)
+        if (ml_s[q * G + tid].x != -INFINITY) Ls += ml_s[q * G + tid].y * exp2f(ml_s[q * G + tid].x - M);
+      ML[tid] = make_float2(M, 1.0f / Ls);
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    for (int i = tid; i < nc * G; i += kAttnThreads) {
+      const float2 ml = ml_s[i];
+      const int gg = i % G;
+      w_s[i] = ml.x == -INFINITY ? 0.f : exp2f(ml.x - ML[gg].x) * ML[gg].y;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    const float4 *po = reinterpret_cast<const float4 *>(p.part_o);
+    float4 *out4 = reinterpret_cast<float4 *>(out);
+    for (int f = tid; f < G * D / 4; f += kAttnThreads) {
+      const int gg = (f * 4) / D;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      int q = 0;
+      for (; q + 8 <= nc; q += 8) {
+        float4 v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = __ldcg(po + (size_t)(q + u) * (G * D / 4) + f);
+        for (int k = 0; k < 8; ++k) v[k] = __ldcg(po + (size_t)slot_s[q + k] * (G * D / 4) + f);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float w = wsm[q + u][g];
-        o.x = fmaf(w, v[u].x, o.x); o.y = fmaf(w, v[u].y, o.y);
-        o.z = fmaf(w, v[u].z, o.z); o.w = fmaf(w, v[u].w, o.w);
+        for (int k = 0; k < 8; ++k) {
+          const float w = w_s[(q + k) * G + gg];
+          o.x = fmaf(w, v[k].x, o.x); o.y = fmaf(w, v[k].y, o.y);
+          o.z = fmaf(w, v[k].z, o.z); o.w = fmaf(w, v[k].w, o.w);
+        }
       }
+      for (; q < nc; ++q) {
+        const float4 v = __ldcg(po + (size_t)slot_s[q] * (G * D / 4) + f);
+        const float w = w_s[q * G + gg];
+        o.x = fmaf(w, v.x, o.x); o.y = fmaf(w, v.y, o.y);
+        o.z = fmaf(w, v.z, o.z); o.w = fmaf(w, v.w, o.w);
+      }
+      out4[f] = o;
     }
-    for (; q < p.splits; ++q) {
-      const float4 v = __ldcg(po + (size_t)q * (G * D / 4) + f);
-      const float w = wsm[q][g];
-      o.x = fmaf(w, v.x, o.x); o.y = fmaf(w, v.y, o.y);
-      o.z = fmaf(w, v.z, o.z); o.w = fmaf(w, v.w, o.w);
-    }
-    out4[f] = o;
+    if (tid == 0) p.count[pair] = 0u;
   }
-  if (tid == 0) p.count[(size_t)b * Hkv + kvh] = 0u;
+}
+
+// Keys per unit: the run of one pass of all warps, cut to the largest power of two that
+// divides the page size (a unit never crosses a page).
+template <int D, int G>
+static int attn_unit_keys_dg(int page_size) {
+  int u = AttnShape<D, G>::CH;
+  while (u > 1 && page_size % u) u >>= 1;
+  return u;
 }
 
 template <int D, int G>
-static cudaError_t attn_launch_dg(const AttnParams &p, int B, cudaStream_t st, bool pdl) {
+static cudaError_t attn_launch_dg(const AttnParams &p, int num_sms, cudaStream_t st, bool pdl) {
+  if (p.unit_keys != attn_unit_keys_dg<D, G>(p.page_size)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.splits, p.n_head_kv, B);
+  // one CTA per SM; no more contributors per pair than the merge scratch holds
+  cfg.gridDim = dim3(num_sms < AttnShape<D, G>::kMaxContrib ? num_sms : AttnShape<D, G>::kMaxContrib);
   cfg.blockDim = dim3(kAttnCtaThreads);
   cfg.dynamicSmemBytes = AttnShape<D, G>::kSmem;
   cfg.stream = st;
@@ -394,14 +502,86 @@ cudaError_t attn_prepare() {
   return e;
 }
 
-cudaError_t attn_launch(const AttnParams &p, int B, cudaStream_t st, bool pdl) {
+int attn_unit_keys(int head_dim, int group, int page_size) {
+#define E3_UNIT(DD, GG) \
+  if (head_dim == DD && group == GG) return attn_unit_keys_dg<DD, GG>(page_size);
+  E3_ATTN_ALL(E3_UNIT)
+#undef E3_UNIT
+  return 0;
+}
+
+cudaError_t attn_launch(const AttnParams &p, int num_sms, cudaStream_t st, bool pdl) {
   const int G = p.n_head / p.n_head_kv;
-  if (p.splits < 1 || p.splits > kMaxAttnSplits) return cudaErrorInvalidValue;
+  if (p.batch < 1 || p.unit_keys < 1 || !p.unit_pre) return cudaErrorInvalidValue;
 #define E3_ATTN_CASE(DD, GG) \
-  if (p.head_dim == DD && G == GG) return attn_launch_dg<DD, GG>(p, B, st, pdl);
+  if (p.head_dim == DD && G == GG) return attn_launch_dg<DD, GG>(p, num_sms, st, pdl);
   E3_ATTN_ALL(E3_ATTN_CASE)
 #undef E3_ATTN_CASE
   return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------------ round plan
+// Unit prefix of every draft step of a round: pre[j][b] = sum over sequences b' < b of
+// ceil(len_j(b') / U), len_j = clamp(kv_len + j + 1, 1, max_cache_len); pre[j][B] is the
+// total.  One CTA; it never signals its dependents early, so every later kernel of the
+// round starts after these tables are complete.
+__global__ void __launch_bounds__(1024) attn_plan_kernel(int B, int gamma, const int32_t *kv_len,
+                                                         int max_cache_len, int U, int32_t *pre) {
+  __shared__ int wsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
+  const int per = (B + nt - 1) / nt;
+  for (int j = 0; j < gamma; ++j) {
+    int32_t *row = pre + (size_t)j * (B + 1);
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int b = tid * per + i;
+      if (b < B) {
+        int len = kv_len[b] + j + 1;
+        if (len > max_cache_len) len = max_cache_len;
+        if (len < 1) len = 1;
+        local += (len + U - 1) / U;
+      }
+    }
+    // exclusive scan of the per-thread sums across the block
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < nt / 32 ? wsum[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += v;
+      }
+      if (lane < nt / 32) wsum[lane] = w;  // inclusive warp prefix
+    }
+    __syncthreads();
+    int run = incl - local + (warp > 0 ? wsum[warp - 1] : 0);
+    for (int i = 0; i < per; ++i) {
+      const int b = tid * per + i;
+      if (b < B) {
+        row[b] = run;
+        int len = kv_len[b] + j + 1;
+        if (len > max_cache_len) len = max_cache_len;
+        if (len < 1) len = 1;
+        run += (len + U - 1) / U;
+      }
+    }
+    if (tid == nt - 1) row[B] = run;  // the last thread's end is the total
+    __syncthreads();
+  }
+}
+
+cudaError_t attn_plan_launch(int B, int gamma, const int32_t *kv_len, int max_cache_len, int U,
+                             int32_t *pre, cudaStream_t st) {
+  if (B < 1 || gamma < 1 || U < 1) return cudaErrorInvalidValue;
+  attn_plan_kernel<<<1, 1024, 0, st>>>(B, gamma, kv_len, max_cache_len, U, pre);
+  return cudaGetLastError();
 }
 
 }  // namespace e3

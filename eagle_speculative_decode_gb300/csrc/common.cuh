@@ -251,9 +251,11 @@ struct AttnParams {
   int step;
   int num_pages, max_pages, page_size, max_cache_len;
   int n_head, n_head_kv, head_dim;
-  int splits;
-  float *part_o;           // [B, H_kv, splits, G, d]
-  float2 *part_ml;         // [B, H_kv, splits, G]
+  int batch;               // sequences B
+  int unit_keys;           // keys per work unit (divides the page size)
+  const int32_t *unit_pre; // [B + 1] unit prefix of this step (round plan)
+  float *part_o;           // [2 * CTAs, G, d] shared pairs' weighted V sums
+  float2 *part_ml;         // [2 * CTAs, G] their (max, sum)
   unsigned int *count;     // [B, H_kv]
   int *status;
 };

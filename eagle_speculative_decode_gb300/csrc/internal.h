@@ -42,7 +42,10 @@ cudaError_t tc_prep_launch(const GemvParams &p, int M, uint16_t *x0, uint16_t *x
 
 bool attn_supported(int head_dim, int group);
 cudaError_t attn_prepare();
-cudaError_t attn_launch(const AttnParams &p, int B, cudaStream_t st, bool pdl);
+int attn_unit_keys(int head_dim, int group, int page_size);
+cudaError_t attn_launch(const AttnParams &p, int num_sms, cudaStream_t st, bool pdl);
+cudaError_t attn_plan_launch(int B, int gamma, const int32_t *kv_len, int max_cache_len, int U,
+                             int32_t *pre, cudaStream_t st);
 
 // Small bookkeeping kernels (small.cu).
 cudaError_t launch_chain_begin(int B, int gamma, unsigned flags, int max_cache_len,
