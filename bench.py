@@ -50,6 +50,44 @@ CONFIGS = {
 }
 
 
+# DRAM traffic (ncu dram__bytes_read.sum + dram__bytes_write.sum, bytes per launch) of the
+# kernels profiled on these workloads, valid only while the kernel's sources are byte for
+# byte the profiled ones (sha256 over the listed csrc files); the summaries under
+# profiles/ give the commands.  Keyed by (config, dominant projection or "attn").
+PROFILED_TRAFFIC = {
+    ("c2", "lmhead"): {"bytes": 262227712 + 3346688,
+                       "sources": ("gemv.cu", "epilogue.cuh", "common.cuh"),
+                       "sha256": "70b482a104a54f839b73b7c648888508817d54d135cd25476b6f8e003becfb02"},
+    ("c4", "attn"): {"bytes": 539156480 + 3380224,
+                     "sources": ("attention.cu", "common.cuh"),
+                     "sha256": "f54e976e2004577d99bb153b103500ba92de69bab0f0ba2637ed2356cb59fb19"},
+    ("c4", "lmhead"): {"bytes": 265020928 + 6003968,
+                       "sources": ("gemm_tc.cu", "epilogue.cuh", "common.cuh"),
+                       "sha256": "07e0e56c23b1d9d9259efedd6d98324c331b09463ad33fd94cdb1734cceea173"},
+}
+
+
+def profiled_traffic(config: str, kind: str):
+    import hashlib
+    e = PROFILED_TRAFFIC.get((config, kind))
+    if e is None:
+        return None
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "eagle_speculative_decode_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in e["sources"]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return e["bytes"] if h.hexdigest() == e["sha256"] else None
+
+
+def kernel_label(kind: str, batch: int) -> str:
+    """Name of the kernel that runs a phase at this batch (projections of three or more
+    items run on the tensor cores, smaller ones on the CUDA-core GEMV)."""
+    if kind == "attn":
+        return "attention"
+    return f"{kind} tcgen05 GEMM" if batch >= 3 else f"{kind} GEMV"
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -437,9 +475,10 @@ def run_mine(args, cfg):
         "step_roofline": {"bytes_per_step": rb, "achieved_gbs": rb / (ms_per_step * 1e-3) / 1e9,
                           "peak_gbs": hbm_peak, "frac": step_frac,
                           "note": f"algorithmic bytes of the whole round / round time, of {peak_src}"},
-        "roofline": {"bound": "hbm", "kernel": f"{dominant} GEMV" if dominant != "attn" else "attention",
+        "roofline": {"bound": "hbm", "kernel": kernel_label(dominant, B),
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": (achieved / hbm_peak) if achieved else None, "traffic": None,
+                     "frac": (achieved / hbm_peak) if achieved else None,
+                     "traffic": profiled_traffic(args.config, dominant),
                      "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
                      "bytes_per_launch": dom_bytes, "us_per_launch": kern_us.get(dominant)},
         "kernel_us": kern_us,

@@ -354,14 +354,8 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
   cudaError_t e = launched(ctx, st,
                            launch_chain_begin(a.B, a.gamma, a.flags, c.max_cache_len, a.kv->kv_len,
                                               ctx->round_start, ctx->geff, a.gamma_eff,
-                                              ctx->status, st, false),
+                                              ctx->status, ctx->unit_keys, ctx->attn_plan, st),
                            PH_SMALL);
-  if (e != cudaSuccess) return e;
-  // the attention's unit partition of every step; the round's later kernels start after it
-  e = launched(ctx, st,
-               attn_plan_launch(a.B, a.gamma, a.kv->kv_len, c.max_cache_len, ctx->unit_keys,
-                                ctx->attn_plan, st),
-               PH_SMALL);
   if (e != cudaSuccess) return e;
   for (int j = 0; j < a.gamma; ++j) {
     // q/k/v + RoPE + KV append

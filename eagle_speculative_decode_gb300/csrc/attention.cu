@@ -87,7 +87,7 @@ __device__ __forceinline__ float seg_reduce_multi(float (&v)[N], int li) {
 }
 
 // The unit partition of one launch: pre[b] = units of one kv head of sequences < b (a
-// table the round's planning kernel wrote for this step);
+// table chain_begin wrote for this step before any later kernel of the round started);
 // CTA c owns units [start(c), start(c + 1)) of the Hkv * pre[B] units in (sequence,
 // kv head, unit) order.
 struct AttnSched {
@@ -518,70 +518,6 @@ cudaError_t attn_launch(const AttnParams &p, int num_sms, cudaStream_t st, bool 
   E3_ATTN_ALL(E3_ATTN_CASE)
 #undef E3_ATTN_CASE
   return cudaErrorInvalidValue;
-}
-
-// ------------------------------------------------------------------ round plan
-// Unit prefix of every draft step of a round: pre[j][b] = sum over sequences b' < b of
-// ceil(len_j(b') / U), len_j = clamp(kv_len + j + 1, 1, max_cache_len); pre[j][B] is the
-// total.  One CTA; it never signals its dependents early, so every later kernel of the
-// round starts after these tables are complete.
-__global__ void __launch_bounds__(1024) attn_plan_kernel(int B, int gamma, const int32_t *kv_len,
-                                                         int max_cache_len, int U, int32_t *pre) {
-  __shared__ int wsum[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
-  const int per = (B + nt - 1) / nt;
-  for (int j = 0; j < gamma; ++j) {
-    int32_t *row = pre + (size_t)j * (B + 1);
-    int local = 0;
-    for (int i = 0; i < per; ++i) {
-      const int b = tid * per + i;
-      if (b < B) {
-        int len = kv_len[b] + j + 1;
-        if (len > max_cache_len) len = max_cache_len;
-        if (len < 1) len = 1;
-        local += (len + U - 1) / U;
-      }
-    }
-    // exclusive scan of the per-thread sums across the block
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      int w = lane < nt / 32 ? wsum[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += v;
-      }
-      if (lane < nt / 32) wsum[lane] = w;  // inclusive warp prefix
-    }
-    __syncthreads();
-    int run = incl - local + (warp > 0 ? wsum[warp - 1] : 0);
-    for (int i = 0; i < per; ++i) {
-      const int b = tid * per + i;
-      if (b < B) {
-        row[b] = run;
-        int len = kv_len[b] + j + 1;
-        if (len > max_cache_len) len = max_cache_len;
-        if (len < 1) len = 1;
-        run += (len + U - 1) / U;
-      }
-    }
-    if (tid == nt - 1) row[B] = run;  // the last thread's end is the total
-    __syncthreads();
-  }
-}
-
-cudaError_t attn_plan_launch(int B, int gamma, const int32_t *kv_len, int max_cache_len, int U,
-                             int32_t *pre, cudaStream_t st) {
-  if (B < 1 || gamma < 1 || U < 1) return cudaErrorInvalidValue;
-  attn_plan_kernel<<<1, 1024, 0, st>>>(B, gamma, kv_len, max_cache_len, U, pre);
-  return cudaGetLastError();
 }
 
 }  // namespace e3

@@ -44,13 +44,12 @@ bool attn_supported(int head_dim, int group);
 cudaError_t attn_prepare();
 int attn_unit_keys(int head_dim, int group, int page_size);
 cudaError_t attn_launch(const AttnParams &p, int num_sms, cudaStream_t st, bool pdl);
-cudaError_t attn_plan_launch(int B, int gamma, const int32_t *kv_len, int max_cache_len, int U,
-                             int32_t *pre, cudaStream_t st);
 
 // Small bookkeeping kernels (small.cu).
 cudaError_t launch_chain_begin(int B, int gamma, unsigned flags, int max_cache_len,
                                const int32_t *kv_len, int32_t *round_start, int32_t *geff,
-                               int32_t *geff_out, int *status, cudaStream_t st, bool pdl);
+                               int32_t *geff_out, int *status, int unit_keys, int32_t *unit_pre,
+                               cudaStream_t st);
 cudaError_t launch_chain_end(int B, int32_t *kv_len, const int32_t *round_start,
                              const int32_t *geff, cudaStream_t st, bool pdl);
 cudaError_t launch_rewind(int B, int32_t *kv_len, const int32_t *round_start, cudaStream_t st);

@@ -19,28 +19,80 @@ static cudaLaunchConfig_t small_cfg(int grid, int block, cudaStream_t st, bool p
   return cfg;
 }
 
-// Records the round start and the per-sequence chain length.  gamma_eff follows the
-// capacity rule: kv_len + gamma_eff + 1 <= max_cache_len.
-__global__ void chain_begin_kernel(int B, int gamma, unsigned flags, int max_cache_len,
-                                   const int32_t *kv_len, int32_t *round_start, int32_t *geff,
-                                   int32_t *geff_out, int *status) {
-  pdl_trigger();
+// Records the round start and the per-sequence chain length, and plans the attention
+// work of every draft step.  gamma_eff follows the capacity rule:
+// kv_len + gamma_eff + 1 <= max_cache_len.  Plan: pre[j][b] = sum over sequences b' < b of
+// ceil(len_j(b') / U), len_j = clamp(kv_len + j + 1, 1, max_cache_len), pre[j][B] the
+// total (the attention's unit partition).  One CTA; it does not signal its dependents
+// early, so every later kernel of the round starts after it has finished.
+__global__ void __launch_bounds__(1024) chain_begin_kernel(int B, int gamma, unsigned flags,
+                                                           int max_cache_len, const int32_t *kv_len,
+                                                           int32_t *round_start, int32_t *geff,
+                                                           int32_t *geff_out, int *status, int U,
+                                                           int32_t *pre) {
   pdl_wait();
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= B) return;
-  const int L = kv_len[b];
-  int ge = gamma;
-  if (L < 0 || L + gamma + 1 > max_cache_len) {
-    if ((flags & EAGLE3_SHRINK_GAMMA) && L >= 0 && max_cache_len - L - 1 >= 1) {
-      ge = max_cache_len - L - 1;
-    } else {
-      ge = 0;
-      set_status(status, EAGLE3_DEV_BAD_LENGTH);
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  for (int b = tid; b < B; b += nt) {
+    const int L = kv_len[b];
+    int ge = gamma;
+    if (L < 0 || L + gamma + 1 > max_cache_len) {
+      if ((flags & EAGLE3_SHRINK_GAMMA) && L >= 0 && max_cache_len - L - 1 >= 1) {
+        ge = max_cache_len - L - 1;
+      } else {
+        ge = 0;
+        set_status(status, EAGLE3_DEV_BAD_LENGTH);
+      }
     }
+    round_start[b] = L < 0 ? 0 : L;
+    geff[b] = ge;
+    if (geff_out) geff_out[b] = ge;
   }
-  round_start[b] = L < 0 ? 0 : L;
-  geff[b] = ge;
-  if (geff_out) geff_out[b] = ge;
+  if (!pre || U < 1) return;
+  __shared__ int wsum[32];
+  const int per = (B + nt - 1) / nt;  // consecutive sequences per thread
+  auto units = [&](int b, int j) {
+    int len = kv_len[b] + j + 1;
+    if (len > max_cache_len) len = max_cache_len;
+    if (len < 1) len = 1;
+    return (len + U - 1) / U;
+  };
+  for (int j = 0; j < gamma; ++j) {
+    int32_t *row = pre + (size_t)j * (B + 1);
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int b = tid * per + i;
+      if (b < B) local += units(b, j);
+    }
+    // exclusive scan of the per-thread sums across the block
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < nt / 32 ? wsum[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += v;
+      }
+      if (lane < nt / 32) wsum[lane] = w;  // inclusive prefix over warps
+    }
+    __syncthreads();
+    int run = incl - local + (warp > 0 ? wsum[warp - 1] : 0);
+    for (int i = 0; i < per; ++i) {
+      const int b = tid * per + i;
+      if (b < B) {
+        row[b] = run;
+        run += units(b, j);
+      }
+    }
+    if (tid == nt - 1) row[B] = run;  // the last thread ends at the total
+    __syncthreads();
+  }
 }
 
 __global__ void chain_end_kernel(int B, int32_t *kv_len, const int32_t *round_start,
@@ -109,11 +161,12 @@ __global__ void prefill_finish_kernel(int b, int n_embd, int kv_len_value, const
 
 cudaError_t launch_chain_begin(int B, int gamma, unsigned flags, int max_cache_len,
                                const int32_t *kv_len, int32_t *round_start, int32_t *geff,
-                               int32_t *geff_out, int *status, cudaStream_t st, bool pdl) {
+                               int32_t *geff_out, int *status, int unit_keys, int32_t *unit_pre,
+                               cudaStream_t st) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = small_cfg((B + 127) / 128, 128, st, pdl, attr);
+  cudaLaunchConfig_t cfg = small_cfg(1, 1024, st, false, attr);
   return cudaLaunchKernelEx(&cfg, chain_begin_kernel, B, gamma, flags, max_cache_len, kv_len,
-                            round_start, geff, geff_out, status);
+                            round_start, geff, geff_out, status, unit_keys, unit_pre);
 }
 
 cudaError_t launch_chain_end(int B, int32_t *kv_len, const int32_t *round_start,
