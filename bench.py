@@ -331,9 +331,18 @@ def run_mine(args, cfg):
                            for r in range(n_rounds_max)]).astype(np.int32)
     n_imp = torch.from_numpy(n_imp_host).to(dev)
     ar = torch.arange(gamma + 1, device=dev, dtype=torch.int32)
+    # The synthetic target's predictions y[b, :gamma] = draft XOR flip: flip is 0 on the
+    # first n_imp drafts and 1 after, so exactly n_imp drafts are accepted; the bonus
+    # column y[b, gamma] is a fixed token.  One launch per round (the target vocabulary is
+    # even, so a flipped id stays in range).
+    assert geo.target_vocab % 2 == 0
+    flip = (ar[None, None, :gamma] >= n_imp[:, :, None]).to(torch.int32)  # [round, B, gamma]
     out = {"draft_tok": torch.empty(B, gamma, dtype=torch.int32, device=dev),
            "gamma_eff": torch.empty(B, dtype=torch.int32, device=dev)}
-    y = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
+    y = torch.full((B, gamma + 1), 7, dtype=torch.int32, device=dev)
+
+    def verify(r, d):
+        torch.bitwise_xor(d, flip[r], out=y[:, :gamma])
     n_acc = torch.empty(B, dtype=torch.int32, device=dev)
     bonus = torch.empty(B, dtype=torch.int32, device=dev)
     ctx_sum = [0.0]
@@ -348,8 +357,7 @@ def run_mine(args, cfg):
         seq.rewind()
         # synthetic target: accepts exactly n_imp[r] drafts, then disagrees
         d = out["draft_tok"]
-        ext = torch.cat([d, ((d[:, -1:] + 7) % geo.target_vocab)], dim=1)
-        torch.where(ar[None, :] < n_imp[r][:, None], ext, (ext + 1) % geo.target_vocab, out=y)
+        verify(r, d)
         seq.accept(d, y, out["gamma_eff"], n_acc=n_acc, bonus=bonus)
         seq.rebuild_after_verify(n_acc, d, bonus, vaux[r], n_acc_host=n_imp_host[r])
 
@@ -399,8 +407,7 @@ def run_mine(args, cfg):
             per_label.setdefault(lab, []).append(ms * 1e3)
         seq.rewind()
         d = out["draft_tok"]
-        ext = torch.cat([d, ((d[:, -1:] + 7) % geo.target_vocab)], dim=1)
-        torch.where(ar[None, :] < n_imp[r][:, None], ext, (ext + 1) % geo.target_vocab, out=y)
+        verify(r, d)
         seq.accept(d, y, out["gamma_eff"], n_acc=n_acc, bonus=bonus)
         seq.rebuild_after_verify(n_acc, d, bonus, vaux[r], n_acc_host=n_imp_host[r])
         r += 1
@@ -433,8 +440,7 @@ def run_mine(args, cfg):
         seq.draft_chain(gamma, out=out)
         seq.rewind()
         d = out["draft_tok"]
-        ext = torch.cat([d, ((d[:, -1:] + 7) % geo.target_vocab)], dim=1)
-        torch.where(ar[None, :] < n_imp[r][:, None], ext, (ext + 1) % geo.target_vocab, out=y)
+        verify(r, d)
         seq.accept(d, y, out["gamma_eff"], n_acc=acc_pair[0], bonus=acc_pair[1])
         seq.rebuild_after_verify(acc_pair[0], d, acc_pair[1], vbuf, n_acc_host=n_imp_host[r])
         host_tok.copy_(d, non_blocking=True)

@@ -858,7 +858,7 @@ int eagle3_rebuild_after_verify(eagle3_ctx *ctx, int B, int gamma, const int32_t
   ctx->last_stream = st;
   const int n = ctx->c.n_embd;
   const int M = B * (gamma + 1);
-  cudaError_t e = enqueue_encode(ctx, verify_aux, M, ctx->genc, st, false);
+  cudaError_t e = enqueue_encode(ctx, verify_aux, M, ctx->genc, st, true);
   if (e == cudaSuccess) {
     GemvParams p = base_params(ctx);
     kv_only_params(ctx, kv, p);

@@ -104,6 +104,8 @@ __global__ void chain_end_kernel(int B, int32_t *kv_len, const int32_t *round_st
 }
 
 __global__ void rewind_kernel(int B, int32_t *kv_len, const int32_t *round_start) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < B) kv_len[b] = round_start[b];
 }
@@ -111,6 +113,8 @@ __global__ void rewind_kernel(int B, int32_t *kv_len, const int32_t *round_start
 // n = leading matches of target_pred[b, i] with draft_tok[b, i]; bonus = target_pred[b, n].
 __global__ void accept_kernel(int B, int gamma, const int32_t *draft_tok, const int32_t *target_pred,
                               const int32_t *gamma_eff, int32_t *n_acc, int32_t *bonus) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   int ge = gamma_eff ? gamma_eff[b] : gamma;
@@ -128,6 +132,8 @@ __global__ void rebuild_finish_kernel(int B, int gamma, int n_embd, const float 
                                       const int32_t *n_acc, const int32_t *bonus, float *bnd_g,
                                       int32_t *bnd_tok, int32_t *kv_len, int max_cache_len,
                                       int *status) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.y;
   int n = n_acc[b];
   if (n < 0 || n > gamma) {
@@ -151,6 +157,8 @@ __global__ void rebuild_finish_kernel(int B, int gamma, int n_embd, const float 
 __global__ void prefill_finish_kernel(int b, int n_embd, int kv_len_value, const float *enc_last,
                                       const int32_t *next_tok, float *bnd_g, int32_t *bnd_tok,
                                       int32_t *kv_len) {
+  pdl_trigger();
+  pdl_wait();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_embd; i += gridDim.x * blockDim.x)
     bnd_g[(size_t)b * n_embd + i] = enc_last[i];
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -176,35 +184,42 @@ cudaError_t launch_chain_end(int B, int32_t *kv_len, const int32_t *round_start,
   return cudaLaunchKernelEx(&cfg, chain_end_kernel, B, kv_len, round_start, geff);
 }
 
+// The bookkeeping kernels are launched as programmatic dependents of whatever kernel
+// precedes them on the stream (each waits for it before touching data), so their launch
+// overlaps the previous kernel's tail.
 cudaError_t launch_rewind(int B, int32_t *kv_len, const int32_t *round_start, cudaStream_t st) {
-  rewind_kernel<<<(B + 127) / 128, 128, 0, st>>>(B, kv_len, round_start);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = small_cfg((B + 127) / 128, 128, st, true, attr);
+  return cudaLaunchKernelEx(&cfg, rewind_kernel, B, kv_len, round_start);
 }
 
 cudaError_t launch_accept(int B, int gamma, const int32_t *draft_tok, const int32_t *target_pred,
                           const int32_t *gamma_eff, int32_t *n_acc, int32_t *bonus,
                           cudaStream_t st) {
-  accept_kernel<<<(B + 127) / 128, 128, 0, st>>>(B, gamma, draft_tok, target_pred, gamma_eff,
-                                                 n_acc, bonus);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = small_cfg((B + 127) / 128, 128, st, true, attr);
+  return cudaLaunchKernelEx(&cfg, accept_kernel, B, gamma, draft_tok, target_pred, gamma_eff, n_acc,
+                            bonus);
 }
 
 cudaError_t launch_rebuild_finish(int B, int gamma, int n_embd, const float *enc_g,
                                   const int32_t *n_acc, const int32_t *bonus, float *bnd_g,
                                   int32_t *bnd_tok, int32_t *kv_len, int max_cache_len,
                                   int *status, cudaStream_t st) {
-  dim3 grid((n_embd + 1023) / 1024, B);
-  rebuild_finish_kernel<<<grid, 256, 0, st>>>(B, gamma, n_embd, enc_g, n_acc, bonus, bnd_g,
-                                              bnd_tok, kv_len, max_cache_len, status);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = small_cfg(1, 256, st, true, attr);
+  cfg.gridDim = dim3((n_embd + 1023) / 1024, B);
+  return cudaLaunchKernelEx(&cfg, rebuild_finish_kernel, B, gamma, n_embd, enc_g, n_acc, bonus, bnd_g,
+                            bnd_tok, kv_len, max_cache_len, status);
 }
 
 cudaError_t launch_prefill_finish(int b, int n_embd, int kv_len_value, const float *enc_last,
                                   const int32_t *next_tok, float *bnd_g, int32_t *bnd_tok,
                                   int32_t *kv_len, cudaStream_t st) {
-  prefill_finish_kernel<<<(n_embd + 1023) / 1024, 256, 0, st>>>(b, n_embd, kv_len_value, enc_last,
-                                                                next_tok, bnd_g, bnd_tok, kv_len);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = small_cfg((n_embd + 1023) / 1024, 256, st, true, attr);
+  return cudaLaunchKernelEx(&cfg, prefill_finish_kernel, b, n_embd, kv_len_value, enc_last, next_tok,
+                            bnd_g, bnd_tok, kv_len);
 }
 
 }  // namespace e3
