@@ -8,7 +8,7 @@
 
 namespace e3 {
 
-constexpr int kGemvThreads = 256;
+constexpr int kGemvThreads = 512;  // GEMV consumer threads (16 warps)
 constexpr int kGemvWarps = kGemvThreads / 32;
 
 // ------------------------------------------------------------------ PDL (griddepcontrol)
@@ -107,8 +107,8 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
-// Barrier among the 256 consumer threads of a GEMV CTA (the producer warp is not in it).
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Barrier among the consumer threads of a GEMV CTA (the producer warp is not in it).
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kGemvThreads) : "memory"); }
 
 // Order-preserving map of a float to uint32 (larger float -> larger key); -0 -> +0.
 __device__ __forceinline__ uint32_t float_order_key(float f) {

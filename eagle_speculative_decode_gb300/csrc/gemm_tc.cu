@@ -41,6 +41,10 @@ constexpr int kTcK = 64;           // k-tile: one 128-byte swizzle row of bf16
 constexpr int kTcAWarp = 8, kTcMmaWarp = 9, kTcBWarp = 10;
 constexpr int kTcThreads = 352;
 constexpr int kTcChunk = 8;        // k-tiles per TMEM accumulation chunk
+constexpr int kTcEpiThreads = 256; // warps 0-7: TMEM drain and epilogues
+
+// Barrier among the 256 epilogue threads (the producer and MMA warps are not in it).
+__device__ __forceinline__ void tc_epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 struct TcArgs {
   CUtensorMap a0;   // weight matrix of the tile (q / fc / o / gate / down / lm_head)
@@ -311,7 +315,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
 
   // per-item tables of this tile
   if constexpr (ModeTraits<MODE>::kNorm) {
-    for (int i = tid; i < N * H; i += kGemvThreads) {
+    for (int i = tid; i < N * H; i += kTcEpiThreads) {
       const int c = i / H, h = i - c * H, item = item0 + c;
       tb.scale[i] = item < A.M ? rsqrtf(A.sumsq[(size_t)item * H + h] / (float)(p.K / H) + p.eps) : 0.f;
     }
@@ -319,7 +323,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
   if constexpr (MODE == GM_QKV) {
     // k / v tiles also look up each kept item's KV page here, once per item
     const bool kv_tile = p.row_base + rt * kTcM >= p.n_head * p.head_dim;
-    for (int c = tid; c < N; c += kGemvThreads) {
+    for (int c = tid; c < N; c += kTcEpiThreads) {
       const int item = item0 + c;
       int pos = 0, seq = 0, keep = 0, page = -1;
       if (item < A.M) {
@@ -345,7 +349,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
       tb.page[c] = page;
     }
   }
-  consumer_sync();
+  tc_epi_sync();
 
   // y = sum over K halves of (raw sum) * (norm scale), in place in acc[0]
 #pragma unroll
@@ -416,17 +420,17 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
         tb.quad_best[quad * N + tc_c0<N>(vi / 16, chalf) + (vi % 16)] = best;
       }
     }
-    consumer_sync();
+    tc_epi_sync();
     if (tid < N) {
       unsigned long long b = tb.run_best[tid];
 #pragma unroll
       for (int q = 0; q < 4; ++q) b = tb.quad_best[q * N + tid] > b ? tb.quad_best[q * N + tid] : b;
       tb.run_best[tid] = b;
     }
-    consumer_sync();
+    tc_epi_sync();
     if (A.item_tiles > 1) {  // the next tile may belong to another item tile
       tc_lm_flush<N>(A, tb, it);
-      consumer_sync();
+      tc_epi_sync();
     }
   } else if constexpr (MODE == GM_GATEUP) {
     // tile rt: gate rows rt*64 + i in tile rows i < 64, the matching up rows in 64 + i
@@ -437,7 +441,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
         for (int i = 0; i < 16; ++i)
           if (tc_has<N>(j, chalf)) tb.stage[(r - 64) * SP + tc_c0<N>(j, chalf) + i] = y[j][i];
     }
-    consumer_sync();
+    tc_epi_sync();
     const int row = rt * 64 + r;
     if (r < 64 && row < p.n_ff) {
 #pragma unroll
@@ -451,7 +455,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
         }
       }
     }
-    consumer_sync();  // the staging area is free again
+    tc_epi_sync();  // the staging area is free again
   } else if constexpr (MODE == GM_QKV) {
     const int d = p.head_dim, R = p.rope_dims, half = R >> 1;
     const int qr = p.n_head * d, kr = p.n_head_kv * d;
@@ -467,7 +471,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         if (tc_has<N>(j, chalf)) tb.stage[r * SP + tc_c0<N>(j, chalf) + i] = y[j][i];
-    consumer_sync();
+    tc_epi_sync();
     if (vrow) {
       // RoPE in registers first (partner from the staging area, angles from the table),
       // then the stores
@@ -506,7 +510,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
         }
       }
     }
-    consumer_sync();  // the staging area is free again
+    tc_epi_sync();  // the staging area is free again
   }
 }
 
@@ -783,12 +787,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             for (int i = 0; i < 16; ++i)
               if (tc_has<N>(j, chalf)) mine[((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM + r] = acc[h][j][i];
         __threadfence();
-        consumer_sync();
+        tc_epi_sync();
         if (tid == 0) {
           const unsigned prev = atomicAdd(args.tile_cnt + sg.t, 1u);
           *last_sh = prev == (unsigned)(c_last - c_first) ? 1 : 0;
         }
-        consumer_sync();
+        tc_epi_sync();
         if (!*last_sh) continue;
         __threadfence();
         // fixed order: the published sums of contributors c_first .. c_last (this CTA's
@@ -833,15 +837,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       // the last CTA to finish decodes every item's argmax
       if (args.item_tiles == 1) tc_lm_flush<N>(args, tb, 0);
       __threadfence();
-      consumer_sync();
+      tc_epi_sync();
       if (tid == 0) {
         const unsigned prev = atomicAdd(pc.am_count, 1u);
         *last_sh = prev == gridDim.x - 1 ? 1 : 0;
       }
-      consumer_sync();
+      tc_epi_sync();
       if (*last_sh) {
         __threadfence();
-        lmhead_finalize(pc, 0, args.M, tid, kGemvThreads);
+        lmhead_finalize(pc, 0, args.M, tid, kTcEpiThreads);
         if (tid == 0) *pc.am_count = 0u;
       }
     }

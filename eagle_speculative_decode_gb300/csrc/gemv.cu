@@ -11,15 +11,15 @@
 // bulk copies (cp.async.bulk, TMA) into an NSTAGE-deep shared-memory ring guarded by
 // mbarriers.  It starts before the kernel waits on its predecessor (programmatic
 // dependent launch), so the next weights are already in flight while the previous
-// kernel drains.  Eight consumer warps stage x (normalised where the op says so) in
+// kernel drains.  Sixteen consumer warps stage x (normalised where the op says so) in
 // shared memory (float32 in two float4 planes -- elements 0-3 and 4-7 of each 8-element
 // vector, conflict-free LDS.128 -- or as the caller's bf16 for the encode), then, per
-// stage, each thread takes 16-byte vectors k = 8 * (tid + 256 j) of all SR rows, so every
+// stage, each thread takes 16-byte vectors k = 8 * (tid + 512 j) of all SR rows, so every
 // x vector it loads serves SR rows; single-item launches keep their x vectors in
 // registers.  RMSNorm is applied after the dot product: the GEMV runs on x * w_norm and
 // the per-item scale 1 / sqrt(mean(x^2) + eps), reduced while x is staged, multiplies the
 // row sums, so no block-wide reduction stands between the dependency wait and the first
-// FMA.  A stage's per-row sums are reduced within the warp and kept per warp; the eight
+// FMA.  A stage's per-row sums are reduced within the warp and kept per warp; the sixteen
 // warp partials are added in a fixed order before the epilogue (deterministic).
 #include <math.h>
 
@@ -31,10 +31,10 @@ namespace e3 {
 
 // -------------------------------------------------------------------- kernel
 constexpr int kStageBytes = 32 * 1024;
-// Single-item launches with K <= 6 * 256 * 8 = 12288 keep x in registers: 6 vectors of 8
-// floats per thread (larger K reads x from shared memory).
-constexpr int kXRegVecs = 6;
-constexpr int kGemvCtaThreads = kGemvThreads + 32;  // 8 consumer warps + 1 producer warp
+// Single-item launches with K <= 3 * 512 * 8 = 12288 keep x in registers: up to 3 vectors
+// of 8 floats per thread (larger K reads x from shared memory).
+constexpr int kXRegVecs = 3;
+constexpr int kGemvCtaThreads = kGemvThreads + 32;  // 16 consumer warps + 1 producer warp
 
 struct GemvSmem {
   int x_bytes, ring_off, stage_bytes, part_off, accs_off, red_off, scale_off, bar_off, flag_off,
