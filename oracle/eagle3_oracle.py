@@ -116,13 +116,137 @@ def argmax_first(x: np.ndarray) -> int:
     return int(np.argmax(x))
 
 
+# ------------------------------------------------------------- quantized drafter KV
+# "memra_engine/eagle.rs", ``Eagle3Scratch``: the drafter KV uses the q8_0-K / q5_1-V
+# quantized layout of the trunk KV, blocks of 32 values (head_dim % 32 == 0), 34 and 24
+# bytes per block.  The page names the formats and sizes only; the encodings below are
+# the plain reading of those names (reading R20): per block, q8_0 keeps an
+# fp16 scale and 32 signed 8-bit codes, q5_1 an fp16 scale, an fp16 minimum and 32
+# unsigned 5-bit codes.  Codes are decided in float32 on the values as the kernel holds
+# them (float32), with the stored (fp16) scale: the same precision on both sides.
+
+QK = 32                   # values per block
+Q8_0_BLOCK_BYTES = 34     # fp16 d + 32 x int8
+Q5_1_BLOCK_BYTES = 24     # fp16 d + fp16 m + uint32 fifth bits + 16 bytes of 4-bit codes
+
+
+def _blocks(x) -> np.ndarray:
+    x = np.asarray(x, dtype=np.float32)
+    if x.shape[-1] % QK:
+        raise ValueError("the last axis must be a multiple of 32")
+    return x.reshape(x.shape[:-1] + (x.shape[-1] // QK, QK))
+
+
+def quantize_q8_0(x):
+    """Per block of 32: d = fp16(max|x| / 127); code = clamp(rint(x / d), -127, 127),
+    all codes 0 when d = 0.  Returns (d as float16 [..., nb], codes int8 [..., nb, 32])."""
+    xb = _blocks(x)
+    amax = np.max(np.abs(xb), axis=-1)
+    d16 = (amax / np.float32(127)).astype(np.float16)
+    d = d16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(d > 0, np.clip(np.rint(xb / np.where(d > 0, d, np.float32(1))), -127, 127), 0)
+    return d16, q.astype(np.int8)
+
+
+def dequantize_q8_0(d16, codes) -> np.ndarray:
+    """x = d * code (exact in float32: an 11-bit scale times an 8-bit code)."""
+    v = d16.astype(np.float32)[..., None] * codes.astype(np.float32)
+    return v.reshape(v.shape[:-2] + (v.shape[-2] * QK,))
+
+
+def quantize_q5_1(x):
+    """Per block of 32: d = fp16((max - min) / 31), m = fp16(min);
+    code = clamp(rint((x - m) / d), 0, 31), all codes 0 when d = 0.
+    Returns (d float16 [..., nb], m float16 [..., nb], codes uint8 [..., nb, 32])."""
+    xb = _blocks(x)
+    mn = np.min(xb, axis=-1)
+    mx = np.max(xb, axis=-1)
+    d16 = ((mx - mn) / np.float32(31)).astype(np.float16)
+    m16 = mn.astype(np.float16)
+    d = d16.astype(np.float32)[..., None]
+    m = m16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(d > 0, np.clip(np.rint((xb - m) / np.where(d > 0, d, np.float32(1))), 0, 31), 0)
+    return d16, m16, q.astype(np.uint8)
+
+
+def dequantize_q5_1(d16, m16, codes) -> np.ndarray:
+    """x = d * code + m in float32 (the product is exact; one rounding for the sum)."""
+    v = d16.astype(np.float32)[..., None] * codes.astype(np.float32) + m16.astype(np.float32)[..., None]
+    return v.astype(np.float32).reshape(v.shape[:-2] + (v.shape[-2] * QK,))
+
+
+def pack_q8_0(d16, codes) -> np.ndarray:
+    """Block bytes: fp16 d (little endian), then the 32 int8 codes in element order."""
+    d16 = np.asarray(d16, dtype=np.float16)
+    out = np.empty(d16.shape + (Q8_0_BLOCK_BYTES,), dtype=np.uint8)
+    out[..., 0:2] = d16[..., None].view(np.uint8).reshape(d16.shape + (2,))
+    out[..., 2:] = np.asarray(codes, dtype=np.int8).view(np.uint8)
+    return out
+
+
+def unpack_q8_0(blocks):
+    b = np.asarray(blocks, dtype=np.uint8)
+    d16 = np.ascontiguousarray(b[..., 0:2]).view(np.float16)[..., 0]
+    return d16, np.ascontiguousarray(b[..., 2:]).view(np.int8)
+
+
+def pack_q5_1(d16, m16, codes) -> np.ndarray:
+    """Block bytes: fp16 d, fp16 m, uint32 whose bit i is bit 4 of code i, then byte j =
+    (code j & 15) | (code (j + 16) & 15) << 4 for j = 0..15."""
+    d16 = np.asarray(d16, dtype=np.float16)
+    m16 = np.asarray(m16, dtype=np.float16)
+    q = np.asarray(codes, dtype=np.uint32)
+    out = np.empty(d16.shape + (Q5_1_BLOCK_BYTES,), dtype=np.uint8)
+    out[..., 0:2] = d16[..., None].view(np.uint8).reshape(d16.shape + (2,))
+    out[..., 2:4] = m16[..., None].view(np.uint8).reshape(m16.shape + (2,))
+    qh = np.sum(((q >> 4) & 1) << np.arange(QK, dtype=np.uint32), axis=-1).astype(np.uint32)
+    out[..., 4:8] = qh[..., None].view(np.uint8).reshape(qh.shape + (4,))
+    out[..., 8:] = ((q[..., :16] & 15) | ((q[..., 16:] & 15) << 4)).astype(np.uint8)
+    return out
+
+
+def unpack_q5_1(blocks):
+    b = np.asarray(blocks, dtype=np.uint8)
+    d16 = np.ascontiguousarray(b[..., 0:2]).view(np.float16)[..., 0]
+    m16 = np.ascontiguousarray(b[..., 2:4]).view(np.float16)[..., 0]
+    qh = np.ascontiguousarray(b[..., 4:8]).view(np.uint32)[..., 0]
+    lo = b[..., 8:].astype(np.uint32)
+    nib = np.concatenate([lo & 15, lo >> 4], axis=-1)
+    hi = (qh[..., None] >> np.arange(QK, dtype=np.uint32)) & 1
+    return d16, m16, (nib | (hi << 4)).astype(np.uint8)
+
+
+KV_FORMATS = ("bf16", "q8_0/q5_1")
+
+
+def store_k(x, kv_format: str) -> np.ndarray:
+    """Value of a K vector as the cache holds it (float64 of the stored form)."""
+    if kv_format == "bf16":
+        return round_bf16(x)
+    return dequantize_q8_0(*quantize_q8_0(np.asarray(x, dtype=np.float64).astype(np.float32))).astype(np.float64)
+
+
+def store_v(x, kv_format: str) -> np.ndarray:
+    """Value of a V vector as the cache holds it (float64 of the stored form)."""
+    if kv_format == "bf16":
+        return round_bf16(x)
+    return dequantize_q5_1(*quantize_q5_1(np.asarray(x, dtype=np.float64).astype(np.float32))).astype(np.float64)
+
+
 # --------------------------------------------------------------------------- drafter
 
 class Drafter:
     """float64 view of the drafter weights (one decoder layer + fc + lm_head + d2t)."""
 
-    def __init__(self, geom, bits: dict, d2t):
+    def __init__(self, geom, bits: dict, d2t, kv_format: str = "bf16"):
+        if kv_format not in KV_FORMATS:
+            raise ValueError(f"kv_format must be one of {KV_FORMATS}")
+        if kv_format != "bf16" and geom.head_dim % QK:
+            raise ValueError("quantized KV needs head_dim % 32 == 0")
         self.geom = geom
+        self.kv_format = kv_format
         self.w = {name: widen_bf16(b) for name, b in bits.items() if name != "embed"}
         self._embed_bits = bits["embed"]
         self.d2t = np.asarray(d2t, dtype=np.int64)
@@ -153,14 +277,14 @@ def layer_input(dr: Drafter, tok: int, g: np.ndarray) -> np.ndarray:
 
 
 def kv_entry(dr: Drafter, tok: int, g: np.ndarray, pos: int):
-    """K (after RoPE) and V of the pair (g, tok) at position pos, stored as bf16.
-    A one-layer drafter's KV at a position depends on nothing else."""
+    """K (after RoPE) and V of the pair (g, tok) at position pos, as stored (bf16, or the
+    q8_0 / q5_1 blocks).  A one-layer drafter's KV at a position depends on nothing else."""
     geo = dr.geom
     cat = layer_input(dr, tok, g)
     k = (dr.w["k"] @ cat).reshape(geo.n_head_kv, geo.head_dim)
     v = (dr.w["v"] @ cat).reshape(geo.n_head_kv, geo.head_dim)
     k = rope_neox(k, pos, geo.rope_dims, geo.rope_theta)
-    return round_bf16(k), round_bf16(v)
+    return store_k(k, dr.kv_format), store_v(v, dr.kv_format)
 
 
 def kv_entries(dr: Drafter, toks, gs: np.ndarray, positions):
@@ -176,7 +300,7 @@ def kv_entries(dr: Drafter, toks, gs: np.ndarray, positions):
     v = (cat @ dr.w["v"].T).reshape(len(toks), geo.n_head_kv, geo.head_dim)
     k = np.stack([rope_neox(k[i], int(p), geo.rope_dims, geo.rope_theta)
                   for i, p in enumerate(positions)]) if len(toks) else k
-    return round_bf16(k), round_bf16(v)
+    return store_k(k, dr.kv_format), store_v(v, dr.kv_format)
 
 
 @dataclass
