@@ -67,9 +67,9 @@ PROFILED_TRAFFIC = {
 }
 
 
-def profiled_traffic(config: str, kind: str):
+def profiled_traffic(config: str, kind: str, kv_format: str = "bf16"):
     import hashlib
-    e = PROFILED_TRAFFIC.get((config, kind))
+    e = PROFILED_TRAFFIC.get((config, kind) if kv_format == "bf16" else (config, kind, kv_format))
     if e is None:
         return None
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "eagle_speculative_decode_gb300", "csrc")
@@ -153,14 +153,23 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ algorithmic bytes
-def phase_bytes(geo, B, ctx_len):
+def kv_bytes_per_position(geo, kv_format):
+    """Bytes of the K and V rows of one position, all kv heads: 2 x 2 bytes per value for
+    bf16; 34 + 24 bytes per 32 values for q8_0 keys and q5_1 values."""
+    if kv_format == "bf16":
+        return 2 * geo.kv_rows * 2
+    return geo.kv_rows // 32 * (34 + 24)
+
+
+def phase_bytes(geo, B, ctx_len, kv_format="bf16"):
     """Bytes each kernel of one draft step must move (weights once per step for all B
     sequences, plus per-sequence activations and KV)."""
     n, F, qr, kr = geo.n_embd, geo.n_ff, geo.q_rows, geo.kv_rows
     act = 4 * B
+    kvp = kv_bytes_per_position(geo, kv_format)
     return {
-        "qkv": (qr + 2 * kr) * 2 * n * 2 + B * (2 * n + 4 * n) + 3 * n * 2 + B * 2 * kr * 2 + act * qr,
-        "attn": B * (ctx_len * 2 * kr * 2 + 2 * qr * 4),
+        "qkv": (qr + 2 * kr) * 2 * n * 2 + B * (2 * n + 4 * n) + 3 * n * 2 + B * kvp + act * qr,
+        "attn": B * (ctx_len * kvp + 2 * qr * 4),
         "o": n * qr * 2 + act * (qr + 2 * n),
         "gateup": 2 * F * n * 2 + act * (n + F) + n * 2,
         "down": n * F * 2 + act * (F + 2 * n),
@@ -168,8 +177,8 @@ def phase_bytes(geo, B, ctx_len):
     }
 
 
-def round_bytes(geo, B, gamma, ctx_len):
-    ph = phase_bytes(geo, B, ctx_len)
+def round_bytes(geo, B, gamma, ctx_len, kv_format="bf16"):
+    ph = phase_bytes(geo, B, ctx_len, kv_format)
     chain = gamma * sum(ph.values())
     rebuild = 3 * geo.n_embd * geo.n_embd * 2 + 2 * geo.kv_rows * 2 * geo.n_embd * 2 \
         + B * (gamma + 1) * (3 * geo.n_embd * 2 + geo.n_embd * 4)
@@ -177,7 +186,7 @@ def round_bytes(geo, B, gamma, ctx_len):
 
 
 # ------------------------------------------------------------------ oracle timing
-def oracle_round_rate(geo_name, gamma, rounds, seed=0):
+def oracle_round_rate(geo_name, gamma, rounds, seed=0, kv_format="bf16"):
     """Times the CPU oracle on one sequence: `rounds` chains of gamma draft steps from a
     32-token prefilled state at the benchmark's geometry.  Returns (draft tok/s, seconds,
     sample description)."""
@@ -185,7 +194,7 @@ def oracle_round_rate(geo_name, gamma, rounds, seed=0):
     from oracle import eagle3_oracle as O
     geo = synth.GEOMETRIES[geo_name]
     wts = synth.make_weights(geo, seed=seed)
-    dr = O.Drafter(geo, wts.bits, wts.d2t)
+    dr = O.Drafter(geo, wts.bits, wts.d2t, kv_format=kv_format)
     P = 32
     toks = synth.make_tokens((P + 1,), geo, seed + 1)
     aux = synth.make_aux((P,), geo, seed + 1)
@@ -195,7 +204,7 @@ def oracle_round_rate(geo_name, gamma, rounds, seed=0):
         O.draft_chain(dr, st, gamma)
     dt = time.perf_counter() - t0
     desc = (f"{rounds} chain(s) of {gamma} draft steps of one sequence from a {P}-token "
-            f"prefilled state, {geo_name} geometry, float64 numpy oracle")
+            f"prefilled state, {geo_name} geometry, {kv_format} KV, float64 numpy oracle")
     return rounds * gamma / dt, dt, desc
 
 
@@ -247,7 +256,7 @@ def run_reference(args, cfg):
     from oracle import eagle3_oracle as O
     geo = synth.GEOMETRIES[cfg["geom"]]
     wts = synth.make_weights(geo, seed=0)
-    dr = O.Drafter(geo, wts.bits, wts.d2t)
+    dr = O.Drafter(geo, wts.bits, wts.d2t, kv_format=args.kv_format)
     P = 32
     toks = synth.make_tokens((P + 1,), geo, 1)
     aux = synth.make_aux((P,), geo, 1)
@@ -267,7 +276,7 @@ def run_reference(args, cfg):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg["workload"]},
+            "config": {"workload": cfg["workload"], "kv_format": args.kv_format},
             "cpu_baseline": {"value": value, "unit": "draft tokens/s", "cores": os.cpu_count(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "draft tokens/s", "h2d_bytes_per_step": 0,
@@ -302,7 +311,7 @@ def run_mine(args, cfg):
     max_cache = int(lens.max()) + (gamma + 1) * rounds + 64
     max_cache = (max_cache + ps - 1) // ps * ps
     model = DraftModel(wts, max_batch=B, max_gamma=gamma, max_cache_len=max_cache, page_size=ps,
-                       device=dev)
+                       device=dev, kv_format=args.kv_format)
     del wts
     if args.tc_min_items:
         model.set_tc_min_items(args.tc_min_items)
@@ -418,14 +427,14 @@ def run_mine(args, cfg):
     names = {1: "qkv", 2: "attn", 3: "o", 4: "gateup", 5: "down", 6: "lmhead"}
     # per launch, per kind: average microseconds (one launch per kind per step when B fits)
     kern_us = {names[k]: float(np.mean(v)) for k, v in per_label.items() if k in names}
-    pb = phase_bytes(geo, B, int(mean_ctx))
+    pb = phase_bytes(geo, B, int(mean_ctx), args.kv_format)
     hbm_peak, tf_peak, peak_src = load_peaks()
     launches_per_kind = {k: max(1, len(per_label.get(kk, [])) // max(1, args.phase_rounds * gamma))
                          for kk, k in names.items()}
     dominant = max(kern_us, key=lambda k: kern_us[k] * launches_per_kind[k]) if kern_us else "lmhead"
     dom_bytes = pb[dominant] / launches_per_kind[dominant]
     achieved = dom_bytes / (kern_us[dominant] * 1e-6) / 1e9 if kern_us else None
-    rb = round_bytes(geo, B, gamma, int(mean_ctx))
+    rb = round_bytes(geo, B, gamma, int(mean_ctx), args.kv_format)
     step_frac = (rb / (ms_per_step * 1e-3) / 1e9) / hbm_peak
 
     # ---- end to end through the C ABI with host buffers
@@ -456,7 +465,8 @@ def run_mine(args, cfg):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
-            rate, secs, desc = oracle_round_rate(cfg["geom"], gamma, args.cpu_rounds)
+            rate, secs, desc = oracle_round_rate(cfg["geom"], gamma, args.cpu_rounds,
+                                                 kv_format=args.kv_format)
             cpu = {"value": rate, "unit": "draft tokens/s", "cores": os.cpu_count(),
                    "kind": "oracle", "sample": desc, "seconds": secs}
         except Exception as e:  # reported, not fatal
@@ -473,7 +483,10 @@ def run_mine(args, cfg):
         "config": {"workload": cfg["workload"], "name": args.config, "batch": B, "gamma": gamma,
                    "prompt": [int(lens.min()), int(lens.max())],
                    "mean_context": round(mean_ctx, 1), "page_size": ps,
-                   "storage": "bf16 weights and KV, float32 activations and accumulation",
+                   "kv_format": args.kv_format,
+                   "storage": ("bf16 weights and KV" if args.kv_format == "bf16" else
+                               "bf16 weights, q8_0 K / q5_1 V cache") +
+                              ", float32 activations and accumulation",
                    "l2": "inputs larger than L2: 0.8 GB of weights streamed per draft step",
                    "step": "chain of gamma draft steps + rewind + accept + rebuild (encode of "
                            "gamma+1 verify features, k/v teacher forcing)",
@@ -486,7 +499,7 @@ def run_mine(args, cfg):
         "roofline": {"bound": "hbm", "kernel": kernel_label(dominant, B),
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": (achieved / hbm_peak) if achieved else None,
-                     "traffic": profiled_traffic(args.config, dominant),
+                     "traffic": profiled_traffic(args.config, dominant, args.kv_format),
                      "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
                      "bytes_per_launch": dom_bytes, "us_per_launch": kern_us.get(dominant)},
         "kernel_us": kern_us,
@@ -516,6 +529,8 @@ def main():
     ap.add_argument("--phase-rounds", type=int, default=3)
     ap.add_argument("--cpu-rounds", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-format", default="bf16", choices=["bf16", "q8_0/q5_1"],
+                    help="drafter KV cache storage: bf16, or q8_0 keys / q5_1 values")
     ap.add_argument("--tc-min-items", type=int, default=0,
                     help="activation rows from which projections use the tensor cores (0: library default)")
     args = ap.parse_args()

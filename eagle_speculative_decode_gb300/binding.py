@@ -30,7 +30,8 @@ EAGLE3_DEV_BAD_LENGTH = 8
 EAGLE3_DEV_TIMEOUT = 16
 
 EXPORTED = (
-    "eagle3_version", "eagle3_error_string", "eagle3_workspace_bytes", "eagle3_plan_gamma",
+    "eagle3_version", "eagle3_error_string", "eagle3_workspace_bytes", "eagle3_kv_row_bytes",
+    "eagle3_plan_gamma",
     "eagle3_init", "eagle3_destroy", "eagle3_encode", "eagle3_prefill", "eagle3_draft_chain",
     "eagle3_rewind", "eagle3_accept", "eagle3_rebuild_after_verify", "eagle3_get_status",
     "eagle3_set_graph_mode", "eagle3_set_tc_min_items", "eagle3_launch_count", "eagle3_profile_begin",
@@ -51,7 +52,11 @@ class Config(ctypes.Structure):
                 ("n_ff", ctypes.c_int), ("draft_vocab", ctypes.c_int),
                 ("target_vocab", ctypes.c_int), ("max_batch", ctypes.c_int),
                 ("max_gamma", ctypes.c_int), ("max_cache_len", ctypes.c_int),
-                ("page_size", ctypes.c_int)]
+                ("page_size", ctypes.c_int), ("kv_format", ctypes.c_int)]
+
+
+EAGLE3_KV_BF16 = 0
+EAGLE3_KV_Q8_0_Q5_1 = 1
 
 
 WEIGHT_FIELDS = ("fc", "in_norm", "hidden_norm", "q", "k", "v", "o", "post_norm", "gate", "up",
@@ -90,6 +95,7 @@ def load() -> ctypes.CDLL:
         "eagle3_version": (ci, []),
         "eagle3_error_string": (ctypes.c_char_p, [ci]),
         "eagle3_workspace_bytes": (ctypes.c_size_t, [P(Config)]),
+        "eagle3_kv_row_bytes": (ci, [P(Config), P(ctypes.c_size_t), P(ctypes.c_size_t)]),
         "eagle3_plan_gamma": (ci, [ci, ci, ci, cu, P(ci)]),
         "eagle3_init": (ci, [P(Config), P(Weights), vp, ctypes.c_size_t, vp, P(vp)]),
         "eagle3_destroy": (ci, [vp]),
@@ -139,6 +145,14 @@ def eagle3_version() -> int:
 
 def eagle3_workspace_bytes(cfg: Config) -> int:
     return int(load().eagle3_workspace_bytes(ctypes.byref(cfg)))
+
+
+def eagle3_kv_row_bytes(cfg: Config):
+    """(K row bytes, V row bytes) of the paged pools for cfg's kv_format."""
+    k, v = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(load().eagle3_kv_row_bytes(ctypes.byref(cfg), ctypes.byref(k), ctypes.byref(v)),
+           "eagle3_kv_row_bytes")
+    return int(k.value), int(v.value)
 
 
 def eagle3_plan_gamma(kv_len: int, gamma: int, max_cache_len: int, flags: int = 0) -> int:

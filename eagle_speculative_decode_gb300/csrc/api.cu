@@ -23,7 +23,7 @@ constexpr int kMaxGraphs = 16;
 
 struct Layout {
   size_t rope, q, attn_o, part_o, part_ml, attn_cnt, x1, act, gwork, tokwork, am_slot, am_cnt,
-      round_start, geff, status, genc, xp0, xp1, xp2, sumsq, tc_part, tc_cnt, attn_plan, total;
+      round_start, geff, status, genc, xp0, xp1, xp2, sumsq, tc_part, tc_cnt, attn_plan, kv_stage, total;
   size_t tc_items, tc_k, tc_part_elems;
 };
 
@@ -53,7 +53,20 @@ bool cfg_valid(const eagle3_config *c) {
                                        std::max(c->n_ff, c->n_head * c->head_dim));
   if (kmax * 4 > kGemvMaxXBytes) return false;
   if ((size_t)c->max_batch * c->n_head_kv > (size_t)kSplitSlots) return false;
+  if (c->kv_format != EAGLE3_KV_BF16 && c->kv_format != EAGLE3_KV_Q8_0_Q5_1) return false;
+  if (c->kv_format == EAGLE3_KV_Q8_0_Q5_1 && c->head_dim % 32) return false;
+  if (attn_unit_keys(c->head_dim, c->n_head / c->n_head_kv, c->page_size, c->kv_format) < 1) return false;
   return true;
+}
+
+// Bytes of one K / V row of the paged pools (one position of one kv head).
+void kv_rows(const eagle3_config &c, size_t *k_row, size_t *v_row) {
+  if (c.kv_format == EAGLE3_KV_Q8_0_Q5_1) {
+    *k_row = (size_t)c.head_dim / 32 * 34;
+    *v_row = (size_t)c.head_dim / 32 * 24;
+  } else {
+    *k_row = *v_row = (size_t)c.head_dim * 2;
+  }
 }
 
 Layout make_layout(const eagle3_config &c) {
@@ -93,6 +106,8 @@ Layout make_layout(const eagle3_config &c) {
   L.tc_part = take(L.tc_part_elems * 4);
   L.tc_cnt = take(kTcCounters * 4);
   L.attn_plan = take((size_t)c.max_gamma * (B + 1) * 4);  // attention unit prefix per step
+  // quantized KV: the projection's float32 k / v before kv_quant writes the blocks
+  L.kv_stage = take(c.kv_format == EAGLE3_KV_Q8_0_Q5_1 ? L.tc_items * 2 * c.n_head_kv * c.head_dim * 4 : 0);
   L.total = align_up(off, 256);
   return L;
 }
@@ -155,6 +170,9 @@ struct eagle3_ctx {
   // attention work units (keys per unit) and the round's unit prefix tables
   int unit_keys;
   int32_t *attn_plan;
+  // KV storage format: bf16, or q8_0 K / q5_1 V written by kv_quant from kv_stage
+  int kv_q, k_row, v_row;
+  float *kv_stage;
   uint16_t *xp0, *xp1, *xp2;  // the three bf16 parts of x
   float *sumsq, *tc_part;
   unsigned *tc_cnt;
@@ -194,8 +212,8 @@ GemvParams base_params(const eagle3_ctx *ctx) {
 }
 
 void set_kv(GemvParams &p, const eagle3_kv *kv) {
-  p.k_pool = kv->k_pool;
-  p.v_pool = kv->v_pool;
+  p.k_pool = static_cast<uint16_t *>(kv->k_pool);
+  p.v_pool = static_cast<uint16_t *>(kv->v_pool);
   p.page_table = kv->page_table;
   p.num_pages = kv->num_pages;
   p.max_pages = kv->max_pages_per_seq;
@@ -296,6 +314,17 @@ bool use_tc(const eagle3_ctx *ctx, const GemvParams &p, int items) {
   return true;
 }
 
+// A q/k/v (or k/v-only) projection over `items` pairs; with quantized KV the epilogue
+// stages float32 k / v and kv_quant writes the q8_0 / q5_1 blocks.
+cudaError_t gemv_items(eagle3_ctx *ctx, GemvParams p, int items, cudaStream_t st, bool pdl);
+cudaError_t qkv_items(eagle3_ctx *ctx, GemvParams p, int items, cudaStream_t st, bool pdl) {
+  p.kv_stage = ctx->kv_stage;
+  cudaError_t e = gemv_items(ctx, p, items, st, pdl);
+  if (e == cudaSuccess && ctx->kv_q)
+    e = launched(ctx, st, kv_quant_launch(p, items, ctx->k_row, ctx->v_row, st, true), PH_SMALL);
+  return e;
+}
+
 // Launch a GEMV over `items` activation rows in as many launches as shared memory needs.
 cudaError_t gemv_items(eagle3_ctx *ctx, GemvParams p, int items, cudaStream_t st, bool pdl) {
   if (use_tc(ctx, p, items)) return tc_items(ctx, p, items, st, pdl);
@@ -380,15 +409,16 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     p.pairs.kv_len = a.kv->kv_len;
     p.pairs.gamma_eff = ctx->geff;
     p.out_f = ctx->q;
-    if ((e = gemv_items(ctx, p, a.B, st, pdl)) != cudaSuccess) return e;
+    if ((e = qkv_items(ctx, p, a.B, st, pdl)) != cudaSuccess) return e;
 
     // attention
     AttnParams ap;
     std::memset(&ap, 0, sizeof(ap));
     ap.q = ctx->q;
     ap.out = ctx->attn_o;
-    ap.k_pool = a.kv->k_pool;
-    ap.v_pool = a.kv->v_pool;
+    ap.k_pool = static_cast<const unsigned char *>(a.kv->k_pool);
+    ap.v_pool = static_cast<const unsigned char *>(a.kv->v_pool);
+    ap.kv_q = ctx->kv_q;
     ap.page_table = a.kv->page_table;
     ap.kv_len = a.kv->kv_len;
     ap.gamma_eff = ctx->geff;
@@ -563,6 +593,12 @@ const char *eagle3_error_string(int code) {
   }
 }
 
+int eagle3_kv_row_bytes(const eagle3_config *cfg, size_t *k_row, size_t *v_row) {
+  if (!cfg_valid(cfg) || !k_row || !v_row) return EAGLE3_ERR_INVALID_ARG;
+  kv_rows(*cfg, k_row, v_row);
+  return EAGLE3_OK;
+}
+
 size_t eagle3_workspace_bytes(const eagle3_config *cfg) {
   if (!cfg_valid(cfg)) return 0;
   return make_layout(*cfg).total;
@@ -637,7 +673,15 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
   ctx->status = reinterpret_cast<int *>(b + L.status);
   ctx->genc = reinterpret_cast<float *>(b + L.genc);
   ctx->attn_plan = reinterpret_cast<int32_t *>(b + L.attn_plan);
-  ctx->unit_keys = attn_unit_keys(cfg->head_dim, cfg->n_head / cfg->n_head_kv, cfg->page_size);
+  ctx->unit_keys = attn_unit_keys(cfg->head_dim, cfg->n_head / cfg->n_head_kv, cfg->page_size, cfg->kv_format);
+  ctx->kv_q = cfg->kv_format == EAGLE3_KV_Q8_0_Q5_1 ? 1 : 0;
+  {
+    size_t kr = 0, vr = 0;
+    kv_rows(*cfg, &kr, &vr);
+    ctx->k_row = (int)kr;
+    ctx->v_row = (int)vr;
+  }
+  ctx->kv_stage = ctx->kv_q ? reinterpret_cast<float *>(b + L.kv_stage) : nullptr;
   ctx->xp0 = reinterpret_cast<uint16_t *>(b + L.xp0);
   ctx->xp1 = reinterpret_cast<uint16_t *>(b + L.xp1);
   ctx->xp2 = reinterpret_cast<uint16_t *>(b + L.xp2);
@@ -764,7 +808,7 @@ int eagle3_prefill(eagle3_ctx *ctx, int B, const int32_t *tokens, int P_max,
         p.pairs.tok_stride = P_max;
         p.pairs.tokens = tokens;
         p.pairs.enc_g = ctx->genc;
-        e = gemv_items(ctx, p, pairs, st, true);
+        e = qkv_items(ctx, p, pairs, st, true);
         if (e != cudaSuccess) break;
       }
       if (p0 + cnt == P)
@@ -870,7 +914,7 @@ int eagle3_rebuild_after_verify(eagle3_ctx *ctx, int B, int gamma, const int32_t
     p.pairs.enc_g = ctx->genc;
     p.pairs.kv_len = kv->kv_len;
     p.pairs.n_acc = n_acc;
-    e = gemv_items(ctx, p, M, st, true);
+    e = qkv_items(ctx, p, M, st, true);
   }
   if (e == cudaSuccess)
     e = launched(ctx, st,

@@ -23,6 +23,7 @@
 // CTA merges its lane groups in shared memory; a pair whose units all fall to this CTA is
 // written out at once, otherwise its (max, sum, weighted V) is published and the last
 // contributing CTA merges the contributions in CTA order.
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -44,8 +45,11 @@ struct ILog2<1> {
   static constexpr int value = 0;
 };
 
-template <int D, int G>
+template <int D, int G, bool KVQ>
 struct AttnShape {
+  // bytes of one key's K and V row: bf16, or q8_0 / q5_1 blocks of 32 values
+  static constexpr int KR = KVQ ? D / 32 * 34 : D * 2;
+  static constexpr int VR = KVQ ? D / 32 * 24 : D * 2;
   static constexpr int LPK = D / 8;             // lanes per key (a segment of the warp)
   static constexpr int KPW = 32 / LPK;          // keys per warp pass
   static constexpr int NP = kAttnWarps * KPW;   // lane groups per CTA
@@ -55,7 +59,7 @@ struct AttnShape {
   static constexpr int SH = ILog2<LPK>::value - ILog2<N>::value;  // lane bits below a score index
   static constexpr int LOG_G = ILog2<G>::value;
   static constexpr int CH = NP * UNR;                     // keys per unit at most (one pass of all warps)
-  static constexpr size_t kStage = (size_t)2 * CH * D * 2;  // K and V rows of a unit, bf16
+  static constexpr size_t kStage = (size_t)CH * (KR + VR);  // K and V rows of a unit
   static constexpr size_t kAcc = (size_t)NP * G * D * 4;    // lane-group partial V sums
   static constexpr size_t kRing = kAttnStages * kStage;
   static constexpr size_t kBar = kRing + kAcc;              // mbarriers and flags
@@ -131,9 +135,10 @@ __device__ __forceinline__ AttnSeg attn_seg(const AttnSched &S, long long u, lon
   return s;
 }
 
-template <int D, int G>
+template <int D, int G, bool KVQ>
 __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const AttnParams p) {
-  using S = AttnShape<D, G>;
+  using S = AttnShape<D, G, KVQ>;
+  constexpr int KR = S::KR, VR = S::VR;
   constexpr int LPK = S::LPK, KPW = S::KPW, NP = S::NP, UNR = S::UNR, N = S::N, SH = S::SH;
   constexpr int LOG_G = S::LOG_G, CH = S::CH;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -219,17 +224,20 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
             break;
           }
           const int pg = pt[k0 / ps];
-          const uint32_t bytes = (uint32_t)(k1 - k0) * D * 2u;
-          mbar_expect_tx(full0 + 8 * slot, 2u * bytes);
+          // bf16 rows: the unit's valid keys; quantized rows: the whole unit (sizes stay
+          // multiples of 16 bytes; the slots past the valid keys are in the same page)
+          const int nk = KVQ ? U : k1 - k0;
+          const uint32_t kbytes = (uint32_t)nk * KR, vbytes = (uint32_t)nk * VR;
+          mbar_expect_tx(full0 + 8 * slot, kbytes + vbytes);
           if (pg < 0 || pg >= p.num_pages) {
             // keep the ring in step: complete the stage without data (consumers skip it)
             set_status(p.status, EAGLE3_DEV_BAD_PAGE);
-            asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * slot), "r"(2u * bytes) : "memory");
+            asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * slot), "r"(kbytes + vbytes) : "memory");
           } else {
-            const size_t off = (((size_t)pg * Hkv + sg.kvh) * ps + k0 % ps) * D;
+            const size_t row = ((size_t)pg * Hkv + sg.kvh) * ps + k0 % ps;
             const uint32_t dst = smem_addr(smem + (size_t)slot * S::kStage);
-            bulk_g2s(dst, p.k_pool + off, bytes, full0 + 8 * slot, pol);
-            bulk_g2s(dst + (uint32_t)(CH * D * 2), p.v_pool + off, bytes, full0 + 8 * slot, pol);
+            bulk_g2s(dst, p.k_pool + row * KR, kbytes, full0 + 8 * slot, pol);
+            bulk_g2s(dst + (uint32_t)(CH * KR), p.v_pool + row * VR, vbytes, full0 + 8 * slot, pol);
           }
           ++g;
         }
@@ -267,10 +275,13 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
     }
     float m_me = -INFINITY, l_me = 0.f;  // running max (log2 domain) and sum of head g_me
     float acc[G][8];                     // running weighted V of this lane's 8 dims, every head
+    float accm[G];                       // quantized V: running sum of p * m (block minimum)
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg)
+    for (int gg = 0; gg < G; ++gg) {
+      accm[gg] = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[gg][i] = 0.f;
+    }
 
     for (int r = sg.r0; r < sg.r1; ++r) {
       const int k0 = r * U;
@@ -284,7 +295,7 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
       const int pg = pt[k0 / ps];
       const bool have = ok && pg >= 0 && pg < p.num_pages;
       const unsigned char *kst = smem + (size_t)slot * S::kStage;
-      const unsigned char *vst = kst + (size_t)CH * D * 2;
+      const unsigned char *vst = kst + (size_t)CH * KR;
       // keys of this lane group: kk = warp * KPW * UNR + uu * KPW + grp
       unsigned vmask = 0u;
       float part_s[N];
@@ -293,16 +304,32 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
         const int kk = warp * KPW * UNR + uu * KPW + grp;
         const bool v = have && kk < n;
         vmask |= v ? (1u << uu) : 0u;
-        uint4 ku = make_uint4(0u, 0u, 0u, 0u);
-        if (v) ku = *reinterpret_cast<const uint4 *>(kst + ((size_t)kk * D + li * 8) * 2);
-        const float kf[8] = {bf_lo(ku.x), bf_hi(ku.x), bf_lo(ku.y), bf_hi(ku.y),
-                             bf_lo(ku.z), bf_hi(ku.z), bf_lo(ku.w), bf_hi(ku.w)};
+        float kf[8];
+        float kscale = 1.f;
+        if constexpr (KVQ) {
+          // q8_0: this lane's 8 codes of block li / 4 (2-byte aligned: four 16-bit loads);
+          // the block scale multiplies the partial dot once
+          const unsigned char *blk = kst + (size_t)kk * KR + (li >> 2) * 34;
+          const uint16_t *c16 = reinterpret_cast<const uint16_t *>(blk + 2 + 8 * (li & 3));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const unsigned u = v ? c16[i] : 0u;
+            kf[2 * i] = (float)(signed char)(u & 0xffu);
+            kf[2 * i + 1] = (float)(signed char)(u >> 8);
+          }
+          kscale = v ? __half2float(*reinterpret_cast<const __half *>(blk)) : 0.f;
+        } else {
+          uint4 ku = make_uint4(0u, 0u, 0u, 0u);
+          if (v) ku = *reinterpret_cast<const uint4 *>(kst + (size_t)kk * KR + li * 16);
+          kf[0] = bf_lo(ku.x); kf[1] = bf_hi(ku.x); kf[2] = bf_lo(ku.y); kf[3] = bf_hi(ku.y);
+          kf[4] = bf_lo(ku.z); kf[5] = bf_hi(ku.z); kf[6] = bf_lo(ku.w); kf[7] = bf_hi(ku.w);
+        }
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
           float d = 0.f;
 #pragma unroll
           for (int i = 0; i < 8; ++i) d = fmaf(qv[gg][i], kf[i], d);
-          part_s[uu * G + gg] = d;
+          part_s[uu * G + gg] = KVQ ? d * kscale : d;
         }
       }
       const bool vld = (vmask >> u_me) & 1u;
@@ -325,19 +352,49 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
         const float c = __shfl_sync(0xffffffffu, corr, gg << SH, LPK);
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[gg][i] *= c;
+        if constexpr (KVQ) accm[gg] *= c;
       }
 #pragma unroll
       for (int uu = 0; uu < UNR; ++uu) {
         const int kk = warp * KPW * UNR + uu * KPW + grp;
-        uint4 vu = make_uint4(0u, 0u, 0u, 0u);
-        if ((vmask >> uu) & 1u) vu = *reinterpret_cast<const uint4 *>(vst + ((size_t)kk * D + li * 8) * 2);
-        const float vf[8] = {bf_lo(vu.x), bf_hi(vu.x), bf_lo(vu.y), bf_hi(vu.y),
-                             bf_lo(vu.z), bf_hi(vu.z), bf_lo(vu.w), bf_hi(vu.w)};
+        const bool vv = (vmask >> uu) & 1u;
+        float vf[8];
+        float vd = 1.f, vm = 0.f;
+        if constexpr (KVQ) {
+          // q5_1: this lane's 8 codes of block li / 4 -- 4 bits from one 8-byte load (low
+          // nibbles for values 0-15 of the block, high for 16-31) and the fifth bit from qh;
+          // v = d * code + m, with p * m summed apart (all 8 values share the block)
+          const unsigned char *blk = vst + (size_t)kk * VR + (li >> 2) * 24;
+          const int e = 8 * (li & 3);
+          uint2 qs = make_uint2(0u, 0u);
+          unsigned qh = 0u;
+          if (vv) {
+            qs = *reinterpret_cast<const uint2 *>(blk + 8 + (e & 15));
+            qh = *reinterpret_cast<const unsigned *>(blk + 4);
+            vd = __half2float(*reinterpret_cast<const __half *>(blk));
+            vm = __half2float(*reinterpret_cast<const __half *>(blk + 2));
+          } else {
+            vd = 0.f;
+          }
+          const int sh = e >= 16 ? 4 : 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const unsigned byte = ((i < 4 ? qs.x : qs.y) >> (8 * (i & 3))) & 0xffu;
+            vf[i] = (float)(((byte >> sh) & 15u) | (((qh >> (e + i)) & 1u) << 4));
+          }
+        } else {
+          uint4 vu = make_uint4(0u, 0u, 0u, 0u);
+          if (vv) vu = *reinterpret_cast<const uint4 *>(vst + (size_t)kk * VR + li * 16);
+          vf[0] = bf_lo(vu.x); vf[1] = bf_hi(vu.x); vf[2] = bf_lo(vu.y); vf[3] = bf_hi(vu.y);
+          vf[4] = bf_lo(vu.z); vf[5] = bf_hi(vu.z); vf[6] = bf_lo(vu.w); vf[7] = bf_hi(vu.w);
+        }
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
           const float pg2 = __shfl_sync(0xffffffffu, pr, (uu * G + gg) << SH, LPK);
+          const float pw = KVQ ? pg2 * vd : pg2;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[gg][i] = fmaf(pg2, vf[i], acc[gg][i]);
+          for (int i = 0; i < 8; ++i) acc[gg][i] = fmaf(pw, vf[i], acc[gg][i]);
+          if constexpr (KVQ) accm[gg] = fmaf(pg2, vm, accm[gg]);
         }
       }
       __syncwarp();
@@ -350,7 +407,7 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
 #pragma unroll
     for (int gg = 0; gg < G; ++gg)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sm_acc[((size_t)part * G + gg) * D + li * 8 + i] = acc[gg][i];
+      for (int i = 0; i < 8; ++i) sm_acc[((size_t)part * G + gg) * D + li * 8 + i] = acc[gg][i] + (KVQ ? accm[gg] : 0.f);
     asm volatile("bar.sync 1, 256;" ::: "memory");
     const bool whole = sg.r0 == 0 && sg.r1 == sg.nu;
     float *out = p.out + (size_t)b * H * D + (size_t)kvh * G * D;
@@ -454,35 +511,43 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
 }
 
 // Keys per unit: the run of one pass of all warps, cut to the largest power of two that
-// divides the page size (a unit never crosses a page).
-template <int D, int G>
+// divides the page size (a unit never crosses a page).  Quantized rows are copied a whole
+// unit at a time, so a unit's K and V bytes must be multiples of 16; 0 when they are not.
+template <int D, int G, bool KVQ>
 static int attn_unit_keys_dg(int page_size) {
-  int u = AttnShape<D, G>::CH;
+  using S = AttnShape<D, G, KVQ>;
+  int u = S::CH;
   while (u > 1 && page_size % u) u >>= 1;
+  if (KVQ && (((size_t)u * S::KR) % 16 || ((size_t)u * S::VR) % 16)) return 0;
   return u;
 }
 
-template <int D, int G>
+template <int D, int G, bool KVQ>
 static cudaError_t attn_launch_dg(const AttnParams &p, int num_sms, cudaStream_t st, bool pdl) {
-  if (p.unit_keys != attn_unit_keys_dg<D, G>(p.page_size)) return cudaErrorInvalidValue;
+  using S = AttnShape<D, G, KVQ>;
+  if (p.unit_keys < 1 || p.unit_keys != attn_unit_keys_dg<D, G, KVQ>(p.page_size)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   // one CTA per SM; no more contributors per pair than the merge scratch holds
-  cfg.gridDim = dim3(num_sms < AttnShape<D, G>::kMaxContrib ? num_sms : AttnShape<D, G>::kMaxContrib);
+  cfg.gridDim = dim3(num_sms < S::kMaxContrib ? num_sms : S::kMaxContrib);
   cfg.blockDim = dim3(kAttnCtaThreads);
-  cfg.dynamicSmemBytes = AttnShape<D, G>::kSmem;
+  cfg.dynamicSmemBytes = S::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<D, G>, p);
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<D, G, KVQ>, p);
 }
 
 template <int D, int G>
 static cudaError_t attn_prepare_dg() {
-  return cudaFuncSetAttribute(attn_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)AttnShape<D, G>::kSmem);
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)AttnShape<D, G, false>::kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_decode_kernel<D, G, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)AttnShape<D, G, true>::kSmem);
+  return e;
 }
 
 bool attn_supported(int head_dim, int group) {
@@ -502,9 +567,10 @@ cudaError_t attn_prepare() {
   return e;
 }
 
-int attn_unit_keys(int head_dim, int group, int page_size) {
-#define E3_UNIT(DD, GG) \
-  if (head_dim == DD && group == GG) return attn_unit_keys_dg<DD, GG>(page_size);
+int attn_unit_keys(int head_dim, int group, int page_size, int kv_q) {
+#define E3_UNIT(DD, GG)                                                                 \
+  if (head_dim == DD && group == GG)                                                   \
+    return kv_q ? attn_unit_keys_dg<DD, GG, true>(page_size) : attn_unit_keys_dg<DD, GG, false>(page_size);
   E3_ATTN_ALL(E3_UNIT)
 #undef E3_UNIT
   return 0;
@@ -513,8 +579,9 @@ int attn_unit_keys(int head_dim, int group, int page_size) {
 cudaError_t attn_launch(const AttnParams &p, int num_sms, cudaStream_t st, bool pdl) {
   const int G = p.n_head / p.n_head_kv;
   if (p.batch < 1 || p.unit_keys < 1 || !p.unit_pre) return cudaErrorInvalidValue;
-#define E3_ATTN_CASE(DD, GG) \
-  if (p.head_dim == DD && G == GG) return attn_launch_dg<DD, GG>(p, num_sms, st, pdl);
+#define E3_ATTN_CASE(DD, GG)                                                             \
+  if (p.head_dim == DD && G == GG)                                                      \
+    return p.kv_q ? attn_launch_dg<DD, GG, true>(p, num_sms, st, pdl) : attn_launch_dg<DD, GG, false>(p, num_sms, st, pdl);
   E3_ATTN_ALL(E3_ATTN_CASE)
 #undef E3_ATTN_CASE
   return cudaErrorInvalidValue;

@@ -223,7 +223,9 @@ struct GemvParams {
   int dbg_stride_b;    // elements between batch rows of dbg (gamma * n or gamma * V_d)
   int dbg_off;         // element offset of this step in a batch row (j * n or j * V_d)
   // KV
-  uint16_t *k_pool, *v_pool;
+  uint16_t *k_pool, *v_pool;  // bf16 rows, or the quantized pools' bytes (kv_quant)
+  float *kv_stage;            // non-null: quantized KV -- the q/k/v epilogue leaves float32
+                              // k (after RoPE) and v here, [item][K, V][n_head_kv * head_dim]
   const int32_t *page_table;
   int num_pages, max_pages, page_size, max_cache_len;
   const float2 *rope;  // [max_cache_len][rope_dims / 2] (cos, sin)
@@ -244,7 +246,7 @@ struct GemvParams {
 struct AttnParams {
   const float *q;          // [B, H * d]
   float *out;              // [B, H * d]
-  const uint16_t *k_pool, *v_pool;
+  const unsigned char *k_pool, *v_pool;  // rows of k_row / v_row bytes (bf16 or q8_0 / q5_1)
   const int32_t *page_table;
   const int32_t *kv_len;   // [B]
   const int32_t *gamma_eff;
@@ -252,6 +254,7 @@ struct AttnParams {
   int num_pages, max_pages, page_size, max_cache_len;
   int n_head, n_head_kv, head_dim;
   int batch;               // sequences B
+  int kv_q;                // 0: bf16 rows; 1: q8_0 K / q5_1 V rows
   int unit_keys;           // keys per work unit (divides the page size)
   const int32_t *unit_pre; // [B + 1] unit prefix of this step (round plan)
   float *part_o;           // [2 * CTAs, G, d] shared pairs' weighted V sums

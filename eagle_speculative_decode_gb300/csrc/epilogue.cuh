@@ -291,6 +291,11 @@ __device__ void epilogue(const GemvParams &p, const float *accs, int row0, int n
         float *q = p.out_f + (size_t)item * qr + (size_t)head * d;
         q[dim0] = a;
         q[dim1] = b;
+      } else if (it.write_kv && p.kv_stage) {
+        // quantized KV: float32 into the staging buffer, kv_quant writes the blocks
+        float *stg = p.kv_stage + ((size_t)item * 2 + (region - 1)) * kr + (size_t)head * d;
+        stg[dim0] = a;
+        stg[dim1] = b;
       } else if (it.write_kv) {
         const int pos = it.pos;
         if (pos < 0 || pos >= p.max_cache_len) {

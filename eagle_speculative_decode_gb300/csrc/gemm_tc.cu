@@ -303,17 +303,15 @@ __device__ __forceinline__ void tc_lm_flush(const TcArgs &A, const TcTables &tb,
   }
 }
 
+// Per-item tables of item tile it: RMSNorm scales and, for q/k/v, each item's position,
+// sequence, keep flag and KV page (status bits for a bad position or page of a kept item).
+// Run by the epilogue warps while the MMAs of the CTA's first chunks are in flight.
 template <int N, int MODE>
-__device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>::H][TcShape<N, MODE>::NCH][16],
-                                 int rt, int it, const TcTables &tb) {
-  using S = TcShape<N, MODE>;
-  constexpr int H = S::H, NCH = S::NCH, SP = N + 1;
+__device__ void tc_tables(const TcArgs &A, int it, const TcTables &tb) {
+  constexpr int H = TcShape<N, MODE>::H;
   const GemvParams &p = A.p;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int quad = warp & 3, chalf = warp >> 2, r = quad * 32 + lane;
+  const int tid = threadIdx.x;
   const int item0 = it * N;
-
-  // per-item tables of this tile
   if constexpr (ModeTraits<MODE>::kNorm) {
     for (int i = tid; i < N * H; i += kTcEpiThreads) {
       const int c = i / H, h = i - c * H, item = item0 + c;
@@ -321,8 +319,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
     }
   }
   if constexpr (MODE == GM_QKV) {
-    // k / v tiles also look up each kept item's KV page here, once per item
-    const bool kv_tile = p.row_base + rt * kTcM >= p.n_head * p.head_dim;
+    // each kept item's KV page, looked up once per item
     for (int c = tid; c < N; c += kTcEpiThreads) {
       const int item = item0 + c;
       int pos = 0, seq = 0, keep = 0, page = -1;
@@ -331,7 +328,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
         pos = pi.pos;
         seq = pi.b;
         keep = pi.write_kv ? 1 : 0;
-        if (kv_tile && keep) {
+        if (keep) {
           if (pos < 0 || pos >= p.max_cache_len) {
             set_status(p.status, EAGLE3_DEV_BAD_POSITION);
           } else {
@@ -349,7 +346,17 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
       tb.page[c] = page;
     }
   }
-  tc_epi_sync();
+}
+
+template <int N, int MODE>
+__device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>::H][TcShape<N, MODE>::NCH][16],
+                                 int rt, int it, const TcTables &tb) {
+  using S = TcShape<N, MODE>;
+  constexpr int H = S::H, NCH = S::NCH, SP = N + 1;
+  const GemvParams &p = A.p;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int quad = warp & 3, chalf = warp >> 2, r = quad * 32 + lane;
+  const int item0 = it * N;
 
   // y = sum over K halves of (raw sum) * (norm scale), in place in acc[0]
 #pragma unroll
@@ -500,6 +507,9 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
           if (item >= A.M) continue;
           if (region == 0) {
             p.out_f[(size_t)item * qr + rr] = y[j][i];
+          } else if (p.kv_stage) {
+            // quantized KV: float32 into the staging buffer, kv_quant writes the blocks
+            if (tb.keep[c]) p.kv_stage[((size_t)item * 2 + (region - 1)) * kr + rr] = y[j][i];
           } else {
             const int pg = tb.page[c];
             if (pg < 0) continue;
@@ -735,8 +745,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     const int nh_tiles = pc.n_embd / kTcK;
     int ch = 0;
     if constexpr (MODE == GM_LMHEAD) {
-      if (tid < N) tb.run_best[tid] = 0ull;  // published by the first tile's consumer_sync
+      if (tid < N) tb.run_best[tid] = 0ull;
     }
+    // per-item tables of the first item tile, while the first chunks are multiplied
+    int tb_it = (int)(tc_seg(u_begin, u_end, ktiles).t % item_tiles);
+    if (u_begin < u_end) tc_tables<N, MODE>(args, tb_it, tb);
+    tc_epi_sync();
     float acc[H][NCH][16];
     for (int u = u_begin; u < u_end;) {
       const TcSeg sg = tc_seg(u, u_end, ktiles);
@@ -803,33 +817,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           for (int j = 0; j < NCH; ++j)
 #pragma unroll
             for (int i = 0; i < 16; ++i) acc[h][j][i] = 0.f;
-        // two contributors per pass: both tiles' loads in flight together, added in order
-        for (int c2 = c_first; c2 <= c_last; c2 += 2) {
-          // a contributor's segment is its first one (slot 0) unless it began earlier
-          const bool two = c2 + 1 <= c_last;
-          const float *src0 = args.part + ((size_t)c2 * 2 + (sched.start(c2) >= t0 ? 0 : 1)) * H * N * kTcM + r;
-          const float *src1 = two ? args.part + ((size_t)(c2 + 1) * 2 + (sched.start(c2 + 1) >= t0 ? 0 : 1)) * H * N * kTcM + r
-                                  : src0;
+        // kU contributors per pass, all their loads in flight together, added in CTA order
+        constexpr int kVals = H * NCH * 16;
+        constexpr int kU = kVals >= 64 ? 2 : (kVals >= 32 ? 4 : 8);
+        for (int c2 = c_first; c2 <= c_last; c2 += kU) {
+          const float *src[kU];
+#pragma unroll
+          for (int q = 0; q < kU; ++q) {
+            const int cq = min(c2 + q, c_last);  // past the last: a repeat load, not added
+            // a contributor's segment is its first one (slot 0) unless it began earlier
+            src[q] = args.part + ((size_t)cq * 2 + (sched.start(cq) >= t0 ? 0 : 1)) * H * N * kTcM + r;
+          }
 #pragma unroll
           for (int h = 0; h < H; ++h)
 #pragma unroll
             for (int j = 0; j < NCH; ++j) {
               if (!tc_has<N>(j, chalf)) continue;
-              float v0[16], v1[16];
+              float v[kU][16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const size_t off = ((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM;
-                v0[i] = __ldcg(src0 + off);
-                v1[i] = two ? __ldcg(src1 + off) : 0.f;
-              }
+              for (int q = 0; q < kU; ++q)
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                acc[h][j][i] += v0[i];
-                if (two) acc[h][j][i] += v1[i];
-              }
+                for (int i = 0; i < 16; ++i)
+                  v[q][i] = __ldcg(src[q] + ((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM);
+#pragma unroll
+              for (int q = 0; q < kU; ++q)
+                if (c2 + q <= c_last) {
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) acc[h][j][i] += v[q][i];
+                }
             }
         }
         if (tid == 0) args.tile_cnt[sg.t] = 0u;
+      }
+      if (it != tb_it) {  // a tile of another item tile: its tables first
+        tc_epi_sync();
+        tc_tables<N, MODE>(args, it, tb);
+        tc_epi_sync();
+        tb_it = it;
       }
       tc_tile_epilogue<N, MODE>(args, acc, rt, it, tb);
     }

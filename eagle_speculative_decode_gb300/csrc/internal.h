@@ -42,7 +42,9 @@ cudaError_t tc_prep_launch(const GemvParams &p, int M, uint16_t *x0, uint16_t *x
 
 bool attn_supported(int head_dim, int group);
 cudaError_t attn_prepare();
-int attn_unit_keys(int head_dim, int group, int page_size);
+int attn_unit_keys(int head_dim, int group, int page_size, int kv_q);
+cudaError_t kv_quant_launch(const GemvParams &p, int items, int k_row, int v_row, cudaStream_t st,
+                            bool pdl);
 cudaError_t attn_launch(const AttnParams &p, int num_sms, cudaStream_t st, bool pdl);
 
 // Small bookkeeping kernels (small.cu).

@@ -23,8 +23,11 @@ def _stream_handle(stream) -> int:
 class DraftModel:
     """Drafter weights resident in HBM plus one library context."""
 
+    KV_FORMATS = {"bf16": B.EAGLE3_KV_BF16, "q8_0/q5_1": B.EAGLE3_KV_Q8_0_Q5_1}
+
     def __init__(self, weights: DrafterWeights, max_batch: int, max_gamma: int,
-                 max_cache_len: int, page_size: int, device="cuda", stream=None):
+                 max_cache_len: int, page_size: int, device="cuda", stream=None,
+                 kv_format: str = "bf16"):
         if not torch.cuda.is_available():
             raise RuntimeError("DraftModel needs a CUDA device")
         self.geom: Geometry = weights.geom
@@ -35,7 +38,9 @@ class DraftModel:
                             rope_theta=g.rope_theta, rms_eps=g.rms_eps, n_ff=g.n_ff,
                             draft_vocab=g.draft_vocab, target_vocab=g.target_vocab,
                             max_batch=max_batch, max_gamma=max_gamma,
-                            max_cache_len=max_cache_len, page_size=page_size)
+                            max_cache_len=max_cache_len, page_size=page_size,
+                            kv_format=self.KV_FORMATS[kv_format])
+        self.kv_format = kv_format
         self.max_batch, self.max_gamma = max_batch, max_gamma
         self.max_cache_len, self.page_size = max_cache_len, page_size
         self.w = {name: _dev_bits(b, self.device) for name, b in weights.bits.items()}
@@ -100,8 +105,9 @@ class SeqBatch:
         self.num_pages = int(num_pages if num_pages is not None else page_table.max() + 1)
         self.page_table_host = page_table
         self.page_table = torch.from_numpy(page_table).to(dev)
-        self.k_pool = torch.zeros(self.num_pages, g.n_head_kv, ps, g.head_dim, dtype=torch.int16, device=dev)
-        self.v_pool = torch.zeros_like(self.k_pool)
+        k_row, v_row = B.eagle3_kv_row_bytes(model.cfg)
+        self.k_pool = torch.zeros(self.num_pages, g.n_head_kv, ps, k_row, dtype=torch.uint8, device=dev)
+        self.v_pool = torch.zeros(self.num_pages, g.n_head_kv, ps, v_row, dtype=torch.uint8, device=dev)
         self.kv_len = torch.zeros(batch, dtype=torch.int32, device=dev)
         self.kv_len_host = np.zeros(batch, dtype=np.int32)
         self.g = torch.zeros(batch, g.n_embd, dtype=torch.float32, device=dev)
@@ -166,11 +172,14 @@ class SeqBatch:
 
     # ---------------------------------------------------------------- inspection
     def kv_entries(self, b: int, lo: int, hi: int):
-        """K and V (bf16 bits, [hi - lo, H_kv, d]) of sequence b at positions lo..hi-1."""
+        """Stored K and V rows of sequence b at positions lo..hi-1: bf16 bits
+        [hi - lo, H_kv, d] (uint16), or the q8_0 / q5_1 row bytes [hi - lo, H_kv, row]."""
         ps = self.model.page_size
         pos = np.arange(lo, hi)
         pages = torch.from_numpy(self.page_table_host[b, pos // ps].astype(np.int64)).to(self.k_pool.device)
         slots = torch.from_numpy((pos % ps).astype(np.int64)).to(self.k_pool.device)
-        k = self.k_pool[pages, :, slots, :]
-        v = self.v_pool[pages, :, slots, :]
-        return k.cpu().numpy().view(np.uint16), v.cpu().numpy().view(np.uint16)
+        k = self.k_pool[pages, :, slots, :].cpu().numpy()
+        v = self.v_pool[pages, :, slots, :].cpu().numpy()
+        if self.model.kv_format == "bf16":
+            return k.view(np.uint16), v.view(np.uint16)
+        return k, v

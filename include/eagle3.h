@@ -65,6 +65,21 @@ typedef struct CUstream_st *eagle3_stream_t;
 #define EAGLE3_DEV_BAD_LENGTH 8     /* kv_len or prompt length out of range */
 #define EAGLE3_DEV_TIMEOUT 16       /* a bounded on-chip wait gave up (the kernel returned) */
 
+/* Drafter KV storage formats (eagle3_config.kv_format).
+ *   EAGLE3_KV_BF16:       each K and V element as bf16.
+ *   EAGLE3_KV_Q8_0_Q5_1:  the quantized drafter KV of "memra_engine/eagle.rs"
+ *                         (Eagle3Scratch): K in q8_0 and V in q5_1 blocks of 32 values,
+ *                         34 and 24 bytes per block; needs head_dim % 32 == 0.  Block
+ *                         bytes (fp16 little endian):
+ *                           q8_0: fp16 d | 32 int8 codes, x = d * code;
+ *                           q5_1: fp16 d | fp16 m | uint32 whose bit i is bit 4 of code i |
+ *                                 byte j = (code j & 15) | (code j+16 & 15) << 4, x = d * code + m.
+ *                         Codes: d = fp16(max|x| / 127), code = rint(x / d) (q8_0);
+ *                         d = fp16((max - min) / 31), m = fp16(min), code = rint((x - m) / d)
+ *                         clamped to [0, 31] (q5_1); float32 arithmetic; all codes 0 when d = 0. */
+#define EAGLE3_KV_BF16 0
+#define EAGLE3_KV_Q8_0_Q5_1 1
+
 /* eagle3_draft_chain flags. */
 #define EAGLE3_SHRINK_GAMMA 1u      /* shrink gamma per sequence to max_cache_len - kv_len - 1 */
 
@@ -86,6 +101,10 @@ typedef struct {
   int max_gamma;       /* largest chain length                                       */
   int max_cache_len;   /* KV positions per sequence (0 .. max_cache_len - 1)         */
   int page_size;       /* KV positions per page                                      */
+  int kv_format;       /* EAGLE3_KV_BF16 (default) or EAGLE3_KV_Q8_0_Q5_1; quantized pools
+                        * are read a page-aligned run of keys at a time, so that run's K and
+                        * V bytes must be multiples of 16 (head_dim 64: page_size % 4 == 0;
+                        * head_dim 128: even page_size; head_dim 256: any page_size)     */
 } eagle3_config;
 
 /* Drafter weights: bf16, PyTorch Linear layout [out, in] row-major, device memory,
@@ -100,13 +119,15 @@ typedef struct {
 } eagle3_weights;
 
 /* Paged drafter KV cache, device memory owned by the caller.
- *   k_pool, v_pool: bf16 [num_pages, n_head_kv, page_size, head_dim] each.
+ *   k_pool, v_pool: [num_pages, n_head_kv, page_size] rows of eagle3_kv_row_bytes bytes:
+ *                   bf16 [head_dim] per row, or head_dim / 32 q8_0 (K) / q5_1 (V) blocks;
+ *                   16-byte aligned.
  *   page_table:     int32 [B, max_pages_per_seq]; position p of sequence b lives in page
  *                   page_table[b, p / page_size] at slot p % page_size.  The caller
  *                   reserves max_cache_len positions per sequence up front.
  *   kv_len:         int32 [B], committed length of each sequence (device copy). */
 typedef struct {
-  uint16_t *k_pool, *v_pool;
+  void *k_pool, *v_pool;
   const int32_t *page_table;
   int num_pages;
   int max_pages_per_seq;
@@ -130,6 +151,12 @@ const char *eagle3_error_string(int code);
 /* Device workspace a context needs for cfg, in bytes; 0 if cfg is invalid or
  * unsupported.  Host-only arithmetic. */
 size_t eagle3_workspace_bytes(const eagle3_config *cfg);
+
+/* Bytes of one K row and one V row of the paged pools (one position of one kv head) for
+ * cfg's kv_format: 2 * head_dim each for bf16; head_dim / 32 * 34 (K) and
+ * head_dim / 32 * 24 (V) for q8_0 / q5_1.  Returns EAGLE3_ERR_INVALID_ARG for an invalid
+ * cfg or null outputs.  Host-only arithmetic. */
+int eagle3_kv_row_bytes(const eagle3_config *cfg, size_t *k_row, size_t *v_row);
 
 /* Capacity rule ("feat(eagle3) ...", review comment on rebuild_after_verify committing
  * k + 1 entries): a chain of gamma drafts at committed length kv_len needs

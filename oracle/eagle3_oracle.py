@@ -276,20 +276,27 @@ def layer_input(dr: Drafter, tok: int, g: np.ndarray) -> np.ndarray:
     return np.concatenate([e_n, g_n])
 
 
-def kv_entry(dr: Drafter, tok: int, g: np.ndarray, pos: int):
-    """K (after RoPE) and V of the pair (g, tok) at position pos, as stored (bf16, or the
-    q8_0 / q5_1 blocks).  A one-layer drafter's KV at a position depends on nothing else."""
+def kv_projection(dr: Drafter, tok: int, g: np.ndarray, pos: int):
+    """K (after RoPE) and V of the pair (g, tok) at position pos before storage, float64
+    [H_kv, d] each ("memra_engine/eagle.rs", Op-sequence: k/v projections of the
+    concatenated normed inputs, RoPE on k).  A one-layer drafter's KV at a position depends
+    on nothing else."""
     geo = dr.geom
     cat = layer_input(dr, tok, g)
     k = (dr.w["k"] @ cat).reshape(geo.n_head_kv, geo.head_dim)
     v = (dr.w["v"] @ cat).reshape(geo.n_head_kv, geo.head_dim)
-    k = rope_neox(k, pos, geo.rope_dims, geo.rope_theta)
+    return rope_neox(k, pos, geo.rope_dims, geo.rope_theta), v
+
+
+def kv_entry(dr: Drafter, tok: int, g: np.ndarray, pos: int):
+    """kv_projection as the cache stores it (bf16, or the q8_0 / q5_1 blocks)."""
+    k, v = kv_projection(dr, tok, g, pos)
     return store_k(k, dr.kv_format), store_v(v, dr.kv_format)
 
 
-def kv_entries(dr: Drafter, toks, gs: np.ndarray, positions):
-    """kv_entry for many pairs at once: the same definition with the projections of all
-    pairs done as one matrix product (rows are independent; a library matmul step)."""
+def kv_projections(dr: Drafter, toks, gs: np.ndarray, positions):
+    """kv_projection for many pairs at once: the same definition with the projections of
+    all pairs done as one matrix product (rows are independent; a library matmul step)."""
     geo = dr.geom
     eps = geo.rms_eps
     toks = np.asarray(toks)
@@ -300,6 +307,12 @@ def kv_entries(dr: Drafter, toks, gs: np.ndarray, positions):
     v = (cat @ dr.w["v"].T).reshape(len(toks), geo.n_head_kv, geo.head_dim)
     k = np.stack([rope_neox(k[i], int(p), geo.rope_dims, geo.rope_theta)
                   for i, p in enumerate(positions)]) if len(toks) else k
+    return k, v
+
+
+def kv_entries(dr: Drafter, toks, gs: np.ndarray, positions):
+    """kv_entry for many pairs at once (kv_projections, then storage)."""
+    k, v = kv_projections(dr, toks, gs, positions)
     return store_k(k, dr.kv_format), store_v(v, dr.kv_format)
 
 
@@ -307,12 +320,14 @@ def kv_entries(dr: Drafter, toks, gs: np.ndarray, positions):
 class StepOut:
     logits: np.ndarray      # [draft_vocab]
     g_next: np.ndarray      # gsum, the pre-norm residual fed back as the next g
-    k: np.ndarray           # [H_kv, d] bf16-valued, the entry appended at pos
+    k: np.ndarray           # [H_kv, d] stored form of the entry appended at pos
     v: np.ndarray
     draft_id: int
     target_id: int
     x1: np.ndarray          # o_proj output + residual
     attn: np.ndarray        # attention output [H * d]
+    k_raw: np.ndarray = None  # this step's k (after RoPE) and v before storage
+    v_raw: np.ndarray = None
 
 
 def layer_after_attention(dr: Drafter, g: np.ndarray, attn: np.ndarray):
@@ -328,9 +343,14 @@ def layer_after_attention(dr: Drafter, g: np.ndarray, attn: np.ndarray):
 
 
 def draft_step(dr: Drafter, prev_tok: int, g: np.ndarray, k_cache: np.ndarray,
-               v_cache: np.ndarray, pos: int) -> StepOut:
+               v_cache: np.ndarray, pos: int, new_kv=None) -> StepOut:
     """One T=1 draft step at position pos over a cache holding positions 0..pos-1
-    ("memra_engine/eagle.rs", Op-sequence and ``draft_token`` / ``attn``)."""
+    ("memra_engine/eagle.rs", Op-sequence and ``draft_token`` / ``attn``).
+
+    new_kv: optional (k, v) stored form to append at pos instead of this step's own.
+    Where a stored form is decided by rounding (a quantization code on a boundary) more
+    than one form is valid; a caller can evaluate the step on the form another
+    implementation stored, after checking it against k_raw / v_raw."""
     geo = dr.geom
     if k_cache.shape[0] != pos:
         raise ValueError("cache must hold exactly the positions before pos")
@@ -338,13 +358,17 @@ def draft_step(dr: Drafter, prev_tok: int, g: np.ndarray, k_cache: np.ndarray,
     cat = layer_input(dr, prev_tok, g)
     q = (dr.w["q"] @ cat).reshape(geo.n_head, geo.head_dim)
     q = rope_neox(q, pos, geo.rope_dims, geo.rope_theta)
-    k_new, v_new = kv_entry(dr, prev_tok, g, pos)
+    k_raw, v_raw = kv_projection(dr, prev_tok, g, pos)
+    if new_kv is None:
+        k_new, v_new = store_k(k_raw, dr.kv_format), store_v(v_raw, dr.kv_format)
+    else:
+        k_new, v_new = (np.asarray(x, dtype=np.float64) for x in new_kv)
     k_all = np.concatenate([k_cache, k_new[None]], axis=0)
     v_all = np.concatenate([v_cache, v_new[None]], axis=0)
     attn = gqa_attention(q, k_all, v_all).reshape(-1)
     x1, gsum, logits = layer_after_attention(dr, g, attn)
     did = argmax_first(logits)
-    return StepOut(logits, gsum, k_new, v_new, did, dr.d2t_map(did), x1, attn)
+    return StepOut(logits, gsum, k_new, v_new, did, dr.d2t_map(did), x1, attn, k_raw, v_raw)
 
 
 # ---------------------------------------------------------------- sequence state
@@ -352,17 +376,21 @@ def draft_step(dr: Drafter, prev_tok: int, g: np.ndarray, k_cache: np.ndarray,
 @dataclass
 class SeqState:
     """Committed drafter state of one sequence."""
-    k: np.ndarray           # [L, H_kv, d] bf16-valued
+    k: np.ndarray           # [L, H_kv, d] stored form (bf16-valued or quantized blocks)
     v: np.ndarray
     g: np.ndarray           # boundary feature fc . a_{N-1}   [n]
     tok: int                # boundary token t_N (target id)
+    k_raw: np.ndarray = None  # [L, H_kv, d] the same entries before storage (float64)
+    v_raw: np.ndarray = None
 
     @property
     def kv_len(self) -> int:
         return int(self.k.shape[0])
 
     def copy(self) -> "SeqState":
-        return SeqState(self.k.copy(), self.v.copy(), self.g.copy(), int(self.tok))
+        return SeqState(self.k.copy(), self.v.copy(), self.g.copy(), int(self.tok),
+                        None if self.k_raw is None else self.k_raw.copy(),
+                        None if self.v_raw is None else self.v_raw.copy())
 
 
 def _empty_kv(geo):
@@ -382,11 +410,12 @@ def prefill(dr: Drafter, tokens, next_tok: int, aux_bits) -> SeqState:
     genc = encode(dr, aux_bits)
     geo = dr.geom
     if n_prompt > 1:
-        k_arr, v_arr = kv_entries(dr, tokens[1:n_prompt], genc[:n_prompt - 1],
-                                  np.arange(n_prompt - 1))
+        k_raw, v_raw = kv_projections(dr, tokens[1:n_prompt], genc[:n_prompt - 1],
+                                      np.arange(n_prompt - 1))
     else:
-        k_arr, v_arr = _empty_kv(geo), _empty_kv(geo)
-    return SeqState(k_arr, v_arr, genc[n_prompt - 1].copy(), int(next_tok))
+        k_raw, v_raw = _empty_kv(geo), _empty_kv(geo)
+    return SeqState(store_k(k_raw, dr.kv_format), store_v(v_raw, dr.kv_format),
+                    genc[n_prompt - 1].copy(), int(next_tok), k_raw, v_raw)
 
 
 def plan_gamma(kv_len: int, gamma: int, max_cache_len: int, shrink: bool) -> int:
@@ -503,10 +532,10 @@ def rebuild_after_verify(dr: Drafter, st: SeqState, n_acc: int, draft_tok, bonus
     venc = encode(dr, np.asarray(verify_aux_bits)[: n_acc + 1])
     pairs = [(int(st.tok), st.g)] + [(int(draft_tok[i - 1]), venc[i - 1])
                                      for i in range(1, n_acc + 1)]
-    ks, vs = [], []
-    for i, (t, gg) in enumerate(pairs):
-        k, v = kv_entry(dr, t, gg, L + i)
-        ks.append(k)
-        vs.append(v)
-    return SeqState(np.concatenate([st.k, np.stack(ks)]), np.concatenate([st.v, np.stack(vs)]),
-                    venc[n_acc].copy(), int(bonus))
+    kr, vr = zip(*[kv_projection(dr, t, gg, L + i) for i, (t, gg) in enumerate(pairs)])
+    kr, vr = np.stack(kr), np.stack(vr)
+    k_raw = None if st.k_raw is None else np.concatenate([st.k_raw, kr])
+    v_raw = None if st.v_raw is None else np.concatenate([st.v_raw, vr])
+    return SeqState(np.concatenate([st.k, store_k(kr, dr.kv_format)]),
+                    np.concatenate([st.v, store_v(vr, dr.kv_format)]),
+                    venc[n_acc].copy(), int(bonus), k_raw, v_raw)

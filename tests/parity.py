@@ -60,6 +60,77 @@ def assert_close_bf16(got, want, what: str, max_abs=MAX_ABS, rel_l2=REL_L2):
     assert rl <= rel_l2, f"{what}: rel-L2 {rl:.3e}"
 
 
+def kv_values(raw, kv_format: str, which: str) -> np.ndarray:
+    """Stored K (which "k") or V rows as float64 [..., H_kv, d], decoded with the oracle's
+    unpackers."""
+    raw = np.asarray(raw)
+    if kv_format == "bf16":
+        return bf16_bits_to_f64(raw)
+    if which == "k":
+        d16, q = O.unpack_q8_0(raw.reshape(raw.shape[:-1] + (-1, O.Q8_0_BLOCK_BYTES)))
+        return O.dequantize_q8_0(d16, q).astype(np.float64)
+    d16, m16, q = O.unpack_q5_1(raw.reshape(raw.shape[:-1] + (-1, O.Q5_1_BLOCK_BYTES)))
+    return O.dequantize_q5_1(d16, m16, q).astype(np.float64)
+
+
+QUANT_REL = 1e-5   # float32 vs float64 k / v inputs to the quantizer, relative to the block's max |x|
+
+
+def _f16_bracket(x, eps_abs):
+    """The fp16 values that x moved by at most eps_abs can round to (nearest even)."""
+    lo = np.asarray(x - eps_abs, dtype=np.float32).astype(np.float16).astype(np.float64)
+    hi = np.asarray(x + eps_abs, dtype=np.float32).astype(np.float16).astype(np.float64)
+    return lo, hi
+
+
+def assert_quant_valid(raw, x, which: str, what: str, rel=QUANT_REL):
+    """The stored q8_0 (which "k") / q5_1 ("v") blocks `raw` are a valid encoding of the
+    oracle's unstored values x [..., d] when the implementation's float32 inputs may differ
+    from x by delta = rel * max|x| of the block: every header field and every code must be
+    one that some input within delta of x produces under the encoding's rule.  Away from
+    rounding boundaries that is exactly the oracle's encoding; at a boundary either
+    neighbour is accepted (where several results are correct, check that the one given is
+    valid)."""
+    raw = np.asarray(raw, dtype=np.uint8)
+    x = np.asarray(x, dtype=np.float64)
+    xb = x.reshape(-1, O.QK)
+    delta = rel * np.abs(xb).max(axis=-1) + 1e-7                     # [blocks]
+    if which == "k":
+        d16, q = O.unpack_q8_0(raw.reshape(-1, O.Q8_0_BLOCK_BYTES))
+        d = d16.astype(np.float64)
+        s = np.abs(xb).max(axis=-1) / 127.0
+        lo, hi = _f16_bracket(s, delta / 127.0)
+        bad_h = (d < lo) | (d > hi)
+        assert not bad_h.any(), f"{what}: q8_0 scale outside its rounding bracket in {int(bad_h.sum())} blocks"
+        dd = np.where(d > 0, d, 1.0)[:, None]
+        t_lo = (xb - delta[:, None]) / dd
+        t_hi = (xb + delta[:, None]) / dd
+        c_lo = np.clip(np.rint(t_lo), -127, 127)
+        c_hi = np.clip(np.rint(t_hi), -127, 127)
+        code = q.astype(np.float64)
+    else:
+        d16, m16, q = O.unpack_q5_1(raw.reshape(-1, O.Q5_1_BLOCK_BYTES))
+        d, m = d16.astype(np.float64), m16.astype(np.float64)
+        s = (xb.max(axis=-1) - xb.min(axis=-1)) / 31.0
+        lo, hi = _f16_bracket(s, 2 * delta / 31.0)
+        mlo, mhi = _f16_bracket(xb.min(axis=-1), delta)
+        bad_h = (d < lo) | (d > hi) | (m < mlo) | (m > mhi)
+        assert not bad_h.any(), f"{what}: q5_1 scale / minimum outside their rounding brackets in {int(bad_h.sum())} blocks"
+        dd = np.where(d > 0, d, 1.0)[:, None]
+        t_lo = (xb - delta[:, None] - m[:, None]) / dd
+        t_hi = (xb + delta[:, None] - m[:, None]) / dd
+        c_lo = np.clip(np.rint(t_lo), 0, 31)
+        c_hi = np.clip(np.rint(t_hi), 0, 31)
+        code = q.astype(np.float64)
+    zero = (d == 0)[:, None]
+    c_lo = np.where(zero, 0, c_lo)
+    c_hi = np.where(zero, 0, c_hi)
+    bad = (code < c_lo) | (code > c_hi)
+    assert not bad.any(), f"{what}: {int(bad.sum())} codes not a nearest code of any input within delta"
+    n_edge = int(np.sum(c_lo != c_hi))
+    assert n_edge <= max(4, code.size // 100), f"{what}: {n_edge} codes on boundaries (delta too wide?)"
+
+
 def top2_margin(logits: np.ndarray) -> float:
     s = np.sort(logits)
     return float(s[-1] - s[-2])
@@ -122,8 +193,46 @@ def check_state(seq, states: dict, what, kv_lo=0):
         assert_close(g[b], st.g, f"{what}: boundary g[{b}]", max_abs=1e-3, rel_l2=1e-5)
         if st.kv_len > kv_lo:
             k, v = seq.kv_entries(b, kv_lo, st.kv_len)
-            assert_close_bf16(bf16_bits_to_f64(k), st.k[kv_lo:], f"{what}: K[{b}]")
-            assert_close_bf16(bf16_bits_to_f64(v), st.v[kv_lo:], f"{what}: V[{b}]")
+            fmt = seq.model.kv_format
+            if fmt == "bf16":
+                assert_close_bf16(bf16_bits_to_f64(k), st.k[kv_lo:], f"{what}: K[{b}]")
+                assert_close_bf16(bf16_bits_to_f64(v), st.v[kv_lo:], f"{what}: V[{b}]")
+            else:
+                assert_quant_valid(k, st.k_raw[kv_lo:], "k", f"{what}: K[{b}]")
+                assert_quant_valid(v, st.v_raw[kv_lo:], "v", f"{what}: V[{b}]")
+
+
+def check_chain_stepwise(seq, dr, b, st, g_eff, out, di, dt) -> int:
+    """Chain of sequence b with a quantized cache, step by step: step j of the oracle runs
+    on the implementation's inputs to that step (its boundary or previous g, its previous
+    token, its stored KV decoded, including the entry it appended at this step), since a
+    code on a rounding boundary may validly differ between the two.  Each appended entry
+    must be a valid encoding of the oracle's k / v of the step (assert_quant_valid); ids
+    follow the margin rule; logits and g are compared with the float tolerance."""
+    fmt = seq.model.kv_format
+    L = st.kv_len
+    kraw, vraw = seq.kv_entries(b, 0, L + g_eff)
+    kd = kv_values(kraw, fmt, "k")
+    vd = kv_values(vraw, fmt, "v")
+    logits = out["logits"][b, :g_eff].cpu().numpy()
+    gdbg = out["g"][b, :g_eff].cpu().numpy().astype(np.float64)
+    g_in, tok_in, ties = st.g, int(st.tok), 0
+    for j in range(g_eff):
+        pos = L + j
+        so = O.draft_step(dr, tok_in, g_in, kd[:pos], vd[:pos], pos, new_kv=(kd[pos], vd[pos]))
+        assert_quant_valid(kraw[pos], so.k_raw, "k", f"spec K b{b} j{j}")
+        assert_quant_valid(vraw[pos], so.v_raw, "v", f"spec V b{b} j{j}")
+        gid = int(di[b, j])
+        if top2_margin(so.logits) > MARGIN:
+            assert gid == so.draft_id, f"b{b} step {j}: GPU id {gid} vs oracle {so.draft_id}"
+        else:
+            ties += 1
+            assert so.logits[gid] >= so.logits.max() - MARGIN, f"b{b} step {j}: GPU id {gid} not near max"
+        assert int(dt[b, j]) == dr.d2t_map(gid), f"b{b} step {j}: d2t of {gid}"
+        assert_close(logits[j], so.logits, f"logits b{b} j{j}")
+        assert_close(gdbg[j], so.g_next, f"g b{b} j{j}")
+        g_in, tok_in = gdbg[j], int(dt[b, j])
+    return ties
 
 
 def run_round(model, dr, seq, states: dict, gamma, n_imposed, seed, flags=0, kv_lo=0):
@@ -143,6 +252,10 @@ def run_round(model, dr, seq, states: dict, gamma, n_imposed, seed, flags=0, kv_
     for b, st in states.items():
         g_eff = O.plan_gamma(st.kv_len, gamma, model.max_cache_len, bool(flags & Bd.EAGLE3_SHRINK_GAMMA))
         assert ge[b] == g_eff
+        assert np.all(dt[b, g_eff:] == -1)
+        if model.kv_format != "bf16":
+            ties += check_chain_stepwise(seq, dr, b, st, g_eff, out, di, dt)
+            continue
         ch, f = oracle_chain_following(dr, st, g_eff, di[b, :g_eff], dt[b, :g_eff])
         ties += f.ties
         assert np.all(dt[b, g_eff:] == -1)

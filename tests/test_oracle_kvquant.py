@@ -146,3 +146,91 @@ def test_quantized_format_needs_blocks_of_32():
     wts = synth.make_weights(synth.TINY, seed=0)
     with pytest.raises(ValueError):
         O.Drafter(g, wts.bits, wts.d2t, kv_format="q8_0/q5_1")
+
+
+
+
+def test_parity_decoder_reads_packed_rows():
+    """The parity tests decode the GPU's pool rows with the oracle's unpackers: packed
+    rows of several blocks decode to the oracle's stored values."""
+    from parity import kv_values
+    x = np.random.default_rng(5).standard_normal((3, 2, 128))
+    kraw = O.pack_q8_0(*O.quantize_q8_0(x.astype(np.float32))).reshape(3, 2, -1)
+    vraw = O.pack_q5_1(*O.quantize_q5_1(x.astype(np.float32))).reshape(3, 2, -1)
+    assert kraw.shape[-1] == 4 * 34 and vraw.shape[-1] == 4 * 24
+    assert np.array_equal(kv_values(kraw, "q8_0/q5_1", "k"), O.store_k(x, "q8_0/q5_1"))
+    assert np.array_equal(kv_values(vraw, "q8_0/q5_1", "v"), O.store_v(x, "q8_0/q5_1"))
+
+
+def test_validity_check_accepts_own_encoding_and_rejects_planted_errors():
+    """assert_quant_valid (the GPU parity bar for stored blocks) is not vacuous: the
+    oracle's own bytes pass; a code moved by one away from a boundary, a scale two fp16
+    steps off, or a wrong minimum fail; at an exact code boundary either neighbour passes."""
+    from parity import assert_quant_valid
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((8, 64))
+    kb = O.pack_q8_0(*O.quantize_q8_0(x.astype(np.float32))).reshape(8, -1)
+    vb = O.pack_q5_1(*O.quantize_q5_1(x.astype(np.float32))).reshape(8, -1)
+    assert_quant_valid(kb, x, "k", "own K")
+    assert_quant_valid(vb, x, "v", "own V")
+
+    def planted(blocks, which, fn):
+        b = blocks.copy()
+        fn(b.reshape(-1, 34 if which == "k" else 24))
+        with pytest.raises(AssertionError):
+            assert_quant_valid(b, x, which, "planted")
+
+    d16, _ = O.quantize_q8_0(x.astype(np.float32))
+    t = x.reshape(-1, 32) / d16.astype(np.float64).reshape(-1)[:, None]
+    blk, i = np.argwhere((np.abs(t - np.rint(t)) < 0.3) & (np.abs(t) < 120))[0]
+
+    def bump_code(flat):
+        flat[blk, 2 + i] = (int(flat[blk, 2 + i]) + 1) & 0xff
+
+    def bump_scale(flat):
+        h = int(flat[3, 0:2].view(np.uint16)[0])
+        flat[3, 0:2] = np.array([h + 2], dtype=np.uint16).view(np.uint8)
+
+    def bump_min(flat):
+        h = int(flat[5, 2:4].view(np.uint16)[0])
+        flat[5, 2:4] = np.array([h + 3], dtype=np.uint16).view(np.uint8)
+
+    planted(kb, "k", bump_code)
+    planted(kb, "k", bump_scale)
+    planted(vb, "v", bump_min)
+    # a value exactly half-way between two q8_0 codes: either neighbour is valid
+    y = np.zeros(32)
+    y[0] = 127.0 * 0.25           # scale 0.25 exactly
+    y[1] = 10.5 * 0.25            # on the boundary between codes 10 and 11
+    for c in (10, 11):
+        codes = np.zeros(32, np.int8)
+        codes[0], codes[1] = 127, c
+        assert_quant_valid(O.pack_q8_0(np.float16(0.25), codes), y, "k", f"tie code {c}")
+    codes[1] = 12
+    with pytest.raises(AssertionError):
+        assert_quant_valid(O.pack_q8_0(np.float16(0.25), codes), y, "k", "two codes off")
+
+
+def test_step_on_its_own_stored_entry_and_raw_state():
+    """draft_step given its own stored entry as new_kv is the same step; prefill and
+    rebuild keep the unstored k / v whose storage is the state's KV."""
+    g = synth.TINY
+    wts = synth.make_weights(g, seed=9)
+    dr = O.Drafter(g, wts.bits, wts.d2t, kv_format="q8_0/q5_1")
+    ptoks = synth.make_tokens(12, g, seed=14)
+    aux = synth.make_aux((11,), g, seed=15)
+    st = O.prefill(dr, ptoks[:11], int(ptoks[11]), aux)
+    assert np.array_equal(O.store_k(st.k_raw, dr.kv_format), st.k)
+    assert np.array_equal(O.store_v(st.v_raw, dr.kv_format), st.v)
+    a = O.draft_step(dr, st.tok, st.g, st.k, st.v, st.kv_len)
+    b = O.draft_step(dr, st.tok, st.g, st.k, st.v, st.kv_len, new_kv=(a.k, a.v))
+    assert np.array_equal(a.logits, b.logits) and np.array_equal(a.g_next, b.g_next)
+    assert np.array_equal(O.store_k(a.k_raw, dr.kv_format), a.k)
+    # a different appended entry changes the step (the override is used)
+    c = O.draft_step(dr, st.tok, st.g, st.k, st.v, st.kv_len, new_kv=(a.k, a.v * 0.5))
+    assert not np.array_equal(a.g_next, c.g_next)
+    vaux = synth.make_aux((4,), g, seed=16)
+    st2 = O.rebuild_after_verify(dr, st, 2, [int(ptoks[1]), int(ptoks[2]), int(ptoks[3])], 7, vaux)
+    assert st2.kv_len == st.kv_len + 3
+    assert np.array_equal(O.store_k(st2.k_raw, dr.kv_format), st2.k)
+    assert np.array_equal(O.store_v(st2.v_raw, dr.kv_format), st2.v)
