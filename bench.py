@@ -58,9 +58,12 @@ PROFILED_TRAFFIC = {
     ("c2", "lmhead"): {"bytes": 262220288 + 3023104,
                        "sources": ("gemv.cu", "epilogue.cuh", "common.cuh"),
                        "sha256": "41a365cfc405be675089bcef7fd28faf3fef1ac0562ce3274da15cbd439f7137"},
-    ("c4", "attn"): {"bytes": 539156480 + 3380224,
+    ("c4", "attn"): {"bytes": 538542336 + 3409920,
                      "sources": ("attention.cu", "common.cuh"),
-                     "sha256": "f54e976e2004577d99bb153b103500ba92de69bab0f0ba2637ed2356cb59fb19"},
+                     "sha256": "411a20dc79418bbbcefe707ac26b3a3bd5605a565738cfea21945d6aedbbe267"},
+    ("c5", "attn", "q8_0/q5_1"): {"bytes": 243909888 + 2840320,
+                                  "sources": ("attention.cu", "common.cuh"),
+                                  "sha256": "411a20dc79418bbbcefe707ac26b3a3bd5605a565738cfea21945d6aedbbe267"},
     ("c4", "lmhead"): {"bytes": 265020928 + 6003968,
                        "sources": ("gemm_tc.cu", "epilogue.cuh", "common.cuh"),
                        "sha256": "07e0e56c23b1d9d9259efedd6d98324c331b09463ad33fd94cdb1734cceea173"},

@@ -1,4 +1,6 @@
-// GQA decode attention over the paged bf16 drafter KV cache.
+// GQA decode attention over the paged drafter KV cache, bf16 or quantized (q8_0 K, q5_1
+// V; a K block's scale multiplies the partial dot once, V = d * code + m with the p * m
+// terms summed apart).
 //
 // For each sequence b and q head h (kv head h / G, G = n_head / n_head_kv): softmax over
 // the keys 0..len-1 of (q . k) / sqrt(d), then sum of p * v ("memra_engine/eagle.rs",
@@ -88,6 +90,29 @@ __device__ __forceinline__ float seg_reduce_multi(float (&v)[N], int li) {
 #pragma unroll
   for (int o = LPK / (2 * N); o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o, LPK);
   return r;
+}
+
+// Four bytes of w as floats without the conversion unit: a byte placed under the exponent
+// of 2^23 (0x4B0000xx) reads as 2^23 + byte exactly, so one byte permute and one add give
+// the value.  Signed bytes are first offset by 128 (w ^ 0x80808080), then 2^23 + 128 is
+// subtracted; both results are exact integers.
+template <bool SIGNED>
+__device__ __forceinline__ void bytes_to_f32x2(uint32_t w, float2 *f) {
+  constexpr float kBias = SIGNED ? -8388736.0f : -8388608.0f;
+  if (SIGNED) w ^= 0x80808080u;
+  const float2 bias = make_float2(kBias, kBias);
+  f[0] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540)),
+                                __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7541))), bias);
+  f[1] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7542)),
+                                __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7543))), bias);
+}
+
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t u) { return make_float2(bf_lo(u), bf_hi(u)); }
+
+// Bit i (i < 4) of x moved to bit 4 of byte i: x * 0x00204081 puts bit i at 8i + 7(j - i)
+// for each j; only j = i lands on a multiple of 8 and no two terms share a bit (no carry).
+__device__ __forceinline__ uint32_t spread4_to_bit4(uint32_t x) {
+  return ((x * 0x00204081u) & 0x01010101u) << 4;
 }
 
 // The unit partition of one launch: pre[b] = units of one kv head of sequences < b (a
@@ -265,22 +290,26 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
     const int b = sg.b, kvh = sg.kvh;
     const int est = est_len(b), fin = final_len(b), L = p.kv_len[b];
     const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
-    float qv[G][8];
+    // q, the running weighted V and the K / V values are float pairs: every multiply-add
+    // of the loop is a packed two-lane FMA
+    float2 qv[G][4];
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
       const float4 *qp = reinterpret_cast<const float4 *>(p.q + (size_t)b * H * D + (size_t)(kvh * G + gg) * D + li * 8);
       const float4 a = __ldcg(qp), c = __ldcg(qp + 1);
-      qv[gg][0] = a.x * qscale; qv[gg][1] = a.y * qscale; qv[gg][2] = a.z * qscale; qv[gg][3] = a.w * qscale;
-      qv[gg][4] = c.x * qscale; qv[gg][5] = c.y * qscale; qv[gg][6] = c.z * qscale; qv[gg][7] = c.w * qscale;
+      qv[gg][0] = make_float2(a.x * qscale, a.y * qscale);
+      qv[gg][1] = make_float2(a.z * qscale, a.w * qscale);
+      qv[gg][2] = make_float2(c.x * qscale, c.y * qscale);
+      qv[gg][3] = make_float2(c.z * qscale, c.w * qscale);
     }
     float m_me = -INFINITY, l_me = 0.f;  // running max (log2 domain) and sum of head g_me
-    float acc[G][8];                     // running weighted V of this lane's 8 dims, every head
+    float2 acc[G][4];                    // running weighted V of this lane's 8 dims, every head
     float accm[G];                       // quantized V: running sum of p * m (block minimum)
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
       accm[gg] = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[gg][i] = 0.f;
+      for (int i = 0; i < 4; ++i) acc[gg][i] = make_float2(0.f, 0.f);
     }
 
     for (int r = sg.r0; r < sg.r1; ++r) {
@@ -304,31 +333,33 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
         const int kk = warp * KPW * UNR + uu * KPW + grp;
         const bool v = have && kk < n;
         vmask |= v ? (1u << uu) : 0u;
-        float kf[8];
+        float2 kf[4];
         float kscale = 1.f;
         if constexpr (KVQ) {
           // q8_0: this lane's 8 codes of block li / 4 (2-byte aligned: four 16-bit loads);
           // the block scale multiplies the partial dot once
           const unsigned char *blk = kst + (size_t)kk * KR + (li >> 2) * 34;
           const uint16_t *c16 = reinterpret_cast<const uint16_t *>(blk + 2 + 8 * (li & 3));
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const unsigned u = v ? c16[i] : 0u;
-            kf[2 * i] = (float)(signed char)(u & 0xffu);
-            kf[2 * i + 1] = (float)(signed char)(u >> 8);
+          uint32_t w0 = 0u, w1 = 0u;
+          if (v) {
+            w0 = __byte_perm(c16[0], c16[1], 0x5410);
+            w1 = __byte_perm(c16[2], c16[3], 0x5410);
           }
+          bytes_to_f32x2<true>(w0, kf);
+          bytes_to_f32x2<true>(w1, kf + 2);
           kscale = v ? __half2float(*reinterpret_cast<const __half *>(blk)) : 0.f;
         } else {
           uint4 ku = make_uint4(0u, 0u, 0u, 0u);
           if (v) ku = *reinterpret_cast<const uint4 *>(kst + (size_t)kk * KR + li * 16);
-          kf[0] = bf_lo(ku.x); kf[1] = bf_hi(ku.x); kf[2] = bf_lo(ku.y); kf[3] = bf_hi(ku.y);
-          kf[4] = bf_lo(ku.z); kf[5] = bf_hi(ku.z); kf[6] = bf_lo(ku.w); kf[7] = bf_hi(ku.w);
+          kf[0] = bf16x2_to_f32x2(ku.x); kf[1] = bf16x2_to_f32x2(ku.y);
+          kf[2] = bf16x2_to_f32x2(ku.z); kf[3] = bf16x2_to_f32x2(ku.w);
         }
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
-          float d = 0.f;
+          float2 d2 = __fmul2_rn(qv[gg][0], kf[0]);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) d = fmaf(qv[gg][i], kf[i], d);
+          for (int i = 1; i < 4; ++i) d2 = __ffma2_rn(qv[gg][i], kf[i], d2);
+          const float d = d2.x + d2.y;
           part_s[uu * G + gg] = KVQ ? d * kscale : d;
         }
       }
@@ -350,15 +381,16 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
 #pragma unroll
       for (int gg = 0; gg < G; ++gg) {
         const float c = __shfl_sync(0xffffffffu, corr, gg << SH, LPK);
+        const float2 c2 = make_float2(c, c);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[gg][i] *= c;
+        for (int i = 0; i < 4; ++i) acc[gg][i] = __fmul2_rn(acc[gg][i], c2);
         if constexpr (KVQ) accm[gg] *= c;
       }
 #pragma unroll
       for (int uu = 0; uu < UNR; ++uu) {
         const int kk = warp * KPW * UNR + uu * KPW + grp;
         const bool vv = (vmask >> uu) & 1u;
-        float vf[8];
+        float2 vf[4];
         float vd = 1.f, vm = 0.f;
         if constexpr (KVQ) {
           // q5_1: this lane's 8 codes of block li / 4 -- 4 bits from one 8-byte load (low
@@ -377,23 +409,24 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
             vd = 0.f;
           }
           const int sh = e >= 16 ? 4 : 0;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const unsigned byte = ((i < 4 ? qs.x : qs.y) >> (8 * (i & 3))) & 0xffu;
-            vf[i] = (float)(((byte >> sh) & 15u) | (((qh >> (e + i)) & 1u) << 4));
-          }
+          const uint32_t hb = qh >> e;  // fifth bits of values e .. e + 7
+          const uint32_t w0 = ((qs.x >> sh) & 0x0F0F0F0Fu) | spread4_to_bit4(hb & 15u);
+          const uint32_t w1 = ((qs.y >> sh) & 0x0F0F0F0Fu) | spread4_to_bit4((hb >> 4) & 15u);
+          bytes_to_f32x2<false>(w0, vf);
+          bytes_to_f32x2<false>(w1, vf + 2);
         } else {
           uint4 vu = make_uint4(0u, 0u, 0u, 0u);
           if (vv) vu = *reinterpret_cast<const uint4 *>(vst + (size_t)kk * VR + li * 16);
-          vf[0] = bf_lo(vu.x); vf[1] = bf_hi(vu.x); vf[2] = bf_lo(vu.y); vf[3] = bf_hi(vu.y);
-          vf[4] = bf_lo(vu.z); vf[5] = bf_hi(vu.z); vf[6] = bf_lo(vu.w); vf[7] = bf_hi(vu.w);
+          vf[0] = bf16x2_to_f32x2(vu.x); vf[1] = bf16x2_to_f32x2(vu.y);
+          vf[2] = bf16x2_to_f32x2(vu.z); vf[3] = bf16x2_to_f32x2(vu.w);
         }
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
           const float pg2 = __shfl_sync(0xffffffffu, pr, (uu * G + gg) << SH, LPK);
           const float pw = KVQ ? pg2 * vd : pg2;
+          const float2 pw2 = make_float2(pw, pw);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[gg][i] = fmaf(pw, vf[i], acc[gg][i]);
+          for (int i = 0; i < 4; ++i) acc[gg][i] = __ffma2_rn(pw2, vf[i], acc[gg][i]);
           if constexpr (KVQ) accm[gg] = fmaf(pg2, vm, accm[gg]);
         }
       }
@@ -407,7 +440,11 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
 #pragma unroll
     for (int gg = 0; gg < G; ++gg)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sm_acc[((size_t)part * G + gg) * D + li * 8 + i] = acc[gg][i] + (KVQ ? accm[gg] : 0.f);
+      for (int i = 0; i < 4; ++i) {
+        const float mm = KVQ ? accm[gg] : 0.f;
+        *reinterpret_cast<float2 *>(sm_acc + ((size_t)part * G + gg) * D + li * 8 + 2 * i) =
+            make_float2(acc[gg][i].x + mm, acc[gg][i].y + mm);
+      }
     asm volatile("bar.sync 1, 256;" ::: "memory");
     const bool whole = sg.r0 == 0 && sg.r1 == sg.nu;
     float *out = p.out + (size_t)b * H * D + (size_t)kvh * G * D;
