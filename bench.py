@@ -465,6 +465,36 @@ def run_mine(args, cfg):
     e2e_s = max_over_ranks(world, e2e_s)
     e2e_val = sum_over_ranks(world, float(B * gamma * args.e2e_steps)) / e2e_s
 
+    # ---- target-side greedy verify of the window (eagle3_verify_greedy): the target head
+    # is the tied embedding [V_t, n]; synthetic last hidden states of the B x (gamma + 1)
+    # window rows; timed apart from the round (the round's verifier is synthetic)
+    verify = None
+    if args.verify_steps > 0:
+        hid_v = torch.from_numpy(synth.make_hidden((B, gamma + 1), geo, seed + 6)).to(dev)
+        t_pred = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
+        head, tnorm = model.w["embed"], model.w["final_norm"]
+        d = out["draft_tok"]
+        for _ in range(3):
+            seq.verify_greedy(head, tnorm, hid_v, d, out["gamma_eff"], target_pred=t_pred,
+                              n_acc=n_acc, bonus=bonus)
+        torch.cuda.synchronize()
+        v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        v0.record()
+        for _ in range(args.verify_steps):
+            seq.verify_greedy(head, tnorm, hid_v, d, out["gamma_eff"], target_pred=t_pred,
+                              n_acc=n_acc, bonus=bonus)
+        v1.record()
+        torch.cuda.synchronize()
+        v_us = v0.elapsed_time(v1) * 1e3 / args.verify_steps
+        rows = B * (gamma + 1)
+        v_bytes = geo.target_vocab * geo.n_embd * 2 + rows * geo.n_embd * 4 + geo.n_embd * 2 + rows * 4
+        verify = {"us_per_call": v_us, "rows": rows, "target_vocab": geo.target_vocab,
+                  "bytes_per_call": v_bytes, "achieved_gbs": v_bytes / (v_us * 1e-6) / 1e9,
+                  "frac": v_bytes / (v_us * 1e-6) / 1e9 / hbm_peak,
+                  "kernel": ("target lm_head tcgen05 GEMM" if rows >= 3 else "target lm_head GEMV")
+                  + " + argmax, then the accept walk",
+                  "note": "target head = the tied embedding bf16 [V_t, n]; float32 synthetic hidden states"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
@@ -514,6 +544,7 @@ def run_mine(args, cfg):
                 "h2d_bytes_per_step": int(vaux[0].numel() * 2),
                 "d2h_bytes_per_step": int(host_tok.numel() * 4 + host_acc.numel() * 4),
                 "steps": args.e2e_steps},
+        "verify": verify,
         "gpu_launches": int(launches),
         "clocks": clk,
     }
@@ -532,6 +563,8 @@ def main():
     ap.add_argument("--phase-rounds", type=int, default=3)
     ap.add_argument("--cpu-rounds", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--verify-steps", type=int, default=10,
+                    help="timed calls of the target-side greedy verify (0: skip)")
     ap.add_argument("--kv-format", default="bf16", choices=["bf16", "q8_0/q5_1"],
                     help="drafter KV cache storage: bf16, or q8_0 keys / q5_1 values")
     ap.add_argument("--tc-min-items", type=int, default=0,

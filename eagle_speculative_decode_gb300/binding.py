@@ -33,7 +33,8 @@ EXPORTED = (
     "eagle3_version", "eagle3_error_string", "eagle3_workspace_bytes", "eagle3_kv_row_bytes",
     "eagle3_plan_gamma",
     "eagle3_init", "eagle3_destroy", "eagle3_encode", "eagle3_prefill", "eagle3_draft_chain",
-    "eagle3_rewind", "eagle3_accept", "eagle3_rebuild_after_verify", "eagle3_get_status",
+    "eagle3_rewind", "eagle3_accept", "eagle3_verify_greedy", "eagle3_rebuild_after_verify",
+    "eagle3_get_status",
     "eagle3_set_graph_mode", "eagle3_set_tc_min_items", "eagle3_launch_count", "eagle3_profile_begin",
     "eagle3_profile_end", "eagle3_profile_interval", "eagle3_lmhead_argmax_noalloc",
 )
@@ -104,6 +105,7 @@ def load() -> ctypes.CDLL:
         "eagle3_draft_chain": (ci, [vp, ci, ci, cu, vp, P(KV), P(Boundary), vp, vp, vp, vp, vp, vp]),
         "eagle3_rewind": (ci, [vp, ci, P(KV), vp]),
         "eagle3_accept": (ci, [vp, ci, ci, vp, vp, vp, vp, vp, vp]),
+        "eagle3_verify_greedy": (ci, [vp, ci, ci, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp]),
         "eagle3_rebuild_after_verify": (ci, [vp, ci, ci, vp, vp, vp, vp, P(KV), P(Boundary), vp]),
         "eagle3_get_status": (ci, [vp, P(ci)]),
         "eagle3_set_graph_mode": (ci, [vp, ci]),
@@ -214,6 +216,16 @@ def eagle3_accept(ctx: int, B: int, gamma: int, draft_tok: int, target_pred: int
                   gamma_eff: int | None, n_acc: int, bonus: int, stream: int = 0) -> None:
     _check(load().eagle3_accept(ctx, int(B), int(gamma), draft_tok, target_pred, gamma_eff,
                                 n_acc, bonus, stream), "eagle3_accept")
+
+
+def eagle3_verify_greedy(ctx: int, B: int, gamma: int, target_lm_head: int, target_norm: int,
+                         target_rms_eps: float, hidden: int, draft_tok: int, gamma_eff: int | None,
+                         target_pred: int, n_acc: int, bonus: int, logits_dbg: int | None,
+                         stream: int = 0) -> None:
+    _check(load().eagle3_verify_greedy(ctx, int(B), int(gamma), target_lm_head, target_norm,
+                                       float(target_rms_eps), hidden, draft_tok, gamma_eff,
+                                       target_pred, n_acc, bonus, logits_dbg, stream),
+           "eagle3_verify_greedy")
 
 
 def eagle3_rebuild_after_verify(ctx: int, B: int, gamma: int, n_acc: int, draft_tok: int,

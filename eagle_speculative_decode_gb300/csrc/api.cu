@@ -28,7 +28,8 @@ struct Layout {
 };
 
 constexpr int kTcMinItems = 3;       // batched projections use the tensor-core GEMM from here
-constexpr size_t kTcCounters = 4096;
+constexpr size_t kTcCounters = 32768;  // (row tile, item tile) arrival counters: the
+                                       // target head of verify has ~2000 row tiles
 constexpr int kTcEncodeChunk = 2048;  // encode rows per tensor-core launch
 constexpr int kTcPrepMaxK = 16384;    // widest float32 input the activation split handles
 
@@ -89,7 +90,7 @@ Layout make_layout(const eagle3_config &c) {
   L.act = take(B * (size_t)c.n_ff * 4);
   L.gwork = take(B * n * 4);
   L.tokwork = take(B * 4);
-  L.am_slot = take(B * 8);
+  L.am_slot = take(B * (c.max_gamma + 1) * 8);  // one per chain item or verify row
   L.am_cnt = take(64 * 4);
   L.round_start = take(B * 4);
   L.geff = take(B * 4);
@@ -282,7 +283,7 @@ cudaError_t tc_items(eagle3_ctx *ctx, const GemvParams &p, int items, cudaStream
       L.a1 = ctx->w.up; L.a1_rows = c.n_ff;
       break;
     case GM_DOWN: L.a0 = ctx->w.down; L.a0_rows = n; break;
-    default: L.a0 = ctx->w.lm_head; L.a0_rows = c.draft_vocab; break;
+    default: L.a0 = p.w0; L.a0_rows = p.rows; break;  // the draft lm_head, or verify's target head
   }
   const int label = (p.mode == GM_QKV && p.row_base > 0) ? PH_KV : gemv_label(p.mode);
   if (p.mode == GM_ENCODE) {
@@ -728,7 +729,8 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
   }
   // Counters and argmax slots start at zero and are returned to zero by their users.
   cudaError_t e = cudaMemsetAsync(b + L.attn_cnt, 0, (size_t)cfg->max_batch * cfg->n_head_kv * 4, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(b + L.am_slot, 0, (size_t)cfg->max_batch * 8, st);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(b + L.am_slot, 0, (size_t)cfg->max_batch * (cfg->max_gamma + 1) * 8, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(b + L.am_cnt, 0, 64 * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(b + L.status, 0, 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(b + L.tc_cnt, 0, kTcCounters * 4, st);
@@ -887,6 +889,46 @@ int eagle3_accept(eagle3_ctx *ctx, int B, int gamma, const int32_t *draft_tok,
   return cuda_err(launched(ctx, st,
                            launch_accept(B, gamma, draft_tok, target_pred, gamma_eff, n_acc, bonus, st),
                            PH_SMALL));
+}
+
+int eagle3_verify_greedy(eagle3_ctx *ctx, int B, int gamma, const uint16_t *target_lm_head,
+                         const uint16_t *target_norm, float target_rms_eps, const float *hidden,
+                         const int32_t *draft_tok, const int32_t *gamma_eff, int32_t *target_pred,
+                         int32_t *n_acc, int32_t *bonus, float *logits_dbg, eagle3_stream_t stream) {
+  if (!ctx || B < 1 || B > ctx->c.max_batch || gamma < 1 || gamma > ctx->c.max_gamma)
+    return EAGLE3_ERR_INVALID_ARG;
+  if (!aligned16(target_lm_head) || !aligned16(target_norm) || !aligned16(hidden)) return EAGLE3_ERR_INVALID_ARG;
+  if (!draft_tok || !target_pred || !n_acc || !bonus || (logits_dbg && !aligned16(logits_dbg)))
+    return EAGLE3_ERR_INVALID_ARG;
+  const eagle3_config &c = ctx->c;
+  if (c.target_vocab % 2 || !(target_rms_eps >= 0.f)) return EAGLE3_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ctx->last_stream = st;
+  // the lm_head + argmax kernels of the chain with the target's head: no d2t (ids are
+  // target ids), every row valid, one output per window row
+  GemvParams p = base_params(ctx);
+  p.mode = GM_LMHEAD;
+  p.rows = c.target_vocab;
+  p.K = c.n_embd;
+  p.w0 = target_lm_head;
+  p.xf = hidden;
+  p.norm0 = target_norm;
+  p.eps = target_rms_eps;
+  p.am_slot = ctx->am_slot;
+  p.am_count = ctx->am_cnt;
+  p.d2t = nullptr;
+  p.draft_vocab = c.target_vocab;
+  p.draft_tok = target_pred;
+  p.gamma = 1;
+  p.step = 0;
+  p.dbg_f = logits_dbg;
+  p.dbg_stride_b = c.target_vocab;
+  p.dbg_off = 0;
+  cudaError_t e = gemv_items(ctx, p, B * (gamma + 1), st, true);
+  if (e == cudaSuccess)
+    e = launched(ctx, st, launch_accept(B, gamma, draft_tok, target_pred, gamma_eff, n_acc, bonus, st),
+                 PH_SMALL);
+  return cuda_err(e);
 }
 
 int eagle3_rebuild_after_verify(eagle3_ctx *ctx, int B, int gamma, const int32_t *n_acc,

@@ -203,12 +203,12 @@ __device__ __forceinline__ void lmhead_finalize(const GemvParams &p, int item0, 
       set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
       id = 0;
     }
-    long long tgt = (long long)id + p.d2t[id];
+    long long tgt = p.d2t ? (long long)id + p.d2t[id] : (long long)id;  // no d2t: target ids
     if (tgt < 0 || tgt >= p.target_vocab) {
       set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
       tgt = 0;
     }
-    const bool valid = p.step < p.gamma_eff[item];
+    const bool valid = !p.gamma_eff || p.step < p.gamma_eff[item];
     const size_t o = (size_t)item * p.gamma + p.step;
     p.draft_tok[o] = valid ? (int32_t)tgt : -1;
     if (p.draft_id) p.draft_id[o] = valid ? (int32_t)id : -1;

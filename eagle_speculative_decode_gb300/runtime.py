@@ -159,6 +159,28 @@ class SeqBatch:
                         n_acc.data_ptr(), bonus.data_ptr(), _stream_handle(stream))
         return n_acc, bonus
 
+    def verify_greedy(self, target_lm_head, target_norm, hidden, draft_tok, gamma_eff=None,
+                      target_rms_eps=None, target_pred=None, n_acc=None, bonus=None,
+                      logits=False, stream=None):
+        """Target-side greedy verify of the drafted window: target_pred [B, gamma + 1] (the
+        target head's argmax at each window position of `hidden` [B, gamma + 1, n] float32),
+        then the accept walk.  target_lm_head / target_norm: bf16 bits as int16 tensors."""
+        dev = self.model.device
+        gamma = draft_tok.shape[1]
+        eps = self.model.geom.rms_eps if target_rms_eps is None else target_rms_eps
+        V = int(target_lm_head.shape[0])
+        target_pred = target_pred if target_pred is not None else \
+            torch.empty(self.B, gamma + 1, dtype=torch.int32, device=dev)
+        n_acc = n_acc if n_acc is not None else torch.empty(self.B, dtype=torch.int32, device=dev)
+        bonus = bonus if bonus is not None else torch.empty(self.B, dtype=torch.int32, device=dev)
+        lg = torch.empty(self.B, gamma + 1, V, dtype=torch.float32, device=dev) if logits else None
+        B.eagle3_verify_greedy(self.model.ctx, self.B, gamma, target_lm_head.data_ptr(),
+                               target_norm.data_ptr(), eps, hidden.data_ptr(), draft_tok.data_ptr(),
+                               gamma_eff.data_ptr() if gamma_eff is not None else None,
+                               target_pred.data_ptr(), n_acc.data_ptr(), bonus.data_ptr(),
+                               lg.data_ptr() if lg is not None else None, _stream_handle(stream))
+        return target_pred, n_acc, bonus, lg
+
     def rebuild_after_verify(self, n_acc, draft_tok, bonus, verify_aux, n_acc_host=None,
                              stream=None):
         gamma = draft_tok.shape[1]

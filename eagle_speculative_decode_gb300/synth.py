@@ -165,6 +165,22 @@ def make_weights(geom: Geometry, seed: int = 0, gains: str = "one_plus",
     return DrafterWeights(geom, bits, make_d2t(geom, seed), seed, gains)
 
 
+def make_target_head(geom: Geometry, seed: int, std: float = 0.02):
+    """Synthetic target output head for the verify step: lm_head bf16 bits
+    [target_vocab, n_embd] ~ N(0, std) and final-norm gains 1 + N(0, std)."""
+    head = normal_bf16((geom.target_vocab, geom.n_embd), seed, (300,), std=std)
+    norm = normal_bf16((geom.n_embd,), seed, (301,), std=std, mean=1.0)
+    return head, norm
+
+
+def make_hidden(shape_prefix: tuple[int, ...], geom: Geometry, seed: int,
+                stream: int = 0) -> np.ndarray:
+    """Synthetic target last hidden states: float32 (bf16-valued) N(0, 1), shape
+    prefix + (n_embd,)."""
+    bits = normal_bf16(tuple(shape_prefix) + (geom.n_embd,), seed, (400, stream))
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
 def make_aux(shape_prefix: tuple[int, ...], geom: Geometry, seed: int,
              stream: int = 0) -> np.ndarray:
     """Auxiliary target features N(0, 1) in bf16, shape prefix + (n_aux, n_embd)."""

@@ -227,6 +227,30 @@ int eagle3_accept(eagle3_ctx *ctx, int B, int gamma, const int32_t *draft_tok,
                   const int32_t *target_pred, const int32_t *gamma_eff, int32_t *n_acc,
                   int32_t *bonus, eagle3_stream_t stream);
 
+/* Greedy verify on the target side ("Add the Eagle3Speculator module for speculative
+ * decoding", PR body: target_verify returns the greedy argmax target id of every window
+ * position; "memra_engine/eagle.rs", generate_spec_eagle steps 3-4).  For sequence b and
+ * window position i = 0..gamma:
+ *   target_pred[b, i] = argmax over v < target_vocab of
+ *                       (target_lm_head . (RMSNorm(hidden[b, i]) * target_norm))[v],
+ * the lowest id among equal maxima (RMSNorm with target_rms_eps), then the accept walk of
+ * eagle3_accept writes n_acc and bonus.
+ *   target_lm_head: bf16 [target_vocab, n_embd] row-major, device, 16-byte aligned.
+ *   target_norm:    bf16 [n_embd], the target's final-norm gain.
+ *   hidden:         float32 [B, gamma + 1, n_embd], the target's last hidden states at
+ *                   the window positions (before its final norm), 16-byte aligned.
+ *   draft_tok [B, gamma], gamma_eff [B] or NULL: as eagle3_accept.
+ *   target_pred:    int32 [B, gamma + 1] out; n_acc, bonus: int32 [B] out.
+ *   logits_dbg:     float32 [B, gamma + 1, target_vocab] or NULL.
+ * Every window row is computed whatever gamma_eff (the head is read once either way).
+ * Uses the context's argmax scratch, so it runs on the context's stream order like the
+ * other calls; it changes no round state.  EAGLE3_ERR_INVALID_ARG for B or gamma out of
+ * range, a null or misaligned pointer, an odd target_vocab or a negative eps. */
+int eagle3_verify_greedy(eagle3_ctx *ctx, int B, int gamma, const uint16_t *target_lm_head,
+                         const uint16_t *target_norm, float target_rms_eps, const float *hidden,
+                         const int32_t *draft_tok, const int32_t *gamma_eff, int32_t *target_pred,
+                         int32_t *n_acc, int32_t *bonus, float *logits_dbg, eagle3_stream_t stream);
+
 /* Rebuild after verify ("feat(eagle3) ...", PR body: rebuild_after_verify; "Add the
  * Eagle3Speculator module", PR body): with verify features v_i (target features at the
  * verify positions N + i, bf16 [B, gamma + 1, 3, n] device) writes the pairs at

@@ -520,6 +520,26 @@ def accept(draft_tok, target_pred, gamma_eff: int | None = None):
     return n, int(target_pred[n])
 
 
+def target_verify(head_bits, norm_bits, hidden, eps: float, rows_per_block: int = 8192):
+    """Greedy verify on the target side ("Add the Eagle3Speculator module for speculative
+    decoding", PR body: target_verify returns, for every window position, the greedy
+    argmax target id; "memra_engine/eagle.rs", ``generate_spec_eagle`` steps 3-4: argmax
+    of the target logits at each position).  logits = head . (RMSNorm(h) * norm) for each
+    hidden row h; ids = the first maximum of each row.  The head is widened to float64
+    rows_per_block vocabulary rows at a time (memory only: each logit is its own dot
+    product).  Returns (logits [..., V], ids [...] int64)."""
+    h = np.asarray(hidden, dtype=np.float64)
+    lead = h.shape[:-1]
+    x = rms_norm(h.reshape(-1, h.shape[-1]), widen_bf16(norm_bits), eps)
+    head = np.asarray(head_bits)
+    V = head.shape[0]
+    logits = np.empty((x.shape[0], V), dtype=np.float64)
+    for r0 in range(0, V, rows_per_block):
+        logits[:, r0:r0 + rows_per_block] = x @ widen_bf16(head[r0:r0 + rows_per_block]).T
+    ids = np.array([argmax_first(l) for l in logits], dtype=np.int64)
+    return logits.reshape(lead + (V,)), ids.reshape(lead)
+
+
 def rebuild_after_verify(dr: Drafter, st: SeqState, n_acc: int, draft_tok, bonus: int,
                          verify_aux_bits) -> SeqState:
     """Teacher-force the accepted prefix into the committed KV and set the next
