@@ -31,6 +31,7 @@ EAGLE3_DEV_TIMEOUT = 16
 
 EXPORTED = (
     "eagle3_version", "eagle3_error_string", "eagle3_workspace_bytes", "eagle3_kv_row_bytes",
+    "eagle3_resolve_rope_dims", "eagle3_config_from_json",
     "eagle3_plan_gamma",
     "eagle3_init", "eagle3_destroy", "eagle3_encode", "eagle3_prefill", "eagle3_draft_chain",
     "eagle3_rewind", "eagle3_accept", "eagle3_verify_greedy", "eagle3_rebuild_after_verify",
@@ -53,9 +54,10 @@ class Config(ctypes.Structure):
                 ("n_ff", ctypes.c_int), ("draft_vocab", ctypes.c_int),
                 ("target_vocab", ctypes.c_int), ("max_batch", ctypes.c_int),
                 ("max_gamma", ctypes.c_int), ("max_cache_len", ctypes.c_int),
-                ("page_size", ctypes.c_int), ("kv_format", ctypes.c_int)]
+                ("page_size", ctypes.c_int), ("flags", ctypes.c_uint), ("kv_format", ctypes.c_int)]
 
 
+EAGLE3_CKPT_NORM_BEFORE_RESIDUAL = 1
 EAGLE3_KV_BF16 = 0
 EAGLE3_KV_Q8_0_Q5_1 = 1
 
@@ -97,6 +99,8 @@ def load() -> ctypes.CDLL:
         "eagle3_error_string": (ctypes.c_char_p, [ci]),
         "eagle3_workspace_bytes": (ctypes.c_size_t, [P(Config)]),
         "eagle3_kv_row_bytes": (ci, [P(Config), P(ctypes.c_size_t), P(ctypes.c_size_t)]),
+        "eagle3_resolve_rope_dims": (ci, [ci, ci, ci, ci, ctypes.c_float]),
+        "eagle3_config_from_json": (ci, [ctypes.c_char_p, P(Config)]),
         "eagle3_plan_gamma": (ci, [ci, ci, ci, cu, P(ci)]),
         "eagle3_init": (ci, [P(Config), P(Weights), vp, ctypes.c_size_t, vp, P(vp)]),
         "eagle3_destroy": (ci, [vp]),
@@ -147,6 +151,22 @@ def eagle3_version() -> int:
 
 def eagle3_workspace_bytes(cfg: Config) -> int:
     return int(load().eagle3_workspace_bytes(ctypes.byref(cfg)))
+
+
+def eagle3_resolve_rope_dims(head_dim: int, rotary_dim: int | None, factor: float | None) -> int:
+    """Rotary width: explicit rotary_dim > partial_rotary_factor * head_dim > full width."""
+    return int(load().eagle3_resolve_rope_dims(int(head_dim), 0 if rotary_dim is None else 1,
+                                               0 if rotary_dim is None else int(rotary_dim),
+                                               0 if factor is None else 1,
+                                               0.0 if factor is None else float(factor)))
+
+
+def eagle3_config_from_json(text: str, cfg: Config | None = None) -> Config:
+    """Drafter shape and flags from a checkpoint config.json text, into cfg (or a new
+    Config whose batch / cache fields are zero)."""
+    cfg = cfg if cfg is not None else Config()
+    _check(load().eagle3_config_from_json(text.encode(), ctypes.byref(cfg)), "eagle3_config_from_json")
+    return cfg
 
 
 def eagle3_kv_row_bytes(cfg: Config):

@@ -23,7 +23,8 @@ constexpr int kMaxGraphs = 16;
 
 struct Layout {
   size_t rope, q, attn_o, part_o, part_ml, attn_cnt, x1, act, gwork, tokwork, am_slot, am_cnt,
-      round_start, geff, status, genc, xp0, xp1, xp2, sumsq, tc_part, tc_cnt, attn_plan, kv_stage, total;
+      round_start, geff, status, genc, xp0, xp1, xp2, sumsq, tc_part, tc_cnt, attn_plan, kv_stage, gres,
+      total;
   size_t tc_items, tc_k, tc_part_elems;
 };
 
@@ -55,6 +56,7 @@ bool cfg_valid(const eagle3_config *c) {
   if (kmax * 4 > kGemvMaxXBytes) return false;
   if ((size_t)c->max_batch * c->n_head_kv > (size_t)kSplitSlots) return false;
   if (c->kv_format != EAGLE3_KV_BF16 && c->kv_format != EAGLE3_KV_Q8_0_Q5_1) return false;
+  if (c->flags & ~EAGLE3_CKPT_NORM_BEFORE_RESIDUAL) return false;
   if (c->kv_format == EAGLE3_KV_Q8_0_Q5_1 && c->head_dim % 32) return false;
   if (attn_unit_keys(c->head_dim, c->n_head / c->n_head_kv, c->page_size, c->kv_format) < 1) return false;
   return true;
@@ -109,6 +111,7 @@ Layout make_layout(const eagle3_config &c) {
   L.attn_plan = take((size_t)c.max_gamma * (B + 1) * 4);  // attention unit prefix per step
   // quantized KV: the projection's float32 k / v before kv_quant writes the blocks
   L.kv_stage = take(c.kv_format == EAGLE3_KV_Q8_0_Q5_1 ? L.tc_items * 2 * c.n_head_kv * c.head_dim * 4 : 0);
+  L.gres = take(c.flags & EAGLE3_CKPT_NORM_BEFORE_RESIDUAL ? B * n * 4 : 0);  // normed residual
   L.total = align_up(off, 256);
   return L;
 }
@@ -174,6 +177,7 @@ struct eagle3_ctx {
   // KV storage format: bf16, or q8_0 K / q5_1 V written by kv_quant from kv_stage
   int kv_q, k_row, v_row;
   float *kv_stage;
+  float *gres;  // norm_before_residual: RMSNorm(g) * hidden_norm of the step, [B, n]
   uint16_t *xp0, *xp1, *xp2;  // the three bf16 parts of x
   float *sumsq, *tc_part;
   unsigned *tc_cnt;
@@ -440,14 +444,22 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     ap.status = ctx->status;
     if ((e = launched(ctx, st, attn_launch(ap, ctx->num_sms, st, pdl), PH_ATTN)) != cudaSuccess) return e;
 
-    // o_proj + residual (pre-norm g of this step)
+    // o_proj + residual: the pre-norm g of this step, or RMSNorm(g) * hidden_norm for
+    // checkpoints with norm_before_residual
+    const float *g_step = j == 0 ? a.bnd->g : ctx->gwork;
+    if (ctx->gres) {
+      if ((e = launched(ctx, st, launch_res_norm(a.B, n, c.rms_eps, g_step, ctx->w.hidden_norm, ctx->gres, st),
+                        PH_SMALL)) != cudaSuccess)
+        return e;
+      g_step = ctx->gres;
+    }
     p = base_params(ctx);
     p.mode = GM_O;
     p.rows = n;
     p.K = qr;
     p.w0 = ctx->w.o;
     p.xf = ctx->attn_o;
-    p.res = j == 0 ? a.bnd->g : ctx->gwork;
+    p.res = g_step;
     p.out_f = ctx->x1;
     if ((e = gemv_items(ctx, p, a.B, st, pdl)) != cudaSuccess) return e;
 
@@ -683,6 +695,7 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
     ctx->v_row = (int)vr;
   }
   ctx->kv_stage = ctx->kv_q ? reinterpret_cast<float *>(b + L.kv_stage) : nullptr;
+  ctx->gres = (cfg->flags & EAGLE3_CKPT_NORM_BEFORE_RESIDUAL) ? reinterpret_cast<float *>(b + L.gres) : nullptr;
   ctx->xp0 = reinterpret_cast<uint16_t *>(b + L.xp0);
   ctx->xp1 = reinterpret_cast<uint16_t *>(b + L.xp1);
   ctx->xp2 = reinterpret_cast<uint16_t *>(b + L.xp2);

@@ -167,6 +167,35 @@ __global__ void prefill_finish_kernel(int b, int n_embd, int kv_len_value, const
   }
 }
 
+// Residual of checkpoints with norm_before_residual: out[b] = RMSNorm(g[b]) * w (w the
+// bf16 hidden_norm gain), one CTA per sequence.
+__global__ void __launch_bounds__(256) res_norm_kernel(int n, float eps, const float *g, const uint16_t *w,
+                                                       float *out) {
+  __shared__ float part[8];
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const float *x = g + (size_t)b * n;
+  float s = 0.f;
+  for (int i = tid; i < n; i += 256) s = fmaf(x[i], x[i], s);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((tid & 31) == 0) part[tid >> 5] = s;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) t += part[i];  // the same order in every thread
+  const float scale = rsqrtf(t / (float)n + eps);
+  for (int i = tid; i < n; i += 256) out[(size_t)b * n + i] = x[i] * scale * bf1(w[i]);
+}
+
+cudaError_t launch_res_norm(int B, int n, float eps, const float *g, const uint16_t *w, float *out,
+                            cudaStream_t st) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = small_cfg(B, 256, st, true, attr);
+  return cudaLaunchKernelEx(&cfg, res_norm_kernel, n, eps, g, w, out);
+}
+
 cudaError_t launch_chain_begin(int B, int gamma, unsigned flags, int max_cache_len,
                                const int32_t *kv_len, int32_t *round_start, int32_t *geff,
                                int32_t *geff_out, int *status, int unit_keys, int32_t *unit_pre,

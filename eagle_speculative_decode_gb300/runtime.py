@@ -27,7 +27,7 @@ class DraftModel:
 
     def __init__(self, weights: DrafterWeights, max_batch: int, max_gamma: int,
                  max_cache_len: int, page_size: int, device="cuda", stream=None,
-                 kv_format: str = "bf16"):
+                 kv_format: str = "bf16", flags: int = 0):
         if not torch.cuda.is_available():
             raise RuntimeError("DraftModel needs a CUDA device")
         self.geom: Geometry = weights.geom
@@ -39,7 +39,7 @@ class DraftModel:
                             draft_vocab=g.draft_vocab, target_vocab=g.target_vocab,
                             max_batch=max_batch, max_gamma=max_gamma,
                             max_cache_len=max_cache_len, page_size=page_size,
-                            kv_format=self.KV_FORMATS[kv_format])
+                            flags=flags, kv_format=self.KV_FORMATS[kv_format])
         self.kv_format = kv_format
         self.max_batch, self.max_gamma = max_batch, max_gamma
         self.max_cache_len, self.page_size = max_cache_len, page_size

@@ -80,6 +80,14 @@ typedef struct CUstream_st *eagle3_stream_t;
 #define EAGLE3_KV_BF16 0
 #define EAGLE3_KV_Q8_0_Q5_1 1
 
+/* Checkpoint flags (eagle3_config.flags) of the EAGLE-3 layer's op sequence
+ * ("memra_engine/eagle.rs", module doc: this checkpoint has norm_before_residual,
+ * norm_before_fc, fc_norm and norm_output all false, and its residual is the PRE-norm g).
+ *   EAGLE3_CKPT_NORM_BEFORE_RESIDUAL: the attention residual is the normed
+ *   RMSNorm(g) * hidden_norm instead of g (x1 = o_proj(attn) + RMSNorm(g) * hidden_norm).
+ * The other three flags are not supported (eagle3_config_from_json refuses them). */
+#define EAGLE3_CKPT_NORM_BEFORE_RESIDUAL 1u
+
 /* eagle3_draft_chain flags. */
 #define EAGLE3_SHRINK_GAMMA 1u      /* shrink gamma per sequence to max_cache_len - kv_len - 1 */
 
@@ -101,6 +109,7 @@ typedef struct {
   int max_gamma;       /* largest chain length                                       */
   int max_cache_len;   /* KV positions per sequence (0 .. max_cache_len - 1)         */
   int page_size;       /* KV positions per page                                      */
+  unsigned flags;      /* EAGLE3_CKPT_* checkpoint flags, 0 for the eagle.rs checkpoint      */
   int kv_format;       /* EAGLE3_KV_BF16 (default) or EAGLE3_KV_Q8_0_Q5_1; quantized pools
                         * are read a page-aligned run of keys at a time, so that run's K and
                         * V bytes must be multiples of 16 (head_dim 64: page_size % 4 == 0;
@@ -157,6 +166,28 @@ size_t eagle3_workspace_bytes(const eagle3_config *cfg);
  * head_dim / 32 * 24 (V) for q8_0 / q5_1.  Returns EAGLE3_ERR_INVALID_ARG for an invalid
  * cfg or null outputs.  Host-only arithmetic. */
 int eagle3_kv_row_bytes(const eagle3_config *cfg, size_t *k_row, size_t *v_row);
+
+/* Rotary width of a drafter config ("memra_engine/eagle.rs", EagleConfig::rope_dim_count
+ * and its tests on the eagle3-qwen35-9b config): an explicit rotary dim count (has_rotary_dim,
+ * even, 2..head_dim) wins over a fraction of head_dim (has_factor), which wins over the full
+ * width; a fraction outside (0, 1] or one that does not give a whole, even number of dims
+ * takes the full width, never a rotation wider than the head.  Returns 0 for an odd or
+ * non-positive head_dim.  Host-only arithmetic. */
+int eagle3_resolve_rope_dims(int head_dim, int has_rotary_dim, int rotary_dim, int has_factor,
+                             float factor);
+
+/* Drafter shape from the text of a checkpoint's config.json ("memra_engine/eagle.rs",
+ * EagleConfig::from_json_str): n_embd (hidden_size), n_head (num_attention_heads), n_head_kv
+ * (num_key_value_heads), head_dim, n_ff (intermediate_size), draft_vocab
+ * (draft_vocab_size), target_vocab (vocab_size), rope_dims (eagle3_resolve_rope_dims of
+ * rotary_dim and partial_rotary_factor, found top-level or under rope_parameters),
+ * rope_theta (default 10000), rms_eps (rms_norm_eps, default 1e-6) and flags
+ * (norm_before_residual).  max_batch, max_gamma, max_cache_len, page_size and kv_format are
+ * left as the caller set them.  EAGLE3_ERR_INVALID_ARG when a required key is missing or
+ * not a positive integer, or the aux-layer list is malformed; EAGLE3_ERR_UNSUPPORTED when
+ * norm_before_fc, fc_norm or norm_output is true or the aux-layer list does not hold three
+ * ids (fc takes three features).  cfg is written only on success.  Host-only. */
+int eagle3_config_from_json(const char *json, eagle3_config *cfg);
 
 /* Capacity rule ("feat(eagle3) ...", review comment on rebuild_after_verify committing
  * k + 1 entries): a chain of gamma drafts at committed length kv_len needs

@@ -240,13 +240,18 @@ def store_v(x, kv_format: str) -> np.ndarray:
 class Drafter:
     """float64 view of the drafter weights (one decoder layer + fc + lm_head + d2t)."""
 
-    def __init__(self, geom, bits: dict, d2t, kv_format: str = "bf16"):
+    def __init__(self, geom, bits: dict, d2t, kv_format: str = "bf16",
+                 norm_before_residual: bool = False):
+        """norm_before_residual: the checkpoint flag of "memra_engine/eagle.rs" (module
+        doc, false for its checkpoint, whose attention residual is the pre-norm g); when
+        true the residual is the normed RMSNorm(g) * hidden_norm instead."""
         if kv_format not in KV_FORMATS:
             raise ValueError(f"kv_format must be one of {KV_FORMATS}")
         if kv_format != "bf16" and geom.head_dim % QK:
             raise ValueError("quantized KV needs head_dim % 32 == 0")
         self.geom = geom
         self.kv_format = kv_format
+        self.norm_before_residual = bool(norm_before_residual)
         self.w = {name: widen_bf16(b) for name, b in bits.items() if name != "embed"}
         self._embed_bits = bits["embed"]
         self.d2t = np.asarray(d2t, dtype=np.int64)
@@ -334,7 +339,8 @@ def layer_after_attention(dr: Drafter, g: np.ndarray, attn: np.ndarray):
     """o_proj + residual (pre-norm g), post-attention RMSNorm, SwiGLU MLP, fused-add
     residual, final RMSNorm and lm_head ("memra_engine/eagle.rs", Op-sequence)."""
     w, eps = dr.w, dr.geom.rms_eps
-    x1 = w["o"] @ attn + g
+    res = rms_norm(g, w["hidden_norm"], eps) if dr.norm_before_residual else g
+    x1 = w["o"] @ attn + res
     z = rms_norm(x1, w["post_norm"], eps)
     act = silu(w["gate"] @ z) * (w["up"] @ z)
     gsum = w["down"] @ act + x1

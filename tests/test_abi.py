@@ -25,7 +25,7 @@ def _cfg(g=synth.FULL, **kw):
     c = dict(n_embd=g.n_embd, n_head=g.n_head, n_head_kv=g.n_head_kv, head_dim=g.head_dim,
              rope_dims=g.rope_dims, rope_theta=g.rope_theta, rms_eps=g.rms_eps, n_ff=g.n_ff,
              draft_vocab=g.draft_vocab, target_vocab=g.target_vocab, max_batch=64, max_gamma=8,
-             max_cache_len=8192, page_size=64, kv_format=Bd.EAGLE3_KV_BF16)
+             max_cache_len=8192, page_size=64, flags=0, kv_format=Bd.EAGLE3_KV_BF16)
     c.update(kw)
     return Bd.Config(**c)
 
@@ -60,7 +60,8 @@ def test_kv_row_bytes_per_format(built_lib):
 def test_invalid_configs_are_refused(built_lib):
     assert Bd.eagle3_workspace_bytes(_cfg()) > 0
     assert Bd.eagle3_workspace_bytes(_cfg(kv_format=Bd.EAGLE3_KV_Q8_0_Q5_1)) > 0
-    for bad in (dict(kv_format=2), dict(kv_format=-1), dict(n_head=15), dict(max_gamma=0),
+    assert Bd.eagle3_workspace_bytes(_cfg(flags=Bd.EAGLE3_CKPT_NORM_BEFORE_RESIDUAL)) > 0
+    for bad in (dict(kv_format=2), dict(kv_format=-1), dict(flags=2), dict(flags=0x80000000), dict(n_head=15), dict(max_gamma=0),
                 dict(max_gamma=65), dict(page_size=0), dict(max_cache_len=1), dict(n_embd=4100),
                 dict(rope_dims=3), dict(rope_theta=0.0), dict(draft_vocab=0)):
         assert Bd.eagle3_workspace_bytes(_cfg(**bad)) == 0, bad

@@ -513,3 +513,20 @@ def test_batched_kv_entries_equal_one_by_one():
         k1, v1 = O.kv_entry(dr, int(toks[i]), gs[i], int(pos[i]))
         assert np.max(np.abs(kb[i] - k1)) <= 2.0 ** -8 * np.max(np.abs(k1))
         assert np.max(np.abs(vb[i] - v1)) <= 2.0 ** -8 * np.max(np.abs(v1))
+
+
+def test_norm_before_residual_flag_uses_the_normed_g():
+    """With the checkpoint flag norm_before_residual the attention residual is
+    RMSNorm(g) * hidden_norm: with W_o = 0 and W_gate = 0, x1 = gsum = the normed g.  A g
+    of equal-magnitude entries normalises to its signs (eps 1e-6 changes the scale by
+    about 5e-7 relative at magnitude 1); gains of 2 on dims 0 and 5 double those dims."""
+    dr = micro_drafter(hidden_norm=np.array([2.0, 1, 1, 1, 1, 2.0, 1, 1]))
+    dr.norm_before_residual = True
+    g_vec = np.array([1.0, -1.0, 1.0, 1.0, -1.0, -1.0, 1.0, 1.0])
+    so = O.draft_step(dr, 3, g_vec, np.zeros((0, 1, 4)), np.zeros((0, 1, 4)), 0)
+    want = np.array([2.0, -1.0, 1.0, 1.0, -1.0, -2.0, 1.0, 1.0]) / math.sqrt(1.0 + 1e-6)
+    np.testing.assert_allclose(so.x1, want, rtol=1e-15)
+    np.testing.assert_array_equal(so.g_next, so.x1)
+    dr.norm_before_residual = False
+    so = O.draft_step(dr, 3, g_vec, np.zeros((0, 1, 4)), np.zeros((0, 1, 4)), 0)
+    np.testing.assert_array_equal(so.x1, g_vec)
