@@ -83,11 +83,14 @@ def profiled_traffic(config: str, kind: str, kv_format: str = "bf16"):
     return e["bytes"] if h.hexdigest() == e["sha256"] else None
 
 
-def kernel_label(kind: str, batch: int) -> str:
-    """Name of the kernel that runs a phase at this batch (projections of three or more
-    items run on the tensor cores, smaller ones on the CUDA-core GEMV)."""
+def kernel_label(kind: str, batch: int, weights: str = "bf16") -> str:
+    """Name of the kernel that runs a phase at this batch (bf16 projections of three or
+    more items run on the tensor cores, smaller ones and every INT4 one on the CUDA-core
+    GEMV)."""
     if kind == "attn":
         return "attention"
+    if weights == "int4":
+        return f"{kind} INT4 GEMV"
     return f"{kind} tcgen05 GEMM" if batch >= 3 else f"{kind} GEMV"
 
 
@@ -164,40 +167,54 @@ def kv_bytes_per_position(geo, kv_format):
     return geo.kv_rows // 32 * (34 + 24)
 
 
-def phase_bytes(geo, B, ctx_len, kv_format="bf16"):
+def matrix_bytes(rows, K, weights="bf16"):
+    """Bytes of a [rows, K] projection: bf16, or INT4 codes plus the (scale, zero) rows
+    (one bf16 pair per 128 inputs, rows padded to a multiple of 4 pairs)."""
+    if weights == "bf16":
+        return rows * K * 2
+    return rows * (K // 2 + ((K // 128 + 3) // 4 * 4) * 4)
+
+
+def phase_bytes(geo, B, ctx_len, kv_format="bf16", weights="bf16"):
     """Bytes each kernel of one draft step must move (weights once per step for all B
     sequences, plus per-sequence activations and KV)."""
     n, F, qr, kr = geo.n_embd, geo.n_ff, geo.q_rows, geo.kv_rows
     act = 4 * B
     kvp = kv_bytes_per_position(geo, kv_format)
+    mb = lambda rows, K: matrix_bytes(rows, K, weights)  # noqa: E731
     return {
-        "qkv": (qr + 2 * kr) * 2 * n * 2 + B * (2 * n + 4 * n) + 3 * n * 2 + B * kvp + act * qr,
+        "qkv": mb(qr + 2 * kr, 2 * n) + B * (2 * n + 4 * n) + 3 * n * 2 + B * kvp + act * qr,
         "attn": B * (ctx_len * kvp + 2 * qr * 4),
-        "o": n * qr * 2 + act * (qr + 2 * n),
-        "gateup": 2 * F * n * 2 + act * (n + F) + n * 2,
-        "down": n * F * 2 + act * (F + 2 * n),
-        "lmhead": geo.draft_vocab * n * 2 + act * n + n * 2 + B * 8,
+        "o": mb(n, qr) + act * (qr + 2 * n),
+        "gateup": mb(2 * F, n) + act * (n + F) + n * 2,
+        "down": mb(n, F) + act * (F + 2 * n),
+        "lmhead": mb(geo.draft_vocab, n) + act * n + n * 2 + B * 8,
     }
 
 
-def round_bytes(geo, B, gamma, ctx_len, kv_format="bf16"):
-    ph = phase_bytes(geo, B, ctx_len, kv_format)
+def round_bytes(geo, B, gamma, ctx_len, kv_format="bf16", weights="bf16"):
+    ph = phase_bytes(geo, B, ctx_len, kv_format, weights)
     chain = gamma * sum(ph.values())
-    rebuild = 3 * geo.n_embd * geo.n_embd * 2 + 2 * geo.kv_rows * 2 * geo.n_embd * 2 \
+    rebuild = 3 * geo.n_embd * geo.n_embd * 2 + matrix_bytes(2 * geo.kv_rows, 2 * geo.n_embd, weights) \
         + B * (gamma + 1) * (3 * geo.n_embd * 2 + geo.n_embd * 4)
     return chain + rebuild
 
 
+def make_bench_weights(geo, weights):
+    from eagle_speculative_decode_gb300 import synth
+    return synth.make_int4_weights(geo, seed=0) if weights == "int4" else synth.make_weights(geo, seed=0)
+
+
 # ------------------------------------------------------------------ oracle timing
-def oracle_round_rate(geo_name, gamma, rounds, seed=0, kv_format="bf16"):
+def oracle_round_rate(geo_name, gamma, rounds, seed=0, kv_format="bf16", weights="bf16"):
     """Times the CPU oracle on one sequence: `rounds` chains of gamma draft steps from a
     32-token prefilled state at the benchmark's geometry.  Returns (draft tok/s, seconds,
     sample description)."""
     from eagle_speculative_decode_gb300 import synth
     from oracle import eagle3_oracle as O
     geo = synth.GEOMETRIES[geo_name]
-    wts = synth.make_weights(geo, seed=seed)
-    dr = O.Drafter(geo, wts.bits, wts.d2t, kv_format=kv_format)
+    wts = make_bench_weights(geo, weights)
+    dr = O.Drafter(geo, wts.bits, wts.d2t, kv_format=kv_format, int4=wts.int4)
     P = 32
     toks = synth.make_tokens((P + 1,), geo, seed + 1)
     aux = synth.make_aux((P,), geo, seed + 1)
@@ -207,7 +224,7 @@ def oracle_round_rate(geo_name, gamma, rounds, seed=0, kv_format="bf16"):
         O.draft_chain(dr, st, gamma)
     dt = time.perf_counter() - t0
     desc = (f"{rounds} chain(s) of {gamma} draft steps of one sequence from a {P}-token "
-            f"prefilled state, {geo_name} geometry, {kv_format} KV, float64 numpy oracle")
+            f"prefilled state, {geo_name} geometry, {weights} weights, {kv_format} KV, float64 numpy oracle")
     return rounds * gamma / dt, dt, desc
 
 
@@ -258,8 +275,8 @@ def run_reference(args, cfg):
     from eagle_speculative_decode_gb300 import synth  # noqa: F401  (generators only)
     from oracle import eagle3_oracle as O
     geo = synth.GEOMETRIES[cfg["geom"]]
-    wts = synth.make_weights(geo, seed=0)
-    dr = O.Drafter(geo, wts.bits, wts.d2t, kv_format=args.kv_format)
+    wts = make_bench_weights(geo, args.weights)
+    dr = O.Drafter(geo, wts.bits, wts.d2t, kv_format=args.kv_format, int4=wts.int4)
     P = 32
     toks = synth.make_tokens((P + 1,), geo, 1)
     aux = synth.make_aux((P,), geo, 1)
@@ -279,7 +296,7 @@ def run_reference(args, cfg):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg["workload"], "kv_format": args.kv_format},
+            "config": {"workload": cfg["workload"], "kv_format": args.kv_format, "weights": args.weights},
             "cpu_baseline": {"value": value, "unit": "draft tokens/s", "cores": os.cpu_count(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "draft tokens/s", "h2d_bytes_per_step": 0,
@@ -307,7 +324,7 @@ def run_mine(args, cfg):
     geo = synth.GEOMETRIES[cfg["geom"]]
     B, gamma, ps = cfg["B"], cfg["gamma"], cfg["page_size"]
     seed = 1000 * rank
-    wts = synth.make_weights(geo, seed=0)
+    wts = make_bench_weights(geo, args.weights)
     lo, hi = cfg["prompt"]
     lens = synth.ragged_lengths(B, lo, hi, seed=seed + 1) if lo != hi else np.full(B, lo, np.int32)
     rounds = args.warmup + args.steps + args.e2e_steps + args.phase_rounds + 2
@@ -430,14 +447,14 @@ def run_mine(args, cfg):
     names = {1: "qkv", 2: "attn", 3: "o", 4: "gateup", 5: "down", 6: "lmhead"}
     # per launch, per kind: average microseconds (one launch per kind per step when B fits)
     kern_us = {names[k]: float(np.mean(v)) for k, v in per_label.items() if k in names}
-    pb = phase_bytes(geo, B, int(mean_ctx), args.kv_format)
+    pb = phase_bytes(geo, B, int(mean_ctx), args.kv_format, args.weights)
     hbm_peak, tf_peak, peak_src = load_peaks()
     launches_per_kind = {k: max(1, len(per_label.get(kk, [])) // max(1, args.phase_rounds * gamma))
                          for kk, k in names.items()}
     dominant = max(kern_us, key=lambda k: kern_us[k] * launches_per_kind[k]) if kern_us else "lmhead"
     dom_bytes = pb[dominant] / launches_per_kind[dominant]
     achieved = dom_bytes / (kern_us[dominant] * 1e-6) / 1e9 if kern_us else None
-    rb = round_bytes(geo, B, gamma, int(mean_ctx), args.kv_format)
+    rb = round_bytes(geo, B, gamma, int(mean_ctx), args.kv_format, args.weights)
     step_frac = (rb / (ms_per_step * 1e-3) / 1e9) / hbm_peak
 
     # ---- end to end through the C ABI with host buffers
@@ -499,7 +516,7 @@ def run_mine(args, cfg):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
             rate, secs, desc = oracle_round_rate(cfg["geom"], gamma, args.cpu_rounds,
-                                                 kv_format=args.kv_format)
+                                                 kv_format=args.kv_format, weights=args.weights)
             cpu = {"value": rate, "unit": "draft tokens/s", "cores": os.cpu_count(),
                    "kind": "oracle", "sample": desc, "seconds": secs}
         except Exception as e:  # reported, not fatal
@@ -516,10 +533,11 @@ def run_mine(args, cfg):
         "config": {"workload": cfg["workload"], "name": args.config, "batch": B, "gamma": gamma,
                    "prompt": [int(lens.min()), int(lens.max())],
                    "mean_context": round(mean_ctx, 1), "page_size": ps,
-                   "kv_format": args.kv_format,
-                   "storage": ("bf16 weights and KV" if args.kv_format == "bf16" else
-                               "bf16 weights, q8_0 K / q5_1 V cache") +
-                              ", float32 activations and accumulation",
+                   "kv_format": args.kv_format, "weights": args.weights,
+                   "storage": ("bf16 weights" if args.weights == "bf16" else
+                               "INT4 projections (128-wide groups, bf16 scale and zero), bf16 fc / norms / embedding")
+                              + (", bf16 KV" if args.kv_format == "bf16" else ", q8_0 K / q5_1 V cache")
+                              + ", float32 activations and accumulation",
                    "l2": "inputs larger than L2: 0.8 GB of weights streamed per draft step",
                    "step": "chain of gamma draft steps + rewind + accept + rebuild (encode of "
                            "gamma+1 verify features, k/v teacher forcing)",
@@ -529,10 +547,11 @@ def run_mine(args, cfg):
         "step_roofline": {"bytes_per_step": rb, "achieved_gbs": rb / (ms_per_step * 1e-3) / 1e9,
                           "peak_gbs": hbm_peak, "frac": step_frac,
                           "note": f"algorithmic bytes of the whole round / round time, of {peak_src}"},
-        "roofline": {"bound": "hbm", "kernel": kernel_label(dominant, B),
+        "roofline": {"bound": "hbm", "kernel": kernel_label(dominant, B, args.weights),
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": (achieved / hbm_peak) if achieved else None,
-                     "traffic": profiled_traffic(args.config, dominant, args.kv_format),
+                     "traffic": profiled_traffic(args.config, dominant, args.kv_format)
+                     if args.weights == "bf16" else None,
                      "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
                      "bytes_per_launch": dom_bytes, "us_per_launch": kern_us.get(dominant)},
         "kernel_us": kern_us,
@@ -565,6 +584,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--verify-steps", type=int, default=10,
                     help="timed calls of the target-side greedy verify (0: skip)")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "int4"],
+                    help="drafter projection weights: bf16, or INT4 codes with bf16 group scale / zero")
     ap.add_argument("--kv-format", default="bf16", choices=["bf16", "q8_0/q5_1"],
                     help="drafter KV cache storage: bf16, or q8_0 keys / q5_1 values")
     ap.add_argument("--tc-min-items", type=int, default=0,

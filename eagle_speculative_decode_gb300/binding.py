@@ -54,10 +54,13 @@ class Config(ctypes.Structure):
                 ("n_ff", ctypes.c_int), ("draft_vocab", ctypes.c_int),
                 ("target_vocab", ctypes.c_int), ("max_batch", ctypes.c_int),
                 ("max_gamma", ctypes.c_int), ("max_cache_len", ctypes.c_int),
-                ("page_size", ctypes.c_int), ("flags", ctypes.c_uint), ("kv_format", ctypes.c_int)]
+                ("page_size", ctypes.c_int), ("flags", ctypes.c_uint), ("kv_format", ctypes.c_int),
+                ("weight_format", ctypes.c_int)]
 
 
 EAGLE3_CKPT_NORM_BEFORE_RESIDUAL = 1
+EAGLE3_W_BF16 = 0
+EAGLE3_W_INT4_G128 = 1
 EAGLE3_KV_BF16 = 0
 EAGLE3_KV_Q8_0_Q5_1 = 1
 
@@ -66,8 +69,11 @@ WEIGHT_FIELDS = ("fc", "in_norm", "hidden_norm", "q", "k", "v", "o", "post_norm"
                  "down", "final_norm", "lm_head", "embed", "d2t")
 
 
+INT4_FIELDS = ("q_sz", "k_sz", "v_sz", "o_sz", "gate_sz", "up_sz", "down_sz", "lm_head_sz")
+
+
 class Weights(ctypes.Structure):
-    _fields_ = [(f, ctypes.c_void_p) for f in WEIGHT_FIELDS]
+    _fields_ = [(f, ctypes.c_void_p) for f in WEIGHT_FIELDS + INT4_FIELDS]
 
 
 class KV(ctypes.Structure):

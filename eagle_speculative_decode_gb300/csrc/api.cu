@@ -57,6 +57,10 @@ bool cfg_valid(const eagle3_config *c) {
   if ((size_t)c->max_batch * c->n_head_kv > (size_t)kSplitSlots) return false;
   if (c->kv_format != EAGLE3_KV_BF16 && c->kv_format != EAGLE3_KV_Q8_0_Q5_1) return false;
   if (c->flags & ~EAGLE3_CKPT_NORM_BEFORE_RESIDUAL) return false;
+  if (c->weight_format != EAGLE3_W_BF16 && c->weight_format != EAGLE3_W_INT4_G128) return false;
+  if (c->weight_format == EAGLE3_W_INT4_G128 &&
+      (c->n_embd % 128 || (c->n_head * c->head_dim) % 128 || c->n_ff % 128))
+    return false;
   if (c->kv_format == EAGLE3_KV_Q8_0_Q5_1 && c->head_dim % 32) return false;
   if (attn_unit_keys(c->head_dim, c->n_head / c->n_head_kv, c->page_size, c->kv_format) < 1) return false;
   return true;
@@ -178,6 +182,7 @@ struct eagle3_ctx {
   int kv_q, k_row, v_row;
   float *kv_stage;
   float *gres;  // norm_before_residual: RMSNorm(g) * hidden_norm of the step, [B, n]
+  int q4;       // INT4 projection weights (EAGLE3_W_INT4_G128)
   uint16_t *xp0, *xp1, *xp2;  // the three bf16 parts of x
   float *sumsq, *tc_part;
   unsigned *tc_cnt;
@@ -314,6 +319,7 @@ cudaError_t tc_items(eagle3_ctx *ctx, const GemvParams &p, int items, cudaStream
 
 bool use_tc(const eagle3_ctx *ctx, const GemvParams &p, int items) {
   if (!ctx->tc_ok || items < ctx->tc_min_items) return false;
+  if (p.sz0) return false;  // INT4 weights run on the GEMV
   if (p.mode != GM_ENCODE && (size_t)items > ctx->L.tc_items) return false;
   if (p.mode != GM_ENCODE && p.K > kTcPrepMaxK) return false;  // the activation split's limit
   return true;
@@ -333,7 +339,7 @@ cudaError_t qkv_items(eagle3_ctx *ctx, GemvParams p, int items, cudaStream_t st,
 // Launch a GEMV over `items` activation rows in as many launches as shared memory needs.
 cudaError_t gemv_items(eagle3_ctx *ctx, GemvParams p, int items, cudaStream_t st, bool pdl) {
   if (use_tc(ctx, p, items)) return tc_items(ctx, p, items, st, pdl);
-  const int nb = gemv_items_per_launch(p.mode, p.K, items);
+  const int nb = gemv_items_per_launch(p, items, ctx->num_sms);
   const int label = (p.mode == GM_QKV && p.row_base > 0) ? PH_KV : gemv_label(p.mode);
   for (int i0 = 0; i0 < items; i0 += nb) {
     p.item0 = i0;
@@ -357,6 +363,25 @@ cudaError_t enqueue_encode(eagle3_ctx *ctx, const uint16_t *aux, int M, float *g
   return gemv_items(ctx, p, M, st, pdl);
 }
 
+// (scale, zero) pairs per INT4 weight row: one per 128 inputs, rounded up to 4 (16 bytes).
+int q4_sz_stride(int K) { return (K / 128 + 3) / 4 * 4; }
+
+// Weight operands of a projection (p.K set): bf16 rows, or INT4 codes with their
+// (scale, zero) rows.
+void set_weights(const eagle3_ctx *ctx, GemvParams &p, const uint16_t *w0, const uint32_t *s0,
+                 const uint16_t *w1 = nullptr, const uint32_t *s1 = nullptr, const uint16_t *w2 = nullptr,
+                 const uint32_t *s2 = nullptr) {
+  p.w0 = w0;
+  p.w1 = w1;
+  p.w2 = w2;
+  if (ctx->q4) {
+    p.sz0 = s0;
+    p.sz1 = s1;
+    p.sz2 = s2;
+    p.sz_stride = q4_sz_stride(p.K);
+  }
+}
+
 void kv_only_params(const eagle3_ctx *ctx, const eagle3_kv *kv, GemvParams &p) {
   const eagle3_config &c = ctx->c;
   set_kv(p, kv);
@@ -364,9 +389,7 @@ void kv_only_params(const eagle3_ctx *ctx, const eagle3_kv *kv, GemvParams &p) {
   p.row_base = c.n_head * c.head_dim;
   p.rows = 2 * c.n_head_kv * c.head_dim;
   p.K = 2 * c.n_embd;
-  p.w0 = ctx->w.q;
-  p.w1 = ctx->w.k;
-  p.w2 = ctx->w.v;
+  set_weights(ctx, p, ctx->w.q, ctx->w.q_sz, ctx->w.k, ctx->w.k_sz, ctx->w.v, ctx->w.v_sz);
   p.norm0 = ctx->w.in_norm;
   p.norm1 = ctx->w.hidden_norm;
 }
@@ -399,9 +422,7 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     p.rows = qr + 2 * kr;
     p.row_base = 0;
     p.K = 2 * n;
-    p.w0 = ctx->w.q;
-    p.w1 = ctx->w.k;
-    p.w2 = ctx->w.v;
+    set_weights(ctx, p, ctx->w.q, ctx->w.q_sz, ctx->w.k, ctx->w.k_sz, ctx->w.v, ctx->w.v_sz);
     p.norm0 = ctx->w.in_norm;
     p.norm1 = ctx->w.hidden_norm;
     p.pairs.kind = PAIR_CHAIN;
@@ -457,7 +478,7 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     p.mode = GM_O;
     p.rows = n;
     p.K = qr;
-    p.w0 = ctx->w.o;
+    set_weights(ctx, p, ctx->w.o, ctx->w.o_sz);
     p.xf = ctx->attn_o;
     p.res = g_step;
     p.out_f = ctx->x1;
@@ -468,8 +489,7 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     p.mode = GM_GATEUP;
     p.rows = 2 * c.n_ff;
     p.K = n;
-    p.w0 = ctx->w.gate;
-    p.w1 = ctx->w.up;
+    set_weights(ctx, p, ctx->w.gate, ctx->w.gate_sz, ctx->w.up, ctx->w.up_sz);
     p.xf = ctx->x1;
     p.norm0 = ctx->w.post_norm;
     p.out_f = ctx->act;
@@ -480,7 +500,7 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     p.mode = GM_DOWN;
     p.rows = n;
     p.K = c.n_ff;
-    p.w0 = ctx->w.down;
+    set_weights(ctx, p, ctx->w.down, ctx->w.down_sz);
     p.xf = ctx->act;
     p.res = ctx->x1;
     p.out_f = ctx->gwork;
@@ -494,7 +514,7 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     p.mode = GM_LMHEAD;
     p.rows = c.draft_vocab;
     p.K = n;
-    p.w0 = ctx->w.lm_head;
+    set_weights(ctx, p, ctx->w.lm_head, ctx->w.lm_head_sz);
     p.xf = ctx->gwork;
     p.norm0 = ctx->w.final_norm;
     p.am_slot = ctx->am_slot;
@@ -638,6 +658,11 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
   if (!cfg_valid(cfg)) return EAGLE3_ERR_UNSUPPORTED;
   const void *wp[] = {w->fc, w->in_norm, w->hidden_norm, w->q, w->k, w->v, w->o, w->post_norm,
                       w->gate, w->up, w->down, w->final_norm, w->lm_head, w->embed, w->d2t};
+  if (cfg->weight_format == EAGLE3_W_INT4_G128) {
+    const void *sp[] = {w->q_sz, w->k_sz, w->v_sz, w->o_sz, w->gate_sz, w->up_sz, w->down_sz, w->lm_head_sz};
+    for (const void *p : sp)
+      if (!aligned16(p)) return EAGLE3_ERR_INVALID_ARG;
+  }
   for (const void *p : wp)
     if (!aligned16(p)) return EAGLE3_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return EAGLE3_ERR_INVALID_ARG;
@@ -695,6 +720,7 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
     ctx->v_row = (int)vr;
   }
   ctx->kv_stage = ctx->kv_q ? reinterpret_cast<float *>(b + L.kv_stage) : nullptr;
+  ctx->q4 = cfg->weight_format == EAGLE3_W_INT4_G128 ? 1 : 0;
   ctx->gres = (cfg->flags & EAGLE3_CKPT_NORM_BEFORE_RESIDUAL) ? reinterpret_cast<float *>(b + L.gres) : nullptr;
   ctx->xp0 = reinterpret_cast<uint16_t *>(b + L.xp0);
   ctx->xp1 = reinterpret_cast<uint16_t *>(b + L.xp1);

@@ -208,8 +208,11 @@ struct GemvParams {
   int item0;      // global index of item 0
   int n_embd, n_head, n_head_kv, head_dim, rope_dims, n_ff, draft_vocab, target_vocab;
   float eps;
-  // weights
+  // weights: bf16 rows, or (sz0 non-null) INT4 code rows of K / 2 bytes with the
+  // (scale, zero) bf16 pairs of each 128-wide k group in sz rows of sz_stride pairs
   const uint16_t *w0, *w1, *w2;
+  const uint32_t *sz0, *sz1, *sz2;
+  int sz_stride;
   const uint16_t *norm0, *norm1;
   const uint16_t *embed;
   // plain inputs

@@ -9,27 +9,47 @@
 
 namespace e3 {
 
+// Weight matrix (0: w0, 1: w1, 2: w2) and row of logical row lr of a mode.
+struct RowRef {
+  int m;
+  size_t row;
+};
+
 template <int MODE>
-__device__ __forceinline__ const uint16_t *row_ptr(const GemvParams &p, int lr) {
-  const size_t K = (size_t)p.K;
+__device__ __forceinline__ RowRef row_ref(const GemvParams &p, int lr) {
   if constexpr (MODE == GM_GATEUP) {
-    return ((lr & 1) ? p.w1 : p.w0) + (size_t)(lr >> 1) * K;
+    return {lr & 1, (size_t)(lr >> 1)};
   } else if constexpr (MODE == GM_QKV) {
     const int d = p.head_dim, R = p.rope_dims;
     const int qr = p.n_head * d, kr = p.n_head_kv * d;
     if (lr < qr + kr) {
       const bool isq = lr < qr;
-      const uint16_t *base = isq ? p.w0 : p.w1;
       const int rr = isq ? lr : lr - qr;
       const int head = rr / d, li = rr - head * d;
       // RoPE partners (i, i + R/2) sit on adjacent logical rows 2i, 2i + 1.
       const int dim = li < R ? ((li & 1) ? (li >> 1) + (R >> 1) : (li >> 1)) : li;
-      return base + ((size_t)head * d + dim) * K;
+      return {isq ? 0 : 1, (size_t)head * d + dim};
     }
-    return p.w2 + (size_t)(lr - qr - kr) * K;
+    return {2, (size_t)(lr - qr - kr)};
   } else {
-    return p.w0 + (size_t)lr * K;
+    return {0, (size_t)lr};
   }
+}
+
+__device__ __forceinline__ const uint16_t *bf16_row(const GemvParams &p, RowRef r) {
+  const uint16_t *base = r.m == 0 ? p.w0 : (r.m == 1 ? p.w1 : p.w2);
+  return base + r.row * (size_t)p.K;
+}
+
+// INT4 weights: w0..w2 hold the packed codes, sz0..sz2 the (scale, zero) rows.
+__device__ __forceinline__ const unsigned char *q4_codes(const GemvParams &p, RowRef r) {
+  const uint16_t *base = r.m == 0 ? p.w0 : (r.m == 1 ? p.w1 : p.w2);
+  return reinterpret_cast<const unsigned char *>(base) + r.row * (size_t)(p.K >> 1);
+}
+
+__device__ __forceinline__ const uint32_t *q4_sz(const GemvParams &p, RowRef r) {
+  const uint32_t *base = r.m == 0 ? p.sz0 : (r.m == 1 ? p.sz1 : p.sz2);
+  return base + r.row * (size_t)p.sz_stride;
 }
 
 template <int N>

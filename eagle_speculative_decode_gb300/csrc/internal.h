@@ -16,8 +16,11 @@ constexpr size_t kGemvMaxXBytes = 128 * 1024;
 constexpr size_t kGemvSmemLimit = 224 * 1024;
 
 cudaError_t gemv_prepare();
-int gemv_items_per_launch(int mode, int K, int items);
+int gemv_items_per_launch(const GemvParams &p, int items, int grid);
 cudaError_t gemv_launch(const GemvParams &p, int grid, cudaStream_t st, bool pdl);
+// INT4-weight instantiations (gemv_q4.cu); nb items per launch as gemv_items_per_launch.
+cudaError_t gemv_q4_prepare();
+cudaError_t gemv_q4_launch(const GemvParams &p, int nb, int grid, cudaStream_t st, bool pdl);
 
 // Tensor-core GEMM (gemm_tc.cu): weights [rows, K] against M activation rows.
 constexpr size_t kTcSmemLimit = 220 * 1024;

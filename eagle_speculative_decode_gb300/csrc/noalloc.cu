@@ -109,7 +109,7 @@ extern "C" int eagle3_lmhead_argmax_noalloc(const uint16_t *lm_head, const uint1
   p.dbg_f = logits;
   p.dbg_stride_b = draft_vocab;
   p.dbg_off = 0;
-  const int nb = e3::gemv_items_per_launch(p.mode, p.K, rows);
+  const int nb = e3::gemv_items_per_launch(p, rows, d.num_sms);
   for (int i0 = 0; i0 < rows; i0 += nb) {
     p.item0 = i0;
     p.items = rows - i0 < nb ? rows - i0 : nb;

@@ -39,18 +39,24 @@ class DraftModel:
                             draft_vocab=g.draft_vocab, target_vocab=g.target_vocab,
                             max_batch=max_batch, max_gamma=max_gamma,
                             max_cache_len=max_cache_len, page_size=page_size,
-                            flags=flags, kv_format=self.KV_FORMATS[kv_format])
+                            flags=flags, kv_format=self.KV_FORMATS[kv_format],
+                            weight_format=B.EAGLE3_W_INT4_G128 if weights.int4 else B.EAGLE3_W_BF16)
         self.kv_format = kv_format
         self.max_batch, self.max_gamma = max_batch, max_gamma
         self.max_cache_len, self.page_size = max_cache_len, page_size
         self.w = {name: _dev_bits(b, self.device) for name, b in weights.bits.items()}
+        self.w_sz = {}
+        for name, (codes, sz) in (weights.int4 or {}).items():  # INT4 projections
+            self.w[name] = torch.from_numpy(np.ascontiguousarray(codes)).to(self.device)
+            self.w_sz[name] = torch.from_numpy(np.ascontiguousarray(sz).view(np.int32)).to(self.device)
         self.d2t = torch.from_numpy(np.ascontiguousarray(weights.d2t)).to(self.device)
         ws_bytes = B.eagle3_workspace_bytes(self.cfg)
         if ws_bytes == 0:
             raise B.Eagle3Error(B.EAGLE3_ERR_UNSUPPORTED, "eagle3_workspace_bytes")
         self.workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=self.device)
         wt = B.Weights(**{f: self.w[f].data_ptr() for f in B.WEIGHT_FIELDS if f != "d2t"},
-                       d2t=self.d2t.data_ptr())
+                       d2t=self.d2t.data_ptr(),
+                       **{f"{k}_sz": v.data_ptr() for k, v in self.w_sz.items()})
         self._weights_struct = wt
         self.ctx = B.eagle3_init(self.cfg, wt, self.workspace.data_ptr(), ws_bytes,
                                  _stream_handle(stream))

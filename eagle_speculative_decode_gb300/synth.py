@@ -147,6 +147,9 @@ class DrafterWeights:
     seed: int = 0
     gains: str = "one_plus"
     extra: dict = field(default_factory=dict)
+    # INT4 projections: name -> (codes uint8 [out, in / 2], sz uint32 [out, stride]) where
+    # sz packs bf16 (scale, zero) as scale | zero << 16; `bits` then omits those names
+    int4: dict | None = None
 
 
 def make_weights(geom: Geometry, seed: int = 0, gains: str = "one_plus",
@@ -179,6 +182,41 @@ def make_hidden(shape_prefix: tuple[int, ...], geom: Geometry, seed: int,
     prefix + (n_embd,)."""
     bits = normal_bf16(tuple(shape_prefix) + (geom.n_embd,), seed, (400, stream))
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+INT4_NAMES = ("q", "k", "v", "o", "gate", "up", "down", "lm_head")
+INT4_GROUP = 128
+
+
+def int4_sz_stride(in_dim: int) -> int:
+    """(scale, zero) pairs per INT4 row: in / 128 rounded up to a multiple of 4."""
+    return (in_dim // INT4_GROUP + 3) // 4 * 4
+
+
+def make_int4_weights(geom: Geometry, seed: int = 0, std: float = 0.02) -> DrafterWeights:
+    """Seeded drafter with INT4 projections (a random-init INT4 model, not a quantized bf16
+    one): codes uniform in 0..15; per 128-wide group a bf16 scale std / 4.6 * exp(0.2 N)
+    (code - 8 has standard deviation about 4.6) and a bf16 zero scale / 2 + N(0, std / 10),
+    which centres the weights (code - 8 has mean -1/2); padding pairs are zero.  fc, the
+    norm gains and the embedding are bf16 as in make_weights."""
+    base = make_weights(geom, seed, skip=INT4_NAMES, std=std)
+    shapes = weight_shapes(geom)
+    int4 = {}
+    for idx, name in enumerate(INT4_NAMES):
+        out_dim, in_dim = shapes[name]
+        rng = _stream(seed, (500, idx))
+        codes = rng.integers(0, 256, size=(out_dim, in_dim // 2), dtype=np.uint8)
+        groups = in_dim // INT4_GROUP
+        scale = (np.float32(std / 4.6) * np.exp(np.float32(0.2) * rng.standard_normal((out_dim, groups),
+                                                                                     dtype=np.float32)))
+        zero = np.float32(0.5) * scale + np.float32(std / 10) * rng.standard_normal((out_dim, groups),
+                                                                                     dtype=np.float32)
+        sz = np.zeros((out_dim, int4_sz_stride(in_dim)), dtype=np.uint32)
+        sz[:, :groups] = f32_to_bf16_bits(scale).astype(np.uint32) | \
+            (f32_to_bf16_bits(zero).astype(np.uint32) << np.uint32(16))
+        int4[name] = (codes, sz)
+    base.int4 = int4
+    return base
 
 
 def make_aux(shape_prefix: tuple[int, ...], geom: Geometry, seed: int,

@@ -80,6 +80,23 @@ typedef struct CUstream_st *eagle3_stream_t;
 #define EAGLE3_KV_BF16 0
 #define EAGLE3_KV_Q8_0_Q5_1 1
 
+/* Drafter weight formats (eagle3_config.weight_format).
+ *   EAGLE3_W_BF16:       every matrix bf16 [out, in].
+ *   EAGLE3_W_INT4_G128:  the per-step projections q, k, v, o, gate, up, down and lm_head
+ *                        as 4-bit weights ("Add a weight-stationary INT4 GEMM for small M",
+ *                        the stack of the Eagle3Speculator PR): a matrix [out, in] is
+ *                        codes, uint8 [out, in / 2] with the code of in-index 2j in the low
+ *                        nibble of byte j and 2j + 1 in the high nibble, and sz, bf16 pairs
+ *                        (scale, zero) [out, sz_stride(in)] for the groups of 128 in-indices,
+ *                        sz_stride(in) = in / 128 rounded up to a multiple of 4 (the pad is
+ *                        unused); w = scale * (code - 8) + zero.  fc, the norm gains and the
+ *                        embedding stay bf16.  Needs n_embd, n_head * head_dim and n_ff
+ *                        multiples of 128.  These projections then run on the CUDA-core
+ *                        GEMV at every batch (one launch streams the weights once for up to
+ *                        8 items). */
+#define EAGLE3_W_BF16 0
+#define EAGLE3_W_INT4_G128 1
+
 /* Checkpoint flags (eagle3_config.flags) of the EAGLE-3 layer's op sequence
  * ("memra_engine/eagle.rs", module doc: this checkpoint has norm_before_residual,
  * norm_before_fc, fc_norm and norm_output all false, and its residual is the PRE-norm g).
@@ -114,17 +131,22 @@ typedef struct {
                         * are read a page-aligned run of keys at a time, so that run's K and
                         * V bytes must be multiples of 16 (head_dim 64: page_size % 4 == 0;
                         * head_dim 128: even page_size; head_dim 256: any page_size)     */
+  int weight_format;   /* EAGLE3_W_BF16 (default) or EAGLE3_W_INT4_G128                    */
 } eagle3_config;
 
 /* Drafter weights: bf16, PyTorch Linear layout [out, in] row-major, device memory,
  * owned by the caller and left unchanged.  Shapes: fc [n, 3n]; q [H d, 2n];
  * k, v [H_kv d, 2n]; o [n, H d]; gate, up [F, n]; down [n, F]; lm_head [V_d, n];
  * embed [V_t, n] (the target's token embedding, indexed by target id); the four
- * RMSNorm gains [n].  d2t: int64 [V_d], target_id = draft_id + d2t[draft_id]. */
+ * RMSNorm gains [n].  d2t: int64 [V_d], target_id = draft_id + d2t[draft_id].
+ * With EAGLE3_W_INT4_G128 the eight projection pointers hold the codes and the *_sz
+ * pointers their (scale, zero) rows (see the format above); otherwise the *_sz pointers
+ * are ignored.  Every pointer 16-byte aligned. */
 typedef struct {
   const uint16_t *fc, *in_norm, *hidden_norm, *q, *k, *v, *o, *post_norm, *gate, *up, *down,
       *final_norm, *lm_head, *embed;
   const int64_t *d2t;
+  const uint32_t *q_sz, *k_sz, *v_sz, *o_sz, *gate_sz, *up_sz, *down_sz, *lm_head_sz;
 } eagle3_weights;
 
 /* Paged drafter KV cache, device memory owned by the caller.

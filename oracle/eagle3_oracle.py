@@ -220,6 +220,29 @@ def unpack_q5_1(blocks):
 
 KV_FORMATS = ("bf16", "q8_0/q5_1")
 
+# ------------------------------------------------------------- INT4 drafter weights
+# The stack of "Add the Eagle3Speculator module for speculative decoding" includes "Add a
+# weight-stationary INT4 GEMM for small M"; the page names nothing more.  The format read
+# here: per output row, 4-bit codes two to a byte (in-index 2j in the low nibble of byte
+# j, 2j + 1 in the high one) and, for each group of 128 in-indices, a bf16 (scale, zero)
+# pair stored as one uint32 (scale in the low half); w = scale * (code - 8) + zero.
+
+INT4_GROUP = 128
+
+
+def dequantize_int4(codes, sz, in_dim: int) -> np.ndarray:
+    """float64 [out, in] of INT4 codes uint8 [out, in / 2] and (scale, zero) uint32 rows."""
+    c = np.asarray(codes, dtype=np.uint8)
+    q = np.empty((c.shape[0], in_dim), dtype=np.float64)
+    q[:, 0::2] = c & 15
+    q[:, 1::2] = c >> 4
+    groups = in_dim // INT4_GROUP
+    pairs = np.asarray(sz, dtype=np.uint32)[:, :groups]
+    scale = widen_bf16((pairs & 0xFFFF).astype(np.uint16))
+    zero = widen_bf16((pairs >> 16).astype(np.uint16))
+    g = np.arange(in_dim) // INT4_GROUP
+    return scale[:, g] * (q - 8.0) + zero[:, g]
+
 
 def store_k(x, kv_format: str) -> np.ndarray:
     """Value of a K vector as the cache holds it (float64 of the stored form)."""
@@ -241,7 +264,7 @@ class Drafter:
     """float64 view of the drafter weights (one decoder layer + fc + lm_head + d2t)."""
 
     def __init__(self, geom, bits: dict, d2t, kv_format: str = "bf16",
-                 norm_before_residual: bool = False):
+                 norm_before_residual: bool = False, int4: dict | None = None):
         """norm_before_residual: the checkpoint flag of "memra_engine/eagle.rs" (module
         doc, false for its checkpoint, whose attention residual is the pre-norm g); when
         true the residual is the normed RMSNorm(g) * hidden_norm instead."""
@@ -253,6 +276,8 @@ class Drafter:
         self.kv_format = kv_format
         self.norm_before_residual = bool(norm_before_residual)
         self.w = {name: widen_bf16(b) for name, b in bits.items() if name != "embed"}
+        for name, (codes, sz) in (int4 or {}).items():  # INT4 projections, dequantized
+            self.w[name] = dequantize_int4(codes, sz, 2 * codes.shape[1])
         self._embed_bits = bits["embed"]
         self.d2t = np.asarray(d2t, dtype=np.int64)
 
