@@ -387,6 +387,18 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
 }
 
 // ------------------------------------------------------------------ launcher
+// Most rows per ring stage: a stage's sums fit one warp reduction (32 / (NB * halves)),
+// at most 8, and for INT4 with several items at most 2 / (NB / 2) so that the per-row sums
+// and the decoded codes of a stage stay in registers (one item keeps 8 rows: the stage's
+// fixed cost then spreads over more rows, which measured faster despite a few spilled
+// registers).
+template <int NB, int MODE, bool Q4>
+constexpr int sr_max() {
+  constexpr int a = 32 / (NB * ModeTraits<MODE>::kHalves) >= 8 ? 8 : 32 / (NB * ModeTraits<MODE>::kHalves);
+  constexpr int q = NB == 1 ? 8 : (NB == 2 ? 2 : 1);
+  return Q4 ? (a < q ? a : q) : a;
+}
+
 // Rows per ring stage: whole rows up to kStageBytes, at most 8, at most 32 / (NB * H) so
 // that a stage's sums fit one warp reduction, and fewer if that keeps >= 4 stages.
 template <int MODE, bool Q4>
@@ -396,6 +408,7 @@ static int stage_rows(int K, int NB, int max_rows, int row_bytes) {
   if (sr < 1) sr = 1;
   if (sr > 8) sr = 8;
   if (sr > 32 / (NB * T::kHalves)) sr = 32 / (NB * T::kHalves);
+  if (Q4 && NB > 1 && sr > (NB == 2 ? 2 : 1)) sr = NB == 2 ? 2 : 1;
   int p2 = 1;
   while (p2 * 2 <= sr) p2 *= 2;
   while (p2 > 1) {
@@ -438,7 +451,7 @@ static cudaError_t dispatch_sr(const GemvParams &p, int grid, cudaStream_t st, b
   if (grid > nunits) grid = nunits;
   if (grid < 1) grid = 1;
   const int max_rows = T::kUnit * ((nunits + grid - 1) / grid);
-  constexpr int SRMAX = 32 / (NB * T::kHalves) >= 8 ? 8 : 32 / (NB * T::kHalves);
+  constexpr int SRMAX = sr_max<NB, MODE, Q4>();
   switch (stage_rows<MODE, Q4>(p.K, NB, max_rows, gemv_row_bytes(Q4, p.K, p.sz_stride))) {
     case 1: return launch_one<NB, 1, MODE, Q4>(p, grid, max_rows, st, pdl);
     case 2: return launch_one<NB, (SRMAX >= 2 ? 2 : 1), MODE, Q4>(p, grid, max_rows, st, pdl);
@@ -461,7 +474,7 @@ static cudaError_t dispatch_nb(const GemvParams &p, int nb, int grid, cudaStream
 template <int NB, int MODE, bool Q4>
 static cudaError_t prepare_nb() {
   using T = ModeTraits<MODE>;
-  constexpr int SRMAX = 32 / (NB * T::kHalves) >= 8 ? 8 : 32 / (NB * T::kHalves);
+  constexpr int SRMAX = sr_max<NB, MODE, Q4>();
   const int lim = (int)kGemvSmemLimit;
   cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB, 1, MODE, Q4>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
   if (e == cudaSuccess)
