@@ -55,18 +55,18 @@ CONFIGS = {
 # byte the profiled ones (sha256 over the listed csrc files); the summaries under
 # profiles/ give the commands.  Keyed by (config, dominant projection or "attn").
 PROFILED_TRAFFIC = {
-    ("c2", "lmhead"): {"bytes": 262220288 + 3023104,
-                       "sources": ("gemv.cu", "epilogue.cuh", "common.cuh"),
-                       "sha256": "41a365cfc405be675089bcef7fd28faf3fef1ac0562ce3274da15cbd439f7137"},
-    ("c4", "attn"): {"bytes": 538542336 + 3409920,
+    ("c2", "lmhead"): {"bytes": 262220288 + 3067392,
+                       "sources": ("gemv.cu", "gemv_kernel.cuh", "epilogue.cuh", "common.cuh"),
+                       "sha256": "a4f4561c88eedfc13af11a289778e2698064ac754aed575b99af06a806bb8048"},
+    ("c4", "attn"): {"bytes": 538557184 + 3470336,
                      "sources": ("attention.cu", "common.cuh"),
-                     "sha256": "411a20dc79418bbbcefe707ac26b3a3bd5605a565738cfea21945d6aedbbe267"},
-    ("c5", "attn", "q8_0/q5_1"): {"bytes": 243909888 + 2840320,
-                                  "sources": ("attention.cu", "common.cuh"),
-                                  "sha256": "411a20dc79418bbbcefe707ac26b3a3bd5605a565738cfea21945d6aedbbe267"},
-    ("c4", "lmhead"): {"bytes": 265020928 + 6003968,
+                     "sha256": "4f4ce1b4205b28d46abaf0fcbb7a89305e1b24cec17f1d1e181340df05345e37"},
+    ("c4", "lmhead"): {"bytes": 265008640 + 5860096,
                        "sources": ("gemm_tc.cu", "epilogue.cuh", "common.cuh"),
-                       "sha256": "07e0e56c23b1d9d9259efedd6d98324c331b09463ad33fd94cdb1734cceea173"},
+                       "sha256": "7290e6c0600a2bd4bc13542c5653997a252b6a717ac3a3c16e9b43d58df7b282"},
+    ("c5", "attn", "q8_0/q5_1"): {"bytes": 243912448 + 3330816,
+                                  "sources": ("attention.cu", "common.cuh"),
+                                  "sha256": "4f4ce1b4205b28d46abaf0fcbb7a89305e1b24cec17f1d1e181340df05345e37"},
 }
 
 
