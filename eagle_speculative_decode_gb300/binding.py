@@ -31,7 +31,7 @@ EAGLE3_DEV_TIMEOUT = 16
 
 EXPORTED = (
     "eagle3_version", "eagle3_error_string", "eagle3_workspace_bytes", "eagle3_kv_row_bytes",
-    "eagle3_resolve_rope_dims", "eagle3_config_from_json",
+    "eagle3_resolve_rope_dims", "eagle3_config_from_json", "eagle3_selftest_bounded_wait",
     "eagle3_plan_gamma",
     "eagle3_init", "eagle3_destroy", "eagle3_encode", "eagle3_prefill", "eagle3_draft_chain",
     "eagle3_rewind", "eagle3_accept", "eagle3_verify_greedy", "eagle3_rebuild_after_verify",
@@ -106,6 +106,7 @@ def load() -> ctypes.CDLL:
         "eagle3_workspace_bytes": (ctypes.c_size_t, [P(Config)]),
         "eagle3_kv_row_bytes": (ci, [P(Config), P(ctypes.c_size_t), P(ctypes.c_size_t)]),
         "eagle3_resolve_rope_dims": (ci, [ci, ci, ci, ci, ctypes.c_float]),
+        "eagle3_selftest_bounded_wait": (ci, [vp, vp, vp]),
         "eagle3_config_from_json": (ci, [ctypes.c_char_p, P(Config)]),
         "eagle3_plan_gamma": (ci, [ci, ci, ci, cu, P(ci)]),
         "eagle3_init": (ci, [P(Config), P(Weights), vp, ctypes.c_size_t, vp, P(vp)]),
@@ -157,6 +158,11 @@ def eagle3_version() -> int:
 
 def eagle3_workspace_bytes(cfg: Config) -> int:
     return int(load().eagle3_workspace_bytes(ctypes.byref(cfg)))
+
+
+def eagle3_selftest_bounded_wait(device_status: int, device_result: int, stream: int = 0) -> None:
+    _check(load().eagle3_selftest_bounded_wait(device_status, device_result, stream),
+           "eagle3_selftest_bounded_wait")
 
 
 def eagle3_resolve_rope_dims(head_dim: int, rotary_dim: int | None, factor: float | None) -> int:

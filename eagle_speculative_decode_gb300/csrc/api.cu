@@ -626,6 +626,11 @@ const char *eagle3_error_string(int code) {
   }
 }
 
+int eagle3_selftest_bounded_wait(int *device_status, int *device_result, eagle3_stream_t stream) {
+  if (!device_status || !device_result) return EAGLE3_ERR_INVALID_ARG;
+  return cuda_err(launch_wait_selftest(device_status, device_result, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int eagle3_kv_row_bytes(const eagle3_config *cfg, size_t *k_row, size_t *v_row) {
   if (!cfg_valid(cfg) || !k_row || !v_row) return EAGLE3_ERR_INVALID_ARG;
   kv_rows(*cfg, k_row, v_row);

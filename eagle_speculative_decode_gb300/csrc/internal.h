@@ -58,6 +58,7 @@ cudaError_t launch_chain_begin(int B, int gamma, unsigned flags, int max_cache_l
 cudaError_t launch_chain_end(int B, int32_t *kv_len, const int32_t *round_start,
                              const int32_t *geff, cudaStream_t st, bool pdl);
 cudaError_t launch_rewind(int B, int32_t *kv_len, const int32_t *round_start, cudaStream_t st);
+cudaError_t launch_wait_selftest(int *status, int *result, cudaStream_t st);
 cudaError_t launch_res_norm(int B, int n, float eps, const float *g, const uint16_t *w, float *out,
                             cudaStream_t st);
 cudaError_t launch_accept(int B, int gamma, const int32_t *draft_tok, const int32_t *target_pred,

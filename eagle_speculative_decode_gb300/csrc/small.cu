@@ -196,6 +196,31 @@ cudaError_t launch_res_norm(int B, int n, float eps, const float *g, const uint1
   return cudaLaunchKernelEx(&cfg, res_norm_kernel, n, eps, g, w, out);
 }
 
+// Self-test of the bounded wait every kernel uses on its mbarriers: one thread waits on a
+// barrier that nothing completes, so the wait gives up, raises EAGLE3_DEV_TIMEOUT in
+// *status and sets the CTA's abort flag; a second wait then returns at once.  Nothing is
+// in flight on the barrier, so the kernel ends normally and the context stays usable.
+__global__ void wait_selftest_kernel(int *status, int *result) {
+  __shared__ __align__(8) unsigned long long bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool first = mbar_wait(smem_addr(&bar), 0, &abort_flag, status);
+    const bool second = mbar_wait(smem_addr(&bar), 0, &abort_flag, status);
+    result[0] = (first ? 1 : 0) | (second ? 2 : 0) | (abort_flag ? 4 : 0);
+  }
+}
+
+cudaError_t launch_wait_selftest(int *status, int *result, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(status, result);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_chain_begin(int B, int gamma, unsigned flags, int max_cache_len,
                                const int32_t *kv_len, int32_t *round_start, int32_t *geff,
                                int32_t *geff_out, int *status, int unit_keys, int32_t *unit_pre,

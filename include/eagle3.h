@@ -189,6 +189,15 @@ size_t eagle3_workspace_bytes(const eagle3_config *cfg);
  * cfg or null outputs.  Host-only arithmetic. */
 int eagle3_kv_row_bytes(const eagle3_config *cfg, size_t *k_row, size_t *v_row);
 
+/* Self-test of the device-side failure path: launches one small kernel whose thread waits
+ * on an mbarrier that nothing completes.  The bounded wait gives up (about a second at
+ * most), ORs EAGLE3_DEV_TIMEOUT into *device_status (device int32, caller-zeroed) and sets
+ * the CTA's abort flag, after which a second wait returns at once; *device_result (device
+ * int32) receives bit 0 = first wait succeeded, bit 1 = second wait succeeded, bit 2 =
+ * abort flag set (4 expected).  The kernel exits normally, so the context stays usable.
+ * Asynchronous on stream.  EAGLE3_ERR_INVALID_ARG for null pointers. */
+int eagle3_selftest_bounded_wait(int *device_status, int *device_result, eagle3_stream_t stream);
+
 /* Rotary width of a drafter config ("memra_engine/eagle.rs", EagleConfig::rope_dim_count
  * and its tests on the eagle3-qwen35-9b config): an explicit rotary dim count (has_rotary_dim,
  * even, 2..head_dim) wins over a fraction of head_dim (has_factor), which wins over the full

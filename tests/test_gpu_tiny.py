@@ -170,3 +170,25 @@ def test_out_of_range_token_sets_status_without_fault(tiny):
     assert st & Bd.EAGLE3_DEV_BAD_TOKEN
     assert model.status() == 0                            # reading clears the word
     seq.rewind()
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable(tiny):
+    """The device failure path without a fault: a wait that nothing completes gives up,
+    raises EAGLE3_DEV_TIMEOUT in the status word and the abort flag (a second wait returns
+    at once); afterwards the same process still runs a round with parity."""
+    wts, model, dr = tiny
+    status = torch.zeros(1, dtype=torch.int32, device=model.device)
+    result = torch.zeros(1, dtype=torch.int32, device=model.device)
+    Bd.eagle3_selftest_bounded_wait(status.data_ptr(), result.data_ptr(),
+                                    torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == Bd.EAGLE3_DEV_TIMEOUT
+    assert int(result.item()) == 4      # first wait gave up, second returned at once, abort set
+    lens = np.array([9])
+    toks, aux, _ = _prompt(1, lens, seed=77)
+    seq = model.new_state(1)
+    gpu_prefill(seq, model, toks, aux, lens)
+    torch.cuda.synchronize()
+    states = oracle_prefill(dr, toks, aux, lens)
+    _round(model, dr, seq, states, 3, np.array([2]), seed=78)
+    assert model.status() == 0
