@@ -247,24 +247,37 @@ def barrier(world):
         dist.barrier()
 
 
+def _all_reduce(x: float, op) -> float:
+    """All-reduce of one float over the ranks: on the GPU with NCCL, on the host with gloo
+    (the CPU tests of the replica bookkeeping)."""
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=op)
+    return float(t.item())
+
+
 def max_over_ranks(world, x: float) -> float:
     if world <= 1:
         return x
-    import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    return _all_reduce(x, dist.ReduceOp.MAX)
 
 
 def sum_over_ranks(world, x: float) -> float:
     if world <= 1:
         return x
-    import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _all_reduce(x, dist.ReduceOp.SUM)
+
+
+def replica_throughput(world, tokens_local: float, elapsed_ms_local: float):
+    """Whole-job throughput of N independent replicas (weak scaling): the tokens of every
+    rank over the slowest rank's time.  Returns (tokens/s, max elapsed ms)."""
+    elapsed = max_over_ranks(world, elapsed_ms_local)
+    tokens = sum_over_ranks(world, tokens_local)
+    return tokens / (elapsed / 1e3), elapsed
 
 
 # ------------------------------------------------------------------ reference arm
@@ -422,9 +435,7 @@ def run_mine(args, cfg):
     mean_ctx = ctx_sum[0] / args.steps
     assert model.status() == 0, "device status word set during the benchmark"
 
-    elapsed_max = max_over_ranks(world, elapsed_ms)
-    tokens_all = sum_over_ranks(world, float(B * gamma * args.steps))
-    value = tokens_all / (elapsed_max / 1e3)
+    value, elapsed_max = replica_throughput(world, float(B * gamma * args.steps), elapsed_ms)
     ms_per_step = elapsed_max / args.steps
 
     # ---- per-kernel durations (direct launches with events between kernels)
