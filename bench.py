@@ -206,26 +206,31 @@ def make_bench_weights(geo, weights):
 
 
 # ------------------------------------------------------------------ oracle timing
-def oracle_round_rate(geo_name, gamma, rounds, seed=0, kv_format="bf16", weights="bf16"):
-    """Times the CPU oracle on one sequence: `rounds` chains of gamma draft steps from a
-    32-token prefilled state at the benchmark's geometry.  Returns (draft tok/s, seconds,
-    sample description)."""
+def oracle_round_rate(geo_name, gamma, rounds, seed=0, kv_format="bf16", weights="bf16",
+                      prompt=32, seconds=0.0):
+    """Times the CPU oracle on one sequence: chains of gamma draft steps from a prefilled
+    state of `prompt` tokens at the benchmark's geometry, at least `rounds` chains and
+    until `seconds` have passed (a bounded sample of the workload).  Returns (draft tok/s,
+    seconds, sample description)."""
     from eagle_speculative_decode_gb300 import synth
     from oracle import eagle3_oracle as O
     geo = synth.GEOMETRIES[geo_name]
     wts = make_bench_weights(geo, weights)
     dr = O.Drafter(geo, wts.bits, wts.d2t, kv_format=kv_format, int4=wts.int4)
-    P = 32
+    P = int(prompt)
     toks = synth.make_tokens((P + 1,), geo, seed + 1)
     aux = synth.make_aux((P,), geo, seed + 1)
     st = O.prefill(dr, toks[:P], int(toks[P]), aux)
     t0 = time.perf_counter()
-    for _ in range(rounds):
+    n = 0
+    while n < max(1, rounds) or (time.perf_counter() - t0 < seconds and n < 10000):
         O.draft_chain(dr, st, gamma)
+        n += 1
     dt = time.perf_counter() - t0
-    desc = (f"{rounds} chain(s) of {gamma} draft steps of one sequence from a {P}-token "
-            f"prefilled state, {geo_name} geometry, {weights} weights, {kv_format} KV, float64 numpy oracle")
-    return rounds * gamma / dt, dt, desc
+    desc = (f"{n} chain(s) of {gamma} draft steps of one sequence from a {P}-token prefilled "
+            f"state (prefill not timed), {geo_name} geometry, {weights} weights, {kv_format} KV, "
+            "float64 numpy oracle")
+    return n * gamma / dt, dt, desc
 
 
 # ------------------------------------------------------------------ distributed
@@ -527,7 +532,9 @@ def run_mine(args, cfg):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
             rate, secs, desc = oracle_round_rate(cfg["geom"], gamma, args.cpu_rounds,
-                                                 kv_format=args.kv_format, weights=args.weights)
+                                                 kv_format=args.kv_format, weights=args.weights,
+                                                 prompt=min(int(lens.min()), 512),
+                                                 seconds=args.cpu_seconds)
             cpu = {"value": rate, "unit": "draft tokens/s", "cores": os.cpu_count(),
                    "kind": "oracle", "sample": desc, "seconds": secs}
         except Exception as e:  # reported, not fatal
@@ -591,7 +598,10 @@ def main():
     ap.add_argument("--config", default="c2", choices=sorted(CONFIGS))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--phase-rounds", type=int, default=3)
-    ap.add_argument("--cpu-rounds", type=int, default=2)
+    ap.add_argument("--cpu-rounds", type=int, default=1,
+                    help="chains the CPU baseline times at least")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU baseline sample length: chains are timed until this many seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--verify-steps", type=int, default=10,
                     help="timed calls of the target-side greedy verify (0: skip)")
