@@ -104,3 +104,21 @@ def test_capacity_rule_matches_the_worked_case(built_lib):
         Bd.eagle3_plan_gamma(-1, 3, 100)
     with pytest.raises(Bd.Eagle3Error):
         Bd.eagle3_plan_gamma(0, 0, 100)
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/eagle3.h compiles as C99 with warnings as errors: the boundary has no C++
+    types, and every declaration is referenced once."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        pytest.skip("no C compiler")
+    names = _declared()
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "eagle3.h"\nvoid *const eagle3_all[] = {\n' +
+                   ",\n".join(f"  (void *){n}" for n in names) + "\n};\n")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-Wno-pedantic", "-I",
+                        os.path.dirname(HEADER), "-c", str(src), "-o", str(tmp_path / "o.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
