@@ -542,6 +542,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   const uint32_t fullB = emptyA + 8 * NA;
   const uint32_t hi_full = fullB + 8 * NB, hi_free = hi_full + 16;
   const uint32_t mma_done = hi_free + 16;
+  const uint32_t fix_bar = mma_done + 8;  // bulk copies of published partials (last tile)
   unsigned char *aux2 = aux + 8 * (2 * NA + 2 * NB + 7);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(aux2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(aux2 + 4);
@@ -585,6 +586,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       mbar_init(hi_free + 8 * i, 8);  // one arrival per epilogue warp
     }
     mbar_init(mma_done, 1);
+    mbar_init(fix_bar, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -747,6 +749,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     if constexpr (MODE == GM_LMHEAD) {
       if (tid < N) tb.run_best[tid] = 0ull;
     }
+    uint32_t fix_phase = 0u;  // parity of fix_bar
     // per-item tables of the first item tile, while the first chunks are multiplied
     int tb_it = (int)(tc_seg(u_begin, u_end, ktiles).t % item_tiles);
     if (u_begin < u_end) tc_tables<N, MODE>(args, tb_it, tb);
@@ -811,41 +814,98 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         __threadfence();
         // fixed order: the published sums of contributors c_first .. c_last (this CTA's
         // own included), one contributor's tile at a time
-#pragma unroll
-        for (int h = 0; h < H; ++h)
-#pragma unroll
-          for (int j = 0; j < NCH; ++j)
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc[h][j][i] = 0.f;
-        // kU contributors per pass, all their loads in flight together, added in CTA order
-        constexpr int kVals = H * NCH * 16;
-        constexpr int kU = kVals >= 64 ? 2 : (kVals >= 32 ? 4 : 8);
-        for (int c2 = c_first; c2 <= c_last; c2 += kU) {
-          const float *src[kU];
-#pragma unroll
-          for (int q = 0; q < kU; ++q) {
-            const int cq = min(c2 + q, c_last);  // past the last: a repeat load, not added
-            // a contributor's segment is its first one (slot 0) unless it began earlier
-            src[q] = args.part + ((size_t)cq * 2 + (sched.start(cq) >= t0 ? 0 : 1)) * H * N * kTcM + r;
-          }
+        auto part_of = [&](int cq) {  // a contributor's segment is its first (slot 0) unless it began earlier
+          return args.part + ((size_t)cq * 2 + (sched.start(cq) >= t0 ? 0 : 1)) * H * N * kTcM;
+        };
+        if (u >= u_end) {
+          // this CTA's last segment: its rings are idle, so one thread bulk-copies every
+          // other contributor's published partial into them (all in flight at once), and
+          // the rows are added in CTA order from shared memory; this CTA's own sums are
+          // still in registers.
+          constexpr int kPart = H * N * kTcM;  // floats per published partial
+          constexpr int kCap = (int)(((size_t)NA * S::kA + (size_t)NB * S::kBStage) / ((size_t)kPart * 4));
+          static_assert(kCap >= 1, "a published partial fits the rings");
+          const float *stg = reinterpret_cast<const float *>(aring);
+          float own[H][NCH][16];
 #pragma unroll
           for (int h = 0; h < H; ++h)
 #pragma unroll
-            for (int j = 0; j < NCH; ++j) {
-              if (!tc_has<N>(j, chalf)) continue;
-              float v[kU][16];
+            for (int j = 0; j < NCH; ++j)
 #pragma unroll
-              for (int q = 0; q < kU; ++q)
+              for (int i = 0; i < 16; ++i) {
+                own[h][j][i] = acc[h][j][i];
+                acc[h][j][i] = 0.f;
+              }
+          for (int c2 = c_first; c2 <= c_last; c2 += kCap) {
+            const int cend = min(c_last, c2 + kCap - 1);
+            const bool others = !(c2 == cend && c2 == cta);
+            if (others) {
+              if (tid == 0) {
+                // the partials were written through the generic proxy by other CTAs and
+                // acquired through the tile counter; order them before the bulk reads
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                mbar_expect_tx(fix_bar, (uint32_t)((cend - c2 + 1 - (cta >= c2 && cta <= cend ? 1 : 0)) * kPart * 4));
+                const uint64_t pol = l2_evict_first_policy();
+                for (int cq = c2; cq <= cend; ++cq)
+                  if (cq != cta)
+                    bulk_g2s(smem_addr(aring + (size_t)(cq - c2) * kPart * 4), part_of(cq), (uint32_t)(kPart * 4),
+                             fix_bar, pol);
+              }
+              mbar_wait(fix_bar, fix_phase, abort_flag, pc.status);
+              fix_phase ^= 1u;
+            }
+            for (int cq = c2; cq <= cend; ++cq) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  v[q][i] = __ldcg(src[q] + ((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM);
+              for (int h = 0; h < H; ++h)
 #pragma unroll
-              for (int q = 0; q < kU; ++q)
-                if (c2 + q <= c_last) {
+                for (int j = 0; j < NCH; ++j) {
+                  if (!tc_has<N>(j, chalf)) continue;
+                  if (cq == cta) {
 #pragma unroll
-                  for (int i = 0; i < 16; ++i) acc[h][j][i] += v[q][i];
+                    for (int i = 0; i < 16; ++i) acc[h][j][i] += own[h][j][i];
+                  } else {
+                    const float *src = stg + (size_t)(cq - c2) * kPart + ((size_t)h * N + tc_c0<N>(j, chalf)) * kTcM + r;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[h][j][i] += src[(size_t)i * kTcM];
+                  }
                 }
             }
+            tc_epi_sync();  // every thread has read this batch before the next overwrites it
+          }
+        } else {
+          // mid-share (the rings are still streaming this CTA's next tile): kU contributors
+          // per pass, all their loads in flight together, added in CTA order
+#pragma unroll
+          for (int h = 0; h < H; ++h)
+#pragma unroll
+            for (int j = 0; j < NCH; ++j)
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc[h][j][i] = 0.f;
+          constexpr int kVals = H * NCH * 16;
+          constexpr int kU = kVals >= 64 ? 2 : (kVals >= 32 ? 4 : 8);
+          for (int c2 = c_first; c2 <= c_last; c2 += kU) {
+            const float *src[kU];
+#pragma unroll
+            for (int q = 0; q < kU; ++q) src[q] = part_of(min(c2 + q, c_last)) + r;  // past the last: not added
+#pragma unroll
+            for (int h = 0; h < H; ++h)
+#pragma unroll
+              for (int j = 0; j < NCH; ++j) {
+                if (!tc_has<N>(j, chalf)) continue;
+                float v[kU][16];
+#pragma unroll
+                for (int q = 0; q < kU; ++q)
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    v[q][i] = __ldcg(src[q] + ((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM);
+#pragma unroll
+                for (int q = 0; q < kU; ++q)
+                  if (c2 + q <= c_last) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[h][j][i] += v[q][i];
+                  }
+              }
+          }
         }
         if (tid == 0) args.tile_cnt[sg.t] = 0u;
       }
