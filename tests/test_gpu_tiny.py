@@ -192,3 +192,41 @@ def test_bounded_wait_times_out_and_the_context_stays_usable(tiny):
     states = oracle_prefill(dr, toks, aux, lens)
     _round(model, dr, seq, states, 3, np.array([2]), seed=78)
     assert model.status() == 0
+
+
+@pytest.mark.parametrize("kv_format", ["bf16", "q8_0/q5_1"])
+def test_out_of_range_page_sets_status_without_fault(built_lib, kv_format):
+    """A page-table entry past the pool: every kernel that would touch that page (the
+    k/v append of prefill and chain, the quantizer, the attention's copies) skips it and
+    raises EAGLE3_DEV_BAD_PAGE; pages in range are still written, and reading the status
+    clears it."""
+    wts = synth.make_weights(G, seed=0)
+    model = DraftModel(wts, max_batch=2, max_gamma=4, max_cache_len=64, page_size=16, kv_format=kv_format)
+    try:
+        pages = (model.max_cache_len + model.page_size - 1) // model.page_size
+        pt = synth.page_table(1, pages)
+        seq = model.new_state(1, page_table=pt)
+        bad = seq.page_table.clone()
+        bad[0, 1] = seq.num_pages + 3               # positions 16..31 map past the pool
+        seq.page_table.copy_(bad)
+        lens = np.array([24])
+        toks, aux, _ = _prompt(1, lens, seed=11)
+        gpu_prefill(seq, model, toks, aux, lens)
+        torch.cuda.synchronize()
+        assert model.status() & Bd.EAGLE3_DEV_BAD_PAGE
+        assert model.status() == 0
+        seq.draft_chain(2)                          # attention reads the bad page: skipped
+        torch.cuda.synchronize()
+        assert model.status() & Bd.EAGLE3_DEV_BAD_PAGE
+        seq.rewind()
+        # the entries of the first page were written normally
+        dr = O.Drafter(G, wts.bits, wts.d2t, kv_format=kv_format)
+        st = oracle_prefill(dr, toks, aux, lens)[0]
+        k, v = seq.kv_entries(0, 0, 16)
+        if kv_format == "bf16":
+            assert np.max(np.abs(O.widen_bf16(k) - st.k[:16])) < 0.1
+        else:
+            from parity import assert_quant_valid
+            assert_quant_valid(k, st.k_raw[:16], "k", "first page K")
+    finally:
+        model.close()
