@@ -320,6 +320,9 @@ cudaError_t tc_items(eagle3_ctx *ctx, const GemvParams &p, int items, cudaStream
 bool use_tc(const eagle3_ctx *ctx, const GemvParams &p, int items) {
   if (!ctx->tc_ok || items < ctx->tc_min_items) return false;
   if (p.sz0) return false;  // INT4 weights run on the GEMV
+  // k/v-only teacher forcing of a few pairs (rebuild): 2 * H_kv * d rows are too few row
+  // tiles for the tensor-core split, whose fix-up then dominates
+  if (p.mode == GM_QKV && p.row_base > 0 && items <= 8) return false;
   if (p.mode != GM_ENCODE && (size_t)items > ctx->L.tc_items) return false;
   if (p.mode != GM_ENCODE && p.K > kTcPrepMaxK) return false;  // the activation split's limit
   return true;
