@@ -245,8 +245,14 @@ struct AccStride {
   static constexpr bool kRowsFast = NB >= 16;
 };
 
-template <int NB, int MODE>
-__device__ void epilogue(const GemvParams &p, const float *accs, int row0, int nrows) {
+// Global row of local row r: tiles of TR rows dealt round robin over the CTAs.
+template <int TR>
+__device__ __forceinline__ int tile_row(int r) {
+  return ((r / TR) * (int)gridDim.x + (int)blockIdx.x) * TR + (r % TR);
+}
+
+template <int NB, int MODE, int TR>
+__device__ void epilogue(const GemvParams &p, const float *accs, int nrows) {
   const int tid = threadIdx.x;
   constexpr int AS = AccStride<NB>::value;
   constexpr bool kRowsFast = AccStride<NB>::kRowsFast;
@@ -258,7 +264,7 @@ __device__ void epilogue(const GemvParams &p, const float *accs, int row0, int n
         if (kRowsFast) break;
         continue;
       }
-      const int item = p.item0 + m, row = row0 + r;
+      const int item = p.item0 + m, row = tile_row<TR>(r);
       float v = accs[r * AS + m];
       if constexpr (MODE != GM_ENCODE) v += p.res[(size_t)item * p.rows + row];
       p.out_f[(size_t)item * p.rows + row] = v;
@@ -276,7 +282,7 @@ __device__ void epilogue(const GemvParams &p, const float *accs, int row0, int n
       }
       const int item = p.item0 + m;
       const float gate = accs[(2 * pr) * AS + m], up = accs[(2 * pr + 1) * AS + m];
-      p.out_f[(size_t)item * p.n_ff + ((row0 >> 1) + pr)] = silu_f(gate) * up;
+      p.out_f[(size_t)item * p.n_ff + (tile_row<TR>(2 * pr) >> 1)] = silu_f(gate) * up;
     }
   } else if constexpr (MODE == GM_QKV) {
     const int d = p.head_dim, R = p.rope_dims, half = R >> 1;
@@ -289,7 +295,7 @@ __device__ void epilogue(const GemvParams &p, const float *accs, int row0, int n
         continue;
       }
       const int item = p.item0 + m;
-      const int lr = p.row_base + row0 + 2 * pr;  // even logical row
+      const int lr = p.row_base + tile_row<TR>(2 * pr);  // even logical row
       float a = accs[(2 * pr) * AS + m], b = accs[(2 * pr + 1) * AS + m];
       const PairItem it = resolve_pair(p.pairs, item, p.n_embd);
       const int region = lr < qr ? 0 : (lr < qr + kr ? 1 : 2);
@@ -346,7 +352,7 @@ __device__ void epilogue(const GemvParams &p, const float *accs, int row0, int n
         unsigned long long best = 0ull;
         for (int r = lane; r < nrows; r += 32) {
           const float v = accs[r * AS + m];
-          const int row = row0 + r;
+          const int row = tile_row<TR>(r);
           if (p.dbg_f) p.dbg_f[(size_t)item * p.dbg_stride_b + p.dbg_off + row] = v;
           const unsigned long long key =
               ((unsigned long long)float_order_key(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);
@@ -367,7 +373,7 @@ __device__ void epilogue(const GemvParams &p, const float *accs, int row0, int n
       unsigned long long best = 0ull;
       for (int r = tid; r < nrows; r += kGemvThreads) {
         const float v = accs[r * AS + m];
-        const int row = row0 + r;
+        const int row = tile_row<TR>(r);
         if (p.dbg_f) p.dbg_f[(size_t)item * p.dbg_stride_b + p.dbg_off + row] = v;
         const unsigned long long key =
             ((unsigned long long)float_order_key(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);

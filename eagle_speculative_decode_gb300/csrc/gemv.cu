@@ -27,7 +27,7 @@ int gemv_items_per_launch(const GemvParams &p, int items, int grid) {
   const int unit = (p.mode == GM_QKV || p.mode == GM_GATEUP) ? 2 : 1;
   const int nunits = p.rows / unit;
   const int g = std::max(1, std::min(grid, nunits));
-  const int max_rows = unit * ((nunits + g - 1) / g);
+  const int max_rows = tiles_max_rows_bound(p.rows, g);
   const int rb = gemv_row_bytes(p.sz0 != nullptr, p.K, p.sz_stride);
   auto fits = [&](int nb) {
     if ((size_t)nb * p.K * eb > kGemvMaxXBytes) return false;

@@ -7,10 +7,11 @@
 // consumes y (partial RoPE + bf16 KV append, residual adds, SwiGLU, argmax + d2t).
 // Ops follow "memra_engine/eagle.rs", module doc "Op-sequence".
 //
-// Data movement (one CTA per SM): the CTA owns a contiguous, balanced range of row
-// pairs.  A producer warp streams those rows, SR whole rows per stage (<= 32 KB), with
-// bulk copies (cp.async.bulk, TMA) into an NSTAGE-deep shared-memory ring guarded by
-// mbarriers.  It starts before the kernel waits on its predecessor (programmatic
+// Data movement (one CTA per SM): rows are dealt to the CTAs in tiles of whole stages
+// (pairs kept together), round robin, so that the SMs stream neighbouring parts of the
+// weights at any moment.  A producer warp streams a CTA's rows, SR whole rows per stage
+// (<= 32 KB), with bulk copies (cp.async.bulk, TMA) into a shared-memory ring of about
+// 96 KB guarded by mbarriers (deeper rings streamed slower).  It starts before the kernel waits on its predecessor (programmatic
 // dependent launch), so the next weights are already in flight while the previous
 // kernel drains.  Sixteen consumer warps stage x (normalised where the op says so) in
 // shared memory (float32 in two float4 planes -- elements 0-3 and 4-7 of each 8-element
@@ -30,9 +31,12 @@
 // each code becomes the float 128 + code by a byte permute under the exponent of 128 and
 // code - 8 by one exact packed add, the dot product with x runs on packed two-lane FMAs,
 // and the group's affine map is applied to the 8-element partial:
-// scale * sum((code - 8) x) + zero * sum(x).
+// scale * sum((code - 8) x) + zero * sum(x).  Single-item INT4 launches with K a multiple
+// of 2048 use the tensor-core variant below (gemv_q4_mma_kernel) instead.
 #pragma once
 #include <math.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "epilogue.cuh"
@@ -73,6 +77,33 @@ __host__ __device__ inline GemvSmem gemv_smem_layout(int NB, int SR, int H, int 
   return L;
 }
 
+// A launch's rows are dealt to the CTAs in tiles of TR rows, round robin (tile t to CTA
+// t % grid), so that at any moment the SMs stream neighbouring parts of the weight
+// matrices; the DRAM serves that faster than one distant contiguous range per SM.  Local
+// row r of CTA b is row ((r / TR) * grid + b) * TR + r % TR; only the last tile of the
+// launch can be partial, and it is the last tile of its CTA.
+__host__ __device__ inline int tiles_max_rows(int rows, int TR, int grid) {
+  const int nt = (rows + TR - 1) / TR;
+  return (nt + grid - 1) / grid * TR;
+}
+__host__ __device__ inline int tiles_rows_of(int rows, int TR, int grid, int b) {
+  const int nt = (rows + TR - 1) / TR;
+  if (b >= nt) return 0;
+  const int mine = (nt - b + grid - 1) / grid;
+  const int last = b + (mine - 1) * grid;
+  const int tail = rows - last * TR;
+  return (mine - 1) * TR + (tail < TR ? tail : TR);
+}
+// The largest per-CTA row count over the tile sizes the GEMV uses (1 to 16 rows).
+__host__ __device__ inline int tiles_max_rows_bound(int rows, int grid) {
+  int m = 0;
+  for (int tr = 1; tr <= 16; tr <<= 1) {
+    const int v = tiles_max_rows(rows, tr, grid);
+    m = v > m ? v : m;
+  }
+  return m;
+}
+
 // Eight INT4 codes of one 32-bit word as the floats code - 8, in the pair order
 // (0, 2), (4, 6), (1, 3), (5, 7) of their k offsets: 0x43_0c_00_00 reads as 128 + c
 // exactly (c < 16 stays below the exponent field), minus 136 (exact integers).
@@ -110,6 +141,51 @@ __device__ __forceinline__ float q4_dot(const float2 (&f)[4], const float2 (&xq)
   return fmaf(bf_lo(sz), d.x + d.y, fmaf(bf_hi(sz), xs, a));
 }
 
+// Tail shared by the GEMV kernels: the RMSNorm scale 1 / sqrt(mean(x^2) + eps) per item and
+// K half from the consumers' shares ss, the per-warp row sums in part ([rows][warps][H][NB])
+// added in warp order and scaled, then the mode's epilogue on the finished rows.
+template <int NB, int MODE, int TR>
+__device__ __forceinline__ void gemv_finish(const GemvParams &p, const float (&ss)[NB][ModeTraits<MODE>::kHalves],
+                                            const float *part, float *accs, float *red, float *scale, int nrows) {
+  using T = ModeTraits<MODE>;
+  constexpr int H = T::kHalves;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if constexpr (T::kNorm) {
+    float v[NB * H];
+#pragma unroll
+    for (int m = 0; m < NB; ++m)
+#pragma unroll
+      for (int h = 0; h < H; ++h) v[m * H + h] = ss[m][h];
+    const float tot = warp_reduce_multi<NB * H>(v, lane);
+    if (warp_reduce_writer<NB * H>(lane)) red[warp * NB * H + warp_reduce_index<NB * H>(lane)] = tot;
+  }
+  consumer_sync();
+  if constexpr (T::kNorm) {
+    if (tid < NB * H) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < kGemvWarps; ++w) t += red[w * NB * H + tid];
+      const float len = (float)(p.K / H);
+      scale[tid] = rsqrtf(t / len + p.eps);
+    }
+    consumer_sync();
+  }
+  for (int e = tid; e < nrows * NB; e += kGemvThreads) {
+    const int r = e / NB, m = e - r * NB;
+    float y = 0.f;
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kGemvWarps; ++w) sum += part[(((size_t)r * kGemvWarps + w) * H + h) * NB + m];
+      y += T::kNorm ? sum * scale[m * H + h] : sum;
+    }
+    accs[e] = y;
+  }
+  consumer_sync();
+  epilogue<NB, MODE, TR>(p, accs, nrows);
+}
+
 template <int NB, int SR, int MODE, bool Q4>
 __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvParams p) {
   using T = ModeTraits<MODE>;
@@ -118,11 +194,10 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.K, KV = K >> 3;
   // rows are handed out in units of 2 where the epilogue pairs rows (RoPE, SwiGLU)
-  const int nunits = p.rows / T::kUnit;
-  const int ub = (int)((long long)blockIdx.x * nunits / gridDim.x);
-  const int ue = (int)((long long)(blockIdx.x + 1) * nunits / gridDim.x);
-  const int row0 = T::kUnit * ub, nrows = T::kUnit * (ue - ub);
-  const int max_rows = T::kUnit * ((nunits + gridDim.x - 1) / gridDim.x);
+  // tiles of whole stages that keep row pairs (RoPE, SwiGLU) together
+  constexpr int TR = SR >= T::kUnit ? SR : T::kUnit;
+  const int nrows = tiles_rows_of(p.rows, TR, gridDim.x, blockIdx.x);
+  const int max_rows = tiles_max_rows(p.rows, TR, gridDim.x);
   const int nst = p.nstage;
   const int szw = Q4 ? p.sz_stride : 0;  // (scale, zero) pairs per row
   const GemvSmem L = gemv_smem_layout(NB, SR, H, T::kBf16X ? 2 : 4, K, nst, max_rows, gemv_row_bytes(Q4, K, szw));
@@ -164,7 +239,7 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
         mbar_expect_tx(full0 + 8 * slot, (uint32_t)rows_here * (row_bytes + sz_bytes));
         const uint32_t dst = smem_addr(ring + (size_t)slot * L.stage_bytes);
         for (int r = 0; r < rows_here; ++r) {
-          const RowRef rr = row_ref<MODE>(p, p.row_base + row0 + st * SR + r);
+          const RowRef rr = row_ref<MODE>(p, p.row_base + tile_row<TR>(st * SR + r));
           if constexpr (Q4) {
             // codes, then the row's (scale, zero) pairs after the stage's SR code rows
             bulk_g2s(dst + r * row_bytes, q4_codes(p, rr), row_bytes, full0 + 8 * slot, pol);
@@ -349,44 +424,312 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
       if (lrow < nrows) part[(((size_t)lrow * kGemvWarps + warp) * H + h) * NB + m] = tot;
     }
   }
-  // RMSNorm scales 1 / sqrt(mean(x^2) + eps) per item and K half
-  if constexpr (T::kNorm) {
-    float v[NB * H];
+  gemv_finish<NB, MODE, TR>(p, ss, part, accs, red, scale, nrows);
+}
+
+// ------------------------------------- INT4, one item, on the tensor cores (mma.sync)
+// Single-item INT4 launches with K a multiple of 2048 run the dot products as warp-level
+// m16n8k16 bf16 MMAs.  The CUDA-core INT4 path spends several instructions per weight on
+// decoding and multiply-adds and is bound by instruction issue; here a code word becomes
+// bf16 pairs 128 + c by one AND-OR each (0x43 is the exponent of 128; a code fills the low
+// mantissa bits) and one MMA does 256 multiply-adds of a warp.  16 weight rows are the A
+// operand; the three bf16 parts x = x0 + x1 + x2 of the activations are columns 0-2 of the
+// n = 8 B operand, so the parts' products add up to float32 products; the accumulators are
+// float32.  The MMA reads its operands from registers, so the decoded codes feed it
+// directly (a tcgen05 MMA would need the decoded tile stored to shared or tensor memory).
+// The MMAs of one 128-input group start from the accumulator -136 * sum(x_p) in part
+// column p and so end on sum((c - 8) x_p); the group's scale and zero then update the row
+// sums: += scale * acc + zero * sum(x_p).
+//
+// A stage is one tile of 16 whole rows: their codes, their (scale, zero) rows and a 16-byte
+// header giving the tile-local row of each of the 16 slots.  The producer sorts the tile's
+// rows by their place in memory and copies each run of consecutive rows with one bulk copy
+// (one or two runs per tile: all rows, or the two halves of RoPE / gate-up pairs), since
+// many small copies stream far below the rate of a few large ones.  Warp w takes inputs
+// [w K / 16, (w + 1) K / 16) of every row; lane (g, q) of the MMA fragments loads the 16
+// bytes (32 codes) of rows g and g + 8 at inputs 128 G + 32 q of each of its groups G.  The
+// order of the 16 inputs of one MMA is free as long as A and B follow the same one, and the
+// B fragments are laid out in shared memory once per launch in that order, at
+// xfrag[mma * 12 + 4 * part + q].
+struct MmaSmem {
+  int xfrag_off, gsum_off, ring_off, stage, part_off, accs_off, red_off, scale_off, bar_off, flag_off, total;
+};
+
+__host__ __device__ inline MmaSmem mma_smem_layout(int H, int K, int sz_stride, int nstage, int max_rows) {
+  MmaSmem L;
+  L.xfrag_off = K * 4;                  // float32 x planes (stage_x) first
+  L.gsum_off = L.xfrag_off + K * 6;     // K / 16 MMAs x 12 lanes x 8 bytes
+  L.ring_off = (L.gsum_off + (K / 128) * 16 + 127) / 128 * 128;
+  L.stage = 16 * (K / 2) + 16 * sz_stride * 4 + 16;
+  L.part_off = L.ring_off + nstage * L.stage;
+  L.accs_off = L.part_off + max_rows * kGemvWarps * H * 4;
+  L.red_off = L.accs_off + max_rows * 4;
+  L.scale_off = L.red_off + kGemvWarps * H * 4;
+  L.bar_off = (L.scale_off + H * 4 + 15) / 16 * 16;
+  L.flag_off = L.bar_off + 2 * nstage * 8;
+  L.total = L.flag_off + 16;
+  return L;
+}
+
+// (lo, hi) -> bf16 pair, round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Three bf16 parts of (a, b), each the rounding of what the previous ones left.
+__device__ __forceinline__ void split3_bf16x2(float a, float b, uint32_t &p0, uint32_t &p1, uint32_t &p2) {
+  p0 = pack_bf16x2(a, b);
+  a -= bf_lo(p0);
+  b -= bf_hi(p0);
+  p1 = pack_bf16x2(a, b);
+  a -= bf_lo(p1);
+  b -= bf_hi(p1);
+  p2 = pack_bf16x2(a, b);
+}
+
+// Eight INT4 codes of one 32-bit word as bf16 pairs 128 + c, in the pair order
+// (0, 4), (1, 5), (2, 6), (3, 7) of their k offsets.
+__device__ __forceinline__ void q4_to_bf16x2(uint32_t w, uint32_t (&r)[4]) {
+  constexpr uint32_t m = 0x000F000Fu, e = 0x43004300u;
+  r[0] = (w & m) | e;
+  r[1] = ((w >> 4) & m) | e;
+  r[2] = ((w >> 8) & m) | e;
+  r[3] = ((w >> 12) & m) | e;
+}
+
+// d += A B for one m16n8k16 tile (A rows g / g + 8 in a0 a2 / a1 a3, B column g in b0 b1).
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The B fragments and the per-group part sums from the float32 x planes that stage_x
+// wrote.  Vector v (inputs 8v .. 8v + 7) is word v % 4 of lane q = (v / 4) % 4 in group
+// v / 16; its pairs (0, 4) .. (3, 7) are the B rows of MMAs 2 (v % 4) and 2 (v % 4) + 1.
+__device__ __forceinline__ void mma_stage_b(const unsigned char *xmem, int K, uint2 *xfrag, float4 *gsum) {
+  const int KV = K >> 3, lane = threadIdx.x & 31;
+  const float4 *xa = reinterpret_cast<const float4 *>(xmem), *xb = xa + KV;
+  for (int v = threadIdx.x; v < KV; v += kGemvThreads) {
+    const float4 lo = xa[v], hi = xb[v];
+    uint32_t p0[4], p1[4], p2[4];
+    split3_bf16x2(lo.x, hi.x, p0[0], p1[0], p2[0]);
+    split3_bf16x2(lo.y, hi.y, p0[1], p1[1], p2[1]);
+    split3_bf16x2(lo.z, hi.z, p0[2], p1[2], p2[2]);
+    split3_bf16x2(lo.w, hi.w, p0[3], p1[3], p2[3]);
+    const int grp = v >> 4, q = (v >> 2) & 3, i = v & 3;
 #pragma unroll
-    for (int m = 0; m < NB; ++m)
-#pragma unroll
-      for (int h = 0; h < H; ++h) v[m * H + h] = ss[m][h];
-    const float tot = warp_reduce_multi<NB * H>(v, lane);
-    if (warp_reduce_writer<NB * H>(lane)) red[warp * NB * H + warp_reduce_index<NB * H>(lane)] = tot;
-  }
-  consumer_sync();
-  if constexpr (T::kNorm) {
-    if (tid < NB * H) {
-      float t = 0.f;
-#pragma unroll
-      for (int w = 0; w < kGemvWarps; ++w) t += red[w * NB * H + tid];
-      const float len = (float)(K / H);
-      scale[tid] = rsqrtf(t / len + p.eps);
+    for (int t = 0; t < 2; ++t) {
+      uint2 *dst = xfrag + (size_t)(grp * 8 + 2 * i + t) * 12 + q;
+      dst[0] = make_uint2(p0[2 * t], p0[2 * t + 1]);
+      dst[4] = make_uint2(p1[2 * t], p1[2 * t + 1]);
+      dst[8] = make_uint2(p2[2 * t], p2[2 * t + 1]);
     }
-    consumer_sync();
-  }
-  for (int e = tid; e < nrows * NB; e += kGemvThreads) {
-    const int r = e / NB, m = e - r * NB;
-    float y = 0.f;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f;
 #pragma unroll
-    for (int h = 0; h < H; ++h) {
-      float sum = 0.f;
-#pragma unroll
-      for (int w = 0; w < kGemvWarps; ++w) sum += part[(((size_t)r * kGemvWarps + w) * H + h) * NB + m];
-      y += T::kNorm ? sum * scale[m * H + h] : sum;
+    for (int j = 0; j < 4; ++j) {
+      s0 += bf_lo(p0[j]) + bf_hi(p0[j]);
+      s1 += bf_lo(p1[j]) + bf_hi(p1[j]);
+      s2 += bf_lo(p2[j]) + bf_hi(p2[j]);
     }
-    accs[e] = y;
+    // the 16 vectors of a group sit on 16 consecutive lanes (K is a multiple of 2048)
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    }
+    if ((lane & 15) == 0) gsum[grp] = make_float4(s0, s1, s2, 0.f);
   }
+}
+
+template <int MODE, int NG>
+__global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_q4_mma_kernel(const GemvParams p) {
+  using T = ModeTraits<MODE>;
+  constexpr int H = T::kHalves;
+  constexpr int TR = 16;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = NG * 2048, CP = K / 2, SP = p.sz_stride * 4;  // NG 128-input groups per warp
+  const int nrows = tiles_rows_of(p.rows, TR, gridDim.x, blockIdx.x);
+  const int max_rows = tiles_max_rows(p.rows, TR, gridDim.x);
+  const int nst = p.nstage;
+  const MmaSmem L = mma_smem_layout(H, K, p.sz_stride, nst, max_rows);
+  const int ntiles = (nrows + TR - 1) / TR;
+
+  unsigned char *ring = smem + L.ring_off;
+  uint2 *xfrag = reinterpret_cast<uint2 *>(smem + L.xfrag_off);
+  float4 *gsum = reinterpret_cast<float4 *>(smem + L.gsum_off);
+  float *part = reinterpret_cast<float *>(smem + L.part_off);  // [max_rows][warps][H]
+  float *accs = reinterpret_cast<float *>(smem + L.accs_off);
+  float *red = reinterpret_cast<float *>(smem + L.red_off);
+  float *scale = reinterpret_cast<float *>(smem + L.scale_off);
+  const uint32_t full0 = smem_addr(smem + L.bar_off);
+  const uint32_t empty0 = full0 + 8 * nst;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
+  const int hdr_off = 16 * CP + 16 * SP;  // slot -> tile-local row, 0xFF for none
+
+  if (tid == 0) {
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, kGemvWarps);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  pdl_trigger();
+
+  if (warp == kGemvWarps) {
+    // ------------------------------------------------------------ producer warp
+    // lane r handles row r of the tile: its place in memory, its rank in memory order, and
+    // (where it starts a run of consecutive rows) the bulk copies of the run
+    const uint64_t pol = l2_evict_first_policy();
+    int issued = 0;
+    for (int st = 0; st < ntiles; ++st) {
+      const int slot = st % nst;
+      if (st >= nst) {
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(empty0 + 8 * slot, ((st / nst) - 1) & 1, abort_flag, p.status) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
+      const int rows_here = min(TR, nrows - st * TR);
+      unsigned char *stg = ring + (size_t)slot * L.stage;
+      const bool live = lane < rows_here;
+      RowRef rr = {0, 0};
+      if (live) rr = row_ref<MODE>(p, p.row_base + tile_row<TR>(st * TR + lane));
+      const unsigned long long key = live ? (((unsigned long long)rr.m << 40) | (unsigned long long)rr.row) : ~0ull;
+      int pos = 0;  // rank of this row in memory order (keys of live rows are distinct)
+#pragma unroll
+      for (int j = 0; j < TR; ++j) pos += __shfl_sync(0xffffffffu, key, j) < key ? 1 : 0;
+      if (live) stg[hdr_off + pos] = (unsigned char)lane;
+      else if (lane < TR) stg[hdr_off + lane] = 0xFF;  // slots rows_here .. TR - 1 hold no row
+      __syncwarp();
+      const int prev = live && pos > 0 ? stg[hdr_off + pos - 1] : 0;
+      const unsigned long long kprev = __shfl_sync(0xffffffffu, key, prev);
+      const bool start = live && (pos == 0 || kprev + 1 != key);
+      const unsigned starts = __reduce_or_sync(0xffffffffu, start ? (1u << pos) : 0u);
+      const uint32_t full = full0 + 8 * slot, dst = smem_addr(stg);
+      if (lane == 0) mbar_expect_tx(full, (uint32_t)rows_here * (uint32_t)(CP + SP));
+      __syncwarp();
+      if (start) {
+        const unsigned later = starts & ~((2u << pos) - 1u);
+        const int len = (later ? __ffs(later) - 1 : rows_here) - pos;
+        bulk_g2s(dst + pos * CP, q4_codes(p, rr), (uint32_t)(len * CP), full, pol);
+        bulk_g2s(dst + 16 * CP + pos * SP, q4_sz(p, rr), (uint32_t)(len * SP), full, pol);
+      }
+      issued = st + 1;
+    }
+    // Never leave copies in flight into shared memory: wait for the last stages issued.
+    if (lane == 0)
+      for (int st = max(0, issued - nst); st < issued; ++st)
+        mbar_wait(full0 + 8 * (st % nst), (st / nst) & 1, abort_flag, p.status);
+    return;
+  }
+
+  // ------------------------------------------------------------ consumer warps
+  pdl_wait();
+  float ss[1][H];
+  stage_x<1, MODE>(p, smem, ss);
   consumer_sync();
-  epilogue<NB, MODE>(p, accs, row0, nrows);
+  mma_stage_b(smem, K, xfrag, gsum);
+  consumer_sync();
+
+  const int g = lane >> 2, q = lane & 3;
+  // warps 0-7 cover the first K half, 8-15 the second (K = 2 n_embd where there are two)
+  const int h = H == 2 && warp >= kGemvWarps / 2 ? 1 : 0;
+  // The warp's B fragments and part sums are the same for every tile: up to two groups
+  // per warp they stay in registers (lanes of columns 3-7 hold zeros); with more, the B
+  // fragments of a group are loaded from shared memory when the group is processed.
+  constexpr bool kBReg = NG <= 2;
+  constexpr int NBR = kBReg ? NG : 1;
+  uint32_t bx[NBR][8], by[NBR][8];
+  auto load_b = [&](int G, uint32_t (&x)[8], uint32_t (&y)[8]) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const uint2 v = lane < 12 ? xfrag[(size_t)(G * 8 + m) * 12 + lane] : make_uint2(0u, 0u);
+      x[m] = v.x;
+      y[m] = v.y;
+    }
+  };
+  float2 S[NG];
+#pragma unroll
+  for (int j = 0; j < NG; ++j) {
+    const int G = warp * NG + j;
+    if constexpr (kBReg) load_b(G, bx[j], by[j]);
+    S[j] = q < 2 ? reinterpret_cast<const float2 *>(gsum + G)[q] : make_float2(0.f, 0.f);
+  }
+  const int a_off = g * CP + warp * NG * 64 + q * 16, b_off = a_off + 8 * CP;
+  const int sa_off = 16 * CP + g * SP + warp * NG * 4, sb_off = sa_off + 8 * SP;
+
+  for (int st = 0; st < ntiles; ++st) {
+    const int slot = st % nst;
+    const bool ok = mbar_wait(full0 + 8 * slot, (st / nst) & 1, abort_flag, p.status);
+    float tt[4] = {0.f, 0.f, 0.f, 0.f};
+    int ra_row = 0xFF, rb_row = 0xFF;
+    if (ok) {
+      const unsigned char *stg = ring + (size_t)slot * L.stage;
+      ra_row = stg[hdr_off + g];
+      rb_row = stg[hdr_off + g + 8];
+#pragma unroll
+      for (int j = 0; j < NG; ++j) {
+        // lane (g, q): 32 codes of rows g and g + 8 at inputs 128 G + 32 q
+        const uint4 ca = *reinterpret_cast<const uint4 *>(stg + a_off + j * 64);
+        const uint4 cb = *reinterpret_cast<const uint4 *>(stg + b_off + j * 64);
+        const uint32_t sa = *reinterpret_cast<const uint32_t *>(stg + sa_off + j * 4);
+        const uint32_t sb = *reinterpret_cast<const uint32_t *>(stg + sb_off + j * 4);
+        // two accumulator chains (MMAs of even / odd t); the first starts at -136 sum(x_p)
+        float acc0[4] = {-136.f * S[j].x, -136.f * S[j].y, -136.f * S[j].x, -136.f * S[j].y};
+        float acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w}, wb[4] = {cb.x, cb.y, cb.z, cb.w};
+        const int jb = kBReg ? j : 0;
+        if constexpr (!kBReg) load_b(warp * NG + j, bx[0], by[0]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t da[4], db[4];
+          q4_to_bf16x2(wa[i], da);
+          q4_to_bf16x2(wb[i], db);
+          mma_16816(acc0, da[0], db[0], da[1], db[1], bx[jb][2 * i], by[jb][2 * i]);
+          mma_16816(acc1, da[2], db[2], da[3], db[3], bx[jb][2 * i + 1], by[jb][2 * i + 1]);
+        }
+        tt[0] = fmaf(bf_lo(sa), acc0[0] + acc1[0], fmaf(bf_hi(sa), S[j].x, tt[0]));
+        tt[1] = fmaf(bf_lo(sa), acc0[1] + acc1[1], fmaf(bf_hi(sa), S[j].y, tt[1]));
+        tt[2] = fmaf(bf_lo(sb), acc0[2] + acc1[2], fmaf(bf_hi(sb), S[j].x, tt[2]));
+        tt[3] = fmaf(bf_lo(sb), acc0[3] + acc1[3], fmaf(bf_hi(sb), S[j].y, tt[3]));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+    // the tile's rows are complete: add the part columns and the four k-pair lanes
+    float v0 = tt[0] + tt[1], v1 = tt[2] + tt[3];
+    v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+    v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+    if (q == 0) {
+#pragma unroll
+      for (int hh = 0; hh < H; ++hh) {
+        if (ra_row < TR) part[((size_t)(st * TR + ra_row) * kGemvWarps + warp) * H + hh] = hh == h ? v0 : 0.f;
+        if (rb_row < TR) part[((size_t)(st * TR + rb_row) * kGemvWarps + warp) * H + hh] = hh == h ? v1 : 0.f;
+      }
+    }
+  }
+  gemv_finish<1, MODE, TR>(p, ss, part, accs, red, scale, nrows);
 }
 
 // ------------------------------------------------------------------ launcher
+// Ring depth: about 96 KB of weights in flight per SM (at least two stages).  Deeper rings
+// measured slower: 152 SMs with ~200 KB each outstanding stream below the rate of ~100 KB.
+constexpr int kRingBytes = 96 * 1024;
+inline int ring_stages_cap(int stage_bytes) {
+  const int n = kRingBytes / stage_bytes;
+  return n < 2 ? 2 : (n > 8 ? 8 : n);
+}
+
 // Most rows per ring stage: a stage's sums fit one warp reduction (32 / (NB * halves)),
 // at most 8, and for INT4 with several items at most 2 / (NB / 2) so that the per-row sums
 // and the decoded codes of a stage stay in registers (one item keeps 8 rows: the stage's
@@ -421,13 +764,16 @@ static int stage_rows(int K, int NB, int max_rows, int row_bytes) {
 }
 
 template <int NB, int SR, int MODE, bool Q4>
-static cudaError_t launch_one(GemvParams p, int grid, int max_rows, cudaStream_t st, bool pdl) {
+static cudaError_t launch_one(GemvParams p, int grid, cudaStream_t st, bool pdl) {
   using T = ModeTraits<MODE>;
+  constexpr int TR = SR >= T::kUnit ? SR : T::kUnit;
+  grid = std::max(1, std::min(grid, (p.rows + TR - 1) / TR));
+  const int max_rows = tiles_max_rows(p.rows, TR, grid);
   const int rb = gemv_row_bytes(Q4, p.K, p.sz_stride);
   const GemvSmem L0 = gemv_smem_layout(NB, SR, T::kHalves, T::kBf16X ? 2 : 4, p.K, 0, max_rows, rb);
   const long long room = (long long)kGemvSmemLimit - L0.total - 64;
   int nst = (int)(room / (SR * rb + 16));
-  if (nst > 8) nst = 8;
+  nst = std::min(nst, ring_stages_cap(SR * rb));
   if (nst < 2) return cudaErrorInvalidValue;
   p.nstage = nst;
   const GemvSmem L = gemv_smem_layout(NB, SR, T::kHalves, T::kBf16X ? 2 : 4, p.K, nst, max_rows, rb);
@@ -450,18 +796,62 @@ static cudaError_t dispatch_sr(const GemvParams &p, int grid, cudaStream_t st, b
   const int nunits = p.rows / T::kUnit;
   if (grid > nunits) grid = nunits;
   if (grid < 1) grid = 1;
-  const int max_rows = T::kUnit * ((nunits + grid - 1) / grid);
+  const int max_rows = tiles_max_rows_bound(p.rows, grid);
   constexpr int SRMAX = sr_max<NB, MODE, Q4>();
   switch (stage_rows<MODE, Q4>(p.K, NB, max_rows, gemv_row_bytes(Q4, p.K, p.sz_stride))) {
-    case 1: return launch_one<NB, 1, MODE, Q4>(p, grid, max_rows, st, pdl);
-    case 2: return launch_one<NB, (SRMAX >= 2 ? 2 : 1), MODE, Q4>(p, grid, max_rows, st, pdl);
-    case 4: return launch_one<NB, (SRMAX >= 4 ? 4 : 1), MODE, Q4>(p, grid, max_rows, st, pdl);
-    default: return launch_one<NB, SRMAX, MODE, Q4>(p, grid, max_rows, st, pdl);
+    case 1: return launch_one<NB, 1, MODE, Q4>(p, grid, st, pdl);
+    case 2: return launch_one<NB, (SRMAX >= 2 ? 2 : 1), MODE, Q4>(p, grid, st, pdl);
+    case 4: return launch_one<NB, (SRMAX >= 4 ? 4 : 1), MODE, Q4>(p, grid, st, pdl);
+    default: return launch_one<NB, SRMAX, MODE, Q4>(p, grid, st, pdl);
+  }
+}
+
+// Ring stages of the INT4 tensor-core GEMV for this launch (0: it does not apply: one item
+// only, K a multiple of 2048, and x, its fragments and two whole-row tiles must fit in
+// shared memory).  About 128 KB in flight per SM, at most four stages.
+template <int MODE>
+static int q4_mma_stages(const GemvParams &p, int grid) {
+  using T = ModeTraits<MODE>;
+  if (T::kBf16X || p.K % 2048 || p.K > 4 * 2048 || p.items != 1) return 0;
+  const int gr = std::max(1, std::min(grid, (p.rows + 15) / 16));
+  const MmaSmem L0 = mma_smem_layout(T::kHalves, p.K, p.sz_stride, 0, tiles_max_rows(p.rows, 16, gr));
+  const long long room = (long long)kGemvSmemLimit - L0.total - 64;
+  int nst = (int)(room / (L0.stage + 16));
+  nst = std::min(nst, std::max(2, std::min(4, (128 * 1024) / L0.stage)));
+  return nst >= 2 ? nst : 0;
+}
+
+template <int MODE>
+static cudaError_t launch_q4_mma(GemvParams p, int grid, int nst, cudaStream_t st, bool pdl) {
+  using T = ModeTraits<MODE>;
+  grid = std::max(1, std::min(grid, (p.rows + 15) / 16));
+  p.nstage = nst;
+  const MmaSmem L = mma_smem_layout(T::kHalves, p.K, p.sz_stride, nst, tiles_max_rows(p.rows, 16, grid));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemvCtaThreads);
+  cfg.dynamicSmemBytes = (size_t)L.total;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  switch (p.K / 2048) {
+    case 1: return cudaLaunchKernelEx(&cfg, gemv_q4_mma_kernel<MODE, 1>, p);
+    case 2: return cudaLaunchKernelEx(&cfg, gemv_q4_mma_kernel<MODE, 2>, p);
+    case 3: return cudaLaunchKernelEx(&cfg, gemv_q4_mma_kernel<MODE, 3>, p);
+    case 4: return cudaLaunchKernelEx(&cfg, gemv_q4_mma_kernel<MODE, 4>, p);
+    default: return cudaErrorInvalidValue;
   }
 }
 
 template <int MODE, bool Q4>
 static cudaError_t dispatch_nb(const GemvParams &p, int nb, int grid, cudaStream_t st, bool pdl) {
+  if constexpr (Q4 && !ModeTraits<MODE>::kBf16X) {
+    const int nst = nb == 1 ? q4_mma_stages<MODE>(p, grid) : 0;
+    if (nst) return launch_q4_mma<MODE>(p, grid, nst, st, pdl);
+  }
   switch (nb) {
     case 1: return dispatch_sr<1, MODE, Q4>(p, grid, st, pdl);
     case 2: return dispatch_sr<2, MODE, Q4>(p, grid, st, pdl);
@@ -489,6 +879,14 @@ static cudaError_t prepare_nb() {
 template <int MODE, bool Q4>
 static cudaError_t prepare_mode() {
   cudaError_t e = prepare_nb<1, MODE, Q4>();
+  if constexpr (Q4 && !ModeTraits<MODE>::kBf16X) {
+    const int lim = (int)kGemvSmemLimit;
+    const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_q4_mma_kernel<MODE, 1>, a, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_q4_mma_kernel<MODE, 2>, a, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_q4_mma_kernel<MODE, 3>, a, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_q4_mma_kernel<MODE, 4>, a, lim);
+  }
   if (e == cudaSuccess) e = prepare_nb<2, MODE, Q4>();
   if (e == cudaSuccess) e = prepare_nb<4, MODE, Q4>();
   if (e == cudaSuccess) e = prepare_nb<8, MODE, Q4>();
