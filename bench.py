@@ -55,9 +55,12 @@ CONFIGS = {
 # byte the profiled ones (sha256 over the listed csrc files); the summaries under
 # profiles/ give the commands.  Keyed by (config, dominant projection or "attn").
 PROFILED_TRAFFIC = {
-    ("c2", "lmhead"): {"bytes": 262220288 + 3067392,
+    ("c2", "lmhead"): {"bytes": 262226688 + 2808832,
                        "sources": ("gemv.cu", "gemv_kernel.cuh", "epilogue.cuh", "common.cuh"),
-                       "sha256": "a4f4561c88eedfc13af11a289778e2698064ac754aed575b99af06a806bb8048"},
+                       "sha256": "b59c2ffd8f8a209452d7b0a58c8b20efa1088f37516967e46927cfa5f9d4df07"},
+    ("c2", "lmhead", "bf16", "int4"): {"bytes": 69714432 + 257280,
+                                      "sources": ("gemv_q4.cu", "gemv_kernel.cuh", "epilogue.cuh", "common.cuh"),
+                                      "sha256": "4accf5f8fc63cdd4dc1e2791871c299f1b8fb8020d58b24314b2673bcf84f1dc"},
     ("c4", "attn"): {"bytes": 538557184 + 3470336,
                      "sources": ("attention.cu", "common.cuh"),
                      "sha256": "4f4ce1b4205b28d46abaf0fcbb7a89305e1b24cec17f1d1e181340df05345e37"},
@@ -70,9 +73,13 @@ PROFILED_TRAFFIC = {
 }
 
 
-def profiled_traffic(config: str, kind: str, kv_format: str = "bf16"):
+def profiled_traffic(config: str, kind: str, kv_format: str = "bf16", weights: str = "bf16"):
     import hashlib
-    e = PROFILED_TRAFFIC.get((config, kind) if kv_format == "bf16" else (config, kind, kv_format))
+    if weights != "bf16":
+        key = (config, kind, kv_format, weights)
+    else:
+        key = (config, kind) if kv_format == "bf16" else (config, kind, kv_format)
+    e = PROFILED_TRAFFIC.get(key)
     if e is None:
         return None
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "eagle_speculative_decode_gb300", "csrc")
@@ -568,7 +575,7 @@ def run_mine(args, cfg):
         "roofline": {"bound": "hbm", "kernel": kernel_label(dominant, B, args.weights),
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": (achieved / hbm_peak) if achieved else None,
-                     "traffic": profiled_traffic(args.config, dominant, args.kv_format)
+                     "traffic": profiled_traffic(args.config, dominant, args.kv_format, args.weights)
                      if args.weights == "bf16" else None,
                      "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
                      "bytes_per_launch": dom_bytes, "us_per_launch": kern_us.get(dominant)},

@@ -11,7 +11,7 @@
 // (pairs kept together), round robin, so that the SMs stream neighbouring parts of the
 // weights at any moment.  A producer warp streams a CTA's rows, SR whole rows per stage
 // (<= 32 KB), with bulk copies (cp.async.bulk, TMA) into a shared-memory ring of about
-// 96 KB guarded by mbarriers (deeper rings streamed slower).  It starts before the kernel waits on its predecessor (programmatic
+// 128 KB guarded by mbarriers.  It starts before the kernel waits on its predecessor (programmatic
 // dependent launch), so the next weights are already in flight while the previous
 // kernel drains.  Sixteen consumer warps stage x (normalised where the op says so) in
 // shared memory (float32 in two float4 planes -- elements 0-3 and 4-7 of each 8-element
@@ -429,20 +429,22 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
 
 // ------------------------------------- INT4, one item, on the tensor cores (mma.sync)
 // Single-item INT4 launches with K a multiple of 2048 run the dot products as warp-level
-// m16n8k16 bf16 MMAs.  The CUDA-core INT4 path spends several instructions per weight on
-// decoding and multiply-adds and is bound by instruction issue; here a code word becomes
-// bf16 pairs 128 + c by one AND-OR each (0x43 is the exponent of 128; a code fills the low
-// mantissa bits) and one MMA does 256 multiply-adds of a warp.  16 weight rows are the A
-// operand; the three bf16 parts x = x0 + x1 + x2 of the activations are columns 0-2 of the
-// n = 8 B operand, so the parts' products add up to float32 products; the accumulators are
-// float32.  The MMA reads its operands from registers, so the decoded codes feed it
-// directly (a tcgen05 MMA would need the decoded tile stored to shared or tensor memory).
-// The MMAs of one 128-input group start from the accumulator -136 * sum(x_p) in part
-// column p and so end on sum((c - 8) x_p); the group's scale and zero then update the row
-// sums: += scale * acc + zero * sum(x_p).
+// m16n8k16 fp16 MMAs.  The CUDA-core INT4 path spends several instructions per weight on
+// decoding and multiply-adds and is bound by instruction issue; here 16 weight rows are
+// the A operand and one MMA does 256 multiply-adds of a warp.  A code word becomes fp16
+// pairs with one AND-OR each (0x64 is the exponent of 1024, whose 10-bit mantissa holds a
+// nibble in bits 0-3 as 1024 + c and in bits 4-7 as 1024 + 16 c; one shift brings bytes 1
+// and 3 down) and then c - 8 exactly by one packed fp16 add or multiply-add, which runs on
+// the FMA pipe while the AND-ORs fill the ALU pipe.  The activations enter as three fp16
+// parts x s = x0 + x1 + x2 in columns 0-2 of the n = 8 B operand, s a power of two per
+// 128-input group that puts the group's largest |x| s in [2^14, 2^15) (no overflow, and
+// the parts keep float32 accuracy); products are exact and the accumulators float32.  The
+// row sums take scale / s * acc + zero * sum(x) per group.  The MMA reads its operands
+// from registers, so the decoded codes feed it directly (a tcgen05 MMA would need them
+// stored to shared or tensor memory first).
 //
 // A stage is one tile of 16 whole rows: their codes, their (scale, zero) rows and a 16-byte
-// header giving the tile-local row of each of the 16 slots.  The producer sorts the tile's
+// header giving the tile-local row of each of the 16 slots.  The producer ranks the tile's
 // rows by their place in memory and copies each run of consecutive rows with one bulk copy
 // (one or two runs per tile: all rows, or the two halves of RoPE / gate-up pairs), since
 // many small copies stream far below the rate of a few large ones.  Warp w takes inputs
@@ -471,56 +473,87 @@ __host__ __device__ inline MmaSmem mma_smem_layout(int H, int K, int sz_stride, 
   return L;
 }
 
-// (lo, hi) -> bf16 pair, round to nearest even.
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+// (lo, hi) -> fp16 pair, round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-
-// Three bf16 parts of (a, b), each the rounding of what the previous ones left.
-__device__ __forceinline__ void split3_bf16x2(float a, float b, uint32_t &p0, uint32_t &p1, uint32_t &p2) {
-  p0 = pack_bf16x2(a, b);
-  a -= bf_lo(p0);
-  b -= bf_hi(p0);
-  p1 = pack_bf16x2(a, b);
-  a -= bf_lo(p1);
-  b -= bf_hi(p1);
-  p2 = pack_bf16x2(a, b);
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t u) {
+  float2 f;
+  asm("{\n .reg .f16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}\n"
+      : "=f"(f.x), "=f"(f.y)
+      : "r"(u));
+  return f;
 }
 
-// Eight INT4 codes of one 32-bit word as bf16 pairs 128 + c, in the pair order
+// Three fp16 parts of (a, b), each the rounding of what the previous ones left.
+__device__ __forceinline__ void split3_f16x2(float a, float b, uint32_t &p0, uint32_t &p1, uint32_t &p2) {
+  p0 = pack_f16x2(a, b);
+  float2 f = f16x2_to_f32x2(p0);
+  a -= f.x;
+  b -= f.y;
+  p1 = pack_f16x2(a, b);
+  f = f16x2_to_f32x2(p1);
+  a -= f.x;
+  b -= f.y;
+  p2 = pack_f16x2(a, b);
+}
+
+// Eight INT4 codes of one 32-bit word as fp16 pairs c - 8 (exact), in the pair order
 // (0, 4), (1, 5), (2, 6), (3, 7) of their k offsets.
-__device__ __forceinline__ void q4_to_bf16x2(uint32_t w, uint32_t (&r)[4]) {
-  constexpr uint32_t m = 0x000F000Fu, e = 0x43004300u;
-  r[0] = (w & m) | e;
-  r[1] = ((w >> 4) & m) | e;
-  r[2] = ((w >> 8) & m) | e;
-  r[3] = ((w >> 12) & m) | e;
+__device__ __forceinline__ void q4_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
+  constexpr uint32_t e = 0x64006400u;              // 1024, 1024
+  constexpr uint32_t lo_bias = 0xE408E408u;        // -1032, -1032
+  constexpr uint32_t sixteenth = 0x2C002C00u;      // 1/16, 1/16
+  constexpr uint32_t hi_bias = 0xD480D480u;        // -72, -72
+  const uint32_t w8 = w >> 8;
+  uint32_t t0 = (w & 0x000F000Fu) | e, t1 = (w & 0x00F000F0u) | e;    // 1024 + c, 1024 + 16 c
+  uint32_t t2 = (w8 & 0x000F000Fu) | e, t3 = (w8 & 0x00F000F0u) | e;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r[0]) : "r"(t0), "r"(lo_bias));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r[1]) : "r"(t1), "r"(sixteenth), "r"(hi_bias));
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r[2]) : "r"(t2), "r"(lo_bias));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r[3]) : "r"(t3), "r"(sixteenth), "r"(hi_bias));
 }
 
-// d += A B for one m16n8k16 tile (A rows g / g + 8 in a0 a2 / a1 a3, B column g in b0 b1).
+// d += A B for one m16n8k16 fp16 tile (A rows g / g + 8 in a0 a2 / a1 a3, B column g in
+// b0 b1), float32 accumulators.
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// The B fragments and the per-group part sums from the float32 x planes that stage_x
-// wrote.  Vector v (inputs 8v .. 8v + 7) is word v % 4 of lane q = (v / 4) % 4 in group
-// v / 16; its pairs (0, 4) .. (3, 7) are the B rows of MMAs 2 (v % 4) and 2 (v % 4) + 1.
-__device__ __forceinline__ void mma_stage_b(const unsigned char *xmem, int K, uint2 *xfrag, float4 *gsum) {
+// The B fragments and the per-group (sum(x), 1 / s) from the float32 x planes that
+// stage_x wrote.  Vector v (inputs 8v .. 8v + 7) is word v % 4 of lane q = (v / 4) % 4 in
+// group v / 16 (whose 16 vectors sit on 16 consecutive lanes, K being a multiple of 2048);
+// its pairs (0, 4) .. (3, 7) are the B rows of MMAs 2 (v % 4) and 2 (v % 4) + 1.
+__device__ __forceinline__ void mma_stage_b(const unsigned char *xmem, int K, uint2 *xfrag, float2 *gsum) {
   const int KV = K >> 3, lane = threadIdx.x & 31;
   const float4 *xa = reinterpret_cast<const float4 *>(xmem), *xb = xa + KV;
   for (int v = threadIdx.x; v < KV; v += kGemvThreads) {
     const float4 lo = xa[v], hi = xb[v];
+    float mx = fmaxf(fmaxf(fmaxf(fabsf(lo.x), fabsf(lo.y)), fmaxf(fabsf(lo.z), fabsf(lo.w))),
+                     fmaxf(fmaxf(fabsf(hi.x), fabsf(hi.y)), fmaxf(fabsf(hi.z), fabsf(hi.w))));
+    float sum = ((lo.x + lo.y) + (lo.z + lo.w)) + ((hi.x + hi.y) + (hi.z + hi.w));
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    }
+    // s = 2^(141 - E) for a group maximum in [2^(E - 127), 2^(E - 126)): max * s in
+    // [2^14, 2^15); exponents clamped to the normal range (an all-zero group takes s = 1)
+    const int E = (int)((__float_as_uint(mx) >> 23) & 0xFFu);
+    int es = E == 0 ? 127 : 268 - E;
+    es = es < 1 ? 1 : (es > 253 ? 253 : es);
+    const float sc = __uint_as_float((uint32_t)es << 23), inv = __uint_as_float((uint32_t)(254 - es) << 23);
     uint32_t p0[4], p1[4], p2[4];
-    split3_bf16x2(lo.x, hi.x, p0[0], p1[0], p2[0]);
-    split3_bf16x2(lo.y, hi.y, p0[1], p1[1], p2[1]);
-    split3_bf16x2(lo.z, hi.z, p0[2], p1[2], p2[2]);
-    split3_bf16x2(lo.w, hi.w, p0[3], p1[3], p2[3]);
+    split3_f16x2(lo.x * sc, hi.x * sc, p0[0], p1[0], p2[0]);
+    split3_f16x2(lo.y * sc, hi.y * sc, p0[1], p1[1], p2[1]);
+    split3_f16x2(lo.z * sc, hi.z * sc, p0[2], p1[2], p2[2]);
+    split3_f16x2(lo.w * sc, hi.w * sc, p0[3], p1[3], p2[3]);
     const int grp = v >> 4, q = (v >> 2) & 3, i = v & 3;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -529,21 +562,7 @@ __device__ __forceinline__ void mma_stage_b(const unsigned char *xmem, int K, ui
       dst[4] = make_uint2(p1[2 * t], p1[2 * t + 1]);
       dst[8] = make_uint2(p2[2 * t], p2[2 * t + 1]);
     }
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      s0 += bf_lo(p0[j]) + bf_hi(p0[j]);
-      s1 += bf_lo(p1[j]) + bf_hi(p1[j]);
-      s2 += bf_lo(p2[j]) + bf_hi(p2[j]);
-    }
-    // the 16 vectors of a group sit on 16 consecutive lanes (K is a multiple of 2048)
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) {
-      s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-    }
-    if ((lane & 15) == 0) gsum[grp] = make_float4(s0, s1, s2, 0.f);
+    if ((lane & 15) == 0) gsum[grp] = make_float2(sum, inv);
   }
 }
 
@@ -563,7 +582,7 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_q4_mma_kernel(const G
 
   unsigned char *ring = smem + L.ring_off;
   uint2 *xfrag = reinterpret_cast<uint2 *>(smem + L.xfrag_off);
-  float4 *gsum = reinterpret_cast<float4 *>(smem + L.gsum_off);
+  float2 *gsum = reinterpret_cast<float2 *>(smem + L.gsum_off);
   float *part = reinterpret_cast<float *>(smem + L.part_off);  // [max_rows][warps][H]
   float *accs = reinterpret_cast<float *>(smem + L.accs_off);
   float *red = reinterpret_cast<float *>(smem + L.red_off);
@@ -656,12 +675,14 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_q4_mma_kernel(const G
       y[m] = v.y;
     }
   };
-  float2 S[NG];
+  float S[NG], inv_s[NG];  // sum(x) on lanes of column 0 (q = 0), else 0; 1 / s
 #pragma unroll
   for (int j = 0; j < NG; ++j) {
     const int G = warp * NG + j;
     if constexpr (kBReg) load_b(G, bx[j], by[j]);
-    S[j] = q < 2 ? reinterpret_cast<const float2 *>(gsum + G)[q] : make_float2(0.f, 0.f);
+    const float2 gs = gsum[G];
+    S[j] = q == 0 ? gs.x : 0.f;
+    inv_s[j] = gs.y;
   }
   const int a_off = g * CP + warp * NG * 64 + q * 16, b_off = a_off + 8 * CP;
   const int sa_off = 16 * CP + g * SP + warp * NG * 4, sb_off = sa_off + 8 * SP;
@@ -682,24 +703,24 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_q4_mma_kernel(const G
         const uint4 cb = *reinterpret_cast<const uint4 *>(stg + b_off + j * 64);
         const uint32_t sa = *reinterpret_cast<const uint32_t *>(stg + sa_off + j * 4);
         const uint32_t sb = *reinterpret_cast<const uint32_t *>(stg + sb_off + j * 4);
-        // two accumulator chains (MMAs of even / odd t); the first starts at -136 sum(x_p)
-        float acc0[4] = {-136.f * S[j].x, -136.f * S[j].y, -136.f * S[j].x, -136.f * S[j].y};
-        float acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        // two accumulator chains (MMAs of even / odd t)
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
         const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w}, wb[4] = {cb.x, cb.y, cb.z, cb.w};
         const int jb = kBReg ? j : 0;
         if constexpr (!kBReg) load_b(warp * NG + j, bx[0], by[0]);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint32_t da[4], db[4];
-          q4_to_bf16x2(wa[i], da);
-          q4_to_bf16x2(wb[i], db);
+          q4_to_f16x2(wa[i], da);
+          q4_to_f16x2(wb[i], db);
           mma_16816(acc0, da[0], db[0], da[1], db[1], bx[jb][2 * i], by[jb][2 * i]);
           mma_16816(acc1, da[2], db[2], da[3], db[3], bx[jb][2 * i + 1], by[jb][2 * i + 1]);
         }
-        tt[0] = fmaf(bf_lo(sa), acc0[0] + acc1[0], fmaf(bf_hi(sa), S[j].x, tt[0]));
-        tt[1] = fmaf(bf_lo(sa), acc0[1] + acc1[1], fmaf(bf_hi(sa), S[j].y, tt[1]));
-        tt[2] = fmaf(bf_lo(sb), acc0[2] + acc1[2], fmaf(bf_hi(sb), S[j].x, tt[2]));
-        tt[3] = fmaf(bf_lo(sb), acc0[3] + acc1[3], fmaf(bf_hi(sb), S[j].y, tt[3]));
+        const float fa = bf_lo(sa) * inv_s[j], fb = bf_lo(sb) * inv_s[j];
+        tt[0] = fmaf(fa, acc0[0] + acc1[0], fmaf(bf_hi(sa), S[j], tt[0]));
+        tt[1] = fmaf(fa, acc0[1] + acc1[1], tt[1]);
+        tt[2] = fmaf(fb, acc0[2] + acc1[2], fmaf(bf_hi(sb), S[j], tt[2]));
+        tt[3] = fmaf(fb, acc0[3] + acc1[3], tt[3]);
       }
     }
     __syncwarp();
@@ -722,9 +743,10 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_q4_mma_kernel(const G
 }
 
 // ------------------------------------------------------------------ launcher
-// Ring depth: about 96 KB of weights in flight per SM (at least two stages).  Deeper rings
-// measured slower: 152 SMs with ~200 KB each outstanding stream below the rate of ~100 KB.
-constexpr int kRingBytes = 96 * 1024;
+// Ring depth: about 128 KB of weights in flight per SM (at least two stages).  Measured on
+// the batch-1 chain: 64 KB 169.5, 96 KB 151.2, 128 KB 147.8 us per step, and the earlier
+// room-limited ring (~200 KB) 152.3.
+constexpr int kRingBytes = 128 * 1024;
 inline int ring_stages_cap(int stage_bytes) {
   const int n = kRingBytes / stage_bytes;
   return n < 2 ? 2 : (n > 8 ? 8 : n);
@@ -808,7 +830,11 @@ static cudaError_t dispatch_sr(const GemvParams &p, int grid, cudaStream_t st, b
 
 // Ring stages of the INT4 tensor-core GEMV for this launch (0: it does not apply: one item
 // only, K a multiple of 2048, and x, its fragments and two whole-row tiles must fit in
-// shared memory).  About 128 KB in flight per SM, at most four stages.
+// shared memory).  As many stages as fit, up to kQ4MmaMaxStages: the consumers hold a
+// stage for about a thousand cycles of decoding and MMAs, so the ring must cover that as
+// well as the DRAM latency.
+constexpr int kQ4MmaMaxStages = 6;
+
 template <int MODE>
 static int q4_mma_stages(const GemvParams &p, int grid) {
   using T = ModeTraits<MODE>;
@@ -817,7 +843,7 @@ static int q4_mma_stages(const GemvParams &p, int grid) {
   const MmaSmem L0 = mma_smem_layout(T::kHalves, p.K, p.sz_stride, 0, tiles_max_rows(p.rows, 16, gr));
   const long long room = (long long)kGemvSmemLimit - L0.total - 64;
   int nst = (int)(room / (L0.stage + 16));
-  nst = std::min(nst, std::max(2, std::min(4, (128 * 1024) / L0.stage)));
+  nst = std::min(nst, kQ4MmaMaxStages);
   return nst >= 2 ? nst : 0;
 }
 
