@@ -64,9 +64,9 @@ PROFILED_TRAFFIC = {
     ("c4", "attn"): {"bytes": 538557184 + 3470336,
                      "sources": ("attention.cu", "common.cuh"),
                      "sha256": "4f4ce1b4205b28d46abaf0fcbb7a89305e1b24cec17f1d1e181340df05345e37"},
-    ("c4", "lmhead"): {"bytes": 265020160 + 5921536,
+    ("c4", "lmhead"): {"bytes": 265011456 + 5742080,
                        "sources": ("gemm_tc.cu", "epilogue.cuh", "common.cuh"),
-                       "sha256": "9ca8e562a07fabf4986de9287f89e9cc08af99746dba11d908355244d3a25169"},
+                       "sha256": "378a7a09171ccb4ed6740f2bb2a0831246676d48c33377a4bac717dbd97cd2a7"},
     ("c5", "attn", "q8_0/q5_1"): {"bytes": 243912448 + 3330816,
                                   "sources": ("attention.cu", "common.cuh"),
                                   "sha256": "4f4ce1b4205b28d46abaf0fcbb7a89305e1b24cec17f1d1e181340df05345e37"},
@@ -91,13 +91,14 @@ def profiled_traffic(config: str, kind: str, kv_format: str = "bf16", weights: s
 
 
 def kernel_label(kind: str, batch: int, weights: str = "bf16") -> str:
-    """Name of the kernel that runs a phase at this batch (bf16 projections of three or
-    more items run on the tensor cores, smaller ones and every INT4 one on the CUDA-core
-    GEMV)."""
+    """Name of the kernel that runs a phase at this batch on the bench's drafter geometry
+    (bf16 projections of three or more items run on the tcgen05 GEMM, smaller ones on the
+    CUDA-core GEMV; single-item INT4 projections with K <= 8192 on the mma.sync tensor-core
+    GEMV, the rest of INT4 on the CUDA-core GEMV)."""
     if kind == "attn":
         return "attention"
     if weights == "int4":
-        return f"{kind} INT4 GEMV"
+        return f"{kind} INT4 mma.sync GEMV" if batch == 1 and kind != "down" else f"{kind} INT4 GEMV"
     return f"{kind} tcgen05 GEMM" if batch >= 3 else f"{kind} GEMV"
 
 
