@@ -208,6 +208,25 @@ def round_bytes(geo, B, gamma, ctx_len, kv_format="bf16", weights="bf16"):
     return chain + rebuild
 
 
+NOMINAL_HBM_GBS = 8000.0  # HBM3e bandwidth of the part's datasheet (≈8 TB/s)
+
+
+def static_config(args, cfg, world=1):
+    """The `config` object both arms print: the workload and the storage formats."""
+    lo, hi = cfg["prompt"]
+    return {"workload": cfg["workload"], "name": args.config, "batch": cfg["B"], "gamma": cfg["gamma"],
+            "prompt": [lo, hi], "page_size": cfg["page_size"],
+            "kv_format": args.kv_format, "weights": args.weights,
+            "storage": ("bf16 weights" if args.weights == "bf16" else
+                        "INT4 projections (128-wide groups, bf16 scale and zero), bf16 fc / norms / embedding")
+                       + (", bf16 KV" if args.kv_format == "bf16" else ", q8_0 K / q5_1 V cache")
+                       + ", float32 activations and accumulation",
+            "l2": "inputs larger than L2: 0.8 GB of weights streamed per draft step",
+            "step": "chain of gamma draft steps + rewind + accept + rebuild (encode of "
+                    "gamma+1 verify features, k/v teacher forcing)",
+            "parallelism": f"replicas x{world}"}
+
+
 def make_bench_weights(geo, weights):
     from eagle_speculative_decode_gb300 import synth
     return synth.make_int4_weights(geo, seed=0) if weights == "int4" else synth.make_weights(geo, seed=0)
@@ -295,7 +314,11 @@ def replica_throughput(world, tokens_local: float, elapsed_ms_local: float):
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, cfg):
-    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    """The reference arm is the float64 CPU oracle, timed as it stands on the host cores on
+    the unit `cpu_baseline` times: one step = one chain of gamma draft steps of one sequence
+    from a prefilled state of the config's prompt length (at most 512 tokens, so that a
+    step stays a bounded sample; prefill not timed)."""
+    rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     from eagle_speculative_decode_gb300 import synth  # noqa: F401  (generators only)
@@ -303,26 +326,27 @@ def run_reference(args, cfg):
     geo = synth.GEOMETRIES[cfg["geom"]]
     wts = make_bench_weights(geo, args.weights)
     dr = O.Drafter(geo, wts.bits, wts.d2t, kv_format=args.kv_format, int4=wts.int4)
-    P = 32
+    del wts
+    P = min(int(cfg["prompt"][0]), 512)
     toks = synth.make_tokens((P + 1,), geo, 1)
     aux = synth.make_aux((P,), geo, 1)
     st = O.prefill(dr, toks[:P], int(toks[P]), aux)
     gamma = cfg["gamma"]
     for _ in range(args.warmup):
-        O.draft_step(dr, int(st.tok), st.g, st.k, st.v, st.kv_len)
+        O.draft_chain(dr, st, gamma)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        O.draft_step(dr, int(st.tok), st.g, st.k, st.v, st.kv_len)
+        O.draft_chain(dr, st, gamma)
     dt = time.perf_counter() - t0
-    value = args.steps / dt
-    sample = (f"each step = one float64 oracle draft step of one sequence ({cfg['geom']} geometry, "
-              f"{P}-token prefilled state); the benchmark's batch of {cfg['B']} and gamma {gamma} "
-              "are not reproduced on the CPU")
+    value = args.steps * gamma / dt
+    sample = (f"each step = one chain of {gamma} float64 oracle draft steps of one sequence from a "
+              f"{P}-token prefilled state ({cfg['geom']} geometry, prefill not timed); the benchmark's "
+              f"batch of {cfg['B']} is not reproduced on the CPU")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "draft tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg["workload"], "kv_format": args.kv_format, "weights": args.weights},
+            "config": static_config(args, cfg, int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": {"value": value, "unit": "draft tokens/s", "cores": os.cpu_count(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "draft tokens/s", "h2d_bytes_per_step": 0,
@@ -480,6 +504,8 @@ def run_mine(args, cfg):
     achieved = dom_bytes / (kern_us[dominant] * 1e-6) / 1e9 if kern_us else None
     rb = round_bytes(geo, B, gamma, int(mean_ctx), args.kv_format, args.weights)
     step_frac = (rb / (ms_per_step * 1e-3) / 1e9) / hbm_peak
+    chain_bytes = gamma * sum(pb.values())
+    chain_frac = (chain_bytes / (chain_ms * 1e-3 / args.steps) / 1e9) / hbm_peak
 
     # ---- end to end through the C ABI with host buffers
     pin_vaux = torch.from_numpy(vaux_host.view(np.int16)).pin_memory()
@@ -555,27 +581,21 @@ def run_mine(args, cfg):
         "metric": METRIC, "value": value, "unit": "draft tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
-        "config": {"workload": cfg["workload"], "name": args.config, "batch": B, "gamma": gamma,
-                   "prompt": [int(lens.min()), int(lens.max())],
-                   "mean_context": round(mean_ctx, 1), "page_size": ps,
-                   "kv_format": args.kv_format, "weights": args.weights,
-                   "storage": ("bf16 weights" if args.weights == "bf16" else
-                               "INT4 projections (128-wide groups, bf16 scale and zero), bf16 fc / norms / embedding")
-                              + (", bf16 KV" if args.kv_format == "bf16" else ", q8_0 K / q5_1 V cache")
-                              + ", float32 activations and accumulation",
-                   "l2": "inputs larger than L2: 0.8 GB of weights streamed per draft step",
-                   "step": "chain of gamma draft steps + rewind + accept + rebuild (encode of "
-                           "gamma+1 verify features, k/v teacher forcing)",
-                   "parallelism": f"replicas x{world}"},
+        "dtype": "bf16" if args.weights == "bf16" else "int4", "data": "synthetic",
+        "config": dict(static_config(args, cfg, world), prompt=[int(lens.min()), int(lens.max())],
+                       mean_context=round(mean_ctx, 1)),
         "us_per_draft_step": ms_per_step * 1e3 / gamma,
         "chain_us_per_draft_step": chain_ms * 1e3 / (args.steps * gamma),
         "step_roofline": {"bytes_per_step": rb, "achieved_gbs": rb / (ms_per_step * 1e-3) / 1e9,
                           "peak_gbs": hbm_peak, "frac": step_frac,
-                          "note": f"algorithmic bytes of the whole round / round time, of {peak_src}"},
+                          "frac_of_nominal": step_frac * hbm_peak / NOMINAL_HBM_GBS,
+                          "chain_frac": chain_frac, "chain_frac_of_nominal": chain_frac * hbm_peak / NOMINAL_HBM_GBS,
+                          "note": f"algorithmic bytes of the whole round (chain: of the gamma draft steps) / "
+                                  f"its time, of {peak_src} hbm_gbs; *_of_nominal: of the 8 TB/s datasheet peak"},
         "roofline": {"bound": "hbm", "kernel": kernel_label(dominant, B, args.weights),
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": (achieved / hbm_peak) if achieved else None,
+                     "frac_of_nominal": (achieved / NOMINAL_HBM_GBS) if achieved else None,
                      "traffic": profiled_traffic(args.config, dominant, args.kv_format, args.weights)
                      if args.weights == "bf16" else None,
                      "peak_source": f"{peak_src} hbm_gbs (copy, burst)",

@@ -219,16 +219,20 @@ __device__ __forceinline__ void lmhead_finalize(const GemvParams &p, int item0, 
     const int item = item0 + m;
     const unsigned long long key = atomicExch(p.am_slot + item, 0ull);
     uint32_t id = 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
+    bool bad = false;
     if (id >= (uint32_t)p.draft_vocab) {
       set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
       id = 0;
+      bad = true;
     }
     long long tgt = p.d2t ? (long long)id + p.d2t[id] : (long long)id;  // no d2t: target ids
     if (tgt < 0 || tgt >= p.target_vocab) {
       set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
       tgt = 0;
+      bad = true;
     }
-    const bool valid = !p.gamma_eff || p.step < p.gamma_eff[item];
+    // without a status word (the context-free entry point) the row itself carries the error
+    const bool valid = (!p.gamma_eff || p.step < p.gamma_eff[item]) && !(bad && !p.status);
     const size_t o = (size_t)item * p.gamma + p.step;
     p.draft_tok[o] = valid ? (int32_t)tgt : -1;
     if (p.draft_id) p.draft_id[o] = valid ? (int32_t)id : -1;

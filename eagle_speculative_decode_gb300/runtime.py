@@ -202,8 +202,13 @@ class SeqBatch:
     def kv_entries(self, b: int, lo: int, hi: int):
         """Stored K and V rows of sequence b at positions lo..hi-1: bf16 bits
         [hi - lo, H_kv, d] (uint16), or the q8_0 / q5_1 row bytes [hi - lo, H_kv, row]."""
+        return self.kv_entries_at(b, np.arange(lo, hi))
+
+    def kv_entries_at(self, b: int, positions):
+        """Stored K and V rows of sequence b at the given positions (any order), in the
+        layout of kv_entries."""
         ps = self.model.page_size
-        pos = np.arange(lo, hi)
+        pos = np.asarray(positions, dtype=np.int64)
         pages = torch.from_numpy(self.page_table_host[b, pos // ps].astype(np.int64)).to(self.k_pool.device)
         slots = torch.from_numpy((pos % ps).astype(np.int64)).to(self.k_pool.device)
         k = self.k_pool[pages, :, slots, :].cpu().numpy()

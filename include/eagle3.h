@@ -91,9 +91,11 @@ typedef struct CUstream_st *eagle3_stream_t;
  *                        sz_stride(in) = in / 128 rounded up to a multiple of 4 (the pad is
  *                        unused); w = scale * (code - 8) + zero.  fc, the norm gains and the
  *                        embedding stay bf16.  Needs n_embd, n_head * head_dim and n_ff
- *                        multiples of 128.  These projections then run on the CUDA-core
- *                        GEMV at every batch (one launch streams the weights once for up to
- *                        8 items). */
+ *                        multiples of 128.  Single-item launches whose input width is a
+ *                        multiple of 2048 run on warp-level tensor-core MMAs (mma.sync) fed
+ *                        by codes decoded in registers; launches of several items, and other
+ *                        widths, run on the CUDA-core GEMV (one launch streams the weights
+ *                        once for up to 8 items). */
 #define EAGLE3_W_BF16 0
 #define EAGLE3_W_INT4_G128 1
 
@@ -370,11 +372,16 @@ int eagle3_profile_interval(const eagle3_ctx *ctx, int i, int *label, float *ms)
  * graph is being captured (cudaMalloc is not allowed there) or a runtime whose memory plan
  * is fixed at start-up and that therefore cannot provide a context workspace.
  *
- * Computes, for each of `rows` float32 vectors x[r] (device, [rows, n_embd]), the draft
- * chain's last kernel: logits = lm_head . (RMSNorm(x[r]) * final_norm), draft_id[r] = the
+ * Computes, for each of `rows` float32 vectors x[r] (device, [rows, n_embd]), what the
+ * draft chain's lm_head step computes, on the chain's CUDA-core GEMV kernel (the chain
+ * itself runs its lm_head on that kernel for one or two rows and on the tensor cores from
+ * three rows on): logits = lm_head . (RMSNorm(x[r]) * final_norm), draft_id[r] = the
  * argmax (lowest index on ties), target_id[r] = draft_id[r] + d2t[draft_id[r]].  Same
  * weights and layouts as eagle3_weights; draft_id and logits ([rows, draft_vocab]) may be
- * NULL; target_id is required.  Every buffer is caller-owned device memory.
+ * NULL; target_id is required.  Every buffer is caller-owned device memory.  There is no
+ * context and so no status word: a row whose target id falls outside [0, target_vocab)
+ * (a d2t table that was never validated) gets -1 in target_id and draft_id instead.  The
+ * inputs must be finite; a NaN in x or the weights is not detected.
  *
  * The kernel's scratch (one argmax slot per row and an arrival counter) lives in a static
  * device array inside the library, so the call allocates nothing: it is limited to
@@ -382,8 +389,9 @@ int eagle3_profile_interval(const eagle3_ctx *ctx, int i, int *label, float *ms)
  * library holds that array (about 520 bytes) until the process exits.  The first call on a
  * device looks the array's device address up; make that first call before any stream
  * capture.  All calls share the array, which keeps the last call's contents (each call
- * clears it on its stream before use): calls that overlap on the GPU -- on different
- * streams, or on devices sharing this process -- race, so serialise them.
+ * clears it on its stream before use).  Each device has its own copy of the array, so
+ * calls race only when they overlap on the same device (issued on different streams, or
+ * from different host threads without ordering); serialise those.
  * Returns EAGLE3_OK, EAGLE3_ERR_INVALID_ARG or EAGLE3_ERR_CUDA. */
 int eagle3_lmhead_argmax_noalloc(const uint16_t *lm_head, const uint16_t *final_norm,
                                  const int64_t *d2t, const float *x, int rows, int n_embd,

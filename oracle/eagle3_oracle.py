@@ -20,7 +20,8 @@ Sources (page title, section):
   * "Add the Eagle3Speculator module for speculative decoding": PR body (shifted
     pairing of hidden state t with token t + 1; reseeding the draft cache after verify).
 
-Readings where the pages are silent or disagree (each is listed in the design doc):
+Readings where the pages are silent or disagree (the plainest one the rest of the pages
+support):
   * RoPE is NeoX rotate-half over the first ``rope_dims`` dims, frequencies
     theta^(-2i/rope_dims); the remaining dims pass through.
   * q head h reads kv head h // (n_head / n_head_kv); scale 1/sqrt(head_dim); the new
@@ -120,7 +121,7 @@ def argmax_first(x: np.ndarray) -> int:
 # "memra_engine/eagle.rs", ``Eagle3Scratch``: the drafter KV uses the q8_0-K / q5_1-V
 # quantized layout of the trunk KV, blocks of 32 values (head_dim % 32 == 0), 34 and 24
 # bytes per block.  The page names the formats and sizes only; the encodings below are
-# the plain reading of those names (reading R20): per block, q8_0 keeps an
+# the plain reading of those names and sizes: per block, q8_0 keeps an
 # fp16 scale and 32 signed 8-bit codes, q5_1 an fp16 scale, an fp16 minimum and 32
 # unsigned 5-bit codes.  Codes are decided in float32 on the values as the kernel holds
 # them (float32), with the stored (fp16) scale: the same precision on both sides.

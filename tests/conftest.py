@@ -19,3 +19,14 @@ def built_lib():
     from eagle_speculative_decode_gb300 import binding, build
     build.build()
     return binding.load()
+
+
+@pytest.fixture(scope="session")
+def full_drafter(built_lib):
+    """Seeded weights of the full drafter geometry (n_embd 4096, draft vocab 32000 ->
+    target vocab 248320) and the oracle's float64 view of them, built once per session
+    (the widening alone takes tens of seconds)."""
+    from eagle_speculative_decode_gb300 import synth
+    from oracle import eagle3_oracle as O
+    wts = synth.make_weights(synth.FULL, seed=0)
+    return wts, O.Drafter(synth.FULL, wts.bits, wts.d2t)

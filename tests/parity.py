@@ -8,6 +8,8 @@ and relative L2 1e-2.
 """
 from __future__ import annotations
 
+import copy
+
 import numpy as np
 import torch
 
@@ -163,6 +165,23 @@ def oracle_chain_following(dr, st, gamma, gpu_ids, gpu_toks):
     return ch, f
 
 
+def with_kv_format(dr: O.Drafter, kv_format: str) -> O.Drafter:
+    """The same oracle drafter (its widened weights shared, not copied) storing its KV in
+    another format."""
+    if kv_format not in O.KV_FORMATS:
+        raise ValueError(kv_format)
+    d = copy.copy(dr)
+    d.kv_format = kv_format
+    return d
+
+
+def stored_state(st: O.SeqState, kv_format: str) -> O.SeqState:
+    """A prefilled oracle state with its entries stored in another KV format (the raw
+    float64 k / v are the same in every format)."""
+    return O.SeqState(O.store_k(st.k_raw, kv_format), O.store_v(st.v_raw, kv_format), st.g.copy(),
+                      int(st.tok), st.k_raw.copy(), st.v_raw.copy())
+
+
 # ----------------------------------------------------------------- round driver
 def upload_prompt(model, toks, aux, lens):
     dev = model.device
@@ -293,3 +312,55 @@ def run_round(model, dr, seq, states: dict, gamma, n_imposed, seed, flags=0, kv_
     check_state(seq, new_states, "rebuild", kv_lo=kv_lo)
     assert seq.model.status() == 0
     return new_states, out, na, bo, vaux, ties
+
+
+# ------------------------------------------------- long contexts: sampled and tracked checks
+def compare_entries(got_k, got_v, k_raw, v_raw, kv_format, what):
+    """Stored K / V rows of the implementation against the oracle's unstored k / v: bf16
+    per R16 (one ulp), quantized blocks per R21 (a valid encoding)."""
+    if kv_format == "bf16":
+        assert_close_bf16(bf16_bits_to_f64(got_k), O.store_k(k_raw, "bf16"), f"{what} K")
+        assert_close_bf16(bf16_bits_to_f64(got_v), O.store_v(v_raw, "bf16"), f"{what} V")
+    else:
+        assert_quant_valid(got_k, k_raw, "k", f"{what} K")
+        assert_quant_valid(got_v, v_raw, "v", f"{what} V")
+
+
+def check_prefill_sampled(seq, dr, toks, aux, lens, b, n_samples, rng, kv_format):
+    """Prefill entries of sequence b at a seeded sample of positions: each entry depends
+    only on its own (aux_p, t_{p+1}, p), so the oracle computes the sampled ones alone.
+    Returns the sampled positions."""
+    P = int(lens[b])
+    if P < 2:
+        return np.zeros(0, np.int64)
+    pos = np.sort(rng.choice(P - 1, size=min(n_samples, P - 1), replace=False))
+    g_p = O.encode(dr, aux[b, pos])
+    kr, vr = O.kv_projections(dr, toks[b, pos + 1], g_p, pos)
+    got_k, got_v = seq.kv_entries_at(b, pos)
+    compare_entries(got_k, got_v, kr, vr, kv_format, f"prefill b{b} sampled")
+    return pos
+
+
+class Tracked:
+    """What the oracle knows of a sequence it did not prefill in full: the committed
+    length and the boundary (g, token).  Enough to check every entry a rebuild writes and
+    the boundary it leaves, without the sequence's whole cache."""
+
+    def __init__(self, L: int, g: np.ndarray, tok: int):
+        self.L, self.g, self.tok = int(L), np.asarray(g, dtype=np.float64), int(tok)
+
+
+def check_rebuild_tracked(seq, dr, b, tr: Tracked, dt_row, n: int, bonus: int, venc_b, kv_format):
+    """The entries rebuild_after_verify wrote for sequence b at L..L+n -- pair 0 = the old
+    boundary (g, token), pair i = (fc v_{i-1}, d_i) -- and the new boundary (fc v_n, bonus)
+    and length L+n+1.  Returns the updated tracker."""
+    toks = [tr.tok] + [int(dt_row[i - 1]) for i in range(1, n + 1)]
+    gs = np.stack([tr.g] + [venc_b[i - 1] for i in range(1, n + 1)])
+    pos = np.arange(tr.L, tr.L + n + 1)
+    kr, vr = O.kv_projections(dr, toks, gs, pos)
+    got_k, got_v = seq.kv_entries_at(b, pos)
+    compare_entries(got_k, got_v, kr, vr, kv_format, f"rebuilt b{b}")
+    assert int(seq.kv_len[b].item()) == tr.L + n + 1
+    assert_close(seq.g[b].cpu().numpy(), venc_b[n], f"new boundary g b{b}", max_abs=1e-3, rel_l2=1e-5)
+    assert int(seq.tok[b].item()) == int(bonus)
+    return Tracked(tr.L + n + 1, venc_b[n], bonus)

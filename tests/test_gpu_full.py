@@ -24,10 +24,8 @@ G = synth.FULL
 
 
 @pytest.fixture(scope="module")
-def full(built_lib):
-    wts = synth.make_weights(G, seed=0)
-    dr = O.Drafter(G, wts.bits, wts.d2t)
-    yield wts, dr
+def full(full_drafter):
+    return full_drafter
 
 
 def _prompt(batch, lens, seed):

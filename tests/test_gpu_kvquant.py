@@ -17,7 +17,8 @@ import torch
 from eagle_speculative_decode_gb300 import synth
 from eagle_speculative_decode_gb300.runtime import DraftModel
 from oracle import eagle3_oracle as O
-from parity import assert_quant_valid, check_state, gpu_prefill, oracle_prefill, run_round
+from parity import (assert_quant_valid, check_state, gpu_prefill, oracle_prefill, run_round,
+                    with_kv_format)
 
 pytestmark = pytest.mark.gpu
 FMT = "q8_0/q5_1"
@@ -124,10 +125,10 @@ def test_tc_rounds_batch20_random_pages(small):
     _rounds(model, dr, seq, toks, aux, lens, 4, [34, 35])
 
 
-def test_full_geometry_batch1_prompt512(built_lib):
+def test_full_geometry_batch1_prompt512(full_drafter):
     g = synth.FULL
-    wts = synth.make_weights(g, seed=0)
-    dr = O.Drafter(g, wts.bits, wts.d2t, kv_format=FMT)
+    wts, dr = full_drafter
+    dr = with_kv_format(dr, FMT)
     model = DraftModel(wts, max_batch=1, max_gamma=3, max_cache_len=1024, page_size=64, kv_format=FMT)
     try:
         lens = np.array([512])
