@@ -133,6 +133,25 @@ def assert_quant_valid(raw, x, which: str, what: str, rel=QUANT_REL):
     assert n_edge <= max(4, code.size // 100), f"{what}: {n_edge} codes on boundaries (delta too wide?)"
 
 
+def assert_bf16_valid(bits, x, what: str, rel=QUANT_REL):
+    """Stored bf16 values `bits` [..., d] are a valid rounding of the oracle's unstored
+    values x when the implementation's float32 inputs may differ from x by delta = rel *
+    max|x| of the row: each must lie between the roundings of x - delta and x + delta.
+    Away from a rounding boundary that is exactly the oracle's own bf16 value."""
+    got = bf16_bits_to_f64(bits)
+    x = np.asarray(x, dtype=np.float64)
+    delta = rel * np.abs(x).max(axis=-1, keepdims=True) + 1e-7
+    lo, hi = O.round_bf16(x - delta), O.round_bf16(x + delta)
+    bad = (got < lo) | (got > hi)
+    assert not bad.any(), f"{what}: {int(bad.sum())} values not a rounding of any input within delta"
+    # not vacuous: a value lies within delta of a rounding boundary with probability about
+    # 2 delta / ulp (bf16's ulp scales with the value, so small values often do); far more
+    # brackets than that would mean delta lets wrong values through
+    n_edge = int(np.sum(lo != hi))
+    expect = float(np.minimum(1.0, 2 * delta / bf16_ulp(x)).sum())
+    assert n_edge <= 2 * expect + 8, f"{what}: {n_edge} values on boundaries, about {expect:.0f} expected"
+
+
 def top2_margin(logits: np.ndarray) -> float:
     s = np.sort(logits)
     return float(s[-1] - s[-2])
@@ -221,13 +240,16 @@ def check_state(seq, states: dict, what, kv_lo=0):
                 assert_quant_valid(v, st.v_raw[kv_lo:], "v", f"{what}: V[{b}]")
 
 
-def check_chain_stepwise(seq, dr, b, st, g_eff, out, di, dt) -> int:
-    """Chain of sequence b with a quantized cache, step by step: step j of the oracle runs
-    on the implementation's inputs to that step (its boundary or previous g, its previous
-    token, its stored KV decoded, including the entry it appended at this step), since a
-    code on a rounding boundary may validly differ between the two.  Each appended entry
-    must be a valid encoding of the oracle's k / v of the step (assert_quant_valid); ids
-    follow the margin rule; logits and g are compared with the float tolerance."""
+def check_chain_stepwise(seq, dr, b, st, g_eff, out, di, dt, report=None) -> int:
+    """Chain of sequence b step by step: step j of the oracle runs on the implementation's
+    inputs to that step (its boundary or previous g, its previous token, its stored KV
+    decoded, including the entry it appended at this step), since a stored value on a
+    rounding boundary -- a quantization code, or a bf16 value one ulp away -- may validly
+    differ between the two, and over a long chain such a difference moves later steps by
+    more than float noise.  Each appended entry must be a valid encoding of the oracle's
+    k / v of the step (assert_quant_valid / assert_bf16_valid); ids follow the margin
+    rule; logits and g are compared with the float tolerance.  `report`, a list, receives
+    (b, j, max-abs error of the logits, of g) per step."""
     fmt = seq.model.kv_format
     L = st.kv_len
     kraw, vraw = seq.kv_entries(b, 0, L + g_eff)
@@ -239,8 +261,12 @@ def check_chain_stepwise(seq, dr, b, st, g_eff, out, di, dt) -> int:
     for j in range(g_eff):
         pos = L + j
         so = O.draft_step(dr, tok_in, g_in, kd[:pos], vd[:pos], pos, new_kv=(kd[pos], vd[pos]))
-        assert_quant_valid(kraw[pos], so.k_raw, "k", f"spec K b{b} j{j}")
-        assert_quant_valid(vraw[pos], so.v_raw, "v", f"spec V b{b} j{j}")
+        if fmt == "bf16":
+            assert_bf16_valid(kraw[pos], so.k_raw, f"spec K b{b} j{j}")
+            assert_bf16_valid(vraw[pos], so.v_raw, f"spec V b{b} j{j}")
+        else:
+            assert_quant_valid(kraw[pos], so.k_raw, "k", f"spec K b{b} j{j}")
+            assert_quant_valid(vraw[pos], so.v_raw, "v", f"spec V b{b} j{j}")
         gid = int(di[b, j])
         if top2_margin(so.logits) > MARGIN:
             assert gid == so.draft_id, f"b{b} step {j}: GPU id {gid} vs oracle {so.draft_id}"
@@ -248,16 +274,22 @@ def check_chain_stepwise(seq, dr, b, st, g_eff, out, di, dt) -> int:
             ties += 1
             assert so.logits[gid] >= so.logits.max() - MARGIN, f"b{b} step {j}: GPU id {gid} not near max"
         assert int(dt[b, j]) == dr.d2t_map(gid), f"b{b} step {j}: d2t of {gid}"
+        if report is not None:
+            report.append((b, j, float(np.abs(logits[j] - so.logits).max()),
+                           float(np.abs(gdbg[j] - so.g_next).max())))
         assert_close(logits[j], so.logits, f"logits b{b} j{j}")
         assert_close(gdbg[j], so.g_next, f"g b{b} j{j}")
         g_in, tok_in = gdbg[j], int(dt[b, j])
     return ties
 
 
-def run_round(model, dr, seq, states: dict, gamma, n_imposed, seed, flags=0, kv_lo=0):
+def run_round(model, dr, seq, states: dict, gamma, n_imposed, seed, flags=0, kv_lo=0, stepwise=False,
+              report=None):
     """One full round on the GPU and, for the sequences in `states`, the oracle: chain
     (ids with the margin rule, logits, g, speculative KV), rewind (kv_len, committed
-    bytes, boundary), accept against imposed target predictions, rebuild."""
+    bytes, boundary), accept against imposed target predictions, rebuild.  The chain is
+    compared end to end (the oracle's own cache and g), or step by step on the stored
+    entries (check_chain_stepwise) with a quantized cache or when `stepwise` is set."""
     geo = model.geom
     Bn = seq.B
     out = seq.draft_chain(gamma, flags=flags, debug=True)
@@ -272,8 +304,8 @@ def run_round(model, dr, seq, states: dict, gamma, n_imposed, seed, flags=0, kv_
         g_eff = O.plan_gamma(st.kv_len, gamma, model.max_cache_len, bool(flags & Bd.EAGLE3_SHRINK_GAMMA))
         assert ge[b] == g_eff
         assert np.all(dt[b, g_eff:] == -1)
-        if model.kv_format != "bf16":
-            ties += check_chain_stepwise(seq, dr, b, st, g_eff, out, di, dt)
+        if model.kv_format != "bf16" or stepwise:
+            ties += check_chain_stepwise(seq, dr, b, st, g_eff, out, di, dt, report)
             continue
         ch, f = oracle_chain_following(dr, st, g_eff, di[b, :g_eff], dt[b, :g_eff])
         ties += f.ties
