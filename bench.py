@@ -482,19 +482,31 @@ def run_mine(args, cfg):
     for _ in range(args.phase_rounds):
         Bd.eagle3_profile_begin(model.ctx, n_ev)
         seq.draft_chain(gamma, out=out)
-        for lab, ms in Bd.eagle3_profile_end(model.ctx):
-            per_label.setdefault(lab, []).append(ms * 1e3)
         seq.rewind()
         d = out["draft_tok"]
         verify(r, d)
         seq.accept(d, y, out["gamma_eff"], n_acc=n_acc, bonus=bonus)
         seq.rebuild_after_verify(n_acc, d, bonus, vaux[r], n_acc_host=n_imp_host[r])
+        for lab, ms in Bd.eagle3_profile_end(model.ctx):
+            per_label.setdefault(lab, []).append(ms * 1e3)
         r += 1
     torch.cuda.synchronize()
     model.set_graph_mode(True)
     names = {1: "qkv", 2: "attn", 3: "o", 4: "gateup", 5: "down", 6: "lmhead"}
     # per launch, per kind: average microseconds (one launch per kind per step when B fits)
     kern_us = {names[k]: float(np.mean(v)) for k, v in per_label.items() if k in names}
+    # the rebuild's two projections, once per round: encode of the gamma + 1 verify
+    # features (fc) and the k/v-only teacher forcing; bytes = weights + activations
+    rb_names = {7: "encode", 8: "kv"}
+    rb_bytes = {"encode": 3 * geo.n_embd * geo.n_embd * 2 + B * (gamma + 1) * (3 * geo.n_embd * 2 + geo.n_embd * 4),
+                "kv": matrix_bytes(2 * geo.kv_rows, 2 * geo.n_embd, args.weights)
+                + B * (gamma + 1) * (geo.n_embd * 2 + geo.n_embd * 4 + kv_bytes_per_position(geo, args.kv_format))}
+    rebuild_us = {}
+    for k, v in per_label.items():
+        if k in rb_names:
+            us = float(np.sum(v)) / max(1, args.phase_rounds)
+            nm = rb_names[k]
+            rebuild_us[nm] = {"us_per_round": us, "gbs": rb_bytes[nm] / (us * 1e-6) / 1e9}
     pb = phase_bytes(geo, B, int(mean_ctx), args.kv_format, args.weights)
     hbm_peak, tf_peak, peak_src = load_peaks()
     launches_per_kind = {k: max(1, len(per_label.get(kk, [])) // max(1, args.phase_rounds * gamma))
@@ -601,6 +613,7 @@ def run_mine(args, cfg):
                      "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
                      "bytes_per_launch": dom_bytes, "us_per_launch": kern_us.get(dominant)},
         "kernel_us": kern_us,
+        "rebuild_kernel_us": rebuild_us,
         "prefill": {"positions": prefill_positions, "ms": prefill_ms,
                     "positions_per_s": prefill_positions / (prefill_ms * 1e-3),
                     "note": "eagle3_prefill of the prompts (encode + k/v teacher forcing), timed once"},

@@ -137,49 +137,114 @@ __device__ void stage_x(const GemvParams &p, unsigned char *xmem, float (&ss)[NB
       }
       continue;
     }
+    // up to VU vectors of a thread are loaded before any of them is stored, so that their
+    // round trips overlap (K = 12288 gives each thread three)
+    constexpr int VU = 3;
     if constexpr (MODE == GM_O || MODE == GM_DOWN) {
       const float4 *src = reinterpret_cast<const float4 *>(p.xf + (size_t)item * K);
-      for (int kv = tid; kv < KV; kv += kGemvThreads) {
-        x0[kv] = src[2 * kv];
-        x1[kv] = src[2 * kv + 1];
+      for (int kv0 = tid; kv0 < KV; kv0 += VU * kGemvThreads) {
+        float4 a[VU], b[VU];
+#pragma unroll
+        for (int u = 0; u < VU; ++u) {
+          const int kv = kv0 + u * kGemvThreads;
+          if (kv < KV) {
+            a[u] = src[2 * kv];
+            b[u] = src[2 * kv + 1];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < VU; ++u) {
+          const int kv = kv0 + u * kGemvThreads;
+          if (kv < KV) {
+            x0[kv] = a[u];
+            x1[kv] = b[u];
+          }
+        }
       }
     } else if constexpr (MODE == GM_GATEUP || MODE == GM_LMHEAD) {
       const float4 *src = reinterpret_cast<const float4 *>(p.xf + (size_t)item * K);
       const uint4 *wn = reinterpret_cast<const uint4 *>(p.norm0);
-      for (int kv = tid; kv < KV; kv += kGemvThreads) {
-        const float4 a = src[2 * kv], b = src[2 * kv + 1];
-        const uint4 w = wn[kv];
-        ss[m][0] += sq8(a, b);
-        x0[kv] = mul4(a, bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
-        x1[kv] = mul4(b, bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w));
+      for (int kv0 = tid; kv0 < KV; kv0 += VU * kGemvThreads) {
+        float4 a[VU], b[VU];
+        uint4 w[VU];
+#pragma unroll
+        for (int u = 0; u < VU; ++u) {
+          const int kv = kv0 + u * kGemvThreads;
+          if (kv < KV) {
+            a[u] = src[2 * kv];
+            b[u] = src[2 * kv + 1];
+            w[u] = wn[kv];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < VU; ++u) {
+          const int kv = kv0 + u * kGemvThreads;
+          if (kv < KV) {
+            ss[m][0] += sq8(a[u], b[u]);
+            x0[kv] = mul4(a[u], bf_lo(w[u].x), bf_hi(w[u].x), bf_lo(w[u].y), bf_hi(w[u].y));
+            x1[kv] = mul4(b[u], bf_lo(w[u].z), bf_hi(w[u].z), bf_lo(w[u].w), bf_hi(w[u].w));
+          }
+        }
       }
-    } else if constexpr (MODE == GM_QKV) {
-      // [embed(tok) * w_in ; g * w_hid]; the two RMSNorm scales come later
-      const int n = p.n_embd, NV = n >> 3;
-      const PairItem it = resolve_pair(p.pairs, item, n);
-      int tok = it.tok;
-      if (tok < 0 || tok >= p.target_vocab) {
-        // only rows whose K/V are kept (or the chain's q) may report a bad token
-        if (tid == 0 && (it.write_kv || p.row_base == 0)) set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
-        tok = 0;
+    }
+  }
+  if constexpr (MODE == GM_QKV) {
+    // [embed(tok) * w_in ; g * w_hid]; the two RMSNorm scales come later.  An item's
+    // embedding row is known only once its token is loaded, so the pairs of a group of
+    // items are resolved together and every global load of the group is issued before any
+    // shared-memory store: two dependent round trips per group instead of several per item.
+    const int n = p.n_embd, NV = n >> 3;
+    constexpr int MB = NB < 4 ? NB : 4;
+    const uint4 *wi = reinterpret_cast<const uint4 *>(p.norm0);
+    const uint4 *wh = reinterpret_cast<const uint4 *>(p.norm1);
+#pragma unroll
+    for (int m0 = 0; m0 < NB; m0 += MB) {
+      const uint4 *er[MB];
+      const float4 *gr[MB];
+#pragma unroll
+      for (int mm = 0; mm < MB; ++mm) {
+        const int m = m0 + mm;
+        er[mm] = nullptr;
+        gr[mm] = nullptr;
+        if (m < p.items) {
+          const PairItem it = resolve_pair(p.pairs, p.item0 + m, n);
+          int tok = it.tok;
+          if (tok < 0 || tok >= p.target_vocab) {
+            // only rows whose K/V are kept (or the chain's q) may report a bad token
+            if (tid == 0 && (it.write_kv || p.row_base == 0)) set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
+            tok = 0;
+          }
+          er[mm] = reinterpret_cast<const uint4 *>(p.embed + (size_t)tok * n);
+          gr[mm] = reinterpret_cast<const float4 *>(it.g);
+        }
       }
-      const uint4 *er = reinterpret_cast<const uint4 *>(p.embed + (size_t)tok * n);
-      const float4 *gr = reinterpret_cast<const float4 *>(it.g);
-      const uint4 *wi = reinterpret_cast<const uint4 *>(p.norm0);
-      const uint4 *wh = reinterpret_cast<const uint4 *>(p.norm1);
       for (int kv = tid; kv < NV; kv += kGemvThreads) {
-        const uint4 u = er[kv];
-        const float4 ea = make_float4(bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y));
-        const float4 eb = make_float4(bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w));
-        const uint4 w = wi[kv];
-        ss[m][0] += sq8(ea, eb);
-        x0[kv] = mul4(ea, bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
-        x1[kv] = mul4(eb, bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w));
-        const float4 a = gr[2 * kv], b = gr[2 * kv + 1];
-        const uint4 hw = wh[kv];
-        ss[m][T::kHalves - 1] += sq8(a, b);
-        x0[NV + kv] = mul4(a, bf_lo(hw.x), bf_hi(hw.x), bf_lo(hw.y), bf_hi(hw.y));
-        x1[NV + kv] = mul4(b, bf_lo(hw.z), bf_hi(hw.z), bf_lo(hw.w), bf_hi(hw.w));
+        uint4 u[MB];
+        float4 a[MB], b[MB];
+#pragma unroll
+        for (int mm = 0; mm < MB; ++mm) {
+          if (er[mm]) {
+            u[mm] = er[mm][kv];
+            a[mm] = gr[mm][2 * kv];
+            b[mm] = gr[mm][2 * kv + 1];
+          }
+        }
+        const uint4 w = wi[kv], hw = wh[kv];
+#pragma unroll
+        for (int mm = 0; mm < MB; ++mm) {
+          const int m = m0 + mm;
+          if (!er[mm]) continue;
+          float4 *x0 = reinterpret_cast<float4 *>(xmem) + (size_t)(m * 2) * KV;
+          float4 *x1 = x0 + KV;
+          const float4 ea = make_float4(bf_lo(u[mm].x), bf_hi(u[mm].x), bf_lo(u[mm].y), bf_hi(u[mm].y));
+          const float4 eb = make_float4(bf_lo(u[mm].z), bf_hi(u[mm].z), bf_lo(u[mm].w), bf_hi(u[mm].w));
+          ss[m][0] += sq8(ea, eb);
+          x0[kv] = mul4(ea, bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+          x1[kv] = mul4(eb, bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w));
+          ss[m][T::kHalves - 1] += sq8(a[mm], b[mm]);
+          x0[NV + kv] = mul4(a[mm], bf_lo(hw.x), bf_hi(hw.x), bf_lo(hw.y), bf_hi(hw.y));
+          x1[NV + kv] = mul4(b[mm], bf_lo(hw.z), bf_hi(hw.z), bf_lo(hw.w), bf_hi(hw.w));
+        }
       }
     }
   }

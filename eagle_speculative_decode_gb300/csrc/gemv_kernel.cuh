@@ -46,9 +46,13 @@ namespace e3 {
 
 // -------------------------------------------------------------------- kernel
 constexpr int kStageBytes = 32 * 1024;
-// Single-item launches with K <= 3 * 512 * 8 = 12288 keep x in registers: up to 3 vectors
-// of 8 floats per thread (larger K reads x from shared memory).
-constexpr int kXRegVecs = 3;
+// x vectors (8 k each) per item and thread that a launch keeps in registers: about 64
+// registers of x in all (a bf16 vector takes 8, an INT4 one 9 with its sum), and no more
+// than K = 3 * 512 * 8 = 12288 needs.  A launch whose K / 8 exceeds 512 times this reads x
+// from shared memory per row instead.
+__host__ __device__ constexpr int gemv_xreg_vecs(int nb, bool q4) {
+  return nb == 1 ? 3 : nb == 2 ? 3 : nb == 4 ? 2 : 1;
+}
 constexpr int kGemvCtaThreads = kGemvThreads + 32;  // 16 consumer warps + 1 producer warp
 
 struct GemvSmem {
@@ -262,27 +266,34 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
   float ss[NB][H];
   stage_x<NB, MODE>(p, xmem, ss);
   consumer_sync();
-  const bool xreg = (NB == 1) && (KV <= kXRegVecs * kGemvThreads);
-  constexpr int XRV = NB == 1 ? kXRegVecs : 1;
-  float xr[Q4 ? 1 : XRV][8];              // bf16 weights: x as loaded
-  float2 xq[Q4 ? XRV : 1][4];             // INT4 weights: x in code pair order, and its sums
-  float xsum[Q4 ? XRV : 1];
+  // x in registers: XRV 8-element vectors per item and thread (k = 8 (tid + 512 j)), so that
+  // every weight vector read from the ring serves all items without x being re-read from
+  // shared memory per row (with several items that re-read, not HBM, would set the pace);
+  // launches whose x does not fit the register budget read it from shared memory per row.
+  constexpr int XRV = gemv_xreg_vecs(NB, Q4);
+  const bool xreg = KV <= XRV * kGemvThreads;
+  float xr[Q4 ? 1 : XRV][NB][8];           // bf16 weights: x as loaded
+  float2 xq[Q4 ? XRV : 1][NB][4];          // INT4 weights: x in code pair order,
+  float xsum[Q4 ? XRV : 1][NB];            // and its sums
   if (xreg) {
 #pragma unroll
-    for (int j = 0; j < (NB == 1 ? kXRegVecs : 0); ++j) {
+    for (int j = 0; j < XRV; ++j) {
       const int kv = tid + j * kGemvThreads;
-      float x[8];
-      if (kv < KV) {
-        load_x8<MODE>(xmem, KV, 0, kv, x);
-      } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = 0.f;
-      }
-      if constexpr (Q4) {
-        q4_x_pairs(x, xq[j], xsum[j]);
-      } else {
+      for (int m = 0; m < NB; ++m) {
+        float x[8];
+        if (kv < KV) {
+          load_x8<MODE>(xmem, KV, m, kv, x);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) xr[j][i] = x[i];
+          for (int i = 0; i < 8; ++i) x[i] = 0.f;
+        }
+        if constexpr (Q4) {
+          q4_x_pairs(x, xq[j][m], xsum[j][m]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) xr[j][m][i] = x[i];
+        }
       }
     }
   }
@@ -300,35 +311,41 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
     if (ok) {
       const unsigned char *stage = ring + (size_t)slot * L.stage_bytes;
       const int rows_here = min(SR, nrows - st * SR);
-      auto fma_rows = [&](int kv, const float (&x)[8], int m, float (&a)[SR][NB]) {
+      // bf16: weight vector kv of every row of the stage against each item's x in registers
+      auto fma_rows = [&](int kv, int j, float (&a)[SR][NB]) {
 #pragma unroll
         for (int r = 0; r < SR; ++r)
           if (r < rows_here) {
             const uint4 w = *reinterpret_cast<const uint4 *>(stage + ((size_t)r * K + (size_t)kv * 8) * 2);
-            a[r][m] = dot8(w, x, a[r][m]);
+#pragma unroll
+            for (int m = 0; m < NB; ++m) a[r][m] = dot8(w, xr[Q4 ? 0 : j][m], a[r][m]);
           }
       };
-      // INT4: the 4 code bytes of k vector kv and its group's (scale, zero) in row r
+      // INT4: the 4 code bytes of k vector kv and its group's (scale, zero) in row r, decoded
+      // once and used for every item
       const uint32_t *szs = reinterpret_cast<const uint32_t *>(stage + (size_t)SR * (K >> 1));
-      auto q4_rows = [&](int kv, const float2 (&x2)[4], float xs, int m, float (&a)[SR][NB]) {
+      auto q4_rows = [&](int kv, int j, float (&a)[SR][NB]) {
 #pragma unroll
         for (int r = 0; r < SR; ++r)
           if (r < rows_here) {
             const uint32_t w = *reinterpret_cast<const uint32_t *>(stage + (size_t)r * (K >> 1) + (size_t)kv * 4);
+            const uint32_t sz = szs[(size_t)r * szw + (kv >> 4)];
             float2 f[4];
             q4_to_f32x2(w, f);
-            a[r][m] = q4_dot(f, x2, xs, szs[(size_t)r * szw + (kv >> 4)], a[r][m]);
+#pragma unroll
+            for (int m = 0; m < NB; ++m)
+              a[r][m] = q4_dot(f, xq[Q4 ? j : 0][m], xsum[Q4 ? j : 0][m], sz, a[r][m]);
           }
       };
       if (xreg && Q4) {
 #pragma unroll
-        for (int j = 0; j < (NB == 1 && Q4 ? kXRegVecs : 0); ++j) {
+        for (int j = 0; j < (Q4 ? XRV : 0); ++j) {
           const int kv = tid + j * kGemvThreads;
           if (kv < KV) {
             if (H == 1 || kv < NVH)
-              q4_rows(kv, xq[j], xsum[j], 0, acc[0]);
+              q4_rows(kv, j, acc[0]);
             else
-              q4_rows(kv, xq[j], xsum[j], 0, acc[H - 1]);
+              q4_rows(kv, j, acc[H - 1]);
           }
         }
       } else if (Q4) {
@@ -365,13 +382,13 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
         }
       } else if (xreg) {
 #pragma unroll
-        for (int j = 0; j < (NB == 1 && !Q4 ? kXRegVecs : 0); ++j) {
+        for (int j = 0; j < (Q4 ? 0 : XRV); ++j) {
           const int kv = tid + j * kGemvThreads;
           if (kv < KV) {
             if (H == 1 || kv < NVH)
-              fma_rows(kv, xr[j], 0, acc[0]);
+              fma_rows(kv, j, acc[0]);
             else
-              fma_rows(kv, xr[j], 0, acc[H - 1]);
+              fma_rows(kv, j, acc[H - 1]);
           }
         }
       } else {
