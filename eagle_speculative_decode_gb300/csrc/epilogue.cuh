@@ -250,6 +250,140 @@ __device__ void stage_x(const GemvParams &p, unsigned char *xmem, float (&ss)[NB
   }
 }
 
+// The x vectors this thread uses, k = 8 (tid + kGemvThreads j) for j < XRV, computed
+// straight into registers (the launches whose x fits there keep no copy of x in shared
+// memory, which leaves the whole ring budget to the weights); the same values and RMSNorm
+// sums as stage_x.  All global loads of the thread are issued before any use.
+template <int NB, int MODE, int XRV>
+__device__ __forceinline__ void stage_x_regs(const GemvParams &p, float (&xr)[XRV][NB][8],
+                                             float (&ss)[NB][ModeTraits<MODE>::kHalves]) {
+  using T = ModeTraits<MODE>;
+  constexpr int H = T::kHalves;
+  const int K = p.K, KV = K >> 3, tid = threadIdx.x;
+#pragma unroll
+  for (int m = 0; m < NB; ++m)
+#pragma unroll
+    for (int h = 0; h < H; ++h) ss[m][h] = 0.f;
+  if constexpr (MODE == GM_QKV) {
+    // [embed(tok) * w_in ; g * w_hid]: e vectors kv < NV, g vectors kv >= NV
+    const int n = p.n_embd, NV = n >> 3;
+    const uint4 *er[NB];
+    const float4 *gr[NB];
+#pragma unroll
+    for (int m = 0; m < NB; ++m) {
+      er[m] = nullptr;
+      gr[m] = nullptr;
+      if (m < p.items) {
+        const PairItem it = resolve_pair(p.pairs, p.item0 + m, n);
+        int tok = it.tok;
+        if (tok < 0 || tok >= p.target_vocab) {
+          // only rows whose K/V are kept (or the chain's q) may report a bad token
+          if (tid == 0 && (it.write_kv || p.row_base == 0)) set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
+          tok = 0;
+        }
+        er[m] = reinterpret_cast<const uint4 *>(p.embed + (size_t)tok * n);
+        gr[m] = reinterpret_cast<const float4 *>(it.g);
+      }
+    }
+    const uint4 *wi = reinterpret_cast<const uint4 *>(p.norm0);
+    const uint4 *wh = reinterpret_cast<const uint4 *>(p.norm1);
+#pragma unroll
+    for (int j = 0; j < XRV; ++j) {
+      const int kv = tid + j * kGemvThreads;
+#pragma unroll
+      for (int m = 0; m < NB; ++m) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+        if (kv < KV && er[m]) {
+          if (kv < NV) {
+            const uint4 u = er[m][kv];
+            a = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+          } else {
+            a = gr[m][2 * (kv - NV)];
+            b = gr[m][2 * (kv - NV) + 1];
+          }
+        }
+        xr[j][m][0] = a.x; xr[j][m][1] = a.y; xr[j][m][2] = a.z; xr[j][m][3] = a.w;
+        xr[j][m][4] = b.x; xr[j][m][5] = b.y; xr[j][m][6] = b.z; xr[j][m][7] = b.w;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < XRV; ++j) {
+      const int kv = tid + j * kGemvThreads;
+      const bool eh = kv < NV;
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (kv < KV) w = eh ? wi[kv] : wh[kv - NV];
+#pragma unroll
+      for (int m = 0; m < NB; ++m) {
+        float4 a, b;
+        if (eh) {
+          const uint32_t u0 = __float_as_uint(xr[j][m][0]), u1 = __float_as_uint(xr[j][m][1]);
+          const uint32_t u2 = __float_as_uint(xr[j][m][2]), u3 = __float_as_uint(xr[j][m][3]);
+          a = make_float4(bf_lo(u0), bf_hi(u0), bf_lo(u1), bf_hi(u1));
+          b = make_float4(bf_lo(u2), bf_hi(u2), bf_lo(u3), bf_hi(u3));
+        } else {
+          a = make_float4(xr[j][m][0], xr[j][m][1], xr[j][m][2], xr[j][m][3]);
+          b = make_float4(xr[j][m][4], xr[j][m][5], xr[j][m][6], xr[j][m][7]);
+        }
+        if (kv < KV) ss[m][eh ? 0 : H - 1] += sq8(a, b);
+        const float4 xa = mul4(a, bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+        const float4 xb = mul4(b, bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w));
+        xr[j][m][0] = xa.x; xr[j][m][1] = xa.y; xr[j][m][2] = xa.z; xr[j][m][3] = xa.w;
+        xr[j][m][4] = xb.x; xr[j][m][5] = xb.y; xr[j][m][6] = xb.z; xr[j][m][7] = xb.w;
+      }
+    }
+  } else if constexpr (T::kBf16X) {
+    // the encode: the caller's bf16 features as they are
+#pragma unroll
+    for (int j = 0; j < XRV; ++j) {
+      const int kv = tid + j * kGemvThreads;
+#pragma unroll
+      for (int m = 0; m < NB; ++m) {
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (kv < KV && m < p.items) u = reinterpret_cast<const uint4 *>(p.xb + (size_t)(p.item0 + m) * K)[kv];
+        xr[j][m][0] = bf_lo(u.x); xr[j][m][1] = bf_hi(u.x); xr[j][m][2] = bf_lo(u.y); xr[j][m][3] = bf_hi(u.y);
+        xr[j][m][4] = bf_lo(u.z); xr[j][m][5] = bf_hi(u.z); xr[j][m][6] = bf_lo(u.w); xr[j][m][7] = bf_hi(u.w);
+      }
+    }
+  } else {
+    // float32 activations: attention output / act as they are, x1 / gsum times the norm gain
+    constexpr bool kNormed = MODE == GM_GATEUP || MODE == GM_LMHEAD;
+#pragma unroll
+    for (int j = 0; j < XRV; ++j) {
+      const int kv = tid + j * kGemvThreads;
+#pragma unroll
+      for (int m = 0; m < NB; ++m) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+        if (kv < KV && m < p.items) {
+          const float4 *src = reinterpret_cast<const float4 *>(p.xf + (size_t)(p.item0 + m) * K);
+          a = __ldcg(src + 2 * kv);
+          b = __ldcg(src + 2 * kv + 1);
+        }
+        xr[j][m][0] = a.x; xr[j][m][1] = a.y; xr[j][m][2] = a.z; xr[j][m][3] = a.w;
+        xr[j][m][4] = b.x; xr[j][m][5] = b.y; xr[j][m][6] = b.z; xr[j][m][7] = b.w;
+      }
+    }
+    if constexpr (kNormed) {
+      const uint4 *wn = reinterpret_cast<const uint4 *>(p.norm0);
+#pragma unroll
+      for (int j = 0; j < XRV; ++j) {
+        const int kv = tid + j * kGemvThreads;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (kv < KV) w = wn[kv];
+#pragma unroll
+        for (int m = 0; m < NB; ++m) {
+          const float4 a = make_float4(xr[j][m][0], xr[j][m][1], xr[j][m][2], xr[j][m][3]);
+          const float4 b = make_float4(xr[j][m][4], xr[j][m][5], xr[j][m][6], xr[j][m][7]);
+          ss[m][0] += sq8(a, b);
+          const float4 xa = mul4(a, bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+          const float4 xb = mul4(b, bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w));
+          xr[j][m][0] = xa.x; xr[j][m][1] = xa.y; xr[j][m][2] = xa.z; xr[j][m][3] = xa.w;
+          xr[j][m][4] = xb.x; xr[j][m][5] = xb.y; xr[j][m][6] = xb.z; xr[j][m][7] = xb.w;
+        }
+      }
+    }
+  }
+}
+
 // x vector kv of item m as 8 floats.
 template <int MODE>
 __device__ __forceinline__ void load_x8(const unsigned char *xmem, int KV, int m, int kv, float (&x)[8]) {

@@ -204,7 +204,12 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
   const int max_rows = tiles_max_rows(p.rows, TR, gridDim.x);
   const int nst = p.nstage;
   const int szw = Q4 ? p.sz_stride : 0;  // (scale, zero) pairs per row
-  const GemvSmem L = gemv_smem_layout(NB, SR, H, T::kBf16X ? 2 : 4, K, nst, max_rows, gemv_row_bytes(Q4, K, szw));
+  constexpr int XRV = gemv_xreg_vecs(NB, Q4);
+  const bool xreg = KV <= XRV * kGemvThreads;
+  // several items with x in registers: x goes straight to registers, none in shared memory
+  const bool xdirect = xreg && NB > 1;
+  const GemvSmem L = gemv_smem_layout(NB, SR, H, xdirect ? 0 : (T::kBf16X ? 2 : 4), K, nst, max_rows,
+                                      gemv_row_bytes(Q4, K, szw));
   const int n_stages = (nrows + SR - 1) / SR;
   const int NVH = H == 2 ? (p.n_embd >> 3) : KV;  // first vector of the second K half
 
@@ -264,37 +269,41 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
   // ------------------------------------------------------------ consumer warps
   pdl_wait();
   float ss[NB][H];
-  stage_x<NB, MODE>(p, xmem, ss);
-  consumer_sync();
   // x in registers: XRV 8-element vectors per item and thread (k = 8 (tid + 512 j)), so that
   // every weight vector read from the ring serves all items without x being re-read from
   // shared memory per row (with several items that re-read, not HBM, would set the pace);
-  // launches whose x does not fit the register budget read it from shared memory per row.
-  constexpr int XRV = gemv_xreg_vecs(NB, Q4);
-  const bool xreg = KV <= XRV * kGemvThreads;
-  float xr[Q4 ? 1 : XRV][NB][8];           // bf16 weights: x as loaded
+  // such launches compute their x straight into registers.  Launches whose x does not fit
+  // the register budget stage it in shared memory and read it per row.
+  float xr[XRV][NB][8];                    // bf16 weights: x as computed
   float2 xq[Q4 ? XRV : 1][NB][4];          // INT4 weights: x in code pair order,
   float xsum[Q4 ? XRV : 1][NB];            // and its sums
-  if (xreg) {
+  if (xdirect) {
+    stage_x_regs<NB, MODE, XRV>(p, xr, ss);
+  } else {
+    stage_x<NB, MODE>(p, xmem, ss);
+    consumer_sync();
+    if (xreg) {
 #pragma unroll
-    for (int j = 0; j < XRV; ++j) {
-      const int kv = tid + j * kGemvThreads;
+      for (int j = 0; j < XRV; ++j) {
+        const int kv = tid + j * kGemvThreads;
 #pragma unroll
-      for (int m = 0; m < NB; ++m) {
-        float x[8];
-        if (kv < KV) {
-          load_x8<MODE>(xmem, KV, m, kv, x);
-        } else {
+        for (int m = 0; m < NB; ++m) {
+          if (kv < KV) {
+            load_x8<MODE>(xmem, KV, m, kv, xr[j][m]);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] = 0.f;
-        }
-        if constexpr (Q4) {
-          q4_x_pairs(x, xq[j][m], xsum[j][m]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) xr[j][m][i] = x[i];
+            for (int i = 0; i < 8; ++i) xr[j][m][i] = 0.f;
+          }
         }
       }
+    }
+  }
+  if constexpr (Q4) {
+    if (xreg) {
+#pragma unroll
+      for (int j = 0; j < XRV; ++j)
+#pragma unroll
+        for (int m = 0; m < NB; ++m) q4_x_pairs(xr[j][m], xq[j][m], xsum[j][m]);
     }
   }
 
@@ -318,7 +327,7 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
           if (r < rows_here) {
             const uint4 w = *reinterpret_cast<const uint4 *>(stage + ((size_t)r * K + (size_t)kv * 8) * 2);
 #pragma unroll
-            for (int m = 0; m < NB; ++m) a[r][m] = dot8(w, xr[Q4 ? 0 : j][m], a[r][m]);
+            for (int m = 0; m < NB; ++m) a[r][m] = dot8(w, xr[j][m], a[r][m]);
           }
       };
       // INT4: the 4 code bytes of k vector kv and its group's (scale, zero) in row r, decoded
@@ -783,6 +792,10 @@ constexpr int sr_max() {
 
 // Rows per ring stage: whole rows up to kStageBytes, at most 8, at most 32 / (NB * H) so
 // that a stage's sums fit one warp reduction, and fewer if that keeps >= 4 stages.
+// Whether a launch of several items keeps x in registers (then it has no copy of x in
+// shared memory; one item still stages x there).
+inline bool gemv_xreg(int K, int NB, bool q4) { return NB > 1 && K / 8 <= gemv_xreg_vecs(NB, q4) * kGemvThreads; }
+
 template <int MODE, bool Q4>
 static int stage_rows(int K, int NB, int max_rows, int row_bytes) {
   using T = ModeTraits<MODE>;
@@ -794,7 +807,8 @@ static int stage_rows(int K, int NB, int max_rows, int row_bytes) {
   int p2 = 1;
   while (p2 * 2 <= sr) p2 *= 2;
   while (p2 > 1) {
-    const GemvSmem L = gemv_smem_layout(NB, p2, T::kHalves, T::kBf16X ? 2 : 4, K, 0, max_rows, row_bytes);
+    const GemvSmem L = gemv_smem_layout(NB, p2, T::kHalves, gemv_xreg(K, NB, Q4) ? 0 : (T::kBf16X ? 2 : 4), K, 0,
+                                        max_rows, row_bytes);
     const long long room = (long long)kGemvSmemLimit - L.total - 64;
     if (room / (p2 * row_bytes + 16) >= 4) break;
     p2 >>= 1;
@@ -809,13 +823,14 @@ static cudaError_t launch_one(GemvParams p, int grid, cudaStream_t st, bool pdl)
   grid = std::max(1, std::min(grid, (p.rows + TR - 1) / TR));
   const int max_rows = tiles_max_rows(p.rows, TR, grid);
   const int rb = gemv_row_bytes(Q4, p.K, p.sz_stride);
-  const GemvSmem L0 = gemv_smem_layout(NB, SR, T::kHalves, T::kBf16X ? 2 : 4, p.K, 0, max_rows, rb);
+  const int xb = gemv_xreg(p.K, NB, Q4) ? 0 : (T::kBf16X ? 2 : 4);
+  const GemvSmem L0 = gemv_smem_layout(NB, SR, T::kHalves, xb, p.K, 0, max_rows, rb);
   const long long room = (long long)kGemvSmemLimit - L0.total - 64;
   int nst = (int)(room / (SR * rb + 16));
   nst = std::min(nst, ring_stages_cap(SR * rb));
   if (nst < 2) return cudaErrorInvalidValue;
   p.nstage = nst;
-  const GemvSmem L = gemv_smem_layout(NB, SR, T::kHalves, T::kBf16X ? 2 : 4, p.K, nst, max_rows, rb);
+  const GemvSmem L = gemv_smem_layout(NB, SR, T::kHalves, xb, p.K, nst, max_rows, rb);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kGemvCtaThreads);
