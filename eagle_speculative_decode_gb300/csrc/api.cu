@@ -174,7 +174,7 @@ struct eagle3_ctx {
   std::vector<int> ev_label;
   std::vector<cudaEvent_t> ev_pool;
   // tensor-core path
-  int tc_ok, tc_min_items;
+  int tc_ok, tc_min_items, tc_sched;
   // attention work units (keys per unit) and the round's unit prefix tables
   int unit_keys;
   int32_t *attn_plan;
@@ -278,6 +278,7 @@ cudaError_t tc_items(eagle3_ctx *ctx, const GemvParams &p, int items, cudaStream
   L.tile_cnt = ctx->tc_cnt;
   L.tile_cnt_elems = kTcCounters;
   L.num_sms = ctx->num_sms;
+  L.schedule = ctx->tc_sched;
   const int n = c.n_embd, qr = c.n_head * c.head_dim, kr = c.n_head_kv * c.head_dim;
   switch (p.mode) {
     case GM_ENCODE: L.a0 = ctx->w.fc; L.a0_rows = n; break;
@@ -755,6 +756,7 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
                      qr % 64 == 0 && (d % 128 == 0 || 128 % d == 0) && cfg->n_ff % 64 == 0;
     ctx->tc_ok = geo && tc_prepare() == cudaSuccess ? 1 : 0;
     ctx->tc_min_items = kTcMinItems;
+    ctx->tc_sched = TC_SCHED_AUTO;
   }
 
   // RoPE table: angle p * theta^(-2i/R) in double, stored as float32 (cos, sin).
@@ -810,6 +812,15 @@ int eagle3_set_tc_min_items(eagle3_ctx *ctx, int min_items) {
   const int v = min_items == 0 ? kTcMinItems : min_items;
   if (v != ctx->tc_min_items) {
     ctx->tc_min_items = v;
+    drop_graphs(ctx);
+  }
+  return EAGLE3_OK;
+}
+
+int eagle3_set_tc_schedule(eagle3_ctx *ctx, int schedule) {
+  if (!ctx || schedule < TC_SCHED_AUTO || schedule > TC_SCHED_CLUSTER) return EAGLE3_ERR_INVALID_ARG;
+  if (schedule != ctx->tc_sched) {
+    ctx->tc_sched = schedule;
     drop_graphs(ctx);
   }
   return EAGLE3_OK;

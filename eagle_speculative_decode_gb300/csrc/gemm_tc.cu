@@ -9,10 +9,17 @@
 // x = x0 + x1 + x2 (exact to float32's 24 bits) and every part is multiplied; bf16
 // features (the encode) are one part.
 //
-// Persistent stream-K schedule: one CTA per SM walks an equal share of all
-// (tile, k-tile) units, tile by tile, so no SM idles in a tail wave.  A tile that two or
-// more CTAs share is finished by the last of them, which adds the others' float32
-// partial sums in CTA order.
+// Two schedules, one CTA per SM:
+//  * cluster split-K, when there are few tiles (T <= 76): each tile gets s CTAs
+//    (2 <= s <= 8, T * s close to the SM count) in one thread-block cluster, each
+//    multiplying a contiguous 1/s of K.  The s float32 partial tiles meet in distributed
+//    shared memory: after one cluster barrier every rank adds, for its own share of the
+//    item columns, the s partials in rank order and runs the tile epilogue on those
+//    columns, so neither the reduction nor the epilogue waits on one CTA.
+//  * persistent stream-K otherwise: every CTA walks an equal share of all (tile, k-tile)
+//    units, tile by tile, so no SM idles in a tail wave.  A tile that two or more CTAs
+//    share is finished by the last of them, which adds the others' float32 partial sums
+//    (published through L2) in CTA order.
 //
 // The three parts sit on consecutive rows of the B tile, so one MMA of width 3N multiplies
 // them all (the x0, x1, x2 products land in adjacent TMEM column blocks).  Precision: a
@@ -57,6 +64,7 @@ struct TcArgs {
   const float *sumsq;  // [M][halves] sum of squares of the staged x (norm modes)
   float *part;         // stream-K partials [grid][2][halves][N][128]
   unsigned *tile_cnt;  // stream-K arrival counters [tiles], zero between launches
+  int csplit;          // cluster split-K: CTAs per tile (= cluster size); 0: stream-K
   int M;               // items in total
   int item_tiles, row_tiles, ktiles;
   int units;           // tiles * ktiles
@@ -165,11 +173,19 @@ struct TcShape {
   static __device__ __forceinline__ uint32_t buf_col(int b) { return (uint32_t)(b * NP); }
 };
 
-// The stream-K partition: CTA c owns units [start(c), start(c + 1)) of the flattened
-// (tile, k-tile) space, tiles ordered row tile major, item tile minor.
+// The partition: CTA c owns units [start(c), start(c + 1)) of the flattened
+// (tile, k-tile) space, tiles ordered row tile major, item tile minor.  Stream-K cuts it
+// into equal shares; cluster split-K gives rank q of tile t's cluster the k-tiles
+// [q * ktiles / s, (q + 1) * ktiles / s) of that tile.
 struct TcSched {
-  int units, grid;
-  __host__ __device__ int start(int c) const { return (int)(((long long)units * c) / grid); }
+  int units, grid, ktiles, csplit;
+  __host__ __device__ int start(int c) const {
+    if (csplit > 0) {
+      const int t = c / csplit, q = c - t * csplit;
+      return t * ktiles + (ktiles * q) / csplit;
+    }
+    return (int)(((long long)units * c) / grid);
+  }
   __host__ __device__ int cta_of(int u) const {
     int c = (int)(((long long)u * grid) / units);
     while (c + 1 < grid && start(c + 1) <= u) ++c;
@@ -205,6 +221,29 @@ __device__ __forceinline__ int tc_chunk_end(int cb, int kt1, int nh_tiles) {
   int ce = min(kt1, (cb / kTcChunk + 1) * kTcChunk);
   if (H == 2 && cb < nh_tiles && ce > nh_tiles) ce = nh_tiles;
   return ce;
+}
+
+// ------------------------------------------------------------------ cluster helpers
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster (no .aligned form: threads may arrive apart).
+// Each thread reaches the kernel's cluster barriers on every path, so the wait ends.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Address of the same shared-memory location in cluster rank `rank`.
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 // One lane of the (converged) warp, the same lane every time for the same mask.
@@ -350,13 +389,15 @@ __device__ void tc_tables(const TcArgs &A, int it, const TcTables &tb) {
 
 template <int N, int MODE>
 __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>::H][TcShape<N, MODE>::NCH][16],
-                                 int rt, int it, const TcTables &tb) {
+                                 int rt, int it, const TcTables &tb, unsigned ownm) {
   using S = TcShape<N, MODE>;
   constexpr int H = S::H, NCH = S::NCH, SP = N + 1;
   const GemvParams &p = A.p;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int quad = warp & 3, chalf = warp >> 2, r = quad * 32 + lane;
   const int item0 = it * N;
+  // chunk j of this thread is written by this CTA (cluster split-K: its share of the columns)
+  auto own = [&](int j) { return tc_has<N>(j, chalf) && ((ownm >> j) & 1u); };
 
   // y = sum over K halves of (raw sum) * (norm scale), in place in acc[0]
 #pragma unroll
@@ -379,7 +420,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
       if constexpr (MODE != GM_ENCODE) {
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
-          if (!tc_has<N>(j, chalf)) continue;
+          if (!own(j)) continue;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int item = item0 + tc_c0<N>(j, chalf) + i;
@@ -389,7 +430,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
       }
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
-        if (!tc_has<N>(j, chalf)) continue;
+        if (!own(j)) continue;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int item = item0 + tc_c0<N>(j, chalf) + i;
@@ -416,8 +457,9 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
         for (int i = 0; i < 16; ++i) {
           const int item = item0 + tc_c0<N>(j, chalf) + i;
           const float v = y[j][i];
-          if (vrow && item < A.M && p.dbg_f) p.dbg_f[(size_t)item * p.dbg_stride_b + p.dbg_off + row] = v;
-          keys[j * 16 + i] = vrow ? (((unsigned long long)float_order_key(v) << 32) |
+          const bool ok = vrow && own(j);
+          if (ok && item < A.M && p.dbg_f) p.dbg_f[(size_t)item * p.dbg_stride_b + p.dbg_off + row] = v;
+          keys[j * 16 + i] = ok ? (((unsigned long long)float_order_key(v) << 32) |
                                      (unsigned long long)(0xFFFFFFFFu - (uint32_t)row))
                                   : 0ull;
         }
@@ -453,7 +495,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
     if (r < 64 && row < p.n_ff) {
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
-        if (!tc_has<N>(j, chalf)) continue;
+        if (!own(j)) continue;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = tc_c0<N>(j, chalf) + i, item = item0 + c;
@@ -486,7 +528,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
         const int i0 = hr < half ? hr : hr - half;
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
-          if (!tc_has<N>(j, chalf)) continue;
+          if (!own(j)) continue;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int c = tc_c0<N>(j, chalf) + i;
@@ -500,7 +542,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
       }
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
-        if (!tc_has<N>(j, chalf)) continue;
+        if (!own(j)) continue;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = tc_c0<N>(j, chalf) + i, item = item0 + c;
@@ -564,6 +606,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   TcSched sched;
   sched.units = args.units;
   sched.grid = gridDim.x;
+  sched.ktiles = args.ktiles;
+  sched.csplit = args.csplit;
   const int cta = blockIdx.x;
   const int u_begin = sched.start(cta), u_end = sched.start(cta + 1);
 
@@ -652,6 +696,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
     for (int q = max(0, g - NA); q < g; ++q) tc_drain_wait(fullA + 8 * (q % NA), (q / NA) & 1);
     __syncwarp();
+    if (args.csplit) cluster_sync_all();  // the epilogue warps' partial exchange
   } else if (warp == kTcBWarp) {
     // ------------------------------------------------------------ activation tiles (L2)
     const bool leader = elect_one();
@@ -688,6 +733,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
     for (int q = max(0, g - NB); q < g; ++q) tc_drain_wait(fullB + 8 * (q % NB), (q / NB) & 1);
     __syncwarp();
+    if (args.csplit) cluster_sync_all();
   } else if (warp == kTcMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     const bool leader = elect_one();
@@ -739,6 +785,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     __syncwarp();
     tc_drain_wait(mma_done, 0);
     __syncwarp();
+    if (args.csplit) cluster_sync_all();
   } else {
     // ------------------------------------------------------------ drain + epilogues
     pdl_wait();  // norm sums, residuals and the outputs' earlier readers
@@ -755,6 +802,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     if (u_begin < u_end) tc_tables<N, MODE>(args, tb_it, tb);
     tc_epi_sync();
     float acc[H][NCH][16];
+    bool cl_synced = false;  // cluster split-K: this thread passed the exchange barrier
     for (int u = u_begin; u < u_end;) {
       const TcSeg sg = tc_seg(u, u_end, ktiles);
       u += sg.kt1 - sg.kt0;
@@ -789,28 +837,86 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         cb = ce;
       }
       const int rt = sg.t / item_tiles, it = sg.t % item_tiles;
-      if (!(sg.kt0 == 0 && sg.kt1 == ktiles)) {
-        // a shared tile: publish this CTA's raw sums; the last contributor adds them all
-        const int t0 = sg.t * ktiles;
-        const int c_first = sched.cta_of(t0), c_last = sched.cta_of(t0 + ktiles - 1);
-        // slot 0: the CTA's first segment; slot 1: a later (its last) segment
-        const int my_slot = sched.start(cta) >= t0 ? 0 : 1;
-        float *mine = args.part + ((size_t)cta * 2 + my_slot) * H * N * kTcM;
+      unsigned ownm = ~0u;
+      if (args.csplit) {
+        // cluster split-K (one segment per CTA): this rank's partial tile into its idle
+        // weight ring, one cluster barrier, then this rank's share of the columns summed
+        // over the ranks in rank order, straight from their shared memory
+        const int cs = args.csplit;
+        const uint32_t rank = cluster_rank();
+        float *red = reinterpret_cast<float *>(aring);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 #pragma unroll
         for (int h = 0; h < H; ++h)
 #pragma unroll
           for (int j = 0; j < NCH; ++j)
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              if (tc_has<N>(j, chalf)) mine[((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM + r] = acc[h][j][i];
-        __threadfence();
-        tc_epi_sync();
-        if (tid == 0) {
-          const unsigned prev = atomicAdd(args.tile_cnt + sg.t, 1u);
-          *last_sh = prev == (unsigned)(c_last - c_first) ? 1 : 0;
+              if (tc_has<N>(j, chalf)) red[((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM + r] = acc[h][j][i];
+        cluster_sync_all();
+        cl_synced = true;
+        ownm = 0u;
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          const int cidx = N >= 32 ? 2 * j + chalf : 0;
+          const bool mine = NCH >= cs ? (j % cs) == (int)rank : (cidx % cs) == (int)rank;
+          if (mine && tc_has<N>(j, chalf)) ownm |= 1u << j;
         }
-        tc_epi_sync();
-        if (!*last_sh) continue;
+        const uint32_t red_addr = smem_addr(red);
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          if (!((ownm >> j) & 1u)) continue;
+#pragma unroll
+          for (int h = 0; h < H; ++h) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[h][j][i] = 0.f;
+            const uint32_t off = (uint32_t)((((size_t)h * N + tc_c0<N>(j, chalf)) * kTcM + r) * 4);
+            for (int q = 0; q < cs; ++q) {
+              const uint32_t src = dsmem_map(red_addr + off, (uint32_t)q);
+              float v[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = ld_dsmem(src + (uint32_t)(i * kTcM * 4));
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc[h][j][i] += v[i];
+            }
+          }
+        }
+      } else if (!(sg.kt0 == 0 && sg.kt1 == ktiles)) {
+        // a shared tile: publish this CTA's raw sums; the last contributor adds them all
+        const int t0 = sg.t * ktiles;
+        const int c_first = sched.cta_of(t0), c_last = sched.cta_of(t0 + ktiles - 1);
+        // slot 0: the CTA's first segment; slot 1: a later (its last) segment
+        const int my_slot = sched.start(cta) >= t0 ? 0 : 1;
+        // The CTA's last segment: when every other contributor has already arrived, this
+        // CTA is the last and keeps its sums in registers (no publish, no arrival).
+        bool last_known = false;
+        if (u >= u_end) {
+          if (tid == 0) {
+            unsigned seen;
+            asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(seen) : "l"(args.tile_cnt + sg.t) : "memory");
+            *last_sh = seen == (unsigned)(c_last - c_first) ? 1 : 0;
+          }
+          tc_epi_sync();
+          last_known = *last_sh != 0;
+        }
+        if (!last_known) {
+          float *mine = args.part + ((size_t)cta * 2 + my_slot) * H * N * kTcM;
+#pragma unroll
+          for (int h = 0; h < H; ++h)
+#pragma unroll
+            for (int j = 0; j < NCH; ++j)
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (tc_has<N>(j, chalf)) mine[((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM + r] = acc[h][j][i];
+          __threadfence();
+          tc_epi_sync();
+          if (tid == 0) {
+            const unsigned prev = atomicAdd(args.tile_cnt + sg.t, 1u);
+            *last_sh = prev == (unsigned)(c_last - c_first) ? 1 : 0;
+          }
+          tc_epi_sync();
+          if (!*last_sh) continue;
+        }
         __threadfence();
         // fixed order: the published sums of contributors c_first .. c_last (this CTA's
         // own included), one contributor's tile at a time
@@ -915,8 +1021,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         tc_epi_sync();
         tb_it = it;
       }
-      tc_tile_epilogue<N, MODE>(args, acc, rt, it, tb);
+      tc_tile_epilogue<N, MODE>(args, acc, rt, it, tb, ownm);
     }
+    if (args.csplit && !cl_synced) cluster_sync_all();  // (a CTA without a segment)
     if constexpr (MODE == GM_LMHEAD) {
       // the last CTA to finish decodes every item's argmax
       if (args.item_tiles == 1) tc_lm_flush<N>(args, tb, 0);
@@ -935,6 +1042,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
   }
   __syncthreads();
+  // no CTA of a cluster leaves while a peer may still read its shared memory
+  if (args.csplit) cluster_sync_all();
   if (warp == kTcMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(S::kTmemCols) : "memory");
@@ -970,6 +1079,34 @@ bool tc_make_map(CUtensorMap *map, const void *base, int rows, int cols, int box
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Clusters of s CTAs (s = 2..8) of one instantiation that fit on the GPU at once (0: none,
+// or not queried); filled by tc_prepare.
+template <int N, int MODE>
+struct TcClusterFit {
+  static int n[9];
+};
+template <int N, int MODE>
+int TcClusterFit<N, MODE>::n[9] = {};
+
+// Cluster split-K width for `tiles` tiles of `ktiles` k-tiles: the s in 2..8 that keeps the
+// most SMs busy (at least two k-tiles per rank, every cluster co-resident), used when it
+// fills at least 80% of the SMs (any fill for TC_SCHED_CLUSTER); 0 = stream-K.
+static int tc_pick_split(const int *fit, long long tiles, int ktiles, int num_sms, int policy) {
+  if (policy == TC_SCHED_STREAM_K) return 0;
+  int best = 0;
+  long long best_ctas = 0;
+  for (int cs = 2; cs <= 8; ++cs) {
+    if (ktiles < 2 * cs || tiles * cs > num_sms) break;
+    if (tiles > fit[cs]) continue;
+    if (tiles * cs > best_ctas) {
+      best = cs;
+      best_ctas = tiles * cs;
+    }
+  }
+  if (policy != TC_SCHED_CLUSTER && best_ctas * 5 < (long long)num_sms * 4) return 0;
+  return best;
+}
+
 template <int N, int MODE>
 static cudaError_t tc_launch_n(const TcLaunch &L, cudaStream_t st, bool pdl) {
   using S = TcShape<N, MODE>;
@@ -998,19 +1135,31 @@ static cudaError_t tc_launch_n(const TcLaunch &L, cudaStream_t st, bool pdl) {
   const long long units = tiles * a.ktiles;
   if (units > (1ll << 30) || tiles > (long long)L.tile_cnt_elems) return cudaErrorInvalidValue;
   a.units = (int)units;
-  const int grid = (int)std::min<long long>(L.num_sms, units);
+  a.csplit = tc_pick_split(TcClusterFit<N, MODE>::n, tiles, a.ktiles, L.num_sms, L.schedule);
+  const int grid = a.csplit ? (int)tiles * a.csplit : (int)std::min<long long>(L.num_sms, units);
   // stream-K partials: two slots per CTA
-  if ((size_t)grid * 2 * S::H * N * kTcM > L.part_elems) return cudaErrorInvalidValue;
+  if (!a.csplit && (size_t)grid * 2 * S::H * N * kTcM > L.part_elems) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = S::kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (a.csplit) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)a.csplit;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = (unsigned)na;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<N, MODE>, a);
 }
 
@@ -1049,8 +1198,29 @@ cudaError_t tc_launch(const TcLaunch &L, cudaStream_t st, bool pdl) {
 
 template <int N, int MODE>
 static cudaError_t tc_prepare_n() {
-  return cudaFuncSetAttribute(gemm_tc_kernel<N, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              TcShape<N, MODE>::kSmem);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<N, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TcShape<N, MODE>::kSmem);
+  if (e != cudaSuccess) return e;
+  for (int cs = 2; cs <= 8; ++cs) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = TcShape<N, MODE>::kSmem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)cs;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<N, MODE>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();  // no cluster launches of this width: stream-K only
+      n = 0;
+    }
+    TcClusterFit<N, MODE>::n[cs] = n;
+  }
+  return cudaSuccess;
 }
 
 template <int MODE>

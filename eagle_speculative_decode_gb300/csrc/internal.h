@@ -36,7 +36,10 @@ struct TcLaunch {
   unsigned *tile_cnt;           // split-K counters (zero between launches)
   size_t tile_cnt_elems;
   int num_sms;
+  int schedule;                 // TC_SCHED_*: how the tiles are split over the SMs
 };
+// eagle3_set_tc_schedule's values
+constexpr int TC_SCHED_AUTO = 0, TC_SCHED_STREAM_K = 1, TC_SCHED_CLUSTER = 2;
 cudaError_t tc_prepare();
 int tc_tile_items(int M, int mode);
 cudaError_t tc_launch(const TcLaunch &L, cudaStream_t st, bool pdl);

@@ -92,6 +92,11 @@ class DraftModel:
         """Items from which projections use the tensor cores (0: the default)."""
         B.eagle3_set_tc_min_items(self.ctx, min_items)
 
+    def set_tc_schedule(self, schedule: int):
+        """Tile schedule of the tensor-core projections: 0 automatic, 1 stream-K,
+        2 cluster split-K wherever it fits."""
+        B.eagle3_set_tc_schedule(self.ctx, schedule)
+
     def status(self) -> int:
         return B.eagle3_get_status(self.ctx)
 

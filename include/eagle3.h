@@ -344,6 +344,18 @@ int eagle3_set_graph_mode(eagle3_ctx *ctx, int enabled);
  * graph is re-captured).  Returns EAGLE3_ERR_INVALID_ARG for a negative value. */
 int eagle3_set_tc_min_items(eagle3_ctx *ctx, int min_items);
 
+/* How a tensor-core projection spreads its 128-row tiles over the SMs.  0 (the default)
+ * chooses per launch: cluster split-K when there are few tiles -- each tile split along K
+ * over a thread-block cluster of 2..8 CTAs whose partial sums meet in distributed shared
+ * memory, every rank finishing its share of the tile's columns -- if that keeps at least
+ * 80% of the SMs busy; persistent stream-K otherwise (equal shares of all k-tiles per
+ * SM, a shared tile finished by its last contributor from partials published in L2).
+ * 1 always uses stream-K; 2 uses cluster split-K wherever 2..8 CTAs per tile fit on the
+ * GPU at once, whatever the fill.  Both give the same results up to the float32
+ * summation order of the partial sums.  Takes effect for later calls (a captured chain
+ * graph is re-captured).  Returns EAGLE3_ERR_INVALID_ARG for another value. */
+int eagle3_set_tc_schedule(eagle3_ctx *ctx, int schedule);
+
 /* ---- measurement (no counterpart on the pages; used by the benchmark) ----------------- */
 
 /* Number of kernels this context has launched since eagle3_init (a graph replay counts

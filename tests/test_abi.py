@@ -122,3 +122,12 @@ def test_header_is_plain_c(tmp_path):
                         os.path.dirname(HEADER), "-c", str(src), "-o", str(tmp_path / "o.o")],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_context_knobs_refuse_a_null_context(built_lib):
+    """The host-only setters check their context before anything else (no GPU needed)."""
+    for call in (lambda: Bd.eagle3_set_tc_schedule(0, 0), lambda: Bd.eagle3_set_tc_min_items(0, 3),
+                 lambda: Bd.eagle3_set_graph_mode(0, True)):
+        with pytest.raises(Bd.Eagle3Error) as ei:
+            call()
+        assert ei.value.code == Bd.EAGLE3_ERR_INVALID_ARG

@@ -1,7 +1,10 @@
 """GPU parity of the batched (tensor-core) projections on a small drafter whose q / k / v
 blocks are whole 128-row tiles (n_embd 256, 8:2 GQA, head 64): item tiles of 16 to 256
 columns with ragged tails, two item tiles in one launch (a 300-token prefill chunk), and
-full rounds at batch 20 and 40, element by element against the CPU oracle."""
+full rounds at batch 20 and 40, element by element against the CPU oracle -- under both
+tile schedules: stream-K (partials through L2, the last contributor finishes a tile) and
+cluster split-K (partials through distributed shared memory, each rank finishes its
+share of the columns), which the automatic choice would not take at this size."""
 import numpy as np
 import pytest
 import torch
@@ -31,8 +34,19 @@ def _prompt(batch, lens, seed):
     return toks, aux
 
 
+STREAM_K, CLUSTER = 1, 2
+
+
+@pytest.fixture(params=[STREAM_K, CLUSTER], ids=["stream_k", "cluster"])
+def schedule(request, small):
+    small[1].set_tc_schedule(request.param)
+    yield request.param
+    small[1].set_tc_schedule(0)
+
+
+@pytest.mark.parametrize("sched", [STREAM_K, CLUSTER], ids=["stream_k", "cluster"])
 @pytest.mark.parametrize("rows", [3, 16, 20, 37, 64, 100, 256, 300])
-def test_tc_encode_exact_integer_case(small, rows):
+def test_tc_encode_exact_integer_case(small, rows, sched):
     """fc in {-1, 0, 1} * 2^-4 and integer features: the tensor-core sums are exact in
     float32, so every output equals the oracle bit for bit -- a check of the operand
     layouts (swizzle, descriptors, item tiles) independent of rounding."""
@@ -46,6 +60,7 @@ def test_tc_encode_exact_integer_case(small, rows):
     bits["fc"] = fc_bits
     m2 = DraftModel(synth.DrafterWeights(G, bits, wts.d2t), max_batch=2, max_gamma=2,
                     max_cache_len=16, page_size=16)
+    m2.set_tc_schedule(sched)
     try:
         got = m2.encode(torch.from_numpy(aux_bits.view(np.int16)).to(m2.device)).cpu().numpy()
     finally:
@@ -54,7 +69,7 @@ def test_tc_encode_exact_integer_case(small, rows):
     assert np.array_equal(got.astype(np.float64), want)
 
 
-def test_tc_rounds_batch20_random_pages(small):
+def test_tc_rounds_batch20_random_pages(small, schedule):
     wts, model, dr = small
     B = 20
     lens = synth.ragged_lengths(B, 1, 60, seed=31)
@@ -71,7 +86,7 @@ def test_tc_rounds_batch20_random_pages(small):
         states = run_round(model, dr, seq, states, 4, n, seed=34 + r)[0]
 
 
-def test_tc_rounds_batch40_long_prompts(small):
+def test_tc_rounds_batch40_long_prompts(small, schedule):
     """Prompts up to 300 tokens: each prefill chunk is one launch over two item tiles."""
     wts, model, dr = small
     B = 40
