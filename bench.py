@@ -385,6 +385,8 @@ def run_mine(args, cfg):
     del wts
     if args.tc_min_items:
         model.set_tc_min_items(args.tc_min_items)
+    if args.tc_schedule:
+        model.set_tc_schedule(args.tc_schedule)
     seq = model.new_state(B)
 
     # prompt: tokens, aux features, the target's next token
@@ -652,6 +654,8 @@ def main():
                     help="drafter KV cache storage: bf16, or q8_0 keys / q5_1 values")
     ap.add_argument("--tc-min-items", type=int, default=0,
                     help="activation rows from which projections use the tensor cores (0: library default)")
+    ap.add_argument("--tc-schedule", type=int, default=0, choices=[0, 1, 2],
+                    help="tensor-core tile schedule: 0 library default, 1 stream-K, 2 cluster split-K where it fits")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

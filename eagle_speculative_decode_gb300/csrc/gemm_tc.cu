@@ -11,7 +11,7 @@
 //
 // Two schedules, one CTA per SM:
 //  * cluster split-K, when there are few tiles (T <= 76): each tile gets s CTAs
-//    (2 <= s <= 8, T * s close to the SM count) in one thread-block cluster, each
+//    (2 <= s <= 8, T * s at least 60% of the SM count) in one thread-block cluster, each
 //    multiplying a contiguous 1/s of K.  The s float32 partial tiles meet in distributed
 //    shared memory: after one cluster barrier every rank adds, for its own share of the
 //    item columns, the s partials in rank order and runs the tile epilogue on those
@@ -62,7 +62,7 @@ struct TcArgs {
   CUtensorMap b2;   // x2 of the split
   GemvParams p;     // epilogue parameters (p.items = M, p.item0 = 0)
   const float *sumsq;  // [M][halves] sum of squares of the staged x (norm modes)
-  float *part;         // stream-K partials [grid][2][halves][N][128]
+  float *part;         // stream-K partials [grid][2][N][128]
   unsigned *tile_cnt;  // stream-K arrival counters [tiles], zero between launches
   int csplit;          // cluster split-K: CTAs per tile (= cluster size); 0: stream-K
   int M;               // items in total
@@ -399,18 +399,7 @@ __device__ void tc_tile_epilogue(const TcArgs &A, float (&acc)[TcShape<N, MODE>:
   // chunk j of this thread is written by this CTA (cluster split-K: its share of the columns)
   auto own = [&](int j) { return tc_has<N>(j, chalf) && ((ownm >> j) & 1u); };
 
-  // y = sum over K halves of (raw sum) * (norm scale), in place in acc[0]
-#pragma unroll
-  for (int j = 0; j < NCH; ++j)
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int c = tc_c0<N>(j, chalf) + i;
-      float v = 0.f;
-#pragma unroll
-      for (int h = 0; h < H; ++h)
-        v += ModeTraits<MODE>::kNorm ? acc[h][j][i] * tb.scale[(c < N ? c : 0) * H + h] : acc[h][j][i];
-      acc[0][j][i] = v;
-    }
+  // y: the tile's sums, the K halves already scaled by their RMSNorm factors and added
   float(&y)[NCH][16] = acc[0];
 
   if constexpr (MODE == GM_ENCODE || MODE == GM_O || MODE == GM_DOWN) {
@@ -837,6 +826,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         cb = ce;
       }
       const int rt = sg.t / item_tiles, it = sg.t % item_tiles;
+      if (it != tb_it) {  // a tile of another item tile: its tables first
+        tc_epi_sync();
+        tc_tables<N, MODE>(args, it, tb);
+        tc_epi_sync();
+        tb_it = it;
+      }
+      // each K half's sum times its RMSNorm scale, the halves added: from here on a
+      // tile's partial sums are one [N][128] block
+      if constexpr (ModeTraits<MODE>::kNorm) {
+#pragma unroll
+        for (int j = 0; j < NCH; ++j)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = tc_c0<N>(j, chalf) + i;
+            float v = 0.f;
+#pragma unroll
+            for (int h = 0; h < H; ++h) v += acc[h][j][i] * tb.scale[(c < N ? c : 0) * H + h];
+            acc[0][j][i] = v;
+          }
+      } else if constexpr (H == 2) {
+#pragma unroll
+        for (int j = 0; j < NCH; ++j)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[0][j][i] += acc[1][j][i];
+      }
       unsigned ownm = ~0u;
       if (args.csplit) {
         // cluster split-K (one segment per CTA): this rank's partial tile into its idle
@@ -847,12 +861,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         float *red = reinterpret_cast<float *>(aring);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 #pragma unroll
-        for (int h = 0; h < H; ++h)
+        for (int j = 0; j < NCH; ++j)
 #pragma unroll
-          for (int j = 0; j < NCH; ++j)
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (tc_has<N>(j, chalf)) red[((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM + r] = acc[h][j][i];
+          for (int i = 0; i < 16; ++i)
+            if (tc_has<N>(j, chalf)) red[((size_t)tc_c0<N>(j, chalf) + i) * kTcM + r] = acc[0][j][i];
         cluster_sync_all();
         cl_synced = true;
         ownm = 0u;
@@ -867,18 +879,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         for (int j = 0; j < NCH; ++j) {
           if (!((ownm >> j) & 1u)) continue;
 #pragma unroll
-          for (int h = 0; h < H; ++h) {
+          for (int i = 0; i < 16; ++i) acc[0][j][i] = 0.f;
+          const uint32_t off = (uint32_t)(((size_t)tc_c0<N>(j, chalf) * kTcM + r) * 4);
+          for (int q = 0; q < cs; ++q) {
+            const uint32_t src = dsmem_map(red_addr + off, (uint32_t)q);
+            float v[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[h][j][i] = 0.f;
-            const uint32_t off = (uint32_t)((((size_t)h * N + tc_c0<N>(j, chalf)) * kTcM + r) * 4);
-            for (int q = 0; q < cs; ++q) {
-              const uint32_t src = dsmem_map(red_addr + off, (uint32_t)q);
-              float v[16];
+            for (int i = 0; i < 16; ++i) v[i] = ld_dsmem(src + (uint32_t)(i * kTcM * 4));
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = ld_dsmem(src + (uint32_t)(i * kTcM * 4));
-#pragma unroll
-              for (int i = 0; i < 16; ++i) acc[h][j][i] += v[i];
-            }
+            for (int i = 0; i < 16; ++i) acc[0][j][i] += v[i];
           }
         }
       } else if (!(sg.kt0 == 0 && sg.kt1 == ktiles)) {
@@ -900,14 +909,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           last_known = *last_sh != 0;
         }
         if (!last_known) {
-          float *mine = args.part + ((size_t)cta * 2 + my_slot) * H * N * kTcM;
+          float *mine = args.part + ((size_t)cta * 2 + my_slot) * N * kTcM;
 #pragma unroll
-          for (int h = 0; h < H; ++h)
+          for (int j = 0; j < NCH; ++j)
 #pragma unroll
-            for (int j = 0; j < NCH; ++j)
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                if (tc_has<N>(j, chalf)) mine[((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM + r] = acc[h][j][i];
+            for (int i = 0; i < 16; ++i)
+              if (tc_has<N>(j, chalf)) mine[((size_t)tc_c0<N>(j, chalf) + i) * kTcM + r] = acc[0][j][i];
           __threadfence();
           tc_epi_sync();
           if (tid == 0) {
@@ -921,27 +928,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         // fixed order: the published sums of contributors c_first .. c_last (this CTA's
         // own included), one contributor's tile at a time
         auto part_of = [&](int cq) {  // a contributor's segment is its first (slot 0) unless it began earlier
-          return args.part + ((size_t)cq * 2 + (sched.start(cq) >= t0 ? 0 : 1)) * H * N * kTcM;
+          return args.part + ((size_t)cq * 2 + (sched.start(cq) >= t0 ? 0 : 1)) * N * kTcM;
         };
         if (u >= u_end) {
           // this CTA's last segment: its rings are idle, so one thread bulk-copies every
           // other contributor's published partial into them (all in flight at once), and
           // the rows are added in CTA order from shared memory; this CTA's own sums are
           // still in registers.
-          constexpr int kPart = H * N * kTcM;  // floats per published partial
+          constexpr int kPart = N * kTcM;  // floats per published partial
           constexpr int kCap = (int)(((size_t)NA * S::kA + (size_t)NB * S::kBStage) / ((size_t)kPart * 4));
           static_assert(kCap >= 1, "a published partial fits the rings");
           const float *stg = reinterpret_cast<const float *>(aring);
-          float own[H][NCH][16];
+          float own[NCH][16];
 #pragma unroll
-          for (int h = 0; h < H; ++h)
+          for (int j = 0; j < NCH; ++j)
 #pragma unroll
-            for (int j = 0; j < NCH; ++j)
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                own[h][j][i] = acc[h][j][i];
-                acc[h][j][i] = 0.f;
-              }
+            for (int i = 0; i < 16; ++i) {
+              own[j][i] = acc[0][j][i];
+              acc[0][j][i] = 0.f;
+            }
           for (int c2 = c_first; c2 <= c_last; c2 += kCap) {
             const int cend = min(c_last, c2 + kCap - 1);
             const bool others = !(c2 == cend && c2 == cta);
@@ -962,19 +967,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             }
             for (int cq = c2; cq <= cend; ++cq) {
 #pragma unroll
-              for (int h = 0; h < H; ++h)
+              for (int j = 0; j < NCH; ++j) {
+                if (!tc_has<N>(j, chalf)) continue;
+                if (cq == cta) {
 #pragma unroll
-                for (int j = 0; j < NCH; ++j) {
-                  if (!tc_has<N>(j, chalf)) continue;
-                  if (cq == cta) {
+                  for (int i = 0; i < 16; ++i) acc[0][j][i] += own[j][i];
+                } else {
+                  const float *src = stg + (size_t)(cq - c2) * kPart + (size_t)tc_c0<N>(j, chalf) * kTcM + r;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[h][j][i] += own[h][j][i];
-                  } else {
-                    const float *src = stg + (size_t)(cq - c2) * kPart + ((size_t)h * N + tc_c0<N>(j, chalf)) * kTcM + r;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[h][j][i] += src[(size_t)i * kTcM];
-                  }
+                  for (int i = 0; i < 16; ++i) acc[0][j][i] += src[(size_t)i * kTcM];
                 }
+              }
             }
             tc_epi_sync();  // every thread has read this batch before the next overwrites it
           }
@@ -982,44 +985,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           // mid-share (the rings are still streaming this CTA's next tile): kU contributors
           // per pass, all their loads in flight together, added in CTA order
 #pragma unroll
-          for (int h = 0; h < H; ++h)
+          for (int j = 0; j < NCH; ++j)
 #pragma unroll
-            for (int j = 0; j < NCH; ++j)
-#pragma unroll
-              for (int i = 0; i < 16; ++i) acc[h][j][i] = 0.f;
-          constexpr int kVals = H * NCH * 16;
+            for (int i = 0; i < 16; ++i) acc[0][j][i] = 0.f;
+          constexpr int kVals = NCH * 16;
           constexpr int kU = kVals >= 64 ? 2 : (kVals >= 32 ? 4 : 8);
           for (int c2 = c_first; c2 <= c_last; c2 += kU) {
             const float *src[kU];
 #pragma unroll
             for (int q = 0; q < kU; ++q) src[q] = part_of(min(c2 + q, c_last)) + r;  // past the last: not added
 #pragma unroll
-            for (int h = 0; h < H; ++h)
+            for (int j = 0; j < NCH; ++j) {
+              if (!tc_has<N>(j, chalf)) continue;
+              float v[kU][16];
 #pragma unroll
-              for (int j = 0; j < NCH; ++j) {
-                if (!tc_has<N>(j, chalf)) continue;
-                float v[kU][16];
+              for (int q = 0; q < kU; ++q)
 #pragma unroll
-                for (int q = 0; q < kU; ++q)
+                for (int i = 0; i < 16; ++i) v[q][i] = __ldcg(src[q] + ((size_t)tc_c0<N>(j, chalf) + i) * kTcM);
 #pragma unroll
-                  for (int i = 0; i < 16; ++i)
-                    v[q][i] = __ldcg(src[q] + ((size_t)h * N + tc_c0<N>(j, chalf) + i) * kTcM);
+              for (int q = 0; q < kU; ++q)
+                if (c2 + q <= c_last) {
 #pragma unroll
-                for (int q = 0; q < kU; ++q)
-                  if (c2 + q <= c_last) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[h][j][i] += v[q][i];
-                  }
-              }
+                  for (int i = 0; i < 16; ++i) acc[0][j][i] += v[q][i];
+                }
+            }
           }
         }
         if (tid == 0) args.tile_cnt[sg.t] = 0u;
-      }
-      if (it != tb_it) {  // a tile of another item tile: its tables first
-        tc_epi_sync();
-        tc_tables<N, MODE>(args, it, tb);
-        tc_epi_sync();
-        tb_it = it;
       }
       tc_tile_epilogue<N, MODE>(args, acc, rt, it, tb, ownm);
     }
@@ -1090,7 +1082,9 @@ int TcClusterFit<N, MODE>::n[9] = {};
 
 // Cluster split-K width for `tiles` tiles of `ktiles` k-tiles: the s in 2..8 that keeps the
 // most SMs busy (at least two k-tiles per rank, every cluster co-resident), used when it
-// fills at least 80% of the SMs (any fill for TC_SCHED_CLUSTER); 0 = stream-K.
+// fills at least 60% of the SMs (any fill for TC_SCHED_CLUSTER); 0 = stream-K.  Measured
+// on the drafter's batched projections, 96 of 152 SMs in clusters beat 152 in stream-K:
+// the stream-K finisher's serial fix-up and epilogue cost more than the idle SMs.
 static int tc_pick_split(const int *fit, long long tiles, int ktiles, int num_sms, int policy) {
   if (policy == TC_SCHED_STREAM_K) return 0;
   int best = 0;
@@ -1103,7 +1097,7 @@ static int tc_pick_split(const int *fit, long long tiles, int ktiles, int num_sm
       best_ctas = tiles * cs;
     }
   }
-  if (policy != TC_SCHED_CLUSTER && best_ctas * 5 < (long long)num_sms * 4) return 0;
+  if (policy != TC_SCHED_CLUSTER && best_ctas * 5 < (long long)num_sms * 3) return 0;
   return best;
 }
 
@@ -1138,7 +1132,7 @@ static cudaError_t tc_launch_n(const TcLaunch &L, cudaStream_t st, bool pdl) {
   a.csplit = tc_pick_split(TcClusterFit<N, MODE>::n, tiles, a.ktiles, L.num_sms, L.schedule);
   const int grid = a.csplit ? (int)tiles * a.csplit : (int)std::min<long long>(L.num_sms, units);
   // stream-K partials: two slots per CTA
-  if (!a.csplit && (size_t)grid * 2 * S::H * N * kTcM > L.part_elems) return cudaErrorInvalidValue;
+  if (!a.csplit && (size_t)grid * 2 * N * kTcM > L.part_elems) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTcThreads);

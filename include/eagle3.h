@@ -348,7 +348,7 @@ int eagle3_set_tc_min_items(eagle3_ctx *ctx, int min_items);
  * chooses per launch: cluster split-K when there are few tiles -- each tile split along K
  * over a thread-block cluster of 2..8 CTAs whose partial sums meet in distributed shared
  * memory, every rank finishing its share of the tile's columns -- if that keeps at least
- * 80% of the SMs busy; persistent stream-K otherwise (equal shares of all k-tiles per
+ * 60% of the SMs busy; persistent stream-K otherwise (equal shares of all k-tiles per
  * SM, a shared tile finished by its last contributor from partials published in L2).
  * 1 always uses stream-K; 2 uses cluster split-K wherever 2..8 CTAs per tile fit on the
  * GPU at once, whatever the fill.  Both give the same results up to the float32
