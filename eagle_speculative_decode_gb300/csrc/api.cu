@@ -23,7 +23,7 @@ constexpr int kMaxGraphs = 16;
 
 struct Layout {
   size_t rope, q, attn_o, part_o, part_ml, attn_cnt, x1, act, gwork, tokwork, am_slot, am_cnt,
-      round_start, geff, status, genc, xp0, xp1, xp2, sumsq, tc_part, tc_cnt, attn_plan, kv_stage, gres,
+      round_start, geff, status, genc, xp0, xp1, xp2, sumsq, gsum, tc_part, tc_cnt, attn_plan, kv_stage, gres,
       total;
   size_t tc_items, tc_k, tc_part_elems;
 };
@@ -109,6 +109,8 @@ Layout make_layout(const eagle3_config &c) {
   L.xp1 = take(L.tc_items * L.tc_k * 2);
   L.xp2 = take(L.tc_items * L.tc_k * 2);
   L.sumsq = take(L.tc_items * 2 * 4);
+  // INT4 weights: each item's sum of x over every 128-wide group of a projection's input
+  L.gsum = take(c.weight_format == EAGLE3_W_INT4_G128 ? L.tc_items * (L.tc_k / 128) * 4 : 0);
   L.tc_part_elems = (size_t)2 * 160 * 128 * 256;
   L.tc_part = take(L.tc_part_elems * 4);
   L.tc_cnt = take(kTcCounters * 4);
@@ -184,6 +186,7 @@ struct eagle3_ctx {
   float *gres;  // norm_before_residual: RMSNorm(g) * hidden_norm of the step, [B, n]
   int q4;       // INT4 projection weights (EAGLE3_W_INT4_G128)
   uint16_t *xp0, *xp1, *xp2;  // the three bf16 parts of x
+  float *gsum;                // INT4: sums of x per 128-wide group (tensor-core path)
   float *sumsq, *tc_part;
   unsigned *tc_cnt;
 };
@@ -279,6 +282,13 @@ cudaError_t tc_items(eagle3_ctx *ctx, const GemvParams &p, int items, cudaStream
   L.tile_cnt_elems = kTcCounters;
   L.num_sms = ctx->num_sms;
   L.schedule = ctx->tc_sched;
+  if (p.sz0) {  // INT4 weights: a* are code rows
+    L.s0 = p.sz0;
+    L.s1 = p.sz1;
+    L.s2 = p.sz2;
+    L.sz_stride = p.sz_stride;
+    L.gsum = ctx->gsum;
+  }
   const int n = c.n_embd, qr = c.n_head * c.head_dim, kr = c.n_head_kv * c.head_dim;
   switch (p.mode) {
     case GM_ENCODE: L.a0 = ctx->w.fc; L.a0_rows = n; break;
@@ -309,7 +319,8 @@ cudaError_t tc_items(eagle3_ctx *ctx, const GemvParams &p, int items, cudaStream
     return cudaSuccess;
   } else {
     cudaError_t e = launched(
-        ctx, st, tc_prep_launch(p, items, ctx->xp0, ctx->xp1, ctx->xp2, ctx->sumsq, st, pdl), PH_SMALL);
+        ctx, st, tc_prep_launch(p, items, ctx->xp0, ctx->xp1, ctx->xp2, ctx->sumsq, p.sz0 ? ctx->gsum : nullptr, st, pdl),
+        PH_SMALL);
     if (e != cudaSuccess) return e;
     L.b0 = ctx->xp0;
     L.b1 = ctx->xp1;
@@ -320,10 +331,10 @@ cudaError_t tc_items(eagle3_ctx *ctx, const GemvParams &p, int items, cudaStream
 
 bool use_tc(const eagle3_ctx *ctx, const GemvParams &p, int items) {
   if (!ctx->tc_ok || items < ctx->tc_min_items) return false;
-  if (p.sz0) return false;  // INT4 weights run on the GEMV
-  // k/v-only teacher forcing of a few pairs (rebuild): 2 * H_kv * d rows are too few row
-  // tiles for the tensor-core split, whose fix-up then dominates
-  if (p.mode == GM_QKV && p.row_base > 0 && items <= 8) return false;
+  if (p.sz0 && (!ctx->gsum || p.K % 128)) return false;  // INT4: the group sums' buffer and whole groups
+  // k/v-only teacher forcing of a few pairs (rebuild) with bf16 weights: the 4-8-item
+  // GEMV measured faster (INT4 takes the tensor cores: its several-item GEMV is slower)
+  if (p.mode == GM_QKV && p.row_base > 0 && items <= 8 && !p.sz0) return false;
   if (p.mode != GM_ENCODE && (size_t)items > ctx->L.tc_items) return false;
   if (p.mode != GM_ENCODE && p.K > kTcPrepMaxK) return false;  // the activation split's limit
   return true;
@@ -735,6 +746,7 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
   ctx->xp1 = reinterpret_cast<uint16_t *>(b + L.xp1);
   ctx->xp2 = reinterpret_cast<uint16_t *>(b + L.xp2);
   ctx->sumsq = reinterpret_cast<float *>(b + L.sumsq);
+  ctx->gsum = ctx->q4 ? reinterpret_cast<float *>(b + L.gsum) : nullptr;
   ctx->tc_part = reinterpret_cast<float *>(b + L.tc_part);
   ctx->tc_cnt = reinterpret_cast<unsigned *>(b + L.tc_cnt);
   ctx->graph_mode = 1;

@@ -30,6 +30,10 @@ struct TcLaunch {
   const void *a0, *a1, *a2;     // weight matrices of the mode (see gemm_tc.cu)
   int a0_rows, a1_rows, a2_rows;
   const uint16_t *b0, *b1, *b2; // activations bf16 [M, K]: one part (encode) or three
+  const uint32_t *s0, *s1, *s2; // INT4 weights: (scale, zero) rows of a0 / a1 / a2 (a* are
+                                // then code rows of K / 2 bytes); null for bf16 weights
+  int sz_stride;                // INT4: pairs per (scale, zero) row
+  const float *gsum;            // INT4: [M][K / 128] sums of x per 128-wide group
   const float *sumsq;           // [M][halves] (norm modes)
   float *part;                  // split-K partials
   size_t part_elems;
@@ -43,8 +47,11 @@ constexpr int TC_SCHED_AUTO = 0, TC_SCHED_STREAM_K = 1, TC_SCHED_CLUSTER = 2;
 cudaError_t tc_prepare();
 int tc_tile_items(int M, int mode);
 cudaError_t tc_launch(const TcLaunch &L, cudaStream_t st, bool pdl);
+// INT4-weight instantiations (gemm_tc_q4.cu)
+cudaError_t tc_q4_prepare();
+cudaError_t tc_q4_launch(const TcLaunch &L, cudaStream_t st, bool pdl);
 cudaError_t tc_prep_launch(const GemvParams &p, int M, uint16_t *x0, uint16_t *x1, uint16_t *x2,
-                           float *sumsq, cudaStream_t st, bool pdl);
+                           float *sumsq, float *gsum, cudaStream_t st, bool pdl);
 
 bool attn_supported(int head_dim, int group);
 cudaError_t attn_prepare();

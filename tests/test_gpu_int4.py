@@ -2,8 +2,11 @@
 zero) per 128 inputs; fc, norms and embedding bf16) against the oracle dequantizing the
 same codes: full rounds through the C ABI on the small drafter (one item per launch with x
 in registers, and 2 to 8 items per launch: the ragged batch and the prefill's k/v-only
-projections), with CUDA graphs and with direct launches, and on the eagle.rs geometry at
-batch 1 / prompt 512 / gamma 3 (the benchmark's configuration) and a batch of 8."""
+projections), with CUDA graphs and with direct launches; batched rounds on a small drafter
+whose projections take the tensor cores (the codes decoded to bf16 in shared memory, each
+128-wide group's sums scaled in the epilogue) under both tile schedules, and on the
+CUDA-core GEMV for comparison; and on the eagle.rs geometry at batch 1 / prompt 512 /
+gamma 3 (the benchmark's configuration) and a batch of 8 (tensor cores)."""
 import numpy as np
 import pytest
 import torch
@@ -57,6 +60,32 @@ def test_int4_ragged_batch(tiny, graphs):
         _rounds(g, model, dr, np.array([5, 33, 17, 1, 60, 2, 9]), 4, [20, 21], seed=22)
     finally:
         model.set_graph_mode(True)
+
+
+@pytest.fixture(scope="module")
+def small_q4(built_lib):
+    g = synth.SMALL
+    wts = synth.make_int4_weights(g, seed=8)
+    model = DraftModel(wts, max_batch=20, max_gamma=4, max_cache_len=160, page_size=16)
+    dr = O.Drafter(g, wts.bits, wts.d2t, int4=wts.int4)
+    yield g, model, dr
+    model.close()
+
+
+@pytest.mark.parametrize("path", ["tc_stream_k", "tc_cluster", "gemv"])
+def test_int4_batched_projections(small_q4, path):
+    """Batch 20 (and prefills of up to 100 positions): 3 or more items per projection run
+    on the tensor cores unless the threshold keeps them on the GEMV."""
+    g, model, dr = small_q4
+    if path == "gemv":
+        model.set_tc_min_items(1 << 20)
+    else:
+        model.set_tc_schedule(1 if path == "tc_stream_k" else 2)
+    try:
+        _rounds(g, model, dr, synth.ragged_lengths(20, 1, 100, seed=70), 4, [71, 72], seed=73)
+    finally:
+        model.set_tc_min_items(0)
+        model.set_tc_schedule(0)
 
 
 def test_int4_full_geometry(built_lib):
