@@ -36,7 +36,8 @@ EXPORTED = (
     "eagle3_init", "eagle3_destroy", "eagle3_encode", "eagle3_prefill", "eagle3_draft_chain",
     "eagle3_rewind", "eagle3_accept", "eagle3_verify_greedy", "eagle3_rebuild_after_verify",
     "eagle3_get_status",
-    "eagle3_set_graph_mode", "eagle3_set_tc_min_items", "eagle3_set_tc_schedule", "eagle3_launch_count", "eagle3_profile_begin",
+    "eagle3_set_graph_mode", "eagle3_set_tc_min_items", "eagle3_set_tc_schedule", "eagle3_set_attention",
+    "eagle3_launch_count", "eagle3_profile_begin",
     "eagle3_profile_end", "eagle3_profile_interval", "eagle3_lmhead_argmax_noalloc",
 )
 
@@ -122,6 +123,7 @@ def load() -> ctypes.CDLL:
         "eagle3_set_graph_mode": (ci, [vp, ci]),
         "eagle3_set_tc_min_items": (ci, [vp, ci]),
         "eagle3_set_tc_schedule": (ci, [vp, ci]),
+        "eagle3_set_attention": (ci, [vp, ci]),
         "eagle3_launch_count": (ctypes.c_ulonglong, [vp]),
         "eagle3_profile_begin": (ci, [vp, ci]),
         "eagle3_profile_end": (ci, [vp, P(ci)]),
@@ -220,6 +222,10 @@ def eagle3_set_tc_min_items(ctx: int, min_items: int) -> None:
 
 def eagle3_set_tc_schedule(ctx: int, schedule: int) -> None:
     _check(load().eagle3_set_tc_schedule(ctx, schedule), "eagle3_set_tc_schedule")
+
+
+def eagle3_set_attention(ctx: int, mode: int) -> None:
+    _check(load().eagle3_set_attention(ctx, mode), "eagle3_set_attention")
 
 
 def eagle3_encode(ctx: int, aux: int, M: int, g: int, stream: int = 0) -> None:

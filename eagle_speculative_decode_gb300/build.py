@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libeagle3.so")
-SOURCES = ["api.cu", "gemv.cu", "gemv_q4.cu", "gemm_tc.cu", "gemm_tc_q4.cu", "attention.cu", "small.cu", "noalloc.cu", "kvquant.cu", "config.cu"]
+SOURCES = ["api.cu", "gemv.cu", "gemv_q4.cu", "gemm_tc.cu", "gemm_tc_q4.cu", "attention.cu", "attention_tc.cu", "small.cu", "noalloc.cu", "kvquant.cu", "config.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -177,6 +177,7 @@ struct eagle3_ctx {
   std::vector<cudaEvent_t> ev_pool;
   // tensor-core path
   int tc_ok, tc_min_items, tc_sched;
+  int attn_mode;  // ATTN_*: which decode attention kernel runs (bf16 KV)
   // attention work units (keys per unit) and the round's unit prefix tables
   int unit_keys;
   int32_t *attn_plan;
@@ -460,6 +461,7 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     ap.k_pool = static_cast<const unsigned char *>(a.kv->k_pool);
     ap.v_pool = static_cast<const unsigned char *>(a.kv->v_pool);
     ap.kv_q = ctx->kv_q;
+    ap.tc = ctx->attn_mode == ATTN_TENSOR_CORES;
     ap.page_table = a.kv->page_table;
     ap.kv_len = a.kv->kv_len;
     ap.gamma_eff = ctx->geff;
@@ -769,6 +771,7 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
     ctx->tc_ok = geo && tc_prepare() == cudaSuccess ? 1 : 0;
     ctx->tc_min_items = kTcMinItems;
     ctx->tc_sched = TC_SCHED_AUTO;
+    ctx->attn_mode = ATTN_CUDA_CORES;
   }
 
   // RoPE table: angle p * theta^(-2i/R) in double, stored as float32 (cos, sin).
@@ -833,6 +836,15 @@ int eagle3_set_tc_schedule(eagle3_ctx *ctx, int schedule) {
   if (!ctx || schedule < TC_SCHED_AUTO || schedule > TC_SCHED_CLUSTER) return EAGLE3_ERR_INVALID_ARG;
   if (schedule != ctx->tc_sched) {
     ctx->tc_sched = schedule;
+    drop_graphs(ctx);
+  }
+  return EAGLE3_OK;
+}
+
+int eagle3_set_attention(eagle3_ctx *ctx, int mode) {
+  if (!ctx || mode < ATTN_CUDA_CORES || mode > ATTN_TENSOR_CORES) return EAGLE3_ERR_INVALID_ARG;
+  if (mode != ctx->attn_mode) {
+    ctx->attn_mode = mode;
     drop_graphs(ctx);
   }
   return EAGLE3_OK;

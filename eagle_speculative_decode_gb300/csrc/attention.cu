@@ -28,6 +28,7 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include "attn_sched.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -113,51 +114,6 @@ __device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t u) { return make_floa
 // for each j; only j = i lands on a multiple of 8 and no two terms share a bit (no carry).
 __device__ __forceinline__ uint32_t spread4_to_bit4(uint32_t x) {
   return ((x * 0x00204081u) & 0x01010101u) << 4;
-}
-
-// The unit partition of one launch: pre[b] = units of one kv head of sequences < b (a
-// table chain_begin wrote for this step before any later kernel of the round started);
-// CTA c owns units [start(c), start(c + 1)) of the Hkv * pre[B] units in (sequence,
-// kv head, unit) order.
-struct AttnSched {
-  const int *pre;
-  int B, Hkv, grid;
-  long long total;
-  __device__ long long start(int c) const { return total * c / grid; }
-  __device__ int cta_of(long long u) const {
-    int c = (int)(u * grid / total);
-    while (c + 1 < grid && start(c + 1) <= u) ++c;
-    while (c > 0 && start(c) > u) --c;
-    return c;
-  }
-  // sequence b whose units hold u: the largest b with Hkv * pre[b] <= u
-  __device__ int seq_of(long long u) const {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if ((long long)Hkv * pre[mid] <= u) lo = mid;
-      else hi = mid - 1;
-    }
-    return lo;
-  }
-};
-
-// A run of units [r0, r1) of pair (b, kvh) inside one CTA's share; pair units nu.
-struct AttnSeg {
-  int b, kvh, r0, r1, nu;
-  long long pair_u0;  // first unit of the pair
-};
-
-__device__ __forceinline__ AttnSeg attn_seg(const AttnSched &S, long long u, long long u_end) {
-  AttnSeg s;
-  s.b = S.seq_of(u);
-  s.nu = S.pre[s.b + 1] - S.pre[s.b];
-  const long long off = u - (long long)S.Hkv * S.pre[s.b];
-  s.kvh = (int)(off / s.nu);
-  s.r0 = (int)(off - (long long)s.kvh * s.nu);
-  s.pair_u0 = u - s.r0;
-  s.r1 = (int)min((long long)s.nu, (long long)s.r0 + (u_end - u));
-  return s;
 }
 
 template <int D, int G, bool KVQ>
@@ -596,7 +552,7 @@ bool attn_supported(int head_dim, int group) {
   X(64, 1) X(64, 2) X(64, 4) X(64, 8) X(128, 1) X(128, 2) X(128, 4) X(128, 8) X(256, 1) X(256, 2) X(256, 4) X(256, 8)
 
 cudaError_t attn_prepare() {
-  cudaError_t e = cudaSuccess;
+  cudaError_t e = attn_tc_prepare();
 #define E3_PREP(DD, GG) \
   if (e == cudaSuccess) e = attn_prepare_dg<DD, GG>();
   E3_ATTN_ALL(E3_PREP)
@@ -616,6 +572,7 @@ int attn_unit_keys(int head_dim, int group, int page_size, int kv_q) {
 cudaError_t attn_launch(const AttnParams &p, int num_sms, cudaStream_t st, bool pdl) {
   const int G = p.n_head / p.n_head_kv;
   if (p.batch < 1 || p.unit_keys < 1 || !p.unit_pre) return cudaErrorInvalidValue;
+  if (p.tc && !p.kv_q && attn_tc_supported(p.head_dim, G, p.unit_keys)) return attn_tc_launch(p, num_sms, st, pdl);
 #define E3_ATTN_CASE(DD, GG)                                                             \
   if (p.head_dim == DD && G == GG)                                                      \
     return p.kv_q ? attn_launch_dg<DD, GG, true>(p, num_sms, st, pdl) : attn_launch_dg<DD, GG, false>(p, num_sms, st, pdl);

@@ -258,6 +258,7 @@ struct AttnParams {
   int n_head, n_head_kv, head_dim;
   int batch;               // sequences B
   int kv_q;                // 0: bf16 rows; 1: q8_0 K / q5_1 V rows
+  int tc;                  // bf16 rows: 1 = the tensor-core kernel (attention_tc.cu)
   int unit_keys;           // keys per work unit (divides the page size)
   const int32_t *unit_pre; // [B + 1] unit prefix of this step (round plan)
   float *part_o;           // [2 * CTAs, G, d] shared pairs' weighted V sums

@@ -44,6 +44,8 @@ struct TcLaunch {
 };
 // eagle3_set_tc_schedule's values
 constexpr int TC_SCHED_AUTO = 0, TC_SCHED_STREAM_K = 1, TC_SCHED_CLUSTER = 2;
+// eagle3_set_attention's values
+constexpr int ATTN_CUDA_CORES = 0, ATTN_TENSOR_CORES = 1;
 cudaError_t tc_prepare();
 int tc_tile_items(int M, int mode);
 cudaError_t tc_launch(const TcLaunch &L, cudaStream_t st, bool pdl);
@@ -59,6 +61,11 @@ int attn_unit_keys(int head_dim, int group, int page_size, int kv_q);
 cudaError_t kv_quant_launch(const GemvParams &p, int items, int k_row, int v_row, cudaStream_t st,
                             bool pdl);
 cudaError_t attn_launch(const AttnParams &p, int num_sms, cudaStream_t st, bool pdl);
+// Tensor-core variant for bf16 KV (attention_tc.cu): d 64 / 128 / 256, G <= 4, units of
+// 16..64 keys (a multiple of 16).
+bool attn_tc_supported(int head_dim, int group, int unit_keys);
+cudaError_t attn_tc_prepare();
+cudaError_t attn_tc_launch(const AttnParams &p, int num_sms, cudaStream_t st, bool pdl);
 
 // Small bookkeeping kernels (small.cu).
 cudaError_t launch_chain_begin(int B, int gamma, unsigned flags, int max_cache_len,

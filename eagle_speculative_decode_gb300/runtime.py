@@ -92,6 +92,11 @@ class DraftModel:
         """Items from which projections use the tensor cores (0: the default)."""
         B.eagle3_set_tc_min_items(self.ctx, min_items)
 
+    def set_attention(self, mode: int):
+        """Decode attention kernel for a bf16 KV cache: 0 CUDA cores (the default),
+        1 tensor cores where they apply."""
+        B.eagle3_set_attention(self.ctx, mode)
+
     def set_tc_schedule(self, schedule: int):
         """Tile schedule of the tensor-core projections: 0 automatic, 1 stream-K,
         2 cluster split-K wherever it fits."""

@@ -356,6 +356,18 @@ int eagle3_set_tc_min_items(eagle3_ctx *ctx, int min_items);
  * graph is re-captured).  Returns EAGLE3_ERR_INVALID_ARG for another value. */
 int eagle3_set_tc_schedule(eagle3_ctx *ctx, int schedule);
 
+/* Which kernel runs the decode attention over a bf16 KV cache.  0 (the default): the
+ * CUDA-core kernel (packed float32 FMAs).  1: the tensor-core kernel -- QK and PV on
+ * warp-level bf16 MMAs, q and the probabilities split into three exact bf16 parts so the
+ * arithmetic keeps float32 accuracy -- wherever it applies (head_dim 64, 128 or 256; at
+ * most 4 q heads per kv head; attention units of 16 to 64 keys, i.e. a page size that is
+ * a multiple of 16), the CUDA-core kernel otherwise.  A quantized KV cache always uses the
+ * CUDA-core kernel.  Both give the same results up to the float32 summation order; on
+ * the drafter's long contexts the CUDA-core kernel is the faster one.  Takes effect for
+ * later calls (a captured chain graph is re-captured).  Returns EAGLE3_ERR_INVALID_ARG for
+ * another value. */
+int eagle3_set_attention(eagle3_ctx *ctx, int mode);
+
 /* ---- measurement (no counterpart on the pages; used by the benchmark) ----------------- */
 
 /* Number of kernels this context has launched since eagle3_init (a graph replay counts

@@ -126,7 +126,8 @@ def test_header_is_plain_c(tmp_path):
 
 def test_context_knobs_refuse_a_null_context(built_lib):
     """The host-only setters check their context before anything else (no GPU needed)."""
-    for call in (lambda: Bd.eagle3_set_tc_schedule(0, 0), lambda: Bd.eagle3_set_tc_min_items(0, 3),
+    for call in (lambda: Bd.eagle3_set_tc_schedule(0, 0), lambda: Bd.eagle3_set_attention(0, 0),
+                 lambda: Bd.eagle3_set_tc_min_items(0, 3),
                  lambda: Bd.eagle3_set_graph_mode(0, True)):
         with pytest.raises(Bd.Eagle3Error) as ei:
             call()

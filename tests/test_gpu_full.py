@@ -53,12 +53,15 @@ def test_batch1_prompt512_gamma3_rounds(full):
         model.close()
 
 
-def test_ragged_batch8_gamma5_random_pages(full):
+@pytest.mark.parametrize("attention", [0, 1], ids=["attn_cuda_cores", "attn_tensor_cores"])
+def test_ragged_batch8_gamma5_random_pages(full, attention):
     """Ragged prompts (shortened from the 512-8192 range so that the oracle runs every
-    position), gamma 5, accept lengths uniform in 0..gamma, non-contiguous pages."""
+    position), gamma 5, accept lengths uniform in 0..gamma, non-contiguous pages; under
+    both decode attention kernels (head 256, 4 q heads per kv head, 64-key units)."""
     wts, dr = full
     B, gamma, ps, max_cache = 8, 5, 64, 1024
     model = DraftModel(wts, max_batch=B, max_gamma=gamma, max_cache_len=max_cache, page_size=ps)
+    model.set_attention(attention)
     try:
         lens = synth.ragged_lengths(B, 64, 384, seed=120)
         toks, aux = _prompt(B, lens, seed=121)

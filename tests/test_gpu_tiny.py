@@ -1,7 +1,8 @@
 """GPU parity of the whole round on the small drafter (n_embd 256, 4:1 GQA, head 64,
 RoPE 16/64, draft vocab 1024 -> 4096), through the C ABI, against the CPU oracle:
 prefill, chain, rewind, accept and rebuild, element by element, over several rounds,
-ragged batches, non-contiguous pages and the capacity boundary."""
+ragged batches, non-contiguous pages and the capacity boundary; the rounds under both
+decode attention kernels (tensor-core and CUDA-core)."""
 import numpy as np
 import pytest
 import torch
@@ -32,11 +33,18 @@ def _prompt(batch, lens, seed, P_max=None):
     return toks, aux, P_max
 
 
+@pytest.fixture(params=[0, 1], ids=["attn_cuda_cores", "attn_tensor_cores"])
+def attention(request, tiny):
+    tiny[1].set_attention(request.param)
+    yield request.param
+    tiny[1].set_attention(0)
+
+
 def _round(model, dr, seq, states, gamma, n_imposed, seed, flags=0):
     return run_round(model, dr, seq, states, gamma, n_imposed, seed, flags)[0]
 
 
-def test_single_sequence_rounds(tiny):
+def test_single_sequence_rounds(tiny, attention):
     wts, model, dr = tiny
     lens = np.array([32])
     toks, aux, _ = _prompt(1, lens, seed=1)
@@ -49,7 +57,7 @@ def test_single_sequence_rounds(tiny):
         states = _round(model, dr, seq, states, 3, np.array([n]), seed=10 + r)
 
 
-def test_ragged_batch_random_pages(tiny):
+def test_ragged_batch_random_pages(tiny, attention):
     wts, model, dr = tiny
     lens = np.array([5, 32, 17, 1])
     toks, aux, _ = _prompt(4, lens, seed=2)
