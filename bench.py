@@ -55,21 +55,18 @@ CONFIGS = {
 # byte the profiled ones (sha256 over the listed csrc files); the summaries under
 # profiles/ give the commands.  Keyed by (config, dominant projection or "attn").
 PROFILED_TRAFFIC = {
-    ("c2", "lmhead"): {"bytes": 262217984 + 2856192,
-                       "sources": ("gemv.cu", "gemv_kernel.cuh", "epilogue.cuh", "common.cuh"),
-                       "sha256": "08a836f1199077fda8eb1b016329037e0c81ec4e2bcf8bde0a03d4958d01a14b"},
-    ("c2", "lmhead", "bf16", "int4"): {"bytes": 69714432 + 257280,
-                                      "sources": ("gemv_q4.cu", "gemv_kernel.cuh", "epilogue.cuh", "common.cuh"),
-                                      "sha256": "4accf5f8fc63cdd4dc1e2791871c299f1b8fb8020d58b24314b2673bcf84f1dc"},
-    ("c4", "attn"): {"bytes": 538557184 + 3470336,
-                     "sources": ("attention.cu", "common.cuh"),
-                     "sha256": "4f4ce1b4205b28d46abaf0fcbb7a89305e1b24cec17f1d1e181340df05345e37"},
+    ("c2", "lmhead"): {"bytes": 262226944 + 2790144,
+                       "sources": ('gemv.cu', 'gemv_kernel.cuh', 'epilogue.cuh', 'common.cuh'),
+                       "sha256": "c67a4f9aa97fa08f163692561904f56c3b80de682d2b1f846d2f2bc82a917ec3"},
+    ("c4", "attn"): {"bytes": 539141888 + 3137792,
+                     "sources": ('attention.cu', 'attn_sched.cuh', 'common.cuh'),
+                     "sha256": "42782b1a48825416cef03dfd80a214f8e9dd40c5cf42736635faf3dcfe590c70"},
     ("c4", "lmhead"): {"bytes": 265027328 + 5622784,
-                       "sources": ("gemm_tc.cuh", "gemm_tc.cu", "epilogue.cuh", "common.cuh"),
+                       "sources": ('gemm_tc.cuh', 'gemm_tc.cu', 'epilogue.cuh', 'common.cuh'),
                        "sha256": "e70dea732e49eac95deaeaae7566bb8a320baec7fe55eb602172b4b48bb2d843"},
-    ("c5", "attn", "q8_0/q5_1"): {"bytes": 243912448 + 3330816,
-                                  "sources": ("attention.cu", "common.cuh"),
-                                  "sha256": "4f4ce1b4205b28d46abaf0fcbb7a89305e1b24cec17f1d1e181340df05345e37"},
+    ("c5", "attn", "q8_0/q5_1"): {"bytes": 243895808 + 3199232,
+                                  "sources": ('attention.cu', 'attn_sched.cuh', 'common.cuh'),
+                                  "sha256": "42782b1a48825416cef03dfd80a214f8e9dd40c5cf42736635faf3dcfe590c70"},
 }
 
 
