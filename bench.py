@@ -89,12 +89,14 @@ def profiled_traffic(config: str, kind: str, kv_format: str = "bf16", weights: s
 
 def kernel_label(kind: str, batch: int, weights: str = "bf16") -> str:
     """Name of the kernel that runs a phase at this batch on the bench's drafter geometry
-    (bf16 projections of three or more items run on the tcgen05 GEMM, smaller ones on the
-    CUDA-core GEMV; single-item INT4 projections with K <= 8192 on the mma.sync tensor-core
-    GEMV, the rest of INT4 on the CUDA-core GEMV)."""
+    (projections of three or more items run on the tcgen05 GEMM -- INT4 codes decoded into
+    tensor memory -- smaller ones on the CUDA-core GEMV; single-item INT4 projections with
+    K <= 8192 on the mma.sync tensor-core GEMV)."""
     if kind == "attn":
         return "attention"
     if weights == "int4":
+        if batch >= 3:
+            return f"{kind} INT4 tcgen05 GEMM"
         return f"{kind} INT4 mma.sync GEMV" if batch == 1 and kind != "down" else f"{kind} INT4 GEMV"
     return f"{kind} tcgen05 GEMM" if batch >= 3 else f"{kind} GEMV"
 
