@@ -530,8 +530,11 @@ def run_mine(args, cfg):
     barrier(world)
     t0 = time.perf_counter()
     for i in range(args.e2e_steps):
-        vbuf.copy_(pin_vaux[r], non_blocking=True)
+        # the chain first (it needs nothing from the host); the round's verify features
+        # (the target's, which exist only after it has seen the drafts) are copied in while
+        # the chain runs, before the rebuild that reads them
         seq.draft_chain(gamma, out=out)
+        vbuf.copy_(pin_vaux[r], non_blocking=True)
         seq.rewind()
         d = out["draft_tok"]
         verify(r, d)
