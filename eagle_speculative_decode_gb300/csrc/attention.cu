@@ -14,7 +14,9 @@
 // in the paged pool -- with bulk copies (TMA) into a 3-stage shared-memory ring guarded by
 // mbarriers, across pair boundaries without a pause.  Units below the committed length
 // were written before the chain started, so they are requested before the kernel waits
-// on its predecessor (programmatic dependent launch).
+// on its predecessor (programmatic dependent launch); for the others, the lengths and the
+// page-table entry (also fixed before the chain) are read before that wait, so only the
+// copy itself follows it.
 //
 // Eight consumer warps take UNR keys per lane group of each unit (a key of d = 256 dims
 // spans a warp, 8 dims = 16 bytes per lane; smaller heads put several keys in a warp).
@@ -184,20 +186,15 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
       for (long long u = u_begin; u < u_end && ok;) {
         const AttnSeg sg = attn_seg(sch, u, u_end);
         u += sg.r1 - sg.r0;
-        const int L = p.kv_len[sg.b], est = est_len(sg.b);
+        // the lengths and the page table were fixed before the chain started: only the
+        // copies of units holding keys the chain writes wait for the previous kernel
+        const int L = p.kv_len[sg.b], est = est_len(sg.b), fin = final_len(sg.b);
         const int32_t *pt = p.page_table + (size_t)sg.b * p.max_pages;
-        int fin = est;
         for (int r = sg.r0; r < sg.r1; ++r) {
           const int k0 = r * U;
           int k1 = min(k0 + U, est);
-          if (k1 > L) {  // this unit holds keys written by the chain: wait for them
-            if (!waited) {
-              pdl_wait();
-              waited = true;
-            }
-            fin = final_len(sg.b);
-            k1 = min(k1, fin);
-          }
+          const bool fresh = k1 > L;  // this unit holds keys written by the chain
+          if (fresh) k1 = min(k1, fin);
           if (k1 <= k0) continue;  // trimmed away: the consumers skip it too
           const int slot = g % kAttnStages;
           if (g >= kAttnStages && !mbar_wait(empty0 + 8 * slot, ((g / kAttnStages) - 1) & 1, abort_flag, p.status)) {
@@ -205,6 +202,10 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
             break;
           }
           const int pg = pt[k0 / ps];
+          if (fresh && !waited) {
+            pdl_wait();
+            waited = true;
+          }
           // bf16 rows: the unit's valid keys; quantized rows: the whole unit (sizes stay
           // multiples of 16 bytes; the slots past the valid keys are in the same page)
           const int nk = KVQ ? U : k1 - k0;
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
   }
 
   // ------------------------------------------------------------ consumer warps
-  pdl_wait();
+  bool waited = false;  // q is written by the previous kernel: wait before the first read
   const float qscale = rsqrtf((float)D) * 1.4426950408889634f;
   // Score index of this lane after the segment reduction: (key u_me, head g_me).
   const int idx_me = li >> SH;
@@ -246,6 +247,10 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
     const int b = sg.b, kvh = sg.kvh;
     const int est = est_len(b), fin = final_len(b), L = p.kv_len[b];
     const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
     // q, the running weighted V and the K / V values are float pairs: every multiply-add
     // of the loop is a packed two-lane FMA
     float2 qv[G][4];
@@ -275,9 +280,9 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
       if (k1 <= k0) continue;
       const int n = k1 - k0;
       const int slot = g % kAttnStages;
+      const int pg = pt[k0 / ps];
       const bool ok = mbar_wait(full0 + 8 * slot, (g / kAttnStages) & 1, abort_flag, p.status);
       ++g;
-      const int pg = pt[k0 / ps];
       const bool have = ok && pg >= 0 && pg < p.num_pages;
       const unsigned char *kst = smem + (size_t)slot * S::kStage;
       const unsigned char *vst = kst + (size_t)CH * KR;
