@@ -22,7 +22,7 @@ constexpr int kSplitSlots = 4096;    // attention partial slots (two per CTA) an
 constexpr int kMaxGraphs = 16;
 
 struct Layout {
-  size_t rope, q, attn_o, part_o, part_ml, attn_cnt, x1, act, gwork, tokwork, am_slot, am_cnt,
+  size_t rope, q, attn_o, part_o, part_ml, attn_cnt, x1, act, gwork, tokwork, am_slot, am_cnt, am_steps,
       round_start, geff, status, genc, xp0, xp1, xp2, sumsq, gsum, tc_part, tc_cnt, attn_plan, kv_stage, gres,
       total;
   size_t tc_items, tc_k, tc_part_elems;
@@ -98,6 +98,7 @@ Layout make_layout(const eagle3_config &c) {
   L.tokwork = take(B * 4);
   L.am_slot = take(B * (c.max_gamma + 1) * 8);  // one per chain item or verify row
   L.am_cnt = take(64 * 4);
+  L.am_steps = take(B * c.max_gamma * 8);  // per chain step and item (GEMV chains)
   L.round_start = take(B * 4);
   L.geff = take(B * 4);
   L.status = take(4);
@@ -156,7 +157,7 @@ struct eagle3_ctx {
   float *q, *attn_o, *part_o, *x1, *act, *gwork, *genc;
   float2 *part_ml;
   unsigned *attn_cnt, *am_cnt;
-  unsigned long long *am_slot;
+  unsigned long long *am_slot, *am_steps;
   int32_t *tokwork, *round_start, *geff;
   int *status;
   int num_sms;
@@ -419,15 +420,36 @@ struct ChainArgs {
   float *logits_dbg, *g_dbg;
 };
 
+// Whether a chain of B sequences runs its q/k/v and its lm_head on the GEMV (then the
+// lm_head's argmax is decoded by the kernel after it).
+bool chain_defers_argmax(const eagle3_ctx *ctx, int B) {
+  const eagle3_config &c = ctx->c;
+  GemvParams q = base_params(ctx);
+  q.mode = GM_QKV;
+  q.K = 2 * c.n_embd;
+  q.sz0 = ctx->q4 ? ctx->w.q_sz : nullptr;
+  GemvParams l = base_params(ctx);
+  l.mode = GM_LMHEAD;
+  l.K = c.n_embd;
+  l.sz0 = ctx->q4 ? ctx->w.lm_head_sz : nullptr;
+  return !use_tc(ctx, q, B) && !use_tc(ctx, l, B);
+}
+
 cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) {
   const eagle3_config &c = ctx->c;
   const int n = c.n_embd, qr = c.n_head * c.head_dim, kr = c.n_head_kv * c.head_dim;
   const bool pdl = true;
   record_event(ctx, st, PH_START);
+  // Chains whose q/k/v and lm_head both run on the GEMV leave each step's argmax in a slot
+  // of the step: the lm_head CTAs fold their maxima in and leave, the next step's q/k/v
+  // decodes the token (and writes the step's outputs), the chain end the last step's.
+  const bool defer = chain_defers_argmax(ctx, a.B);
+  const int ss = c.max_batch;  // slot row stride
   cudaError_t e = launched(ctx, st,
                            launch_chain_begin(a.B, a.gamma, a.flags, c.max_cache_len, a.kv->kv_len,
                                               ctx->round_start, ctx->geff, a.gamma_eff,
-                                              ctx->status, ctx->unit_keys, ctx->attn_plan, st),
+                                              ctx->status, ctx->unit_keys, ctx->attn_plan,
+                                              defer ? ctx->am_steps : nullptr, a.gamma * ss, st),
                            PH_SMALL);
   if (e != cudaSuccess) return e;
   for (int j = 0; j < a.gamma; ++j) {
@@ -450,6 +472,19 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     p.pairs.step_g = ctx->gwork;
     p.pairs.kv_len = a.kv->kv_len;
     p.pairs.gamma_eff = ctx->geff;
+    if (defer && j > 0) {
+      p.pairs.step_key = ctx->am_steps + (size_t)(j - 1) * ss;
+      p.pairs.d2t = ctx->w.d2t;
+      p.pairs.draft_vocab = c.draft_vocab;
+      p.pairs.target_vocab = c.target_vocab;
+      // the previous step's outputs (written by CTA 0)
+      p.d2t = ctx->w.d2t;
+      p.draft_tok = a.draft_tok;
+      p.draft_id = a.draft_id;
+      p.next_tok = ctx->tokwork;
+      p.gamma_eff = ctx->geff;
+      p.gamma = a.gamma;
+    }
     p.out_f = ctx->q;
     if ((e = qkv_items(ctx, p, a.B, st, pdl)) != cudaSuccess) return e;
 
@@ -534,8 +569,9 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     set_weights(ctx, p, ctx->w.lm_head, ctx->w.lm_head_sz);
     p.xf = ctx->gwork;
     p.norm0 = ctx->w.final_norm;
-    p.am_slot = ctx->am_slot;
+    p.am_slot = defer ? ctx->am_steps + (size_t)j * ss : ctx->am_slot;
     p.am_count = ctx->am_cnt;
+    p.am_defer = defer ? 1 : 0;
     p.d2t = ctx->w.d2t;
     p.draft_tok = a.draft_tok;
     p.draft_id = a.draft_id;
@@ -548,7 +584,19 @@ cudaError_t enqueue_chain(eagle3_ctx *ctx, const ChainArgs &a, cudaStream_t st) 
     p.dbg_off = j * c.draft_vocab;
     if ((e = gemv_items(ctx, p, a.B, st, pdl)) != cudaSuccess) return e;
   }
-  return launched(ctx, st, launch_chain_end(a.B, a.kv->kv_len, ctx->round_start, ctx->geff, st, pdl),
+  ChainLast last;
+  std::memset(&last, 0, sizeof(last));
+  if (defer) {
+    last.slot = ctx->am_steps + (size_t)(a.gamma - 1) * ss;
+    last.gamma = a.gamma;
+    last.draft_vocab = c.draft_vocab;
+    last.target_vocab = c.target_vocab;
+    last.d2t = ctx->w.d2t;
+    last.draft_tok = a.draft_tok;
+    last.draft_id = a.draft_id;
+    last.status = ctx->status;
+  }
+  return launched(ctx, st, launch_chain_end(a.B, a.kv->kv_len, ctx->round_start, ctx->geff, last, st, pdl),
                   PH_SMALL);
 }
 
@@ -728,6 +776,7 @@ int eagle3_init(const eagle3_config *cfg, const eagle3_weights *w, void *workspa
   ctx->tokwork = reinterpret_cast<int32_t *>(b + L.tokwork);
   ctx->am_slot = reinterpret_cast<unsigned long long *>(b + L.am_slot);
   ctx->am_cnt = reinterpret_cast<unsigned *>(b + L.am_cnt);
+  ctx->am_steps = reinterpret_cast<unsigned long long *>(b + L.am_steps);
   ctx->round_start = reinterpret_cast<int32_t *>(b + L.round_start);
   ctx->geff = reinterpret_cast<int32_t *>(b + L.geff);
   ctx->status = reinterpret_cast<int *>(b + L.status);

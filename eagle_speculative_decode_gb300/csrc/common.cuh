@@ -136,6 +136,11 @@ struct PairSource {
   const int32_t *bnd_tok;    // chain j == 0, rebuild i == 0
   const float *bnd_g;        // [B, n]
   const int32_t *step_tok;   // chain j > 0: token of this step per b [B]
+  // chain j > 0 with the argmax left in its slot: the winning (order key, ~row) of step
+  // j - 1 per b, decoded here (step_tok is then not read)
+  const unsigned long long *step_key;
+  const int64_t *d2t;        // draft id -> target id offsets (null: the ids are target ids)
+  int draft_vocab, target_vocab;
   const float *step_g;       // chain j > 0: g of this step [B, n]
   const int32_t *draft_tok;  // rebuild: [B, gamma]
   const float *enc_g;        // rebuild: [B, gamma + 1, n]; prefill: [items, n]
@@ -153,6 +158,42 @@ struct PairItem {
   bool write_kv;
 };
 
+// The draft id and target id of an argmax slot's winning key (order key << 32 | ~row);
+// false when either is out of range.
+__device__ __forceinline__ bool argmax_ids(unsigned long long key, const int64_t *d2t, int draft_vocab,
+                                           int target_vocab, uint32_t &id, long long &tgt) {
+  id = 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
+  if (id >= (uint32_t)draft_vocab) {
+    id = 0;
+    tgt = 0;
+    return false;
+  }
+  tgt = d2t ? (long long)id + d2t[id] : (long long)id;
+  if (tgt < 0 || tgt >= target_vocab) {
+    tgt = 0;
+    return false;
+  }
+  return true;
+}
+
+// A chain's step whose lm_head left its argmax in the step's slots (am_defer): thread t
+// writes item t's draft token and id of that step and the next step's token, as
+// lmhead_finalize does; run by the kernel after it (the next step's q/k/v, or the chain
+// end for the last step) once that lm_head has completed.
+__device__ __forceinline__ void chain_step_outputs(const unsigned long long *slot, int step, int item, int gamma,
+                                                   const int32_t *gamma_eff, const int64_t *d2t, int draft_vocab,
+                                                   int target_vocab, int32_t *draft_tok, int32_t *draft_id,
+                                                   int32_t *next_tok, int *status) {
+  uint32_t id;
+  long long tgt;
+  if (!argmax_ids(slot[item], d2t, draft_vocab, target_vocab, id, tgt)) set_status(status, EAGLE3_DEV_BAD_TOKEN);
+  const bool valid = !gamma_eff || step < gamma_eff[item];
+  const size_t o = (size_t)item * gamma + step;
+  draft_tok[o] = valid ? (int32_t)tgt : -1;
+  if (draft_id) draft_id[o] = valid ? (int32_t)id : -1;
+  if (next_tok) next_tok[item] = (int32_t)tgt;
+}
+
 __device__ __forceinline__ PairItem resolve_pair(const PairSource &s, int item, int n_embd) {
   PairItem it;
   if (s.kind == PAIR_CHAIN) {
@@ -161,7 +202,13 @@ __device__ __forceinline__ PairItem resolve_pair(const PairSource &s, int item, 
       it.tok = s.bnd_tok[item];
       it.g = s.bnd_g + (size_t)item * n_embd;
     } else {
-      it.tok = s.step_tok[item];
+      if (s.step_key) {
+        uint32_t id;
+        long long tgt;
+        it.tok = argmax_ids(s.step_key[item], s.d2t, s.draft_vocab, s.target_vocab, id, tgt) ? (int)tgt : -1;
+      } else {
+        it.tok = s.step_tok[item];
+      }
       it.g = s.step_g + (size_t)item * n_embd;
     }
     it.pos = s.kv_len[item] + s.step;
@@ -243,6 +290,9 @@ struct GemvParams {
   int gamma, step;
   int *status;
   int nstage;           // stages in the weight ring (set by the launcher)
+  // lm_head of a chain whose next q/k/v decodes the argmax: the CTAs only fold their
+  // maxima into am_slot (no arrival count, no last-CTA decode)
+  int am_defer;
 };
 
 // ----------------------------------------------------------------- attention

@@ -417,19 +417,10 @@ __device__ __forceinline__ void lmhead_finalize(const GemvParams &p, int item0, 
   for (int m = tid; m < items; m += nthreads) {
     const int item = item0 + m;
     const unsigned long long key = atomicExch(p.am_slot + item, 0ull);
-    uint32_t id = 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
-    bool bad = false;
-    if (id >= (uint32_t)p.draft_vocab) {
-      set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
-      id = 0;
-      bad = true;
-    }
-    long long tgt = p.d2t ? (long long)id + p.d2t[id] : (long long)id;  // no d2t: target ids
-    if (tgt < 0 || tgt >= p.target_vocab) {
-      set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
-      tgt = 0;
-      bad = true;
-    }
+    uint32_t id;
+    long long tgt;  // no d2t: the draft ids are target ids
+    const bool bad = !argmax_ids(key, p.d2t, p.draft_vocab, p.target_vocab, id, tgt);
+    if (bad) set_status(p.status, EAGLE3_DEV_BAD_TOKEN);
     // without a status word (the context-free entry point) the row itself carries the error
     const bool valid = (!p.gamma_eff || p.step < p.gamma_eff[item]) && !(bad && !p.status);
     const size_t o = (size_t)item * p.gamma + p.step;
@@ -596,6 +587,8 @@ __device__ void epilogue(const GemvParams &p, const float *accs, int nrows) {
       }
       consumer_sync();
     }
+    // deferred: the launch's completion publishes the maxima to the kernel that decodes them
+    if (p.am_defer) return;
     if (tid == 0) {
       __threadfence();
       const unsigned prev = atomicAdd(p.am_count, 1u);

@@ -190,6 +190,17 @@ __device__ __forceinline__ void gemv_finish(const GemvParams &p, const float (&s
   epilogue<NB, MODE, TR>(p, accs, nrows);
 }
 
+// A chain step's q/k/v whose previous lm_head left its argmax in the slots: CTA 0 writes
+// that step's draft tokens and ids (its other CTAs decode the token themselves).
+template <int MODE>
+__device__ __forceinline__ void chain_prev_outputs(const GemvParams &p) {
+  if constexpr (MODE == GM_QKV) {
+    if (p.pairs.kind == PAIR_CHAIN && p.pairs.step_key && blockIdx.x == 0 && (int)threadIdx.x < p.items)
+      chain_step_outputs(p.pairs.step_key, p.pairs.step - 1, p.item0 + (int)threadIdx.x, p.gamma, p.gamma_eff, p.d2t,
+                         p.draft_vocab, p.target_vocab, p.draft_tok, p.draft_id, p.next_tok, p.status);
+  }
+}
+
 template <int NB, int SR, int MODE, bool Q4>
 __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvParams p) {
   using T = ModeTraits<MODE>;
@@ -268,6 +279,7 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
 
   // ------------------------------------------------------------ consumer warps
   pdl_wait();
+  chain_prev_outputs<MODE>(p);
   float ss[NB][H];
   // x in registers: XRV 8-element vectors per item and thread (k = 8 (tid + 512 j)), so that
   // every weight vector read from the ring serves all items without x being re-read from
@@ -678,6 +690,7 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_q4_mma_kernel(const G
 
   // ------------------------------------------------------------ consumer warps
   pdl_wait();
+  chain_prev_outputs<MODE>(p);
   float ss[1][H];
   stage_x<1, MODE>(p, smem, ss);
   consumer_sync();

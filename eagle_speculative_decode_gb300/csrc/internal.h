@@ -68,12 +68,22 @@ cudaError_t attn_tc_prepare();
 cudaError_t attn_tc_launch(const AttnParams &p, int num_sms, cudaStream_t st, bool pdl);
 
 // Small bookkeeping kernels (small.cu).
+// slots / n_slots: the chain's per-step argmax slots, zeroed first (null: none)
 cudaError_t launch_chain_begin(int B, int gamma, unsigned flags, int max_cache_len,
                                const int32_t *kv_len, int32_t *round_start, int32_t *geff,
                                int32_t *geff_out, int *status, int unit_keys, int32_t *unit_pre,
-                               cudaStream_t st);
+                               unsigned long long *slots, int n_slots, cudaStream_t st);
+// The last step of a chain whose lm_head left its argmax in the slots (slot null: its
+// lm_head decoded it itself).
+struct ChainLast {
+  const unsigned long long *slot;  // [B] of the last step
+  int gamma, draft_vocab, target_vocab;
+  const int64_t *d2t;
+  int32_t *draft_tok, *draft_id;
+  int *status;
+};
 cudaError_t launch_chain_end(int B, int32_t *kv_len, const int32_t *round_start,
-                             const int32_t *geff, cudaStream_t st, bool pdl);
+                             const int32_t *geff, const ChainLast &last, cudaStream_t st, bool pdl);
 cudaError_t launch_rewind(int B, int32_t *kv_len, const int32_t *round_start, cudaStream_t st);
 cudaError_t launch_wait_selftest(int *status, int *result, cudaStream_t st);
 cudaError_t launch_res_norm(int B, int n, float eps, const float *g, const uint16_t *w, float *out,

@@ -29,9 +29,12 @@ __global__ void __launch_bounds__(1024) chain_begin_kernel(int B, int gamma, uns
                                                            int max_cache_len, const int32_t *kv_len,
                                                            int32_t *round_start, int32_t *geff,
                                                            int32_t *geff_out, int *status, int U,
-                                                           int32_t *pre) {
+                                                           int32_t *pre, unsigned long long *slots,
+                                                           int n_slots) {
   pdl_wait();
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  // argmax slots of a chain whose steps leave their maxima there (zero before the first)
+  for (int i = tid; slots && i < n_slots; i += nt) slots[i] = 0ull;
   for (int b = tid; b < B; b += nt) {
     const int L = kv_len[b];
     int ge = gamma;
@@ -96,11 +99,17 @@ __global__ void __launch_bounds__(1024) chain_begin_kernel(int B, int gamma, uns
 }
 
 __global__ void chain_end_kernel(int B, int32_t *kv_len, const int32_t *round_start,
-                                 const int32_t *geff) {
+                                 const int32_t *geff, ChainLast last) {
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b < B) kv_len[b] = round_start[b] + geff[b];
+  if (b < B) {
+    // the last step's tokens, where its lm_head left the argmax in the slots
+    if (last.slot)
+      chain_step_outputs(last.slot, last.gamma - 1, b, last.gamma, geff, last.d2t, last.draft_vocab,
+                         last.target_vocab, last.draft_tok, last.draft_id, nullptr, last.status);
+    kv_len[b] = round_start[b] + geff[b];
+  }
 }
 
 __global__ void rewind_kernel(int B, int32_t *kv_len, const int32_t *round_start) {
@@ -224,18 +233,18 @@ cudaError_t launch_wait_selftest(int *status, int *result, cudaStream_t st) {
 cudaError_t launch_chain_begin(int B, int gamma, unsigned flags, int max_cache_len,
                                const int32_t *kv_len, int32_t *round_start, int32_t *geff,
                                int32_t *geff_out, int *status, int unit_keys, int32_t *unit_pre,
-                               cudaStream_t st) {
+                               unsigned long long *slots, int n_slots, cudaStream_t st) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = small_cfg(1, 1024, st, false, attr);
   return cudaLaunchKernelEx(&cfg, chain_begin_kernel, B, gamma, flags, max_cache_len, kv_len,
-                            round_start, geff, geff_out, status, unit_keys, unit_pre);
+                            round_start, geff, geff_out, status, unit_keys, unit_pre, slots, n_slots);
 }
 
 cudaError_t launch_chain_end(int B, int32_t *kv_len, const int32_t *round_start,
-                             const int32_t *geff, cudaStream_t st, bool pdl) {
+                             const int32_t *geff, const ChainLast &last, cudaStream_t st, bool pdl) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = small_cfg((B + 127) / 128, 128, st, pdl, attr);
-  return cudaLaunchKernelEx(&cfg, chain_end_kernel, B, kv_len, round_start, geff);
+  return cudaLaunchKernelEx(&cfg, chain_end_kernel, B, kv_len, round_start, geff, last);
 }
 
 // The bookkeeping kernels are launched as programmatic dependents of whatever kernel
