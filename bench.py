@@ -55,18 +55,18 @@ CONFIGS = {
 # byte the profiled ones (sha256 over the listed csrc files); the summaries under
 # profiles/ give the commands.  Keyed by (config, dominant projection or "attn").
 PROFILED_TRAFFIC = {
-    ("c2", "lmhead"): {"bytes": 262226944 + 2790144,
-                       "sources": ('gemv.cu', 'gemv_kernel.cuh', 'epilogue.cuh', 'common.cuh'),
-                       "sha256": "c67a4f9aa97fa08f163692561904f56c3b80de682d2b1f846d2f2bc82a917ec3"},
-    ("c4", "attn"): {"bytes": 539141888 + 3137792,
-                     "sources": ('attention.cu', 'attn_sched.cuh', 'common.cuh'),
-                     "sha256": "42782b1a48825416cef03dfd80a214f8e9dd40c5cf42736635faf3dcfe590c70"},
-    ("c4", "lmhead"): {"bytes": 265027328 + 5622784,
-                       "sources": ('gemm_tc.cuh', 'gemm_tc.cu', 'epilogue.cuh', 'common.cuh'),
-                       "sha256": "e70dea732e49eac95deaeaae7566bb8a320baec7fe55eb602172b4b48bb2d843"},
-    ("c5", "attn", "q8_0/q5_1"): {"bytes": 243895808 + 3199232,
-                                  "sources": ('attention.cu', 'attn_sched.cuh', 'common.cuh'),
-                                  "sha256": "42782b1a48825416cef03dfd80a214f8e9dd40c5cf42736635faf3dcfe590c70"},
+    ('c2', 'lmhead'): {"bytes": 262219776 + 2749696,
+                      "sources": ('gemv.cu', 'gemv_kernel.cuh', 'epilogue.cuh', 'common.cuh'),
+                      "sha256": "a52de8f3a7abfa46237002e1558fc6888972aa56598836a8a812a11db62cc868"},
+    ('c4', 'attn'): {"bytes": 539141376 + 3132160,
+                    "sources": ('attention.cu', 'attn_sched.cuh', 'common.cuh'),
+                    "sha256": "f1c15ad2a3315885ac9c99241d4de4ae3d67abc8c143441bff022c8afb18017e"},
+    ('c4', 'lmhead'): {"bytes": 265026560 + 5626880,
+                      "sources": ('gemm_tc.cuh', 'gemm_tc.cu', 'epilogue.cuh', 'common.cuh'),
+                      "sha256": "9a91526e826f19bab67fb100a50526ab97a65ddf8646787cb860a78f4feeb383"},
+    ('c5', 'attn', 'q8_0/q5_1'): {"bytes": 243893760 + 2939904,
+                                 "sources": ('attention.cu', 'attn_sched.cuh', 'common.cuh'),
+                                 "sha256": "f1c15ad2a3315885ac9c99241d4de4ae3d67abc8c143441bff022c8afb18017e"},
 }
 
 
