@@ -146,11 +146,13 @@ __device__ __forceinline__ float q4_dot(const float2 (&f)[4], const float2 (&xq)
 }
 
 // Tail shared by the GEMV kernels: the RMSNorm scale 1 / sqrt(mean(x^2) + eps) per item and
-// K half from the consumers' shares ss, the per-warp row sums in part ([rows][warps][H][NB])
-// added in warp order and scaled, then the mode's epilogue on the finished rows.
+// K half from the consumers' shares ss, the per-warp row sums in part ([warps][H][NB][rows],
+// rows prs apart: the threads that each add up one row read consecutive words, free of bank
+// conflicts) added in warp order and scaled, then the mode's epilogue on the finished rows.
 template <int NB, int MODE, int TR>
 __device__ __forceinline__ void gemv_finish(const GemvParams &p, const float (&ss)[NB][ModeTraits<MODE>::kHalves],
-                                            const float *part, float *accs, float *red, float *scale, int nrows) {
+                                            const float *part, int prs, float *accs, float *red, float *scale,
+                                            int nrows) {
   using T = ModeTraits<MODE>;
   constexpr int H = T::kHalves;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -181,7 +183,7 @@ __device__ __forceinline__ void gemv_finish(const GemvParams &p, const float (&s
     for (int h = 0; h < H; ++h) {
       float sum = 0.f;
 #pragma unroll
-      for (int w = 0; w < kGemvWarps; ++w) sum += part[(((size_t)r * kGemvWarps + w) * H + h) * NB + m];
+      for (int w = 0; w < kGemvWarps; ++w) sum += part[(((size_t)w * H + h) * NB + m) * prs + r];
       y += T::kNorm ? sum * scale[m * H + h] : sum;
     }
     accs[e] = y;
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
 
   unsigned char *xmem = smem;
   unsigned char *ring = smem + L.ring_off;
-  float *part = reinterpret_cast<float *>(smem + L.part_off);  // [max_rows][warps][H][NB]
+  float *part = reinterpret_cast<float *>(smem + L.part_off);  // [warps][H][NB][max_rows]
   float *accs = reinterpret_cast<float *>(smem + L.accs_off);  // [max_rows][NB]
   float *red = reinterpret_cast<float *>(smem + L.red_off);    // [warps][NB * H]
   float *scale = reinterpret_cast<float *>(smem + L.scale_off);  // [NB * H]
@@ -459,10 +461,10 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_kernel(const GemvPara
       const int idx = warp_reduce_index<N>(lane);
       const int m = idx % NB, r = (idx / NB) % SR, h = idx / (NB * SR);
       const int lrow = st * SR + r;
-      if (lrow < nrows) part[(((size_t)lrow * kGemvWarps + warp) * H + h) * NB + m] = tot;
+      if (lrow < nrows) part[(((size_t)warp * H + h) * NB + m) * max_rows + lrow] = tot;
     }
   }
-  gemv_finish<NB, MODE, TR>(p, ss, part, accs, red, scale, nrows);
+  gemv_finish<NB, MODE, TR>(p, ss, part, max_rows, accs, red, scale, nrows);
 }
 
 // ------------------------------------- INT4, one item, on the tensor cores (mma.sync)
@@ -621,7 +623,7 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_q4_mma_kernel(const G
   unsigned char *ring = smem + L.ring_off;
   uint2 *xfrag = reinterpret_cast<uint2 *>(smem + L.xfrag_off);
   float2 *gsum = reinterpret_cast<float2 *>(smem + L.gsum_off);
-  float *part = reinterpret_cast<float *>(smem + L.part_off);  // [max_rows][warps][H]
+  float *part = reinterpret_cast<float *>(smem + L.part_off);  // [warps][H][max_rows]
   float *accs = reinterpret_cast<float *>(smem + L.accs_off);
   float *red = reinterpret_cast<float *>(smem + L.red_off);
   float *scale = reinterpret_cast<float *>(smem + L.scale_off);
@@ -773,12 +775,12 @@ __global__ void __launch_bounds__(kGemvCtaThreads, 1) gemv_q4_mma_kernel(const G
     if (q == 0) {
 #pragma unroll
       for (int hh = 0; hh < H; ++hh) {
-        if (ra_row < TR) part[((size_t)(st * TR + ra_row) * kGemvWarps + warp) * H + hh] = hh == h ? v0 : 0.f;
-        if (rb_row < TR) part[((size_t)(st * TR + rb_row) * kGemvWarps + warp) * H + hh] = hh == h ? v1 : 0.f;
+        if (ra_row < TR) part[((size_t)warp * H + hh) * max_rows + st * TR + ra_row] = hh == h ? v0 : 0.f;
+        if (rb_row < TR) part[((size_t)warp * H + hh) * max_rows + st * TR + rb_row] = hh == h ? v1 : 0.f;
       }
     }
   }
-  gemv_finish<1, MODE, TR>(p, ss, part, accs, red, scale, nrows);
+  gemv_finish<1, MODE, TR>(p, ss, part, max_rows, accs, red, scale, nrows);
 }
 
 // ------------------------------------------------------------------ launcher
