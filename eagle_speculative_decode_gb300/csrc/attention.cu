@@ -130,8 +130,6 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
   const uint32_t empty0 = full0 + 8 * kAttnStages;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kBar + 2 * kAttnStages * 8);
   __shared__ float2 sm_ml[NP][G];
-  __shared__ float sm_w[NP][G];  // merge weights of the lane groups per head
-  __shared__ float2 sm_M[G];     // per head: (max, sum) over the lane groups
   __shared__ int last_sh;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -414,30 +412,20 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
     // this CTA's (max, sum, weighted V) of the pair: in place in sm_acc lane group 0 and
     // sm_ml, or written out when no other CTA holds units of the pair
     const int mine = cta * 2 + (sch.start(cta) >= sg.pair_u0 ? 0 : 1);  // partial slot
-    // per head: the lane groups' maximum M, their weights exp2(m - M) and the sum L, once
-    // for all D outputs of the head
-    if (tid < G) {
-      float M = -INFINITY;
-#pragma unroll
-      for (int q = 0; q < NP; ++q) M = fmaxf(M, sm_ml[q][tid].x);
-      float Ls = 0.f;
-#pragma unroll
-      for (int q = 0; q < NP; ++q) {
-        const float2 ml = sm_ml[q][tid];
-        const float w = M != -INFINITY ? exp2f(ml.x - M) : 0.f;
-        sm_w[q][tid] = w;
-        Ls += ml.y * w;
-      }
-      sm_M[tid] = make_float2(M, Ls);
-    }
-    asm volatile("bar.sync 1, 256;" ::: "memory");
     for (int e = tid; e < G * D; e += kAttnThreads) {
       const int gg = e / D, dim = e - gg * D;
-      const float M = sm_M[gg].x, Ls = sm_M[gg].y;
-      float O = 0.f;
+      float M = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < NP; ++q) M = fmaxf(M, sm_ml[q][gg].x);
+      float Ls = 0.f, O = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
-        for (int q = 0; q < NP; ++q) O += sm_acc[((size_t)q * G + gg) * D + dim] * sm_w[q][gg];
+        for (int q = 0; q < NP; ++q) {
+          const float2 ml = sm_ml[q][gg];
+          const float w = exp2f(ml.x - M);
+          Ls += ml.y * w;
+          O += sm_acc[((size_t)q * G + gg) * D + dim] * w;
+        }
       }
       if (whole) {
         out[e] = O / Ls;
@@ -474,16 +462,6 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
       slot_s[i] = c2 * 2 + (sch.start(c2) >= pu0 ? 0 : 1);
     }
     asm volatile("bar.sync 1, 256;" ::: "memory");
-    // the first eight contributors' slices of this thread are requested now, so that their
-    // round trip overlaps the weights' computation (bf16 rows and groups up to 4: the other
-    // instantiations have no registers to spare)
-    constexpr int NPRE = (!KVQ && G <= 4) ? 8 : 0;
-    const float4 *po = reinterpret_cast<const float4 *>(p.part_o);
-    const int n0 = nc < NPRE ? nc : NPRE;
-    float4 pre[NPRE > 0 ? NPRE : 1];
-#pragma unroll
-    for (int k = 0; k < NPRE; ++k)
-      if (k < n0 && tid < G * D / 4) pre[k] = __ldcg(po + (size_t)slot_s[k] * (G * D / 4) + tid);
     for (int i = tid; i < nc * G; i += kAttnThreads) ml_s[i] = __ldcg(&p.part_ml[(size_t)slot_s[i / G] * G + i % G]);
     asm volatile("bar.sync 1, 256;" ::: "memory");
     if (tid < G) {
@@ -501,21 +479,12 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) attn_decode_kernel(const A
       w_s[i] = ml.x == -INFINITY ? 0.f : exp2f(ml.x - ML[gg].x) * ML[gg].y;
     }
     asm volatile("bar.sync 1, 256;" ::: "memory");
+    const float4 *po = reinterpret_cast<const float4 *>(p.part_o);
     float4 *out4 = reinterpret_cast<float4 *>(out);
     for (int f = tid; f < G * D / 4; f += kAttnThreads) {
       const int gg = (f * 4) / D;
       float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
       int q = 0;
-      if (f == tid) {  // the prefetched contributors, in the same order
-#pragma unroll
-        for (int k = 0; k < NPRE; ++k)
-          if (k < n0) {
-            const float w = w_s[k * G + gg];
-            o.x = fmaf(w, pre[k].x, o.x); o.y = fmaf(w, pre[k].y, o.y);
-            o.z = fmaf(w, pre[k].z, o.z); o.w = fmaf(w, pre[k].w, o.w);
-          }
-        q = n0;
-      }
       for (; q + 8 <= nc; q += 8) {
         float4 v[8];
 #pragma unroll
